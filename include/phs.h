@@ -1,0 +1,292 @@
+/*
+ * phs.h -- C ABI of the paged hybrid sliding-window decode library
+ * (libphs.so, CUDA, sm_103a).
+ *
+ * The library computes one decode step of attention for a batch of requests
+ * whose KV cache is split into two pools, as described on the "Xiaomi
+ * MiMo-V2.5 inference system" page (section 2, "KVCache system rebuild",
+ * dual pools):
+ *   - a Full-attention pool of fixed-size pages reached through per-request
+ *     block tables; pages may be shared by several requests through a
+ *     reference count ("Kimi K3 context caching" page, section 1: copy on
+ *     write and reference counts in the page table);
+ *   - a sliding-window (SWA) pool that is a per-request ring buffer of W
+ *     tokens (MiMo page, section 2: ring buffer, storage O(W)).
+ * plus the KV append that writes each new token into its page or ring slot
+ * and a block-wise INT8 quantiser with one fp32 absmax scale per 32 tokens per
+ * KV head ("Kimi K2.5 architecture deep dive" page, sections 2.2 and 2.3).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument named *dev / pool / table / q / out / workspace
+ *     is a DEVICE pointer unless the comment says "host".  The caller owns
+ *     all memory.  The library allocates nothing and keeps no state between
+ *     calls except a per-thread cache of device properties.
+ *   - bf16 tensors are IEEE bfloat16 (2 bytes).  Layouts are C order:
+ *       Full pool  K, V : [num_pages][Hkv][page_size][D]       bf16
+ *       SWA ring   K, V : [num_rings][Hkv][window][D]          bf16
+ *       INT8 pool  K, V : [num_qpages][Hkv][32][D]             int8
+ *       INT8 scales     : [num_qpages][Hkv]                    fp32
+ *       q, out          : [batch][Hq][D]                       bf16 / fp32
+ *       k_new, v_new    : [batch][Hkv][D]                      bf16
+ *       block_table     : [batch][max_pages_per_seq]           int32
+ *   - Query head i attends with KV head i / (Hq / Hkv).
+ *   - seq_lens[b] is the request's length AFTER this step's token has been
+ *     appended; decode is "append, then attend", so the new token attends to
+ *     itself.  Token t of request b lives in page block_table[b][t / 16] at
+ *     slot t % 16.  In the ring the newest token is at slot ring_pos[b] and
+ *     token t at (ring_pos[b] - (seq_lens[b] - 1 - t)) mod W; an SWA layer
+ *     attends to the last min(seq_lens[b], W) tokens.
+ *   - All work is queued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).
+ *   - Argument errors are detected on the host and returned synchronously as
+ *     a negative phs_status, before anything is launched.
+ *   - Errors that depend on device data (a page id outside the pool, a
+ *     sequence longer than its block table, an append into a shared page, a
+ *     wait that timed out) are recorded in *dev_status when dev_status is not
+ *     NULL: a device int32 the caller zeroes; the first error code written
+ *     wins.  The offending item is skipped; nothing traps.
+ *   - Supported shapes: page_size 16, head_dim 64 or 128, Hq a multiple of Hkv
+ *     with group size Hq/Hkv <= 16, window a multiple of 16 (<= 4096).
+ *     Anything else returns PHS_EUNSUPPORTED.
+ */
+#ifndef PHS_H_
+#define PHS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PHS_OK = 0,
+    PHS_EINVAL = -1,        /* null pointer, non-positive size, bad enum */
+    PHS_ESHAPE = -2,        /* inconsistent shapes between arguments */
+    PHS_ERANGE = -3,        /* (device) index outside its pool or table */
+    PHS_ESHARED = -4,       /* (device) append into a page with refcount != 1 */
+    PHS_EWORKSPACE = -5,    /* workspace missing or too small */
+    PHS_ECUDA = -6,         /* a CUDA runtime/driver call failed */
+    PHS_EUNSUPPORTED = -7,  /* valid but unsupported shape */
+    PHS_ETIMEOUT = -8,      /* (device) a bounded wait gave up */
+    PHS_EALIGN = -9         /* a pointer is not 16-byte aligned */
+} phs_status;
+
+enum { PHS_OUT_BF16 = 0, PHS_OUT_F32 = 1 };
+
+/* Paged Full-attention pool. */
+typedef struct {
+    void *k;              /* device, bf16 [num_pages][Hkv][page_size][D] */
+    void *v;              /* device, same layout as k */
+    int64_t num_pages;
+    int32_t page_size;    /* tokens per page; must be 16 */
+    int32_t num_kv_heads; /* Hkv */
+    int32_t head_dim;     /* D: 64 or 128 */
+} phs_paged_pool;
+
+/* SWA ring pool: one ring of `window` token slots per ring id. */
+typedef struct {
+    void *k;              /* device, bf16 [num_rings][Hkv][window][D] */
+    void *v;
+    int64_t num_rings;
+    int32_t window;       /* W, a multiple of 16 */
+    int32_t num_kv_heads;
+    int32_t head_dim;
+} phs_ring_pool;
+
+/* INT8 pool: 32-token pages of codes plus one fp32 scale per page and head. */
+typedef struct {
+    int8_t *k;            /* device, int8 [num_qpages][Hkv][32][D] */
+    int8_t *v;
+    float *k_scale;       /* device, fp32 [num_qpages][Hkv] */
+    float *v_scale;
+    int64_t num_qpages;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+} phs_int8_pool;
+
+/* ------------------------------------------------------------------------
+ * KV append, Full pool.
+ * Source: "Kimi K3 context caching" page, section 1 (a request that extends
+ * a shared prefix gets new physical blocks only for its own new tokens) and
+ * MiMo page, section 2 (the Full pool grows on demand).
+ * For each request b with seq_lens[b] >= 1, copies k_new[b] and v_new[b]
+ * ([Hkv][D] bf16) into slot (seq_lens[b]-1) % 16 of page
+ * block_table[b][(seq_lens[b]-1) / 16], for every KV head.  A byte copy.
+ * page_refcount (device, int32 [num_pages], may be NULL): when given, a
+ * target page whose count is not 1 is not written and PHS_ESHARED is
+ * recorded in *dev_status (copy on write is the allocator's job).
+ * Out-of-range page ids / table positions record PHS_ERANGE.
+ * ---------------------------------------------------------------------- */
+int phs_kv_append_paged(const phs_paged_pool *pool, const void *k_new, const void *v_new,
+                        const int32_t *block_table, int32_t max_pages_per_seq,
+                        const int32_t *seq_lens, int32_t batch,
+                        const int32_t *page_refcount, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * KV append, SWA ring.
+ * Source: MiMo page, section 2 (ring buffer of W slots, window-based
+ * eviction: the new token overwrites the one leaving the window).
+ * Writes k_new[b], v_new[b] into slot ring_pos[b] of ring ring_ids[b]
+ * (ring_ids may be NULL: request b owns ring b).  ring_pos is the slot of
+ * the token being appended (device, int32 [batch], in [0, W)).
+ * ---------------------------------------------------------------------- */
+int phs_kv_append_ring(const phs_ring_pool *ring, const void *k_new, const void *v_new,
+                       const int32_t *ring_ids, const int32_t *ring_pos, int32_t batch,
+                       int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Block-32 INT8 quantiser.
+ * Source: "Kimi K2.5 architecture deep dive" page, sections 2.2-2.3 (warm
+ * KV as INT8 with block-wise quantisation, a scale per group of 32 tokens).
+ * For each request b and each 32-token block j in
+ * [first_qblock[b], first_qblock[b] + num_qblocks[b]) (device int32 arrays),
+ * for each KV head, separately for K and V: reads the 32 x D bf16 group
+ * (tokens 32j .. 32j+31 through src_block_table), computes in IEEE fp32
+ *     a = max |x|,  s = a / 127,  code = clamp(rint(x / s), -127, 127)
+ * (rint rounds half to even; a == 0 gives s = 0 and all codes 0), and stores
+ * the codes in INT8 page dst_qtable[b][j] and s in the matching scale slot.
+ * max_qblocks bounds num_qblocks[b] (host int; sizes the grid).
+ * ---------------------------------------------------------------------- */
+int phs_kv_quant_int8_block32(const phs_paged_pool *src, const int32_t *src_block_table,
+                              int32_t src_max_pages, const phs_int8_pool *dst,
+                              const int32_t *dst_qtable, int32_t dst_max_qpages,
+                              const int32_t *first_qblock, const int32_t *num_qblocks,
+                              int32_t max_qblocks, int32_t batch, int32_t *dev_status,
+                              void *stream);
+
+/* ------------------------------------------------------------------------
+ * Workspace for split-KV Full-attention decode, in bytes.
+ * tokens_per_split: 0 = the library's choice (the same choice the decode
+ * call makes for the same arguments); otherwise a positive multiple of 32.
+ * has_int8: 1 if the decode call will pass an INT8 pool.
+ * ---------------------------------------------------------------------- */
+size_t phs_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_seq_len,
+                                  int32_t tokens_per_split, int32_t has_int8);
+
+/* The split length (tokens) the decode call uses for these arguments. */
+int32_t phs_decode_tokens_per_split(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len,
+                                    int32_t tokens_per_split);
+
+/* ------------------------------------------------------------------------
+ * Full-attention decode over the paged pool, one query token per request.
+ * Source: MiMo page, section 1 (Full layers attend over the whole sequence;
+ * decode latency follows the KV bytes read) and the textbook definition
+ *     out[b][i] = softmax_t(softmax_scale * q[b][i] . K_b[t]) V_b[t],
+ *     t in [0, seq_lens[b]).
+ * Optional INT8 region (int8 != NULL): tokens t < qlens[b] (a multiple of
+ * 32) are read from INT8 page qtable[b][t / 32] (device int32
+ * [batch][max_qpages_per_seq]) and dequantised as (float)code * scale;
+ * tokens t >= qlens[b] are read from bf16 pages block_table[b][t / 16].
+ * The sequence is cut into splits of tokens_per_split tokens (INT8 and bf16
+ * regions are split separately); one CTA reduces one (request, KV head,
+ * split) for all Hq/Hkv query heads of the group; a second kernel merges the
+ * splits by log-sum-exp.  max_seq_len (host int) bounds seq_lens[b].
+ * out: [batch][Hq][D], bf16 (out_dtype PHS_OUT_BF16) or fp32.
+ * workspace: device, at least phs_decode_workspace_bytes(...) bytes, 256-byte
+ * aligned; contents need no initialisation and are overwritten.
+ * Requests with seq_lens[b] == 0 get an all-zero output row.
+ * ---------------------------------------------------------------------- */
+int phs_attn_decode_full_paged(const void *q, int32_t num_q_heads, const phs_paged_pool *pool,
+                               const int32_t *block_table, int32_t max_pages_per_seq,
+                               const int32_t *seq_lens, int32_t max_seq_len,
+                               const phs_int8_pool *int8, const int32_t *qtable,
+                               int32_t max_qpages_per_seq, const int32_t *qlens,
+                               int32_t batch, float softmax_scale, int32_t tokens_per_split,
+                               void *out, int32_t out_dtype, void *workspace,
+                               size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* The two phases of phs_attn_decode_full_paged, exposed separately so that
+ * each kernel can be timed on its own.  The split phase writes every
+ * single-split request's final output directly and the partial (m, l, o)
+ * of multi-split requests into the workspace; the merge phase finishes the
+ * multi-split requests.  Same arguments and meaning as above. */
+int phs_attn_decode_full_paged_split(const void *q, int32_t num_q_heads,
+                                     const phs_paged_pool *pool, const int32_t *block_table,
+                                     int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                     int32_t max_seq_len, const phs_int8_pool *int8,
+                                     const int32_t *qtable, int32_t max_qpages_per_seq,
+                                     const int32_t *qlens, int32_t batch, float softmax_scale,
+                                     int32_t tokens_per_split, void *out, int32_t out_dtype,
+                                     void *workspace, size_t workspace_bytes,
+                                     int32_t *dev_status, void *stream);
+
+/* Cross-split merge: for each (request, query head) with more than one
+ * split, M = max_s m_s, L = sum_s l_s 2^(m_s - M),
+ * out = sum_s 2^(m_s - M) o_s / L.  qlens may be NULL (no INT8 region). */
+int phs_attn_merge_splits(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, const int32_t *seq_lens, int32_t max_seq_len,
+                          const int32_t *qlens, int32_t has_int8, int32_t tokens_per_split,
+                          void *out, int32_t out_dtype, const void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Sliding-window decode over the SWA ring.
+ * Source: MiMo page, section 1 (SWA layers, window 128, attend to the most
+ * recent tokens) and section 2 (ring buffer of capacity W).
+ * out[b][i] = softmax attention of q[b][i] over the last min(seq_lens[b], W)
+ * tokens of request b, read from ring ring_ids[b] (NULL = identity) whose
+ * newest token is at slot ring_pos[b].  No workspace.
+ * ---------------------------------------------------------------------- */
+int phs_attn_decode_swa_ring(const void *q, int32_t num_q_heads, const phs_ring_pool *ring,
+                             const int32_t *ring_ids, const int32_t *ring_pos,
+                             const int32_t *seq_lens, int32_t batch, float softmax_scale,
+                             void *out, int32_t out_dtype, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * One decode step of a hybrid layer stack.
+ * Source: MiMo page, section 1 (70 layers: 10 Full attention, 60 sliding
+ * window of 128) and section 2 (dual pools; SWA reads overlap layer by
+ * layer).  For every layer in `layers` (host array): if do_append, append
+ * k_new/v_new into the layer's pool (paged for Full layers through the
+ * shared block_table, ring slot ring_pos for SWA layers), then attend:
+ * Full layers through phs_attn_decode_full_paged, SWA layers through the
+ * ring.  All SWA layers go into one launch; each Full layer is one split
+ * launch plus one merge launch, all reusing `workspace`
+ * (phs_hybrid_stack_workspace_bytes).  Layers are independent: the step
+ * runs each layer on its own q (no model weights are involved).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    int32_t is_full;      /* 1 = Full-attention layer, 0 = SWA layer */
+    const void *q;        /* device, bf16 [batch][Hq][D] */
+    const void *k_new;    /* device, bf16 [batch][Hkv][D] (used if do_append) */
+    const void *v_new;
+    void *out;            /* device, [batch][Hq][D], out_dtype */
+    phs_paged_pool paged; /* Full layers */
+    phs_ring_pool ring;   /* SWA layers */
+} phs_layer;
+
+int phs_attn_decode_hybrid_stack(const phs_layer *layers, int32_t num_layers,
+                                 int32_t num_q_heads, int32_t batch,
+                                 const int32_t *block_table, int32_t max_pages_per_seq,
+                                 const int32_t *seq_lens, int32_t max_seq_len,
+                                 const int32_t *ring_ids, const int32_t *ring_pos,
+                                 float softmax_scale, int32_t do_append, int32_t out_dtype,
+                                 void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream);
+
+size_t phs_hybrid_stack_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t max_seq_len);
+
+/* KV tokens held by a hybrid stack (host arrays in, host results out):
+ * Full layers hold seq_lens[b] tokens per request, SWA layers
+ * min(seq_lens[b], window).  Source: MiMo page, section 1 (the 10/60 stack
+ * holds about 1/7 of an all-Full stack's KV at long lengths). */
+int phs_hybrid_kv_tokens(const int32_t *layer_is_full_host, int32_t num_layers,
+                         const int32_t *seq_lens_host, int32_t batch, int32_t window,
+                         int64_t *full_tokens, int64_t *swa_tokens);
+
+/* Plain device-to-device copy kernel (16-byte vector loads and stores), the
+ * in-run HBM bandwidth yardstick.  dst and src 16-byte aligned, bytes a
+ * multiple of 16. */
+int phs_copy_d2d(void *dst, const void *src, size_t bytes, void *stream);
+
+const char *phs_status_str(int status);
+int32_t phs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PHS_H_ */

@@ -1,0 +1,395 @@
+"""paged_hybrid_sliding_gb300 -- decode attention over a hybrid paged KV
+cache (a paged Full-attention pool plus per-request SWA ring buffers), KV
+append and block-32 INT8 quantisation, as hand-written CUDA for sm_103a
+behind the C ABI of include/phs.h.
+
+This module only marshals torch tensors into the C ABI: every step runs in
+the library's kernels.  Tensors must be CUDA, contiguous and of the dtype
+stated; the stream defaults to torch's current stream.  Errors returned by
+the library raise PhsError.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+__all__ = [
+    "PhsError", "PagedPool", "RingPool", "Int8Pool", "Layer",
+    "kv_append_paged", "kv_append_ring", "kv_quant_int8_block32",
+    "decode_workspace_bytes", "decode_tokens_per_split",
+    "attn_decode_full_paged", "attn_decode_full_paged_split", "attn_merge_splits",
+    "attn_decode_swa_ring", "attn_decode_hybrid_stack", "hybrid_stack_workspace_bytes",
+    "hybrid_kv_tokens", "copy_d2d", "lib", "PAGE", "QBLOCK",
+]
+
+PAGE = 16
+QBLOCK = 32
+OUT_BF16, OUT_F32 = 0, 1
+
+
+class PhsError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        msg = lib().phs_status_str(code).decode()
+        super().__init__(f"{what}: {msg} ({code})")
+
+
+def lib():
+    return _lib.load()
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise PhsError(code, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, dims=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dims, got {t.dim()}")
+    return t
+
+
+def _opt(t, dtype, name, dims=None):
+    return None if t is None else _need(t, dtype, name, dims)
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _out_code(dtype):
+    if dtype == torch.bfloat16:
+        return OUT_BF16
+    if dtype == torch.float32:
+        return OUT_F32
+    raise ValueError("out dtype must be bfloat16 or float32")
+
+
+@dataclass
+class PagedPool:
+    """Full-attention pool: k, v bf16 [num_pages, Hkv, 16, D]."""
+    k: torch.Tensor
+    v: torch.Tensor
+
+    def c(self):
+        _need(self.k, torch.bfloat16, "pool.k", 4)
+        _need(self.v, torch.bfloat16, "pool.v", 4)
+        if self.k.shape != self.v.shape:
+            raise ValueError("pool.k and pool.v shapes differ")
+        n, h, p, d = self.k.shape
+        return _lib.PagedPoolC(self.k.data_ptr(), self.v.data_ptr(), n, p, h, d)
+
+    @staticmethod
+    def empty(num_pages, num_kv_heads, head_dim, device="cuda"):
+        shape = (num_pages, num_kv_heads, PAGE, head_dim)
+        return PagedPool(torch.empty(shape, dtype=torch.bfloat16, device=device),
+                         torch.empty(shape, dtype=torch.bfloat16, device=device))
+
+
+@dataclass
+class RingPool:
+    """SWA ring pool: k, v bf16 [num_rings, Hkv, W, D]."""
+    k: torch.Tensor
+    v: torch.Tensor
+
+    def c(self):
+        _need(self.k, torch.bfloat16, "ring.k", 4)
+        _need(self.v, torch.bfloat16, "ring.v", 4)
+        if self.k.shape != self.v.shape:
+            raise ValueError("ring.k and ring.v shapes differ")
+        n, h, w, d = self.k.shape
+        return _lib.RingPoolC(self.k.data_ptr(), self.v.data_ptr(), n, w, h, d)
+
+    @staticmethod
+    def empty(num_rings, num_kv_heads, window, head_dim, device="cuda"):
+        shape = (num_rings, num_kv_heads, window, head_dim)
+        return RingPool(torch.empty(shape, dtype=torch.bfloat16, device=device),
+                        torch.empty(shape, dtype=torch.bfloat16, device=device))
+
+
+@dataclass
+class Int8Pool:
+    """INT8 pool: codes int8 [num_qpages, Hkv, 32, D], scales fp32 [num_qpages, Hkv]."""
+    k: torch.Tensor
+    v: torch.Tensor
+    k_scale: torch.Tensor
+    v_scale: torch.Tensor
+
+    def c(self):
+        _need(self.k, torch.int8, "int8.k", 4)
+        _need(self.v, torch.int8, "int8.v", 4)
+        _need(self.k_scale, torch.float32, "int8.k_scale", 2)
+        _need(self.v_scale, torch.float32, "int8.v_scale", 2)
+        n, h, q, d = self.k.shape
+        if q != QBLOCK or self.v.shape != self.k.shape or tuple(self.k_scale.shape) != (n, h) \
+                or tuple(self.v_scale.shape) != (n, h):
+            raise ValueError("inconsistent INT8 pool shapes")
+        return _lib.Int8PoolC(self.k.data_ptr(), self.v.data_ptr(), self.k_scale.data_ptr(),
+                              self.v_scale.data_ptr(), n, h, d)
+
+    @staticmethod
+    def empty(num_qpages, num_kv_heads, head_dim, device="cuda"):
+        shape = (num_qpages, num_kv_heads, QBLOCK, head_dim)
+        return Int8Pool(torch.empty(shape, dtype=torch.int8, device=device),
+                        torch.empty(shape, dtype=torch.int8, device=device),
+                        torch.empty((num_qpages, num_kv_heads), dtype=torch.float32, device=device),
+                        torch.empty((num_qpages, num_kv_heads), dtype=torch.float32, device=device))
+
+
+# ------------------------------------------------------------------ append --
+def kv_append_paged(pool: PagedPool, k_new, v_new, block_table, seq_lens, page_refcount=None,
+                    status=None, stream=None):
+    """Write token seq_lens[b]-1 of every request into its page slot."""
+    pc = pool.c()
+    _need(k_new, torch.bfloat16, "k_new", 3)
+    _need(v_new, torch.bfloat16, "v_new", 3)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _opt(page_refcount, torch.int32, "page_refcount", 1)
+    _opt(status, torch.int32, "status")
+    _check(lib().phs_kv_append_paged(ctypes.byref(pc), _ptr(k_new), _ptr(v_new), _ptr(block_table),
+                                     block_table.shape[1], _ptr(seq_lens), seq_lens.shape[0],
+                                     _ptr(page_refcount), _ptr(status), _stream(stream)),
+           "kv_append_paged")
+
+
+def kv_append_ring(ring: RingPool, k_new, v_new, ring_pos, ring_ids=None, status=None,
+                   stream=None):
+    """Write the new token of every request into ring slot ring_pos[b]."""
+    rc = ring.c()
+    _need(k_new, torch.bfloat16, "k_new", 3)
+    _need(v_new, torch.bfloat16, "v_new", 3)
+    _need(ring_pos, torch.int32, "ring_pos", 1)
+    _opt(ring_ids, torch.int32, "ring_ids", 1)
+    _opt(status, torch.int32, "status")
+    _check(lib().phs_kv_append_ring(ctypes.byref(rc), _ptr(k_new), _ptr(v_new), _ptr(ring_ids),
+                                    _ptr(ring_pos), ring_pos.shape[0], _ptr(status),
+                                    _stream(stream)), "kv_append_ring")
+
+
+def kv_quant_int8_block32(src: PagedPool, src_block_table, dst: Int8Pool, dst_qtable,
+                          first_qblock, num_qblocks, max_qblocks: int, status=None, stream=None):
+    """Quantise 32-token blocks of the bf16 pages into INT8 codes + fp32 scales."""
+    sc, dc = src.c(), dst.c()
+    _need(src_block_table, torch.int32, "src_block_table", 2)
+    _need(dst_qtable, torch.int32, "dst_qtable", 2)
+    _need(first_qblock, torch.int32, "first_qblock", 1)
+    _need(num_qblocks, torch.int32, "num_qblocks", 1)
+    _opt(status, torch.int32, "status")
+    _check(lib().phs_kv_quant_int8_block32(
+        ctypes.byref(sc), _ptr(src_block_table), src_block_table.shape[1], ctypes.byref(dc),
+        _ptr(dst_qtable), dst_qtable.shape[1], _ptr(first_qblock), _ptr(num_qblocks),
+        int(max_qblocks), first_qblock.shape[0], _ptr(status), _stream(stream)),
+        "kv_quant_int8_block32")
+
+
+# ------------------------------------------------------------------ decode --
+def decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                           tokens_per_split=0, has_int8=False) -> int:
+    n = lib().phs_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                                         tokens_per_split, int(bool(has_int8)))
+    if n == 0:
+        raise ValueError("unsupported decode shape")
+    return int(n)
+
+
+def decode_tokens_per_split(batch, num_kv_heads, max_seq_len, tokens_per_split=0) -> int:
+    t = lib().phs_decode_tokens_per_split(batch, num_kv_heads, max_seq_len, tokens_per_split)
+    _check(min(int(t), 0), "decode_tokens_per_split")
+    return int(t)
+
+
+def _decode_args(q, pool, block_table, seq_lens, int8, qtable, qlens, out, out_dtype, status):
+    _need(q, torch.bfloat16, "q", 3)
+    pc = pool.c()
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    ic = None
+    if int8 is not None:
+        ic = int8.c()
+        _need(qtable, torch.int32, "qtable", 2)
+        _need(qlens, torch.int32, "qlens", 1)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    _need(out, out.dtype, "out", 3)
+    _opt(status, torch.int32, "status")
+    return pc, ic, out
+
+
+def _workspace(workspace, nbytes, device):
+    if workspace is None:
+        return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    _need(workspace, torch.uint8, "workspace", 1)
+    return workspace
+
+
+def attn_decode_full_paged(q, pool: PagedPool, block_table, seq_lens, max_seq_len: int,
+                           softmax_scale=None, int8: Int8Pool | None = None, qtable=None,
+                           qlens=None, tokens_per_split=0, out=None, out_dtype=torch.bfloat16,
+                           workspace=None, status=None, stream=None):
+    """Split-KV decode over the paged pool (optionally INT8 below qlens[b]);
+    returns out [B, Hq, D]."""
+    pc, ic, out = _decode_args(q, pool, block_table, seq_lens, int8, qtable, qlens, out,
+                               out_dtype, status)
+    B, Hq, D = q.shape
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    need = decode_workspace_bytes(B, Hq, pool.k.shape[1], D, max_seq_len, tokens_per_split,
+                                  int8 is not None)
+    ws = _workspace(workspace, need, q.device)
+    _check(lib().phs_attn_decode_full_paged(
+        _ptr(q), Hq, ctypes.byref(pc), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        int(max_seq_len), None if ic is None else ctypes.byref(ic), _ptr(qtable),
+        0 if qtable is None else qtable.shape[1], _ptr(qlens), B, scale, int(tokens_per_split),
+        _ptr(out), _out_code(out.dtype), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
+        "attn_decode_full_paged")
+    return out
+
+
+def attn_decode_full_paged_split(q, pool: PagedPool, block_table, seq_lens, max_seq_len: int,
+                                 workspace, out, softmax_scale=None, int8=None, qtable=None,
+                                 qlens=None, tokens_per_split=0, status=None, stream=None):
+    """Split phase only (see attn_merge_splits)."""
+    pc, ic, out = _decode_args(q, pool, block_table, seq_lens, int8, qtable, qlens, out,
+                               out.dtype, status)
+    B, Hq, D = q.shape
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    _need(workspace, torch.uint8, "workspace", 1)
+    _check(lib().phs_attn_decode_full_paged_split(
+        _ptr(q), Hq, ctypes.byref(pc), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        int(max_seq_len), None if ic is None else ctypes.byref(ic), _ptr(qtable),
+        0 if qtable is None else qtable.shape[1], _ptr(qlens), B, scale, int(tokens_per_split),
+        _ptr(out), _out_code(out.dtype), _ptr(workspace), workspace.numel(), _ptr(status),
+        _stream(stream)), "attn_decode_full_paged_split")
+    return out
+
+
+def attn_merge_splits(out, num_kv_heads, seq_lens, max_seq_len: int, workspace, qlens=None,
+                      has_int8=False, tokens_per_split=0, stream=None):
+    """Merge phase only: finishes requests that the split phase cut in pieces."""
+    B, Hq, D = out.shape
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _opt(qlens, torch.int32, "qlens", 1)
+    _need(workspace, torch.uint8, "workspace", 1)
+    _check(lib().phs_attn_merge_splits(B, Hq, num_kv_heads, D, _ptr(seq_lens), int(max_seq_len),
+                                       _ptr(qlens), int(bool(has_int8)), int(tokens_per_split),
+                                       _ptr(out), _out_code(out.dtype), _ptr(workspace),
+                                       workspace.numel(), _stream(stream)), "attn_merge_splits")
+    return out
+
+
+def attn_decode_swa_ring(q, ring: RingPool, ring_pos, seq_lens, ring_ids=None,
+                         softmax_scale=None, out=None, out_dtype=torch.bfloat16, status=None,
+                         stream=None):
+    """Sliding-window decode over each request's ring; returns out [B, Hq, D]."""
+    _need(q, torch.bfloat16, "q", 3)
+    rc = ring.c()
+    _need(ring_pos, torch.int32, "ring_pos", 1)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _opt(ring_ids, torch.int32, "ring_ids", 1)
+    _opt(status, torch.int32, "status")
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    _need(out, out.dtype, "out", 3)
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    _check(lib().phs_attn_decode_swa_ring(_ptr(q), Hq, ctypes.byref(rc), _ptr(ring_ids),
+                                          _ptr(ring_pos), _ptr(seq_lens), B, scale, _ptr(out),
+                                          _out_code(out.dtype), _ptr(status), _stream(stream)),
+           "attn_decode_swa_ring")
+    return out
+
+
+@dataclass
+class Layer:
+    """One layer of a hybrid stack: Full (paged pool) or SWA (ring pool)."""
+    q: torch.Tensor
+    out: torch.Tensor
+    paged: PagedPool | None = None
+    ring: RingPool | None = None
+    k_new: torch.Tensor | None = None
+    v_new: torch.Tensor | None = None
+
+    def c(self):
+        L = _lib.LayerC()
+        L.is_full = 1 if self.paged is not None else 0
+        L.q = self.q.data_ptr()
+        L.out = self.out.data_ptr()
+        L.k_new = 0 if self.k_new is None else self.k_new.data_ptr()
+        L.v_new = 0 if self.v_new is None else self.v_new.data_ptr()
+        if self.paged is not None:
+            L.paged = self.paged.c()
+        else:
+            L.ring = self.ring.c()
+        return L
+
+
+def hybrid_stack_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len):
+    return int(lib().phs_hybrid_stack_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                                      max_seq_len))
+
+
+def attn_decode_hybrid_stack(layers, num_q_heads, seq_lens, max_seq_len, block_table=None,
+                             ring_pos=None, ring_ids=None, softmax_scale=None, do_append=True,
+                             workspace=None, status=None, stream=None):
+    """One decode step (append + attend) over every layer of a hybrid stack."""
+    arr = (_lib.LayerC * len(layers))(*[L.c() for L in layers])
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _opt(block_table, torch.int32, "block_table", 2)
+    _opt(ring_pos, torch.int32, "ring_pos", 1)
+    _opt(ring_ids, torch.int32, "ring_ids", 1)
+    _opt(status, torch.int32, "status")
+    B = seq_lens.shape[0]
+    q0 = layers[0].q
+    D = q0.shape[2]
+    out_code = _out_code(layers[0].out.dtype)
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    nfull = sum(1 for L in layers if L.paged is not None)
+    if workspace is None and nfull:
+        hkv = next(L.paged.k.shape[1] for L in layers if L.paged is not None)
+        workspace = torch.empty(hybrid_stack_workspace_bytes(B, num_q_heads, hkv, D, max_seq_len),
+                                dtype=torch.uint8, device=q0.device)
+    _check(lib().phs_attn_decode_hybrid_stack(
+        arr, len(layers), num_q_heads, B, _ptr(block_table),
+        0 if block_table is None else block_table.shape[1], _ptr(seq_lens), int(max_seq_len),
+        _ptr(ring_ids), _ptr(ring_pos), scale, int(bool(do_append)), out_code, _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _ptr(status), _stream(stream)),
+        "attn_decode_hybrid_stack")
+
+
+def hybrid_kv_tokens(layer_is_full, seq_lens_host, window):
+    """(Full-layer tokens, SWA-layer tokens) held by a stack; host lists in."""
+    import numpy as np
+    lf = np.ascontiguousarray(layer_is_full, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
+    f, w = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().phs_hybrid_kv_tokens(lf.ctypes.data, lf.shape[0], sl.ctypes.data, sl.shape[0],
+                                      int(window), ctypes.byref(f), ctypes.byref(w)),
+           "hybrid_kv_tokens")
+    return f.value, w.value
+
+
+def copy_d2d(dst, src, stream=None):
+    """HBM copy kernel: dst <- src (same byte size, 16-byte multiples)."""
+    if dst.numel() * dst.element_size() != src.numel() * src.element_size():
+        raise ValueError("copy_d2d size mismatch")
+    _check(lib().phs_copy_d2d(_ptr(dst), _ptr(src), src.numel() * src.element_size(),
+                              _stream(stream)), "copy_d2d")

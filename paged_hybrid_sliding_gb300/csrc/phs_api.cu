@@ -1,0 +1,679 @@
+// phs_api.cu -- the extern "C" entry points declared in include/phs.h:
+// argument validation, TMA tensor-map encoding, split planning, and the
+// hybrid layer-stack driver.  All compute happens in the kernels of
+// phs_decode.cu, phs_swa.cu, phs_append.cu and phs_quant.cu.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "phs_internal.h"
+
+namespace phs {
+
+int swa_smem_bytes(int D, int G, int batch);
+
+namespace {
+
+constexpr int kMaxSplitTokens = 4096;
+constexpr int kMaxWindow = 4096;
+
+// ---------------------------------------------------------- device info --
+struct DevInfo {
+  int device = -1;
+  int sms = 0;
+  int smem_optin = 0;
+};
+
+int dev_info(DevInfo& out) {
+  thread_local DevInfo cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PHS_ECUDA;
+  if (cache.device != dev) {
+    DevInfo d;
+    d.device = dev;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PHS_ECUDA;
+    if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+      return PHS_ECUDA;
+    cache = d;
+  }
+  out = cache;
+  return PHS_OK;
+}
+
+// ---------------------------------------------------------- tensor maps --
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 pool viewed as a 2-D tensor of `rows` rows of D elements; boxes of
+// 16 rows x 64 columns (128 bytes) with the 128-byte swizzle.
+int map_bf16_rows(CUtensorMap* m, const void* base, int64_t rows, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PHS_ECUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PHS_OK : PHS_ECUDA;
+}
+
+// int8 codes, rows of D bytes; boxes of 32 rows x D with the 128-byte
+// (D = 128) or 64-byte (D = 64) swizzle.
+int map_i8_rows(CUtensorMap* m, const void* base, int64_t rows, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PHS_ECUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(D), 32};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                   es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PHS_OK : PHS_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(int Hq, int Hkv, int D) {
+  if (Hq <= 0 || Hkv <= 0) return PHS_EINVAL;
+  if (Hq % Hkv != 0) return PHS_ESHAPE;
+  if (Hq / Hkv > 16) return PHS_EUNSUPPORTED;
+  if (D != 64 && D != 128) return PHS_EUNSUPPORTED;
+  return PHS_OK;
+}
+
+int check_paged(const phs_paged_pool* pool) {
+  if (!pool || !pool->k || !pool->v) return PHS_EINVAL;
+  if (pool->num_pages <= 0 || pool->num_kv_heads <= 0) return PHS_EINVAL;
+  if (pool->page_size != kPage) return PHS_EUNSUPPORTED;
+  if (pool->head_dim != 64 && pool->head_dim != 128) return PHS_EUNSUPPORTED;
+  if (pool->num_pages * pool->num_kv_heads * kPage > INT32_MAX) return PHS_EUNSUPPORTED;
+  if (!aligned16(pool->k) || !aligned16(pool->v)) return PHS_EALIGN;
+  return PHS_OK;
+}
+
+int check_ring(const phs_ring_pool* ring) {
+  if (!ring || !ring->k || !ring->v) return PHS_EINVAL;
+  if (ring->num_rings <= 0 || ring->num_kv_heads <= 0 || ring->window <= 0) return PHS_EINVAL;
+  if (ring->window % kPage != 0 || ring->window > kMaxWindow) return PHS_EUNSUPPORTED;
+  if (ring->head_dim != 64 && ring->head_dim != 128) return PHS_EUNSUPPORTED;
+  if (ring->num_rings * ring->num_kv_heads * ring->window > INT32_MAX) return PHS_EUNSUPPORTED;
+  if (!aligned16(ring->k) || !aligned16(ring->v)) return PHS_EALIGN;
+  return PHS_OK;
+}
+
+int check_int8(const phs_int8_pool* p) {
+  if (!p || !p->k || !p->v || !p->k_scale || !p->v_scale) return PHS_EINVAL;
+  if (p->num_qpages <= 0 || p->num_kv_heads <= 0) return PHS_EINVAL;
+  if (p->head_dim != 64 && p->head_dim != 128) return PHS_EUNSUPPORTED;
+  if (p->num_qpages * p->num_kv_heads * kQBlock > INT32_MAX) return PHS_EUNSUPPORTED;
+  if (!aligned16(p->k) || !aligned16(p->v)) return PHS_EALIGN;
+  return PHS_OK;
+}
+
+int32_t plan_tokens_per_split(int B, int Hkv, int max_seq, int requested, int sms) {
+  if (requested > 0) return requested;
+  // Long splits keep the partial-result traffic small (about 0.4% of the KV
+  // bytes at 1024 tokens); shorter ones are used only when the grid would
+  // otherwise fill fewer than ~4 waves of 2 CTAs per SM.
+  int t = 1024;
+  const long long target = 8LL * std::max(sms, 1);
+  while (t > 128) {
+    const long long ctas = static_cast<long long>(B) * Hkv * ((max_seq + t - 1) / t);
+    if (ctas >= target) break;
+    t /= 2;
+  }
+  return t;
+}
+
+int max_splits_for(int max_seq, int T, bool has_int8) {
+  return std::max(1, (max_seq + T - 1) / T + (has_int8 ? 1 : 0));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t ws_o_bytes(int B, int Hkv, int ms, int G, int D) {
+  return align256(static_cast<size_t>(B) * Hkv * ms * G * D * sizeof(float));
+}
+
+size_t ws_bytes(int B, int Hkv, int ms, int G, int D) {
+  return ws_o_bytes(B, Hkv, ms, G, D) +
+         align256(static_cast<size_t>(B) * Hkv * ms * G * 2 * sizeof(float));
+}
+
+struct DecodePlan {
+  int T = 0, max_splits = 0, G = 0, D = 0, Hkv = 0;
+  bool has_int8 = false;
+  size_t need = 0;
+};
+
+int make_plan(DecodePlan& pl, int B, int Hq, int Hkv, int D, int max_seq, int tps,
+              bool has_int8) {
+  int st = check_dims(Hq, Hkv, D);
+  if (st) return st;
+  if (B <= 0 || max_seq < 0) return PHS_EINVAL;
+  if (tps < 0 || (tps > 0 && (tps % kQBlock != 0 || tps > kMaxSplitTokens)))
+    return PHS_EUNSUPPORTED;
+  DevInfo di;
+  if ((st = dev_info(di))) return st;
+  pl.T = plan_tokens_per_split(B, Hkv, max_seq, tps, di.sms);
+  pl.max_splits = max_splits_for(max_seq, pl.T, has_int8);
+  pl.G = Hq / Hkv;
+  pl.D = D;
+  pl.Hkv = Hkv;
+  pl.has_int8 = has_int8;
+  pl.need = ws_bytes(B, Hkv, pl.max_splits, pl.G, D);
+  return PHS_OK;
+}
+
+// Shared preamble of the decode entry points.
+struct DecodeCall {
+  DecodePlan pl;
+  SplitArgs a;
+  MergeArgs m;
+  CUtensorMap tk, tv, tk8, tv8;
+};
+
+int prepare_decode(DecodeCall& c, const void* q, int Hq, const phs_paged_pool* pool,
+                   const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                   int max_seq, const phs_int8_pool* int8, const int32_t* qtable, int max_qpages,
+                   const int32_t* qlens, int B, float softmax_scale, int tps, void* out,
+                   int out_dtype, void* workspace, size_t ws_size, int32_t* dev_status) {
+  int st = check_paged(pool);
+  if (st) return st;
+  if (!q || !block_table || !seq_lens || !out) return PHS_EINVAL;
+  if (max_pages <= 0 || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return PHS_EINVAL;
+  if (out_dtype != PHS_OUT_BF16 && out_dtype != PHS_OUT_F32) return PHS_EINVAL;
+  const int D = pool->head_dim, Hkv = pool->num_kv_heads;
+  if (int8) {
+    if ((st = check_int8(int8))) return st;
+    if (!qtable || !qlens || max_qpages <= 0) return PHS_EINVAL;
+    if (int8->head_dim != D || int8->num_kv_heads != Hkv) return PHS_ESHAPE;
+  }
+  if ((st = make_plan(c.pl, B, Hq, Hkv, D, max_seq, tps, int8 != nullptr))) return st;
+  if (!workspace || ws_size < c.pl.need) return PHS_EWORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PHS_EALIGN;
+  if (!aligned16(q)) return PHS_EALIGN;
+
+  std::memset(&c.a, 0, sizeof(c.a));
+  c.a.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  c.a.block_table = block_table;
+  c.a.seq_lens = seq_lens;
+  c.a.qtable = int8 ? qtable : nullptr;
+  c.a.qlens = int8 ? qlens : nullptr;
+  c.a.k_scale = int8 ? int8->k_scale : nullptr;
+  c.a.v_scale = int8 ? int8->v_scale : nullptr;
+  c.a.out = out;
+  c.a.ws_o = reinterpret_cast<float*>(workspace);
+  c.a.ws_ml = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) +
+                                       ws_o_bytes(B, Hkv, c.pl.max_splits, c.pl.G, D));
+  c.a.status = dev_status;
+  c.a.num_pages = pool->num_pages;
+  c.a.num_qpages = int8 ? int8->num_qpages : 0;
+  c.a.Hq = Hq;
+  c.a.Hkv = Hkv;
+  c.a.G = c.pl.G;
+  c.a.max_pages = max_pages;
+  c.a.max_qpages = int8 ? max_qpages : 0;
+  c.a.n_clamp = static_cast<int>(std::min<long long>(max_seq, 1LL * max_pages * kPage));
+  c.a.T = c.pl.T;
+  c.a.max_splits = c.pl.max_splits;
+  c.a.out_f32 = out_dtype == PHS_OUT_F32;
+  c.a.scale_log2 = softmax_scale * 1.4426950408889634f;
+
+  std::memset(&c.m, 0, sizeof(c.m));
+  c.m.seq_lens = seq_lens;
+  c.m.qlens = c.a.qlens;
+  c.m.ws_o = c.a.ws_o;
+  c.m.ws_ml = c.a.ws_ml;
+  c.m.out = out;
+  c.m.Hq = Hq;
+  c.m.Hkv = Hkv;
+  c.m.G = c.pl.G;
+  c.m.n_clamp = c.a.n_clamp;
+  c.m.T = c.pl.T;
+  c.m.max_splits = c.pl.max_splits;
+  c.m.out_f32 = c.a.out_f32;
+
+  const int64_t rows = pool->num_pages * Hkv * kPage;
+  if ((st = map_bf16_rows(&c.tk, pool->k, rows, D))) return st;
+  if ((st = map_bf16_rows(&c.tv, pool->v, rows, D))) return st;
+  if (int8) {
+    const int64_t qrows = int8->num_qpages * Hkv * kQBlock;
+    if ((st = map_i8_rows(&c.tk8, int8->k, qrows, D))) return st;
+    if ((st = map_i8_rows(&c.tv8, int8->v, qrows, D))) return st;
+  } else {
+    c.tk8 = c.tk;  // unused by bf16-only launches
+    c.tv8 = c.tv;
+  }
+  return PHS_OK;
+}
+
+}  // namespace
+}  // namespace phs
+
+using namespace phs;
+
+extern "C" {
+
+int32_t phs_version(void) { return 1; }
+
+const char* phs_status_str(int s) {
+  switch (s) {
+    case PHS_OK: return "ok";
+    case PHS_EINVAL: return "invalid argument";
+    case PHS_ESHAPE: return "inconsistent shapes";
+    case PHS_ERANGE: return "index out of range";
+    case PHS_ESHARED: return "append into a shared page";
+    case PHS_EWORKSPACE: return "workspace missing or too small";
+    case PHS_ECUDA: return "CUDA call failed";
+    case PHS_EUNSUPPORTED: return "unsupported shape";
+    case PHS_ETIMEOUT: return "device wait timed out";
+    case PHS_EALIGN: return "pointer not aligned";
+    default: return "unknown status";
+  }
+}
+
+int phs_kv_append_paged(const phs_paged_pool* pool, const void* k_new, const void* v_new,
+                        const int32_t* block_table, int32_t max_pages_per_seq,
+                        const int32_t* seq_lens, int32_t batch, const int32_t* page_refcount,
+                        int32_t* dev_status, void* stream) {
+  int st = check_paged(pool);
+  if (st) return st;
+  if (!k_new || !v_new || !block_table || !seq_lens || batch < 0 || max_pages_per_seq <= 0)
+    return PHS_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PHS_EALIGN;
+  if (batch == 0) return PHS_OK;
+  AppendParams<1> p;
+  std::memset(&p, 0, sizeof(p));
+  p.layer[0] = AppendLayer{pool->k, pool->v, k_new, v_new, pool->num_pages};
+  p.table = block_table;
+  p.seq_lens = seq_lens;
+  p.refcount = page_refcount;
+  p.status = dev_status;
+  p.num_layers = 1;
+  p.B = batch;
+  p.Hkv = pool->num_kv_heads;
+  p.D = pool->head_dim;
+  p.max_pages = max_pages_per_seq;
+  p.is_ring = 0;
+  return launch_append<1>(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int phs_kv_append_ring(const phs_ring_pool* ring, const void* k_new, const void* v_new,
+                       const int32_t* ring_ids, const int32_t* ring_pos, int32_t batch,
+                       int32_t* dev_status, void* stream) {
+  int st = check_ring(ring);
+  if (st) return st;
+  if (!k_new || !v_new || !ring_pos || batch < 0) return PHS_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PHS_EALIGN;
+  if (batch == 0) return PHS_OK;
+  AppendParams<1> p;
+  std::memset(&p, 0, sizeof(p));
+  p.layer[0] = AppendLayer{ring->k, ring->v, k_new, v_new, ring->num_rings};
+  p.table = ring_ids;
+  p.ring_pos = ring_pos;
+  p.status = dev_status;
+  p.num_layers = 1;
+  p.B = batch;
+  p.Hkv = ring->num_kv_heads;
+  p.D = ring->head_dim;
+  p.W = ring->window;
+  p.is_ring = 1;
+  return launch_append<1>(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int phs_kv_quant_int8_block32(const phs_paged_pool* src, const int32_t* src_block_table,
+                              int32_t src_max_pages, const phs_int8_pool* dst,
+                              const int32_t* dst_qtable, int32_t dst_max_qpages,
+                              const int32_t* first_qblock, const int32_t* num_qblocks,
+                              int32_t max_qblocks, int32_t batch, int32_t* dev_status,
+                              void* stream) {
+  int st = check_paged(src);
+  if (st) return st;
+  if ((st = check_int8(dst))) return st;
+  if (!src_block_table || !dst_qtable || !first_qblock || !num_qblocks) return PHS_EINVAL;
+  if (src_max_pages <= 0 || dst_max_qpages <= 0 || batch < 0 || max_qblocks < 0)
+    return PHS_EINVAL;
+  if (dst->head_dim != src->head_dim || dst->num_kv_heads != src->num_kv_heads) return PHS_ESHAPE;
+  if (batch == 0 || max_qblocks == 0) return PHS_OK;
+  QuantArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.k_src = reinterpret_cast<const __nv_bfloat16*>(src->k);
+  a.v_src = reinterpret_cast<const __nv_bfloat16*>(src->v);
+  a.src_table = src_block_table;
+  a.k_codes = dst->k;
+  a.v_codes = dst->v;
+  a.k_scale = dst->k_scale;
+  a.v_scale = dst->v_scale;
+  a.dst_qtable = dst_qtable;
+  a.first_qblock = first_qblock;
+  a.num_qblocks = num_qblocks;
+  a.status = dev_status;
+  a.num_pages = src->num_pages;
+  a.num_qpages = dst->num_qpages;
+  a.src_max_pages = src_max_pages;
+  a.dst_max_qpages = dst_max_qpages;
+  a.Hkv = src->num_kv_heads;
+  a.D = src->head_dim;
+  return launch_quant(a, max_qblocks, batch, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int32_t phs_decode_tokens_per_split(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len,
+                                    int32_t tokens_per_split) {
+  DevInfo di;
+  if (dev_info(di)) return PHS_ECUDA;
+  if (tokens_per_split < 0 || (tokens_per_split > 0 && (tokens_per_split % kQBlock != 0 ||
+                                                        tokens_per_split > kMaxSplitTokens)))
+    return PHS_EUNSUPPORTED;
+  return plan_tokens_per_split(batch, num_kv_heads, max_seq_len, tokens_per_split, di.sms);
+}
+
+size_t phs_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_seq_len,
+                                  int32_t tokens_per_split, int32_t has_int8) {
+  DecodePlan pl;
+  if (make_plan(pl, batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, tokens_per_split,
+                has_int8 != 0))
+    return 0;
+  return pl.need;
+}
+
+int phs_attn_decode_full_paged_split(const void* q, int32_t num_q_heads,
+                                     const phs_paged_pool* pool, const int32_t* block_table,
+                                     int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                     int32_t max_seq_len, const phs_int8_pool* int8,
+                                     const int32_t* qtable, int32_t max_qpages_per_seq,
+                                     const int32_t* qlens, int32_t batch, float softmax_scale,
+                                     int32_t tokens_per_split, void* out, int32_t out_dtype,
+                                     void* workspace, size_t workspace_bytes,
+                                     int32_t* dev_status, void* stream) {
+  DecodeCall c;
+  int st = prepare_decode(c, q, num_q_heads, pool, block_table, max_pages_per_seq, seq_lens,
+                          max_seq_len, int8, qtable, max_qpages_per_seq, qlens, batch,
+                          softmax_scale, tokens_per_split, out, out_dtype, workspace,
+                          workspace_bytes, dev_status);
+  if (st) return st;
+  return launch_split_decode(c.pl.D, c.tk, c.tv, c.tk8, c.tv8, c.a, batch,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+int phs_attn_merge_splits(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, const int32_t* seq_lens, int32_t max_seq_len,
+                          const int32_t* qlens, int32_t has_int8, int32_t tokens_per_split,
+                          void* out, int32_t out_dtype, const void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  DecodePlan pl;
+  int st = make_plan(pl, batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                     tokens_per_split, has_int8 != 0);
+  if (st) return st;
+  if (!seq_lens || !out) return PHS_EINVAL;
+  if (has_int8 && !qlens) return PHS_EINVAL;
+  if (out_dtype != PHS_OUT_BF16 && out_dtype != PHS_OUT_F32) return PHS_EINVAL;
+  if (!workspace || workspace_bytes < pl.need) return PHS_EWORKSPACE;
+  MergeArgs m;
+  std::memset(&m, 0, sizeof(m));
+  m.seq_lens = seq_lens;
+  m.qlens = has_int8 ? qlens : nullptr;
+  m.ws_o = reinterpret_cast<const float*>(workspace);
+  m.ws_ml = reinterpret_cast<const float*>(reinterpret_cast<const char*>(workspace) +
+                                           ws_o_bytes(batch, num_kv_heads, pl.max_splits, pl.G,
+                                                      head_dim));
+  m.out = out;
+  m.Hq = num_q_heads;
+  m.Hkv = num_kv_heads;
+  m.G = pl.G;
+  m.n_clamp = max_seq_len;
+  m.T = pl.T;
+  m.max_splits = pl.max_splits;
+  m.out_f32 = out_dtype == PHS_OUT_F32;
+  return launch_merge(head_dim, m, batch, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int phs_attn_decode_full_paged(const void* q, int32_t num_q_heads, const phs_paged_pool* pool,
+                               const int32_t* block_table, int32_t max_pages_per_seq,
+                               const int32_t* seq_lens, int32_t max_seq_len,
+                               const phs_int8_pool* int8, const int32_t* qtable,
+                               int32_t max_qpages_per_seq, const int32_t* qlens, int32_t batch,
+                               float softmax_scale, int32_t tokens_per_split, void* out,
+                               int32_t out_dtype, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream) {
+  DecodeCall c;
+  int st = prepare_decode(c, q, num_q_heads, pool, block_table, max_pages_per_seq, seq_lens,
+                          max_seq_len, int8, qtable, max_qpages_per_seq, qlens, batch,
+                          softmax_scale, tokens_per_split, out, out_dtype, workspace,
+                          workspace_bytes, dev_status);
+  if (st) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_split_decode(c.pl.D, c.tk, c.tv, c.tk8, c.tv8, c.a, batch, s))) return st;
+  return launch_merge(c.pl.D, c.m, batch, s);
+}
+
+int phs_attn_decode_swa_ring(const void* q, int32_t num_q_heads, const phs_ring_pool* ring,
+                             const int32_t* ring_ids, const int32_t* ring_pos,
+                             const int32_t* seq_lens, int32_t batch, float softmax_scale,
+                             void* out, int32_t out_dtype, int32_t* dev_status, void* stream) {
+  int st = check_ring(ring);
+  if (st) return st;
+  if (!q || !ring_pos || !seq_lens || !out || batch < 0) return PHS_EINVAL;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return PHS_EINVAL;
+  if (out_dtype != PHS_OUT_BF16 && out_dtype != PHS_OUT_F32) return PHS_EINVAL;
+  const int D = ring->head_dim, Hkv = ring->num_kv_heads;
+  if ((st = check_dims(num_q_heads, Hkv, D))) return st;
+  if (!aligned16(q)) return PHS_EALIGN;
+  if (batch == 0) return PHS_OK;
+  DevInfo di;
+  if ((st = dev_info(di))) return st;
+  if (swa_smem_bytes(D, num_q_heads / Hkv, batch) > di.smem_optin) return PHS_EUNSUPPORTED;
+  SwaParams<1> p;
+  std::memset(&p, 0, sizeof(p));
+  if ((st = map_bf16_rows(&p.tk[0], ring->k, ring->num_rings * Hkv * ring->window, D))) return st;
+  if ((st = map_bf16_rows(&p.tv[0], ring->v, ring->num_rings * Hkv * ring->window, D))) return st;
+  p.q[0] = reinterpret_cast<const __nv_bfloat16*>(q);
+  p.out[0] = out;
+  p.num_rings[0] = ring->num_rings;
+  p.ring_ids = ring_ids;
+  p.ring_pos = ring_pos;
+  p.seq_lens = seq_lens;
+  p.status = dev_status;
+  p.num_layers = 1;
+  p.B = batch;
+  p.Hq = num_q_heads;
+  p.Hkv = Hkv;
+  p.G = num_q_heads / Hkv;
+  p.W = ring->window;
+  p.out_f32 = out_dtype == PHS_OUT_F32;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  return launch_swa_decode<1>(D, p, di.sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t phs_hybrid_stack_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t max_seq_len) {
+  return phs_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, 0, 0);
+}
+
+int phs_attn_decode_hybrid_stack(const phs_layer* layers, int32_t num_layers,
+                                 int32_t num_q_heads, int32_t batch, const int32_t* block_table,
+                                 int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                 int32_t max_seq_len, const int32_t* ring_ids,
+                                 const int32_t* ring_pos, float softmax_scale, int32_t do_append,
+                                 int32_t out_dtype, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_status, void* stream) {
+  if (!layers || num_layers <= 0 || batch < 0 || !seq_lens) return PHS_EINVAL;
+  if (out_dtype != PHS_OUT_BF16 && out_dtype != PHS_OUT_F32) return PHS_EINVAL;
+  if (batch == 0) return PHS_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int st;
+  // ---- validate every layer before launching anything
+  int D = -1, Hkv = -1, W = -1;
+  int nfull = 0, nswa = 0;
+  for (int i = 0; i < num_layers; ++i) {
+    const phs_layer& L = layers[i];
+    if (!L.q || !L.out) return PHS_EINVAL;
+    if (do_append && (!L.k_new || !L.v_new)) return PHS_EINVAL;
+    int d, h;
+    if (L.is_full) {
+      if ((st = check_paged(&L.paged))) return st;
+      d = L.paged.head_dim;
+      h = L.paged.num_kv_heads;
+      ++nfull;
+    } else {
+      if ((st = check_ring(&L.ring))) return st;
+      d = L.ring.head_dim;
+      h = L.ring.num_kv_heads;
+      if (W < 0) W = L.ring.window;
+      if (L.ring.window != W) return PHS_ESHAPE;
+      ++nswa;
+    }
+    if (D < 0) {
+      D = d;
+      Hkv = h;
+    }
+    if (d != D || h != Hkv) return PHS_ESHAPE;
+    if (!aligned16(L.q) || (do_append && (!aligned16(L.k_new) || !aligned16(L.v_new))))
+      return PHS_EALIGN;
+  }
+  if ((st = check_dims(num_q_heads, Hkv, D))) return st;
+  if (nfull && (!block_table || max_pages_per_seq <= 0)) return PHS_EINVAL;
+  if (nswa && !ring_pos) return PHS_EINVAL;
+  DevInfo di;
+  if ((st = dev_info(di))) return st;
+  if (nswa && swa_smem_bytes(D, num_q_heads / Hkv, batch) > di.smem_optin) return PHS_EUNSUPPORTED;
+  if (nfull) {
+    DecodePlan pl;
+    if ((st = make_plan(pl, batch, num_q_heads, Hkv, D, max_seq_len, 0, false))) return st;
+    if (!workspace || workspace_bytes < pl.need) return PHS_EWORKSPACE;
+  }
+
+  // ---- appends: all Full layers in one launch, all SWA layers in one
+  if (do_append) {
+    for (int pass = 0; pass < 2; ++pass) {
+      const bool full = pass == 0;
+      AppendParams<kAppendMaxLayers> p;
+      std::memset(&p, 0, sizeof(p));
+      p.table = full ? block_table : ring_ids;
+      p.seq_lens = seq_lens;
+      p.ring_pos = ring_pos;
+      p.status = dev_status;
+      p.B = batch;
+      p.Hkv = Hkv;
+      p.D = D;
+      p.max_pages = max_pages_per_seq;
+      p.W = W;
+      p.is_ring = full ? 0 : 1;
+      for (int i = 0; i < num_layers; ++i) {
+        const phs_layer& L = layers[i];
+        if ((L.is_full != 0) != full) continue;
+        p.layer[p.num_layers++] =
+            full ? AppendLayer{L.paged.k, L.paged.v, L.k_new, L.v_new, L.paged.num_pages}
+                 : AppendLayer{L.ring.k, L.ring.v, L.k_new, L.v_new, L.ring.num_rings};
+        if (p.num_layers == kAppendMaxLayers) {
+          if ((st = launch_append<kAppendMaxLayers>(p, s))) return st;
+          p.num_layers = 0;
+        }
+      }
+      if (p.num_layers && (st = launch_append<kAppendMaxLayers>(p, s))) return st;
+    }
+  }
+
+  // ---- SWA layers: one launch (per 64 layers)
+  if (nswa) {
+    SwaParams<kSwaMaxLayers>* p = new SwaParams<kSwaMaxLayers>();
+    std::memset(p, 0, sizeof(*p));
+    p->ring_ids = ring_ids;
+    p->ring_pos = ring_pos;
+    p->seq_lens = seq_lens;
+    p->status = dev_status;
+    p->B = batch;
+    p->Hq = num_q_heads;
+    p->Hkv = Hkv;
+    p->G = num_q_heads / Hkv;
+    p->W = W;
+    p->out_f32 = out_dtype == PHS_OUT_F32;
+    p->scale_log2 = softmax_scale * 1.4426950408889634f;
+    st = PHS_OK;
+    for (int i = 0; i < num_layers && st == PHS_OK; ++i) {
+      const phs_layer& L = layers[i];
+      if (L.is_full) continue;
+      const int k = p->num_layers;
+      const int64_t rows = L.ring.num_rings * Hkv * W;
+      if ((st = map_bf16_rows(&p->tk[k], L.ring.k, rows, D))) break;
+      if ((st = map_bf16_rows(&p->tv[k], L.ring.v, rows, D))) break;
+      p->q[k] = reinterpret_cast<const __nv_bfloat16*>(L.q);
+      p->out[k] = L.out;
+      p->num_rings[k] = L.ring.num_rings;
+      if (++p->num_layers == kSwaMaxLayers) {
+        st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, s);
+        p->num_layers = 0;
+      }
+    }
+    if (st == PHS_OK && p->num_layers) st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, s);
+    delete p;
+    if (st) return st;
+  }
+
+  // ---- Full layers: split + merge per layer, reusing the workspace
+  for (int i = 0; i < num_layers; ++i) {
+    const phs_layer& L = layers[i];
+    if (!L.is_full) continue;
+    st = phs_attn_decode_full_paged(L.q, num_q_heads, &L.paged, block_table, max_pages_per_seq,
+                                    seq_lens, max_seq_len, nullptr, nullptr, 0, nullptr, batch,
+                                    softmax_scale, 0, L.out, out_dtype, workspace,
+                                    workspace_bytes, dev_status, stream);
+    if (st) return st;
+  }
+  return PHS_OK;
+}
+
+int phs_hybrid_kv_tokens(const int32_t* layer_is_full_host, int32_t num_layers,
+                         const int32_t* seq_lens_host, int32_t batch, int32_t window,
+                         int64_t* full_tokens, int64_t* swa_tokens) {
+  if (!layer_is_full_host || !seq_lens_host || !full_tokens || !swa_tokens) return PHS_EINVAL;
+  if (num_layers < 0 || batch < 0 || window <= 0) return PHS_EINVAL;
+  int64_t f = 0, w = 0;
+  for (int l = 0; l < num_layers; ++l)
+    for (int b = 0; b < batch; ++b) {
+      const int64_t n = seq_lens_host[b] > 0 ? seq_lens_host[b] : 0;
+      if (layer_is_full_host[l])
+        f += n;
+      else
+        w += std::min<int64_t>(n, window);
+    }
+  *full_tokens = f;
+  *swa_tokens = w;
+  return PHS_OK;
+}
+
+int phs_copy_d2d(void* dst, const void* src, size_t bytes, void* stream) {
+  if (!dst || !src) return PHS_EINVAL;
+  if (!aligned16(dst) || !aligned16(src) || (bytes & 15u)) return PHS_EALIGN;
+  DevInfo di;
+  int st = dev_info(di);
+  if (st) return st;
+  return launch_copy(dst, src, bytes, di.sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,100 @@
+// phs_append.cu -- KV append into the paged Full pool or the SWA rings (one
+// or many layers per launch), and the plain HBM copy kernel used as the
+// in-run bandwidth yardstick.
+//
+// Sources: "Kimi K3 context caching" page, section 1 (a request extending a
+// shared prefix writes only into blocks of its own; shared blocks are held
+// by reference count) and "Xiaomi MiMo-V2.5 inference system" page,
+// section 2 (Full pool grows on demand; SWA ring evicts by window).
+#include "phs_common.cuh"
+#include "phs_internal.h"
+
+namespace phs {
+
+// grid (B, layers); one thread per 16-byte piece of one head's K and V row.
+template <int MAXL>
+__global__ void phs_append_kernel(const __grid_constant__ AppendParams<MAXL> p) {
+  const int b = blockIdx.x, li = blockIdx.y;
+  const int per_head = p.D / 8;  // 16-byte pieces per row
+  const int t = threadIdx.x;
+  if (t >= p.Hkv * per_head) return;
+  const int h = t / per_head, piece = t % per_head;
+  const AppendLayer& L = p.layer[li];
+  int64_t row;  // destination row (token slot) in units of D elements
+  if (p.is_ring) {
+    const int r = p.table ? p.table[b] : b;
+    const int slot = p.ring_pos[b];
+    if (r < 0 || r >= L.num || slot < 0 || slot >= p.W) {
+      if (t == 0) set_status(p.status, PHS_ERANGE);
+      return;
+    }
+    row = (static_cast<int64_t>(r) * p.Hkv + h) * p.W + slot;
+  } else {
+    const int n = p.seq_lens[b];
+    if (n < 1) return;
+    const int tok = n - 1;
+    const int lp = tok / kPage;
+    if (lp >= p.max_pages) {
+      if (t == 0) set_status(p.status, PHS_ERANGE);
+      return;
+    }
+    const int page = p.table[static_cast<size_t>(b) * p.max_pages + lp];
+    if (page < 0 || page >= L.num) {
+      if (t == 0) set_status(p.status, PHS_ERANGE);
+      return;
+    }
+    if (p.refcount && p.refcount[page] != 1) {
+      if (t == 0) set_status(p.status, PHS_ESHARED);
+      return;
+    }
+    row = (static_cast<int64_t>(page) * p.Hkv + h) * kPage + tok % kPage;
+  }
+  const size_t src = (static_cast<size_t>(b) * p.Hkv + h) * p.D / 8 + piece;
+  const size_t dst = static_cast<size_t>(row) * p.D / 8 + piece;
+  reinterpret_cast<uint4*>(L.k)[dst] = reinterpret_cast<const uint4*>(L.k_new)[src];
+  reinterpret_cast<uint4*>(L.v)[dst] = reinterpret_cast<const uint4*>(L.v_new)[src];
+}
+
+template <int MAXL>
+int launch_append(const AppendParams<MAXL>& p, cudaStream_t stream) {
+  if (p.B <= 0 || p.num_layers <= 0) return PHS_OK;
+  const int threads = ((p.Hkv * p.D / 8) + 31) / 32 * 32;
+  dim3 grid(p.B, p.num_layers);
+  phs_append_kernel<MAXL><<<grid, threads, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+}
+
+template int launch_append<1>(const AppendParams<1>&, cudaStream_t);
+template int launch_append<kAppendMaxLayers>(const AppendParams<kAppendMaxLayers>&, cudaStream_t);
+
+// ------------------------------------------------------------------ copy --
+__global__ void __launch_bounds__(512) phs_copy_kernel(uint4* __restrict__ dst,
+                                                       const uint4* __restrict__ src, size_t n) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // four independent 16-byte loads in flight per thread
+  for (; i + 3 * stride < n; i += 4 * stride) {
+    const uint4 a = __ldcs(src + i);
+    const uint4 b = __ldcs(src + i + stride);
+    const uint4 c = __ldcs(src + i + 2 * stride);
+    const uint4 d = __ldcs(src + i + 3 * stride);
+    __stcs(dst + i, a);
+    __stcs(dst + i + stride, b);
+    __stcs(dst + i + 2 * stride, c);
+    __stcs(dst + i + 3 * stride, d);
+  }
+  for (; i < n; i += stride) __stcs(dst + i, __ldcs(src + i));
+}
+
+int launch_copy(void* dst, const void* src, size_t bytes, int num_sms, cudaStream_t stream) {
+  const size_t n = bytes / 16;
+  if (n == 0) return PHS_OK;
+  size_t blocks = static_cast<size_t>(num_sms) * 4;
+  const size_t need = (n + 511) / 512;
+  if (blocks > need) blocks = need;
+  phs_copy_kernel<<<static_cast<unsigned>(blocks), 512, 0, stream>>>(
+      reinterpret_cast<uint4*>(dst), reinterpret_cast<const uint4*>(src), n);
+  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+}
+
+}  // namespace phs

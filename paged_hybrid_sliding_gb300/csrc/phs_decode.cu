@@ -1,0 +1,348 @@
+// phs_decode.cu -- split-KV ("flash-decoding") Full-attention decode over
+// the paged pool, with an optional INT8 region, and the cross-split merge.
+//
+// Grid: one CTA per (split, KV head, request).  A split is a run of
+// tokens_per_split tokens of one request; the INT8 region [0, qlen) and the
+// bf16 region [qlen, n) are split separately so that every CTA handles one
+// chunk kind.  The CTA's 4 warps take the split's chunks round-robin; each
+// warp streams its chunks through its own ring of S shared-memory stages
+// filled by TMA (two 2-D tiled loads per 16-token bf16 page: K and V, each
+// D/64 boxes of 16 x 64 with the 128-byte swizzle; or one 32 x D box each
+// for a 32-token INT8 page), and reduces them with the GQA-packed mma
+// kernels of phs_attn.cuh.  The 4 warp states are merged through shared
+// memory; a request with a single split writes its output directly, others
+// write (m, l, o) partials that phs_merge_kernel combines.
+//
+// Sources: "Xiaomi MiMo-V2.5 inference system" page, sections 1-2 (Full
+// layers attend over the whole sequence through the authoritative Full
+// index; decode cost follows the KV bytes read); "Kimi K3 context caching"
+// page, section 1 (KV in non-contiguous physical blocks through a page
+// table); "Kimi K2.5 architecture deep dive" page, sections 2.2-2.3 (INT8
+// block-wise warm zone, one scale per 32 tokens).
+#include "phs_attn.cuh"
+#include "phs_internal.h"
+
+namespace phs {
+
+constexpr int kSplitWarps = 4;
+constexpr int kMaxChunksPerWarp = 64;  // tokens_per_split <= 4096
+
+template <int D>
+struct SplitLayout {
+  static constexpr int kStage = ChunkGeom<D>::kStageBytes;
+  static constexpr int kStages = (D == 128) ? 3 : 4;
+  static constexpr int kStagesBytes = kSplitWarps * kStages * kStage;
+  static constexpr int kIdsOff = kStagesBytes;
+  static constexpr int kIdsBytes = kSplitWarps * kMaxChunksPerWarp * 12;
+  static constexpr int kBarOff = kIdsOff + kIdsBytes;
+  static constexpr int kBytes = kBarOff + kSplitWarps * kStages * 8;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void store_out(void* out, size_t idx, float v, int f32) {
+  if (f32)
+    reinterpret_cast<float*>(out)[idx] = v;
+  else
+    reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+}
+
+// Number of splits of a request and validation of its INT8 length.
+// Returns -1 if the request's lengths are invalid.
+__device__ __forceinline__ int request_splits(int n, int qlen, int T) {
+  if (n < 0 || qlen < 0 || qlen > n || (qlen % kQBlock) != 0) return -1;
+  return (qlen + T - 1) / T + (n - qlen + T - 1) / T;
+}
+
+template <int D, bool TWO>
+__global__ void __launch_bounds__(kSplitWarps * 32)
+    phs_split_decode_kernel(const __grid_constant__ CUtensorMap tk,
+                            const __grid_constant__ CUtensorMap tv,
+                            const __grid_constant__ CUtensorMap tk8,
+                            const __grid_constant__ CUtensorMap tv8, const SplitArgs a) {
+  using L = SplitLayout<D>;
+  constexpr int S = L::kStages;
+  constexpr int NW = kSplitWarps;
+  constexpr int GR = TWO ? 16 : 8;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+
+  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.G;
+
+  int n = a.seq_lens[b];
+  if (n > a.n_clamp) {  // longer than its block table or the stated bound
+    if (s == 0 && h == 0 && threadIdx.x == 0) set_status(a.status, PHS_ERANGE);
+    n = a.n_clamp;
+  }
+  const int qlen = a.qlens ? a.qlens[b] : 0;
+  const int T = a.T;
+  const int ns = min(request_splits(n, qlen, T), a.max_splits);
+  if (ns < 0) {
+    if (s == 0 && h == 0 && threadIdx.x == 0) set_status(a.status, PHS_ERANGE);
+    return;
+  }
+  const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
+  if (ns == 0) {  // empty request: zero output
+    if (s == 0)
+      for (int e = threadIdx.x; e < G * D; e += blockDim.x) store_out(a.out, out_row0 + e, 0.f, a.out_f32);
+    return;
+  }
+  if (s >= ns) return;
+
+  const int nsq = (qlen + T - 1) / T;
+  const bool is_i8 = s < nsq;
+  int t0, t1, nch;
+  if (is_i8) {
+    t0 = s * T;
+    t1 = min(t0 + T, qlen);
+    nch = (t1 - t0) / kQBlock;
+  } else {
+    t0 = qlen + (s - nsq) * T;
+    t1 = min(t0 + T, n);
+    nch = (t1 - t0 + kPage - 1) / kPage;
+  }
+  const int my_n = warp < nch ? (nch - warp + NW - 1) / NW : 0;
+
+  // ---- chunk ids (physical page / INT8 page) and INT8 scales of this warp
+  int32_t* ids = reinterpret_cast<int32_t*>(smem + L::kIdsOff) + warp * kMaxChunksPerWarp * 3;
+  float* kss = reinterpret_cast<float*>(ids + kMaxChunksPerWarp);
+  float* vss = kss + kMaxChunksPerWarp;
+  for (int j = lane; j < my_n; j += 32) {
+    const int ci = warp + j * NW;
+    int id;
+    float ks = 0.f, vs = 0.f;
+    if (is_i8) {
+      const int lq = t0 / kQBlock + ci;
+      id = lq < a.max_qpages ? a.qtable[static_cast<size_t>(b) * a.max_qpages + lq] : -1;
+      if (id < 0 || id >= a.num_qpages) {
+        set_status(a.status, PHS_ERANGE);
+        id = -1;
+      } else {
+        ks = __ldg(a.k_scale + static_cast<size_t>(id) * a.Hkv + h);
+        vs = __ldg(a.v_scale + static_cast<size_t>(id) * a.Hkv + h);
+      }
+    } else {
+      const int lp = t0 / kPage + ci;  // < max_pages: n was clamped above
+      id = a.block_table[static_cast<size_t>(b) * a.max_pages + lp];
+      if (id < 0 || id >= a.num_pages) {
+        set_status(a.status, PHS_ERANGE);
+        id = -1;
+      }
+    }
+    ids[j] = id;
+    kss[j] = ks;
+    vss[j] = vs;
+  }
+  const uint32_t bar0 = smem_u32(smem + L::kBarOff) + warp * S * 8;
+  if (lane == 0) {
+    for (int i = 0; i < S; ++i) mbar_init(bar0 + 8 * i, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const uint32_t sbase = smem_u32(smem) + warp * S * L::kStage;
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](int j) {  // lane 0 only
+    const uint32_t bar = bar0 + 8 * (j % S);
+    const uint32_t dst = sbase + (j % S) * L::kStage;
+    const int id = ids[j];
+    if (id < 0) {
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+      return;
+    }
+    mbar_arrive_expect_tx(bar, L::kStage);
+    if (is_i8) {
+      const int row = (id * a.Hkv + h) * kQBlock;
+      tma_load_2d(dst, &tk8, 0, row, bar, pol);
+      tma_load_2d(dst + L::kStage / 2, &tv8, 0, row, bar, pol);
+    } else {
+      const int row = (id * a.Hkv + h) * kPage;
+#pragma unroll
+      for (int sub = 0; sub < D / 64; ++sub) {
+        tma_load_2d(dst + sub * 2048, &tk, sub * 64, row, bar, pol);
+        tma_load_2d(dst + L::kStage / 2 + sub * 2048, &tv, sub * 64, row, bar, pol);
+      }
+    }
+  };
+  if (lane == 0) {
+    if (is_i8) {
+      prefetch_tmap(&tk8);
+      prefetch_tmap(&tv8);
+    } else {
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+    }
+    for (int j = 0; j < S && j < my_n; ++j) issue(j);
+  }
+
+  // ---- queries of the group (overlaps the first loads)
+  QFrags<D, TWO> qf;
+  const __nv_bfloat16* qg = a.q + out_row0;
+  if (is_i8)
+    load_q_f16_i8order(qf, qg, G, lane);
+  else
+    load_q_bf16(qf, qg, G, lane);
+
+  WarpState<D, TWO> st;
+  st.reset();
+  int j = 0;
+  for (; j < my_n; ++j) {
+    const uint32_t bar = bar0 + 8 * (j % S);
+    const bool done = mbar_wait(bar, (j / S) & 1);
+    if (!__all_sync(0xffffffffu, done)) {
+      if (lane == 0) set_status(a.status, PHS_ETIMEOUT);
+      break;
+    }
+    const int id = ids[j];
+    const uint32_t sK = sbase + (j % S) * L::kStage;
+    const uint32_t sV = sK + L::kStage / 2;
+    if (id >= 0) {
+      if (is_i8) {
+        consume_i8<D, TWO>(st, qf, sK, sV, kss[j], vss[j], a.scale_log2, lane);
+      } else {
+        const int tc = t0 + kPage * (warp + j * NW);
+        const int nv = t1 - tc;
+        const uint32_t valid = nv >= kPage ? 0xFFFFu : ((1u << nv) - 1u);
+        if (valid != 0xFFFFu) {
+          zero_invalid_v_rows<D>(smem + (sV - smem_u32(smem)), valid, lane);
+          __syncwarp();
+        }
+        consume_bf16<D, TWO>(st, qf, sK, sV, valid, a.scale_log2, lane);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && j + S < my_n) {
+      fence_proxy_async_smem();
+      issue(j + S);
+    }
+  }
+  if (j < my_n && lane == 0) {
+    // gave up: drain (bounded) the loads this warp still has in flight
+    for (int k = j; k < my_n && k < j + S; ++k) (void)mbar_wait(bar0 + 8 * (k % S), (k / S) & 1);
+  }
+
+  // ---- warp result -> shared memory -> CTA merge
+  const int g = lane >> 2, qd = lane & 3;
+  float lsum[2];
+#pragma unroll
+  for (int rh = 0; rh < 2; ++rh) lsum[rh] = warp_sum_quad(st.l[rh]);
+  const float oscale = is_i8 ? st.u : 1.f;
+  __syncthreads();  // every warp is done with its stages
+  float* sO = reinterpret_cast<float*>(smem);
+  float* sM = sO + NW * GR * D;
+  float* sL = sM + NW * GR;
+#pragma unroll
+  for (int rh = 0; rh < (TWO ? 2 : 1); ++rh) {
+    const int row = g + 8 * rh;
+    if (row < G) {
+#pragma unroll
+      for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int col = is_i8 ? acc_col<true>(nt, e, qd) : acc_col<false>(nt, e, qd);
+          sO[(warp * GR + row) * D + col] = st.o[nt][2 * rh + e] * oscale;
+        }
+      if (qd == 0) {
+        sM[warp * GR + row] = st.m[rh];
+        sL[warp * GR + row] = lsum[rh];
+      }
+    }
+  }
+  __syncthreads();
+  const size_t part = (static_cast<size_t>(b) * a.Hkv + h) * a.max_splits + s;
+  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+    const int row = e / D, d = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, sM[w * GR + row]);
+    float Lsum = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float mw = sM[w * GR + row];
+      const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      Lsum += sL[w * GR + row] * f;
+      O += sO[(w * GR + row) * D + d] * f;
+    }
+    if (ns == 1) {
+      store_out(a.out, out_row0 + e, Lsum > 0.f ? O / Lsum : 0.f, a.out_f32);
+    } else {
+      a.ws_o[(part * G + row) * D + d] = O;
+      if (d == 0) {
+        a.ws_ml[(part * G + row) * 2] = M;
+        a.ws_ml[(part * G + row) * 2 + 1] = Lsum;
+      }
+    }
+  }
+}
+
+// Cross-split log-sum-exp merge for requests with more than one split.
+template <int D>
+__global__ void __launch_bounds__(128) phs_merge_kernel(const MergeArgs a) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int G = a.G;
+  const int n = min(a.seq_lens[b], a.n_clamp);
+  const int qlen = a.qlens ? a.qlens[b] : 0;
+  const int ns = min(request_splits(n, qlen, a.T), a.max_splits);
+  if (ns <= 1) return;
+  const size_t part0 = (static_cast<size_t>(b) * a.Hkv + h) * a.max_splits;
+  const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
+  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+    const int row = e / D, d = e % D;
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, a.ws_ml[((part0 + s) * G + row) * 2]);
+    float Lsum = 0.f, O = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float ms = a.ws_ml[((part0 + s) * G + row) * 2];
+      const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
+      Lsum += a.ws_ml[((part0 + s) * G + row) * 2 + 1] * f;
+      O += a.ws_o[((part0 + s) * G + row) * D + d] * f;
+    }
+    store_out(a.out, out_row0 + e, Lsum > 0.f ? O / Lsum : 0.f, a.out_f32);
+  }
+}
+
+// ------------------------------------------------------------ launchers --
+template <int D, bool TWO>
+static int launch_split_t(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tk8,
+                          const CUtensorMap& tv8, const SplitArgs& a, int B, cudaStream_t stream) {
+  auto kern = phs_split_decode_kernel<D, TWO>;
+  const int smem = SplitLayout<D>::kAlloc;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return PHS_ECUDA;
+  dim3 grid(a.max_splits, a.Hkv, B);
+  kern<<<grid, kSplitWarps * 32, smem, stream>>>(tk, tv, tk8, tv8, a);
+  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+}
+
+int launch_split_decode(int D, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const CUtensorMap& tk8, const CUtensorMap& tv8, const SplitArgs& a,
+                        int B, cudaStream_t stream) {
+  const bool two = a.G > 8;
+  if (D == 128) {
+    return two ? launch_split_t<128, true>(tk, tv, tk8, tv8, a, B, stream)
+               : launch_split_t<128, false>(tk, tv, tk8, tv8, a, B, stream);
+  }
+  if (D == 64) {
+    return two ? launch_split_t<64, true>(tk, tv, tk8, tv8, a, B, stream)
+               : launch_split_t<64, false>(tk, tv, tk8, tv8, a, B, stream);
+  }
+  return PHS_EUNSUPPORTED;
+}
+
+int launch_merge(int D, const MergeArgs& a, int B, cudaStream_t stream) {
+  dim3 grid(a.Hkv, B);
+  if (D == 128)
+    phs_merge_kernel<128><<<grid, 128, 0, stream>>>(a);
+  else if (D == 64)
+    phs_merge_kernel<64><<<grid, 128, 0, stream>>>(a);
+  else
+    return PHS_EUNSUPPORTED;
+  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+}
+
+}  // namespace phs

@@ -1,0 +1,135 @@
+// phs_internal.h -- argument blocks and launchers shared between the
+// kernels' translation units and the C-ABI front end (phs_api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "phs.h"
+
+namespace phs {
+
+constexpr int kPage = 16;    // tokens per Full-pool page
+constexpr int kQBlock = 32;  // tokens per INT8 page / scale group
+
+// ----------------------------------------------------- split-KV decode --
+struct SplitArgs {
+  const __nv_bfloat16* q;   // [B][Hq][D]
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* qtable;    // INT8 page table, or null
+  const int32_t* qlens;     // INT8 lengths, or null
+  const float* k_scale;
+  const float* v_scale;
+  void* out;
+  float* ws_o;              // [B][Hkv][max_splits][G][D]
+  float* ws_ml;             // [B][Hkv][max_splits][G][2]
+  int32_t* status;
+  int64_t num_pages;
+  int64_t num_qpages;
+  int Hq, Hkv, G;
+  int max_pages;            // block table row length
+  int max_qpages;           // INT8 table row length
+  int n_clamp;              // lengths above this are an error and clamped
+  int T;                    // tokens per split (multiple of 32)
+  int max_splits;
+  int out_f32;
+  float scale_log2;         // softmax_scale * log2(e)
+};
+
+struct MergeArgs {
+  const int32_t* seq_lens;
+  const int32_t* qlens;
+  const float* ws_o;
+  const float* ws_ml;
+  void* out;
+  int Hq, Hkv, G;
+  int n_clamp;
+  int T;
+  int max_splits;
+  int out_f32;
+};
+
+int launch_split_decode(int D, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const CUtensorMap& tk8, const CUtensorMap& tv8, const SplitArgs& a,
+                        int B, cudaStream_t stream);
+int launch_merge(int D, const MergeArgs& a, int B, cudaStream_t stream);
+
+// ------------------------------------------------------------ SWA ring --
+constexpr int kSwaMaxLayers = 64;
+
+template <int MAXL>
+struct SwaParams {
+  CUtensorMap tk[MAXL];
+  CUtensorMap tv[MAXL];
+  const __nv_bfloat16* q[MAXL];
+  void* out[MAXL];
+  int64_t num_rings[MAXL];
+  const int32_t* ring_ids;  // null = identity
+  const int32_t* ring_pos;
+  const int32_t* seq_lens;
+  int32_t* status;
+  int num_layers, B, Hq, Hkv, G, W;
+  int out_f32;
+  float scale_log2;
+};
+
+template <int MAXL>
+int launch_swa_decode(int D, const SwaParams<MAXL>& p, int num_sms, cudaStream_t stream);
+
+// -------------------------------------------------------------- append --
+constexpr int kAppendMaxLayers = 64;
+
+struct AppendLayer {
+  void* k;
+  void* v;
+  const void* k_new;
+  const void* v_new;
+  int64_t num;  // pages (paged) or rings (ring)
+};
+
+template <int MAXL>
+struct AppendParams {
+  AppendLayer layer[MAXL];
+  const int32_t* table;     // paged: block table; ring: ring ids (may be null)
+  const int32_t* seq_lens;  // paged
+  const int32_t* ring_pos;  // ring
+  const int32_t* refcount;  // paged, may be null
+  int32_t* status;
+  int num_layers, B, Hkv, D;
+  int max_pages;            // paged
+  int W;                    // ring
+  int is_ring;
+};
+
+template <int MAXL>
+int launch_append(const AppendParams<MAXL>& p, cudaStream_t stream);
+
+// ----------------------------------------------------------- quantiser --
+struct QuantArgs {
+  const __nv_bfloat16* k_src;
+  const __nv_bfloat16* v_src;
+  const int32_t* src_table;
+  int8_t* k_codes;
+  int8_t* v_codes;
+  float* k_scale;
+  float* v_scale;
+  const int32_t* dst_qtable;
+  const int32_t* first_qblock;
+  const int32_t* num_qblocks;
+  int32_t* status;
+  int64_t num_pages, num_qpages;
+  int src_max_pages, dst_max_qpages;
+  int Hkv, D;
+};
+
+int launch_quant(const QuantArgs& a, int max_qblocks, int B, cudaStream_t stream);
+
+// ---------------------------------------------------------------- copy --
+int launch_copy(void* dst, const void* src, size_t bytes, int num_sms, cudaStream_t stream);
+
+int swa_smem_bytes(int D, int G, int batch);
+
+}  // namespace phs
