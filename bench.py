@@ -52,10 +52,14 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash():
+SPLIT_KERNEL_SOURCES = ("phs_decode.cu", "phs_attn.cuh", "phs_common.cuh", "phs_internal.h")
+
+
+def kernel_source_hash(files=SPLIT_KERNEL_SOURCES):
+    """Hash of the sources the split-KV decode kernel is compiled from."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "paged_hybrid_sliding_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
+    for name in files:
         with open(os.path.join(d, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -136,12 +140,11 @@ class ClockSampler:
 class PagedFullWorkload:
     """Paged Full-attention decode, batch 64 (one step = append + decode)."""
 
-    name = "paged_full_b64_hq32_hkv8_d128_p16_seqU[1K,32K]"
-
-    def __init__(self, device, seed=2):
+    def __init__(self, device, seed=2, batch=64):
         import paged_hybrid_sliding_gb300 as phs
         self.phs = phs
-        self.w = w = synth.paged_full(seed=seed)
+        self.w = w = synth.paged_full(seed=seed, B=batch)
+        self.name = f"paged_full_b{batch}_hq32_hkv8_d128_p16_seqU[1K,32K]"
         self.device = device
         B, Hq, Hkv, D = w.B, w.Hq, w.Hkv, w.D
         self.k = synth.normal_bf16((w.num_pages, Hkv, 16, D), seed * 100 + 1, device=device)
@@ -267,7 +270,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     import paged_hybrid_sliding_gb300 as phs
     phs.lib()
-    wl = PagedFullWorkload(device)
+    wl = PagedFullWorkload(device, batch=args.batch)
     for _ in range(args.warmup):
         wl.step()
     torch.cuda.synchronize()
@@ -395,7 +398,8 @@ def run_reference(args, rank, budget_s=40.0):
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": PagedFullWorkload.name, "sample": sample},
+            "config": {"workload": "paged_full_b64_hq32_hkv8_d128_p16_seqU[1K,32K]",
+                       "sample": sample},
             "tokens_per_s": round(toks * args.steps / t, 1),
             "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "kind": "oracle",
                              "cores": oracle.max_threads(), "sample": sample},
@@ -410,6 +414,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="phs", choices=["phs", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=64,
+                    help="requests in the paged workload (64 = the benchmark case)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -204,11 +204,10 @@ def kv_quant_int8_block32(src: PagedPool, src_block_table, dst: Int8Pool, dst_qt
 # ------------------------------------------------------------------ decode --
 def decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
                            tokens_per_split=0, has_int8=False) -> int:
-    n = lib().phs_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
-                                         tokens_per_split, int(bool(has_int8)))
-    if n == 0:
-        raise ValueError("unsupported decode shape")
-    return int(n)
+    """Workspace bytes for a decode call; 0 if the shape is not supported."""
+    return int(lib().phs_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                                max_seq_len, tokens_per_split,
+                                                int(bool(has_int8))))
 
 
 def decode_tokens_per_split(batch, num_kv_heads, max_seq_len, tokens_per_split=0) -> int:
@@ -237,7 +236,9 @@ def _decode_args(q, pool, block_table, seq_lens, int8, qtable, qlens, out, out_d
 
 def _workspace(workspace, nbytes, device):
     if workspace is None:
-        return torch.empty(nbytes, dtype=torch.uint8, device=device)
+        # a zero size means the library rejects the shape: let the call
+        # report the precise status
+        return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
     _need(workspace, torch.uint8, "workspace", 1)
     return workspace
 
