@@ -20,7 +20,8 @@
  *   - Every pointer argument named *dev / pool / table / q / out / workspace
  *     is a DEVICE pointer unless the comment says "host".  The caller owns
  *     all memory.  The library allocates nothing and keeps no state between
- *     calls except a per-thread cache of device properties.
+ *     calls except a per-thread cache of device properties (and the built-in
+ *     scratch of phs_attn_decode_full_paged_noalloc, described there).
  *   - bf16 tensors are IEEE bfloat16 (2 bytes).  Layouts are C order:
  *       Full pool  K, V : [num_pages][Hkv][page_size][D]       bf16
  *       SWA ring   K, V : [num_rings][Hkv][window][D]          bf16
@@ -69,7 +70,9 @@ typedef enum {
     PHS_ECUDA = -6,         /* a CUDA runtime/driver call failed */
     PHS_EUNSUPPORTED = -7,  /* valid but unsupported shape */
     PHS_ETIMEOUT = -8,      /* (device) a bounded wait gave up */
-    PHS_EALIGN = -9         /* a pointer is not 16-byte aligned */
+    PHS_EALIGN = -9,        /* a pointer is not 16-byte aligned */
+    PHS_ESCRATCH = -10      /* request needs more than the built-in scratch of
+                               phs_attn_decode_full_paged_noalloc */
 } phs_status;
 
 enum { PHS_OUT_BF16 = 0, PHS_OUT_F32 = 1 };
@@ -220,6 +223,42 @@ int phs_attn_merge_splits(int32_t batch, int32_t num_q_heads, int32_t num_kv_hea
                           const int32_t *qlens, int32_t has_int8, int32_t tokens_per_split,
                           void *out, int32_t out_dtype, const void *workspace,
                           size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Full-attention decode that allocates nothing: the same computation, the
+ * same arguments and the same results as phs_attn_decode_full_paged, minus
+ * the workspace.  The pages have no counterpart to this call; it exists for
+ * callers that cannot hand the library a workspace: plug-ins and callbacks
+ * running inside a host framework that owns all device memory and does not
+ * expose its allocator, serving engines that reserve nearly all of HBM for
+ * the KV pool up front (so a late cudaMalloc would fail), and latency-bound
+ * decode loops where cudaMalloc/cudaFree and the device-wide synchronisation
+ * they imply are not acceptable.
+ *
+ * Scratch: the split partials live in a file-scope device array of
+ * PHS_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU which loads the library
+ * holds until the process exits.  The library's first call of this entry
+ * point on a device looks up the array's device address (no allocation);
+ * make that first call before any stream capture.  All calls share the one
+ * array and keep no state in it between calls, so calls that overlap on
+ * the GPU (on different streams, or from several threads) race: serialise
+ * them.  When tokens_per_split is 0 the library picks the split length as
+ * the decode call does and, if the partials would not fit, lengthens the
+ * splits (up to 4096 tokens); a request that still does not fit, or an
+ * explicit tokens_per_split that does not fit, returns PHS_ESCRATCH before
+ * anything is launched.  Nothing here calls cudaMalloc, cudaFree or any
+ * allocating routine.
+ * ---------------------------------------------------------------------- */
+#define PHS_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+int phs_attn_decode_full_paged_noalloc(const void *q, int32_t num_q_heads,
+                                       const phs_paged_pool *pool, const int32_t *block_table,
+                                       int32_t max_pages_per_seq, const int32_t *seq_lens,
+                                       int32_t max_seq_len, const phs_int8_pool *int8,
+                                       const int32_t *qtable, int32_t max_qpages_per_seq,
+                                       const int32_t *qlens, int32_t batch, float softmax_scale,
+                                       int32_t tokens_per_split, void *out, int32_t out_dtype,
+                                       int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
  * Sliding-window decode over the SWA ring.

@@ -23,6 +23,7 @@ __all__ = [
     "kv_append_paged", "kv_append_ring", "kv_quant_int8_block32",
     "decode_workspace_bytes", "decode_tokens_per_split",
     "attn_decode_full_paged", "attn_decode_full_paged_split", "attn_merge_splits",
+    "attn_decode_full_paged_noalloc", "NOALLOC_SCRATCH_BYTES",
     "attn_decode_swa_ring", "attn_decode_hybrid_stack", "hybrid_stack_workspace_bytes",
     "hybrid_kv_tokens", "copy_d2d", "lib", "PAGE", "QBLOCK",
 ]
@@ -30,6 +31,7 @@ __all__ = [
 PAGE = 16
 QBLOCK = 32
 OUT_BF16, OUT_F32 = 0, 1
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class PhsError(RuntimeError):
@@ -262,6 +264,30 @@ def attn_decode_full_paged(q, pool: PagedPool, block_table, seq_lens, max_seq_le
         0 if qtable is None else qtable.shape[1], _ptr(qlens), B, scale, int(tokens_per_split),
         _ptr(out), _out_code(out.dtype), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
         "attn_decode_full_paged")
+    return out
+
+
+def attn_decode_full_paged_noalloc(q, pool: PagedPool, block_table, seq_lens,
+                                   max_seq_len: int, out, softmax_scale=None,
+                                   int8: Int8Pool | None = None, qtable=None, qlens=None,
+                                   tokens_per_split=0, status=None, stream=None):
+    """Same as attn_decode_full_paged, for callers that cannot provide a
+    workspace (a host framework that owns all device memory, an engine that
+    has reserved nearly all of HBM, a loop that must not call cudaMalloc).
+    The partials go to the library's built-in 32 MiB scratch per GPU; `out`
+    must be given.  Calls that overlap on the GPU share that scratch and
+    race, so serialise them.  Raises PhsError (PHS_ESCRATCH) when the
+    request needs more scratch than that."""
+    pc, ic, out = _decode_args(q, pool, block_table, seq_lens, int8, qtable, qlens, out,
+                               out.dtype, status)
+    B, Hq, D = q.shape
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    _check(lib().phs_attn_decode_full_paged_noalloc(
+        _ptr(q), Hq, ctypes.byref(pc), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        int(max_seq_len), None if ic is None else ctypes.byref(ic), _ptr(qtable),
+        0 if qtable is None else qtable.shape[1], _ptr(qlens), B, scale, int(tokens_per_split),
+        _ptr(out), _out_code(out.dtype), _ptr(status), _stream(stream)),
+        "attn_decode_full_paged_noalloc")
     return out
 
 

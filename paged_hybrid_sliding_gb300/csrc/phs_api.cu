@@ -292,6 +292,7 @@ const char* phs_status_str(int s) {
     case PHS_EUNSUPPORTED: return "unsupported shape";
     case PHS_ETIMEOUT: return "device wait timed out";
     case PHS_EALIGN: return "pointer not aligned";
+    case PHS_ESCRATCH: return "request exceeds the no-allocation entry point's built-in scratch";
     default: return "unknown status";
   }
 }
@@ -677,3 +678,69 @@ int phs_copy_d2d(void* dst, const void* src, size_t bytes, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// No-allocation decode.  The split partials go to this file-scope array
+// instead of a caller workspace.  In host code the array's name is only a
+// stand-in: its device address is looked up once per device with
+// cudaGetSymbolAddress and passed to the kernels.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char phs_noalloc_scratch[PHS_NOALLOC_SCRATCH_BYTES];
+
+namespace phs {
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+
+// Device address of the scratch on the current device (looked up on the
+// first call per device), or null if the lookup fails.
+void* noalloc_scratch_on_current_device() {
+  static std::mutex mu;
+  static void* addr[kNoAllocMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, phs_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace phs
+
+extern "C" int phs_attn_decode_full_paged_noalloc(
+    const void* q, int32_t num_q_heads, const phs_paged_pool* pool, const int32_t* block_table,
+    int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
+    const phs_int8_pool* int8, const int32_t* qtable, int32_t max_qpages_per_seq,
+    const int32_t* qlens, int32_t batch, float softmax_scale, int32_t tokens_per_split, void* out,
+    int32_t out_dtype, int32_t* dev_status, void* stream) {
+  int st = check_paged(pool);
+  if (st) return st;
+  // choose a split length whose partials fit the scratch
+  const bool has_int8 = int8 != nullptr;
+  DecodePlan pl;
+  if ((st = make_plan(pl, batch, num_q_heads, pool->num_kv_heads, pool->head_dim, max_seq_len,
+                      tokens_per_split, has_int8)))
+    return st;
+  int tps = pl.T;
+  while (pl.need > PHS_NOALLOC_SCRATCH_BYTES && tokens_per_split == 0 && tps < kMaxSplitTokens) {
+    tps *= 2;
+    if ((st = make_plan(pl, batch, num_q_heads, pool->num_kv_heads, pool->head_dim, max_seq_len,
+                        tps, has_int8)))
+      return st;
+  }
+  if (pl.need > PHS_NOALLOC_SCRATCH_BYTES) return PHS_ESCRATCH;
+  void* scratch = noalloc_scratch_on_current_device();
+  if (!scratch) return PHS_ECUDA;
+  DecodeCall c;
+  st = prepare_decode(c, q, num_q_heads, pool, block_table, max_pages_per_seq, seq_lens,
+                      max_seq_len, int8, qtable, max_qpages_per_seq, qlens, batch, softmax_scale,
+                      tps, out, out_dtype, scratch, PHS_NOALLOC_SCRATCH_BYTES, dev_status);
+  if (st) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_split_decode(c.pl.D, c.tk, c.tv, c.tk8, c.tv8, c.a, batch, s))) return st;
+  return launch_merge(c.pl.D, c.m, batch, s);
+}
