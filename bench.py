@@ -136,9 +136,58 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ----------------------------------------------------- config 2 workload --
-class PagedFullWorkload:
+# --------------------------------------------------------------- workloads --
+def host_pages(pool_t, block_table, rows, n_after):
+    """Host bit copy of the pages the selected requests reference, with a
+    block table remapped onto that compact copy."""
+    pages = [block_table[b, :int(synth.pages_needed(n_after[b]))] for b in rows]
+    idx = torch.from_numpy(np.concatenate(pages).astype(np.int64)).to(pool_t.device)
+    host = synth.bits(pool_t.index_select(0, idx))
+    bt = np.full((len(rows), max(len(p) for p in pages)), -1, np.int32)
+    o = 0
+    for i, p in enumerate(pages):
+        bt[i, :len(p)] = np.arange(o, o + len(p))
+        o += len(p)
+    return host, bt
+
+
+def pinned(t):
+    return t.cpu().pin_memory()
+
+
+def nbytes(*ts):
+    return sum(t.numel() * t.element_size() for t in ts)
+
+
+def rows_for_budget(n_after, order, per_token_s, budget_s):
+    rows, acc = [], 0.0
+    for b in order:
+        if rows and acc + per_token_s * float(n_after[b]) > budget_s:
+            break
+        rows.append(int(b))
+        acc += per_token_s * float(n_after[b])
+    return rows
+
+
+class Workload:
+    """One decode step of a synthetic workload on the device.  Subclasses
+    set the byte / token accounting and implement step() (inputs resident),
+    e2e_step() (public API from pinned host buffers) and cpu_baseline()."""
+    kernel = "phs_split_decode_kernel"
+    l2 = "inputs larger than L2 (K/V read per step >> 129 MB)"
+
+    def kernel_seconds(self, evs):
+        return statistics.fmean(a.elapsed_time(b) for a, b in evs) / 1e3 if evs else None
+
+    def new_events(self, steps):
+        return [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(self.kernel_launches_per_step)] for _ in range(steps)]
+
+
+class PagedFullWorkload(Workload):
     """Paged Full-attention decode, batch 64 (one step = append + decode)."""
+
+    kernel_launches_per_step = 1
 
     def __init__(self, device, seed=2, batch=64):
         import paged_hybrid_sliding_gb300 as phs
@@ -167,39 +216,32 @@ class PagedFullWorkload:
         app = 2 * B * Hkv * D * 2 * 2
         tables = int(synth.pages_needed(w.n_after).sum()) * 4 + B * 4
         self.bytes_per_step = kv + qo + app + tables
-        self.split_bytes = kv + B * Hq * D * 2 + tables
+        self.kernel_bytes = kv + B * Hq * D * 2 + tables
         self.launches_per_step = 3
-        # pinned host copies of the per-step inputs for the end-to-end leg
-        self.h_q = self.q.cpu().pin_memory()
-        self.h_kn = self.kn.cpu().pin_memory()
-        self.h_vn = self.vn.cpu().pin_memory()
-        self.h_bt = self.bt.cpu().pin_memory()
-        self.h_sl = self.sl.cpu().pin_memory()
+        self.extra = {"batch": B, "tokens_per_split": self.tps}
+        self.h_q, self.h_kn, self.h_vn = pinned(self.q), pinned(self.kn), pinned(self.vn)
+        self.h_bt, self.h_sl = pinned(self.bt), pinned(self.sl)
         self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
-        self.h2d_bytes = sum(t.numel() * t.element_size()
-                             for t in (self.h_q, self.h_kn, self.h_vn, self.h_bt, self.h_sl))
-        self.d2h_bytes = self.h_out.numel() * self.h_out.element_size()
+        self.h2d_bytes = nbytes(self.h_q, self.h_kn, self.h_vn, self.h_bt, self.h_sl)
+        self.d2h_bytes = nbytes(self.h_out)
 
     def step(self, ev=None):
         phs = self.phs
         phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl)
         if ev is not None:
-            ev[0].record()
+            ev[0][0].record()
         phs.attn_decode_full_paged_split(self.q, self.pool, self.bt, self.sl, self.max_seq,
                                          self.ws, self.out, tokens_per_split=self.tps)
         if ev is not None:
-            ev[1].record()
+            ev[0][1].record()
         phs.attn_merge_splits(self.out, self.w.Hkv, self.sl, self.max_seq, self.ws,
                               tokens_per_split=self.tps)
 
     def e2e_step(self):
-        """Public API from host buffers: inputs in, output out, every step."""
         phs = self.phs
-        self.q.copy_(self.h_q, non_blocking=True)
-        self.kn.copy_(self.h_kn, non_blocking=True)
-        self.vn.copy_(self.h_vn, non_blocking=True)
-        self.bt.copy_(self.h_bt, non_blocking=True)
-        self.sl.copy_(self.h_sl, non_blocking=True)
+        for d, h in ((self.q, self.h_q), (self.kn, self.h_kn), (self.vn, self.h_vn),
+                     (self.bt, self.h_bt), (self.sl, self.h_sl)):
+            d.copy_(h, non_blocking=True)
         phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl)
         phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl, self.max_seq,
                                    out=self.out, tokens_per_split=self.tps, workspace=self.ws)
@@ -209,40 +251,478 @@ class PagedFullWorkload:
         """The oracle as it stands on a sample of requests of this step."""
         import oracle
         w = self.w
-        order = list(range(w.B))
-        # one request first to size the sample to the time budget
-        t_one, _ = self._oracle_time([order[0]])
-        per_tok = t_one / float(w.n_after[order[0]])
-        rows, acc = [], 0.0
-        for b in order:
-            rows.append(b)
-            acc += per_tok * float(w.n_after[b])
-            if acc >= budget_s:
-                break
+        t1, _ = self._oracle_time([0])
+        rows = rows_for_budget(w.n_after, range(w.B), t1 / float(w.n_after[0]), budget_s)
         t, toks = self._oracle_time(rows)
         kv_bytes = toks * w.Hkv * w.D * 2 * 2
         return {"value": kv_bytes / t / 1e9, "unit": "GB/s", "tokens_per_s": toks / t,
                 "cores": oracle.max_threads(), "kind": "oracle",
                 "sample": f"{len(rows)} of {w.B} requests of one decode step "
-                          f"({toks} tokens, all 32 query heads), fp64 oracle, {t:.2f} s"}
+                          f"({toks} tokens, all {w.Hq} query heads), fp64 oracle, {t:.2f} s"}
 
     def _oracle_time(self, rows):
         import oracle
         w = self.w
-        pages = [w.block_table[b, :int(synth.pages_needed(w.n_after[b]))] for b in rows]
-        idx = torch.from_numpy(np.concatenate(pages).astype(np.int64)).to(self.device)
-        hk = synth.bits(self.k.index_select(0, idx))
-        hv = synth.bits(self.v.index_select(0, idx))
-        bt = np.full((len(rows), max(len(p) for p in pages)), -1, np.int32)
-        o = 0
-        for i, p in enumerate(pages):
-            bt[i, :len(p)] = np.arange(o, o + len(p))
-            o += len(p)
+        hk, bt = host_pages(self.k, w.block_table, rows, w.n_after)
+        hv, _ = host_pages(self.v, w.block_table, rows, w.n_after)
         qh = synth.bits(self.q)[rows]
         sl = w.n_after[rows]
         t0 = time.perf_counter()
         oracle.decode_full_paged(qh, hk, hv, bt, sl, w.softmax_scale)
         return time.perf_counter() - t0, int(sl.sum())
+
+
+class TinyHybridWorkload(Workload):
+    """Batch 2, 4 q / 2 KV heads, D 64: one Full (paged) + one SWA (ring)
+    layer, append + attend through the hybrid-stack call.  Latency-bound."""
+
+    kernel_launches_per_step = 0
+    l2 = "latency-bound case: ~0.2 MB per step, resident in L2"
+
+    def __init__(self, device, seed=1):
+        import paged_hybrid_sliding_gb300 as phs
+        self.phs = phs
+        self.w = w = synth.tiny_hybrid(seed=seed)
+        self.name = "tiny_hybrid_b2_hq4_hkv2_d64_full+swa_w128"
+        B, Hq, Hkv, D, W = w.B, w.Hq, w.Hkv, w.D, w.W
+        g = seed * 100
+        self.kp = synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 1, device=device)
+        self.vp = synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 2, device=device)
+        self.kr = synth.normal_bf16((B, Hkv, W, D), g + 3, device=device)
+        self.vr = synth.normal_bf16((B, Hkv, W, D), g + 4, device=device)
+        self.qf = synth.normal_bf16((B, Hq, D), g + 5, device=device)
+        self.qs = synth.normal_bf16((B, Hq, D), g + 6, device=device)
+        self.kn = synth.normal_bf16((B, Hkv, D), g + 7, device=device)
+        self.vn = synth.normal_bf16((B, Hkv, D), g + 8, device=device)
+        self.of = torch.empty((B, Hq, D), dtype=torch.float32, device=device)
+        self.os = torch.empty((B, Hq, D), dtype=torch.float32, device=device)
+        self.bt = torch.from_numpy(w.block_table).to(device)
+        self.sl = torch.from_numpy(w.n_after).to(device)
+        self.rp = torch.from_numpy(w.ring_pos).to(device)
+        self.layers = [
+            phs.Layer(q=self.qf, out=self.of, paged=phs.PagedPool(self.kp, self.vp),
+                      k_new=self.kn, v_new=self.vn),
+            phs.Layer(q=self.qs, out=self.os, ring=phs.RingPool(self.kr, self.vr),
+                      k_new=self.kn, v_new=self.vn)]
+        self.max_seq = int(w.n_after.max())
+        self.ws = torch.empty(phs.hybrid_stack_workspace_bytes(B, Hq, Hkv, D, self.max_seq),
+                              dtype=torch.uint8, device=device)
+        full_tok = int(w.n_after.sum())
+        swa_tok = int(np.minimum(w.n_after, W).sum())
+        self.tokens_per_step = full_tok + swa_tok
+        tok_bytes = Hkv * D * 2 * 2
+        self.bytes_per_step = (full_tok + swa_tok) * tok_bytes + 2 * 2 * B * Hq * D * 2 + \
+            2 * 2 * B * Hkv * D * 2
+        self.kernel_bytes = None
+        self.launches_per_step = 5   # 2 appends, SWA decode, split, merge
+        self.extra = {"batch": B, "layers": "1 Full + 1 SWA(W=128)"}
+        self.host = [pinned(t) for t in (self.qf, self.qs, self.kn, self.vn, self.sl, self.rp,
+                                         self.bt)]
+        self.dev_in = [self.qf, self.qs, self.kn, self.vn, self.sl, self.rp, self.bt]
+        self.h_of = torch.empty_like(self.of, device="cpu").pin_memory()
+        self.h_os = torch.empty_like(self.os, device="cpu").pin_memory()
+        self.h2d_bytes = nbytes(*self.host)
+        self.d2h_bytes = nbytes(self.h_of, self.h_os)
+
+    def step(self, ev=None):
+        self.phs.attn_decode_hybrid_stack(self.layers, self.w.Hq, self.sl, self.max_seq,
+                                          block_table=self.bt, ring_pos=self.rp,
+                                          workspace=self.ws)
+
+    def e2e_step(self):
+        for d, h in zip(self.dev_in, self.host):
+            d.copy_(h, non_blocking=True)
+        self.step()
+        self.h_of.copy_(self.of, non_blocking=True)
+        self.h_os.copy_(self.os, non_blocking=True)
+
+    def cpu_baseline(self):
+        import oracle
+        w = self.w
+        hk, hv = synth.bits(self.kp), synth.bits(self.vp)
+        hkr, hvr = synth.bits(self.kr), synth.bits(self.vr)
+        kn, vn = synth.bits(self.kn), synth.bits(self.vn)
+        qf, qs = synth.bits(self.qf), synth.bits(self.qs)
+        reps = 200
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            oracle.append_paged(hk, hv, kn, vn, w.block_table, w.n_after)
+            oracle.append_ring(hkr, hvr, kn, vn, None, w.ring_pos)
+            oracle.decode_full_paged(qf, hk, hv, w.block_table, w.n_after, w.softmax_scale)
+            oracle.decode_swa_ring(qs, hkr, hvr, None, w.ring_pos, w.n_after, w.softmax_scale)
+        t = (time.perf_counter() - t0) / reps
+        return {"value": self.bytes_per_step / t / 1e9, "unit": "GB/s",
+                "us_per_step": t * 1e6, "cores": oracle.max_threads(), "kind": "oracle",
+                "sample": f"the whole step (2 appends + 2 decodes), mean of {reps} repetitions"}
+
+
+class HybridStackWorkload(Workload):
+    """70 layers (Full iff layer % 7 == 6: 10 Full, 60 SWA W=128), batch 256,
+    32 q / 8 KV heads, D 128, lengths log-uniform in [4K, 128K]; one step =
+    append into every layer + attend every layer, one hybrid-stack call.
+    Ten distinct 37.6 GB Full pools do not fit one GPU: `distinct` pools are
+    allocated and the Full layers use them round-robin (each layer still
+    streams its whole pool, far above L2, so no layer reads another's data
+    from cache)."""
+
+    kernel_launches_per_step = 0
+
+    def __init__(self, device, seed=3, distinct=4):
+        import paged_hybrid_sliding_gb300 as phs
+        self.phs = phs
+        self.w = w = synth.hybrid_stack(seed=seed)
+        B, Hq, Hkv, D, W = w.B, w.Hq, w.Hkv, w.D, w.W
+        lf = w.extra["layer_is_full"]
+        self.name = "hybrid_stack_70l_10full_60swa_w128_b256_hq32_hkv8_d128_seqlogU[4K,128K]"
+        g = seed * 1000
+        self.pools = [phs.PagedPool(
+            synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 10 * i + 1, device=device),
+            synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 10 * i + 2, device=device))
+            for i in range(distinct)]
+        self.layers, nf = [], 0
+        self.dev_in, self.host, self.outs, self.h_outs = [], [], [], []
+        for l, full in enumerate(lf):
+            q = synth.normal_bf16((B, Hq, D), g + 500 + 3 * l, device=device)
+            kn = synth.normal_bf16((B, Hkv, D), g + 501 + 3 * l, device=device)
+            vn = synth.normal_bf16((B, Hkv, D), g + 502 + 3 * l, device=device)
+            out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
+            if full:
+                L = phs.Layer(q=q, out=out, paged=self.pools[nf % distinct], k_new=kn, v_new=vn)
+                nf += 1
+            else:
+                ring = phs.RingPool(synth.normal_bf16((B, Hkv, W, D), g + 800 + 2 * l,
+                                                      device=device),
+                                    synth.normal_bf16((B, Hkv, W, D), g + 801 + 2 * l,
+                                                      device=device))
+                L = phs.Layer(q=q, out=out, ring=ring, k_new=kn, v_new=vn)
+            self.layers.append(L)
+            self.dev_in += [q, kn, vn]
+            self.outs.append(out)
+        self.bt = torch.from_numpy(w.block_table).to(device)
+        self.sl = torch.from_numpy(w.n_after).to(device)
+        self.rp = torch.from_numpy(w.ring_pos).to(device)
+        self.dev_in += [self.bt, self.sl, self.rp]
+        self.host = [pinned(t) for t in self.dev_in]
+        self.h_outs = [torch.empty_like(o, device="cpu").pin_memory() for o in self.outs]
+        self.max_seq = int(w.n_after.max())
+        self.ws = torch.empty(phs.hybrid_stack_workspace_bytes(B, Hq, Hkv, D, self.max_seq),
+                              dtype=torch.uint8, device=device)
+        nfull, nswa = int(lf.sum()), int(len(lf) - lf.sum())
+        full_tok = int(w.n_after.sum())
+        swa_tok = int(np.minimum(w.n_after, W).sum())
+        tok_bytes = Hkv * D * 2 * 2
+        self.tokens_per_step = nfull * full_tok + nswa * swa_tok
+        small = len(lf) * (2 * B * Hq * D * 2 + 2 * B * Hkv * D * 2 * 2)
+        tables = nfull * (int(synth.pages_needed(w.n_after).sum()) * 4)
+        self.bytes_per_step = self.tokens_per_step * tok_bytes + small + tables
+        self.full_layer_bytes = full_tok * tok_bytes + B * Hq * D * 2 + \
+            int(synth.pages_needed(w.n_after).sum()) * 4
+        self.swa_bytes = nswa * (swa_tok * tok_bytes + B * Hq * D * 2)
+        self.kernel_bytes = self.full_layer_bytes
+        self.launches_per_step = 2 + 1 + 2 * nfull
+        self.extra = {"batch": B, "layers": f"{nfull} Full + {nswa} SWA(W=128)",
+                      "distinct_full_pools": distinct, "full_layers_aliased_onto": distinct,
+                      "full_bytes_per_step": nfull * self.full_layer_bytes,
+                      "swa_bytes_per_step": self.swa_bytes,
+                      "kv_tokens_stored_ratio_vs_all_full":
+                          round((nfull * full_tok + nswa * swa_tok) / (len(lf) * full_tok), 4)}
+        self.h2d_bytes = nbytes(*self.host)
+        self.d2h_bytes = nbytes(*self.h_outs)
+
+    def step(self, ev=None):
+        self.phs.attn_decode_hybrid_stack(self.layers, self.w.Hq, self.sl, self.max_seq,
+                                          block_table=self.bt, ring_pos=self.rp,
+                                          workspace=self.ws)
+
+    def e2e_step(self):
+        for d, h in zip(self.dev_in, self.host):
+            d.copy_(h, non_blocking=True)
+        self.step()
+        for h, o in zip(self.h_outs, self.outs):
+            h.copy_(o, non_blocking=True)
+
+    def kernel_times(self, reps=3):
+        """Average launch time of the split kernel on the Full layers and of
+        the SWA kernel on all SWA layers (separate timed loops)."""
+        phs = self.phs
+        w = self.w
+        full = [L for L in self.layers if L.paged is not None]
+        ts = []
+        for _ in range(reps):
+            for L in full:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                phs.attn_decode_full_paged_split(L.q, L.paged, self.bt, self.sl, self.max_seq,
+                                                 self.ws, L.out)
+                b.record()
+                ts.append((a, b))
+        torch.cuda.synchronize()
+        split_s = statistics.fmean(a.elapsed_time(b) for a, b in ts) / 1e3
+        swa = [phs.Layer(q=L.q, out=L.out, ring=L.ring) for L in self.layers if L.ring is not None]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.phs.attn_decode_hybrid_stack(swa, w.Hq, self.sl, self.max_seq, ring_pos=self.rp,
+                                          do_append=False)
+        a.record()
+        for _ in range(reps):
+            self.phs.attn_decode_hybrid_stack(swa, w.Hq, self.sl, self.max_seq, ring_pos=self.rp,
+                                              do_append=False)
+        b.record()
+        torch.cuda.synchronize()
+        swa_s = a.elapsed_time(b) / 1e3 / reps
+        return split_s, swa_s
+
+    def cpu_baseline(self, budget_s=12.0):
+        import oracle
+        w = self.w
+        L = next(L for L in self.layers if L.paged is not None)
+        order = [int(b) for b in np.argsort(w.n_after)]
+        hk, bt = host_pages(L.paged.k, w.block_table, order[:1], w.n_after)
+        hv, _ = host_pages(L.paged.v, w.block_table, order[:1], w.n_after)
+        t0 = time.perf_counter()
+        oracle.decode_full_paged(synth.bits(L.q)[order[:1]], hk, hv, bt, w.n_after[order[:1]],
+                                 w.softmax_scale)
+        per_tok = (time.perf_counter() - t0) / float(w.n_after[order[0]])
+        rows = rows_for_budget(w.n_after, order, per_tok, budget_s)
+        hk, bt = host_pages(L.paged.k, w.block_table, rows, w.n_after)
+        hv, _ = host_pages(L.paged.v, w.block_table, rows, w.n_after)
+        t0 = time.perf_counter()
+        oracle.decode_full_paged(synth.bits(L.q)[rows], hk, hv, bt, w.n_after[rows],
+                                 w.softmax_scale)
+        t = time.perf_counter() - t0
+        toks = int(w.n_after[rows].sum())
+        return {"value": toks * w.Hkv * w.D * 4 / t / 1e9, "unit": "GB/s",
+                "tokens_per_s": toks / t, "cores": oracle.max_threads(), "kind": "oracle",
+                "sample": f"{len(rows)} of {w.B} requests of one Full layer ({toks} tokens), "
+                          f"fp64 oracle, {t:.2f} s"}
+
+
+class Int8Workload(Workload):
+    """Batch 32, 65,536 cached tokens: tokens [0, 64512) as INT8 (one fp32
+    absmax/127 scale per 32 tokens per KV head, quantised on the GPU at set
+    up), the last 1025 in bf16; K/V N(0,1) with 1% N(0, 8^2) outliers.  One
+    step = append into the bf16 tail + split-KV decode + merge."""
+
+    kernel_launches_per_step = 1
+
+    def __init__(self, device, seed=4):
+        import paged_hybrid_sliding_gb300 as phs
+        self.phs = phs
+        self.w = w = synth.int8_block32(seed=seed)
+        B, Hq, Hkv, D = w.B, w.Hq, w.Hkv, w.D
+        self.name = "int8_block32_b32_n65536_hot1024_hq32_hkv8_d128"
+        g = seed * 100
+        self.k = synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 1, device=device,
+                                   outlier_p=0.01)
+        self.v = synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 2, device=device,
+                                   outlier_p=0.01)
+        self.pool = phs.PagedPool(self.k, self.v)
+        self.qlen = w.extra["qlen"]
+        self.qt = torch.from_numpy(w.extra["qtable"]).to(device)
+        self.i8 = phs.Int8Pool.empty(w.extra["num_qpages"], Hkv, D, device=device)
+        self.bt = torch.from_numpy(w.block_table).to(device)
+        nqb = (self.qlen // 32).astype(np.int32)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        phs.kv_quant_int8_block32(self.pool, self.bt, self.i8, self.qt,
+                                  torch.zeros(B, dtype=torch.int32, device=device),
+                                  torch.from_numpy(nqb).to(device), int(nqb.max()))
+        b.record()
+        torch.cuda.synchronize()
+        qbytes = int(nqb.sum()) * 32 * Hkv * D * 2 * (2 + 1)
+        self.quant_setup = {"ms": round(a.elapsed_time(b), 3),
+                            "GB/s": round(qbytes / (a.elapsed_time(b) / 1e3) / 1e9, 1),
+                            "bytes": qbytes}
+        self.q = synth.normal_bf16((B, Hq, D), g + 3, device=device)
+        self.kn = synth.normal_bf16((B, Hkv, D), g + 4, device=device)
+        self.vn = synth.normal_bf16((B, Hkv, D), g + 5, device=device)
+        self.sl = torch.from_numpy(w.n_after).to(device)
+        self.ql = torch.from_numpy(self.qlen).to(device)
+        self.max_seq = int(w.n_after.max())
+        self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
+        self.tps = phs.decode_tokens_per_split(B, Hkv, self.max_seq)
+        self.ws = torch.empty(phs.decode_workspace_bytes(B, Hq, Hkv, D, self.max_seq, self.tps,
+                                                         has_int8=True),
+                              dtype=torch.uint8, device=device)
+        i8_tok = int(self.qlen.sum())
+        bf_tok = int((w.n_after - self.qlen).sum())
+        self.tokens_per_step = i8_tok + bf_tok
+        codes = i8_tok * Hkv * D * 2
+        scales = i8_tok // 32 * Hkv * 4 * 2
+        tail = bf_tok * Hkv * D * 2 * 2
+        tables = int(synth.pages_needed(w.n_after - self.qlen).sum()) * 4 + i8_tok // 32 * 4
+        self.kernel_bytes = codes + scales + tail + B * Hq * D * 2 + tables
+        self.bytes_per_step = self.kernel_bytes + B * Hq * D * 2 + 2 * B * Hkv * D * 2 * 2
+        self.launches_per_step = 3
+        self.extra = {"batch": B, "int8_tokens": i8_tok, "bf16_tokens": bf_tok,
+                      "codes_bytes": codes, "scale_bytes": scales, "bf16_tail_bytes": tail,
+                      "tokens_per_split": self.tps, "quantiser_setup": self.quant_setup}
+        self.host = [pinned(t) for t in (self.q, self.kn, self.vn, self.sl)]
+        self.dev_in = [self.q, self.kn, self.vn, self.sl]
+        self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
+        self.h2d_bytes = nbytes(*self.host)
+        self.d2h_bytes = nbytes(self.h_out)
+
+    def _decode(self, split_only=False):
+        phs = self.phs
+        if split_only:
+            phs.attn_decode_full_paged_split(self.q, self.pool, self.bt, self.sl, self.max_seq,
+                                             self.ws, self.out, int8=self.i8, qtable=self.qt,
+                                             qlens=self.ql, tokens_per_split=self.tps)
+        else:
+            phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl, self.max_seq,
+                                       int8=self.i8, qtable=self.qt, qlens=self.ql,
+                                       tokens_per_split=self.tps, out=self.out,
+                                       workspace=self.ws)
+
+    def step(self, ev=None):
+        self.phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl)
+        if ev is not None:
+            ev[0][0].record()
+        self._decode(split_only=True)
+        if ev is not None:
+            ev[0][1].record()
+        self.phs.attn_merge_splits(self.out, self.w.Hkv, self.sl, self.max_seq, self.ws,
+                                   qlens=self.ql, has_int8=True, tokens_per_split=self.tps)
+
+    def e2e_step(self):
+        for d, h in zip(self.dev_in, self.host):
+            d.copy_(h, non_blocking=True)
+        self.phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl)
+        self._decode()
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def cpu_baseline(self):
+        import oracle
+        w = self.w
+        rows = [0]
+        hk, bt = host_pages(self.k, w.block_table, rows, w.n_after)
+        hv, _ = host_pages(self.v, w.block_table, rows, w.n_after)
+        nq = int(self.qlen[0] // 32)
+        ids = self.qt[0, :nq].long()
+        i8 = dict(k_codes=self.i8.k.index_select(0, ids).cpu().numpy(),
+                  v_codes=self.i8.v.index_select(0, ids).cpu().numpy(),
+                  k_scale=self.i8.k_scale.index_select(0, ids).cpu().numpy(),
+                  v_scale=self.i8.v_scale.index_select(0, ids).cpu().numpy(),
+                  qtable=np.arange(nq, dtype=np.int32)[None], qlens=self.qlen[rows])
+        t0 = time.perf_counter()
+        oracle.decode_full_paged(synth.bits(self.q)[rows], hk, hv, bt, w.n_after[rows],
+                                 w.softmax_scale, int8=i8)
+        t = time.perf_counter() - t0
+        b = self.kernel_bytes / w.B
+        return {"value": b / t / 1e9, "unit": "GB/s", "tokens_per_s": float(w.n_after[0]) / t,
+                "cores": oracle.max_threads(), "kind": "oracle",
+                "sample": f"1 of {w.B} requests ({int(w.n_after[0])} tokens, INT8 + bf16 tail),"
+                          f" fp64 oracle, {t:.2f} s"}
+
+
+class SharedPrefixWorkload(Workload):
+    """64 requests sharing one 250,000-token prefix (15,625 pages, refcount
+    64) + a unique 512-token suffix each; 128 decode steps with append.  One
+    bench step = one decode step; the timed loop walks the 128 steps."""
+
+    kernel_launches_per_step = 1
+    l2 = "logical K/V bytes per step 65.7 GB >> L2; the shared prefix is reused through L2"
+
+    def __init__(self, device, seed=5):
+        import paged_hybrid_sliding_gb300 as phs
+        self.phs = phs
+        self.w = w = synth.shared_prefix(seed=seed)
+        B, Hq, Hkv, D = w.B, w.Hq, w.Hkv, w.D
+        self.name = "shared_prefix_250000_b64_suffix512_128steps_hq32_hkv8_d128"
+        g = seed * 100
+        self.k = synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 1, device=device)
+        self.v = synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 2, device=device)
+        self.pool = phs.PagedPool(self.k, self.v)
+        self.bt = torch.from_numpy(w.block_table).to(device)
+        self.rc = torch.from_numpy(w.extra["refcount"]).to(device)
+        self.nsteps = w.extra["steps"]
+        self.sls = [torch.from_numpy((w.n_pre + 1 + k).astype(np.int32)).to(device)
+                    for k in range(self.nsteps)]
+        self.q = synth.normal_bf16((B, Hq, D), g + 3, device=device)
+        self.kn = synth.normal_bf16((B, Hkv, D), g + 4, device=device)
+        self.vn = synth.normal_bf16((B, Hkv, D), g + 5, device=device)
+        self.max_seq = int(w.n_pre.max()) + self.nsteps
+        self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
+        self.tps = phs.decode_tokens_per_split(B, Hkv, self.max_seq)
+        self.ws = torch.empty(phs.decode_workspace_bytes(B, Hq, Hkv, D, self.max_seq, self.tps),
+                              dtype=torch.uint8, device=device)
+        self.k_idx = 0
+        mean_n = float(w.n_pre.mean()) + (self.nsteps + 1) / 2
+        tok_bytes = Hkv * D * 2 * 2
+        self.tokens_per_step = int(round(B * mean_n))
+        self.bytes_per_step = self.tokens_per_step * tok_bytes + 2 * B * Hq * D * 2 + \
+            2 * B * Hkv * D * 2 * 2
+        self.kernel_bytes = self.tokens_per_step * tok_bytes + B * Hq * D * 2
+        npref = w.extra["prefix_pages"]
+        unique_tok = npref * 16 + B * (float(w.n_pre.mean()) - npref * 16 + (self.nsteps + 1) / 2)
+        self.unique_bytes = int(unique_tok * tok_bytes)
+        self.launches_per_step = 3
+        self.extra = {"batch": B, "logical_bytes_per_step": self.bytes_per_step,
+                      "unique_kv_bytes_per_step": self.unique_bytes,
+                      "tokens_per_split": self.tps}
+        self.h_q, self.h_kn, self.h_vn = pinned(self.q), pinned(self.kn), pinned(self.vn)
+        self.h_sls = [pinned(s) for s in self.sls]
+        self.sl_in = torch.empty_like(self.sls[0])
+        self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
+        self.h2d_bytes = nbytes(self.h_q, self.h_kn, self.h_vn, self.h_sls[0])
+        self.d2h_bytes = nbytes(self.h_out)
+
+    def step(self, ev=None):
+        phs = self.phs
+        sl = self.sls[self.k_idx % self.nsteps]
+        self.k_idx += 1
+        phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, sl, page_refcount=self.rc)
+        if ev is not None:
+            ev[0][0].record()
+        phs.attn_decode_full_paged_split(self.q, self.pool, self.bt, sl, self.max_seq, self.ws,
+                                         self.out, tokens_per_split=self.tps)
+        if ev is not None:
+            ev[0][1].record()
+        phs.attn_merge_splits(self.out, self.w.Hkv, sl, self.max_seq, self.ws,
+                              tokens_per_split=self.tps)
+
+    def e2e_step(self):
+        k = self.k_idx % self.nsteps
+        self.k_idx += 1
+        for d, h in ((self.q, self.h_q), (self.kn, self.h_kn), (self.vn, self.h_vn),
+                     (self.sl_in, self.h_sls[k])):
+            d.copy_(h, non_blocking=True)
+        self.phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl_in,
+                                 page_refcount=self.rc)
+        self.phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl_in, self.max_seq,
+                                        out=self.out, tokens_per_split=self.tps,
+                                        workspace=self.ws)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def cpu_baseline(self):
+        import oracle
+        w = self.w
+        rows = [0]
+        n = w.n_pre + 1
+        hk, bt = host_pages(self.k, w.block_table, rows, n)
+        hv, _ = host_pages(self.v, w.block_table, rows, n)
+        t0 = time.perf_counter()
+        oracle.decode_full_paged(synth.bits(self.q)[rows], hk, hv, bt, n[rows], w.softmax_scale)
+        t = time.perf_counter() - t0
+        toks = int(n[0])
+        return {"value": toks * w.Hkv * w.D * 4 / t / 1e9, "unit": "GB/s",
+                "tokens_per_s": toks / t, "cores": oracle.max_threads(), "kind": "oracle",
+                "sample": f"1 of {w.B} requests of one step ({toks} tokens), fp64 oracle, "
+                          f"{t:.2f} s"}
+
+
+def make_workload(config, device, args):
+    if config == 1:
+        return TinyHybridWorkload(device)
+    if config == 2:
+        return PagedFullWorkload(device, batch=args.batch)
+    if config == 3:
+        return HybridStackWorkload(device, distinct=args.distinct_pools)
+    if config == 4:
+        return Int8Workload(device)
+    if config == 5:
+        return SharedPrefixWorkload(device)
+    raise ValueError(config)
 
 
 # ------------------------------------------------------------------ arms --
@@ -270,12 +750,11 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     import paged_hybrid_sliding_gb300 as phs
     phs.lib()
-    wl = PagedFullWorkload(device, batch=args.batch)
+    wl = make_workload(args.config, device, args)
     for _ in range(args.warmup):
         wl.step()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    evs = wl.new_events(args.steps)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
@@ -283,23 +762,30 @@ def run_gpu(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         start.record()
         for i in range(args.steps):
-            wl.step(evs[i])
+            wl.step(evs[i] if evs else None)
         stop.record()
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     t = start.elapsed_time(stop) / 1e3
-    split_t = statistics.fmean(a.elapsed_time(b) for a, b in evs) / 1e3
+    flat = [p for e in evs for p in e]
+    kernel_s = wl.kernel_seconds(flat)
     if world > 1:
         tt = torch.tensor([t], device=device)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         t = float(tt.item())
+    extra_kernels = {}
+    if isinstance(wl, HybridStackWorkload):
+        kernel_s, swa_s = wl.kernel_times()
+        extra_kernels["phs_swa_decode_kernel"] = {
+            "bytes_per_launch": wl.swa_bytes, "avg_launch_ms": round(swa_s * 1e3, 4),
+            "achieved_gbs": round(wl.swa_bytes / swa_s / 1e9, 1)}
 
     # end-to-end through the public API with host buffers
     for _ in range(3):
         wl.e2e_step()
     torch.cuda.synchronize()
-    e2e_steps = max(10, args.steps // 4)
+    e2e_steps = max(3, args.steps // 4)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         wl.e2e_step()
@@ -310,8 +796,6 @@ def run_gpu(args, rank, world, local_rank):
     peak, peak_kind = peaks()
     ms = t / args.steps * 1e3
     value = wl.bytes_per_step * args.steps * world / t / 1e9
-    achieved = wl.split_bytes / split_t / 1e9
-    traffic = recorded_traffic("phs_split_decode_kernel", wl.name)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -325,25 +809,33 @@ def run_gpu(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": wl.name, "batch": wl.w.B, "kv_tokens_per_step": wl.tokens_per_step,
-                   "bytes_per_step": wl.bytes_per_step, "tokens_per_split": wl.tps,
-                   "l2": "inputs larger than L2 (K/V read per step >> 129 MB)",
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": {"workload": wl.name, "kv_tokens_per_step": wl.tokens_per_step,
+                   "bytes_per_step": wl.bytes_per_step, "l2": wl.l2,
+                   "parallelism": "replicas" if world > 1 else "single", **wl.extra},
         "tokens_per_s": round(wl.tokens_per_step * args.steps * world / t, 1),
         "pct_of_peak": round(100 * value / world / peak, 2),
         "copy_gbs": round(copy_gbs, 1),
         "pct_of_copy": round(100 * value / world / copy_gbs, 2),
-        "roofline": {"bound": "hbm", "kernel": "phs_split_decode_kernel",
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "bytes_per_launch": wl.split_bytes,
-                     "avg_launch_ms": round(split_t * 1e3, 4), "traffic": traffic},
         "e2e": {"value": round(wl.bytes_per_step * e2e_steps * world / t_e2e / 1e9, 1),
                 "unit": "GB/s", "h2d_bytes_per_step": wl.h2d_bytes,
                 "d2h_bytes_per_step": wl.d2h_bytes, "steps": e2e_steps},
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if isinstance(wl, TinyHybridWorkload):
+        line["us_per_step"] = round(ms * 1e3, 2)
+    if kernel_s is not None and wl.kernel_bytes:
+        achieved = wl.kernel_bytes / kernel_s / 1e9
+        line["roofline"] = {
+            "bound": "hbm", "kernel": wl.kernel, "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+            "bytes_per_launch": wl.kernel_bytes, "avg_launch_ms": round(kernel_s * 1e3, 4),
+            "traffic": recorded_traffic(wl.kernel, wl.name)}
+        if isinstance(wl, SharedPrefixWorkload):
+            line["roofline"]["bytes_are"] = "logical (prefix pages reused through L2)"
+            line["roofline"]["unique_kv_gbs"] = round(wl.unique_bytes / kernel_s / 1e9, 1)
+    if extra_kernels:
+        line["other_kernels"] = extra_kernels
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = wl.cpu_baseline()
     return line
@@ -416,6 +908,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=64,
                     help="requests in the paged workload (64 = the benchmark case)")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
+                    help="1 tiny hybrid, 2 paged Full batch 64 (default), 3 70-layer hybrid "
+                         "stack, 4 INT8 block-32, 5 shared 250K prefix")
+    ap.add_argument("--distinct-pools", type=int, default=4,
+                    help="config 3: distinct 37.6 GB Full pools allocated (layers alias them)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -184,6 +184,7 @@ int make_plan(DecodePlan& pl, int B, int Hq, int Hkv, int D, int max_seq, int tp
   pl.D = D;
   pl.Hkv = Hkv;
   pl.has_int8 = has_int8;
+  if (pl.max_splits > 65535) return PHS_EUNSUPPORTED;  // grid z limit
   pl.need = ws_bytes(B, Hkv, pl.max_splits, pl.G, D);
   return PHS_OK;
 }

@@ -70,7 +70,9 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
 
-  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // request index fastest: CTAs that read the same shared-prefix pages for
+  // different requests run close together in time and share them through L2
+  const int b = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
 
@@ -281,9 +283,15 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
 }
 
 // Cross-split log-sum-exp merge for requests with more than one split.
+// One CTA per (request, KV head); warp w merges query rows w, w+4, ...  The
+// lanes first reduce (max m, sum l) over the splits in parallel, then each
+// lane accumulates D/32 output columns over the splits with independent
+// vector loads.
 template <int D>
 __global__ void __launch_bounds__(128) phs_merge_kernel(const MergeArgs a) {
-  const int h = blockIdx.x, b = blockIdx.y;
+  constexpr int V = D / 32;  // columns per lane (4 or 2)
+  const int h = blockIdx.y, b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
   const int n = min(a.seq_lens[b], a.n_clamp);
   const int qlen = a.qlens ? a.qlens[b] : 0;
@@ -291,18 +299,50 @@ __global__ void __launch_bounds__(128) phs_merge_kernel(const MergeArgs a) {
   if (ns <= 1) return;
   const size_t part0 = (static_cast<size_t>(b) * a.Hkv + h) * a.max_splits;
   const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
-  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-    const int row = e / D, d = e % D;
+  for (int row = warp; row < G; row += 4) {
+    const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + part0 * G + row;
     float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, a.ws_ml[((part0 + s) * G + row) * 2]);
-    float Lsum = 0.f, O = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const float ms = a.ws_ml[((part0 + s) * G + row) * 2];
-      const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
-      Lsum += a.ws_ml[((part0 + s) * G + row) * 2 + 1] * f;
-      O += a.ws_o[((part0 + s) * G + row) * D + d] * f;
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, ml[static_cast<size_t>(s) * G].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float Lsum = 0.f;
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    const float* ob = a.ws_o + (part0 * G + row) * D + lane * V;
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      // weight of split s0 + lane, then broadcast one split at a time
+      float wl = 0.f;
+      if (s0 + lane < ns) {
+        const float2 v = ml[static_cast<size_t>(s0 + lane) * G];
+        wl = v.x == -INFINITY ? 0.f : exp2f(v.x - M);
+        Lsum += v.y * wl;
+      }
+      const int cnt = min(32, ns - s0);
+#pragma unroll 4
+      for (int k = 0; k < cnt; ++k) {
+        const float w = __shfl_sync(0xffffffffu, wl, k);
+        const float* src = ob + static_cast<size_t>(s0 + k) * G * D;
+        if constexpr (V == 4) {
+          const float4 o = *reinterpret_cast<const float4*>(src);
+          acc[0] += w * o.x;
+          acc[1] += w * o.y;
+          acc[2] += w * o.z;
+          acc[3] += w * o.w;
+        } else {
+          const float2 o = *reinterpret_cast<const float2*>(src);
+          acc[0] += w * o.x;
+          acc[1] += w * o.y;
+        }
+      }
     }
-    store_out(a.out, out_row0 + e, Lsum > 0.f ? O / Lsum : 0.f, a.out_f32);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      store_out(a.out, out_row0 + static_cast<size_t>(row) * D + lane * V + i, acc[i] * inv,
+                a.out_f32);
   }
 }
 
@@ -314,7 +354,7 @@ static int launch_split_t(const CUtensorMap& tk, const CUtensorMap& tv, const CU
   const int smem = SplitLayout<D>::kAlloc;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return PHS_ECUDA;
-  dim3 grid(a.max_splits, a.Hkv, B);
+  dim3 grid(B, a.Hkv, a.max_splits);
   kern<<<grid, kSplitWarps * 32, smem, stream>>>(tk, tv, tk8, tv8, a);
   return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
 }
@@ -335,7 +375,7 @@ int launch_split_decode(int D, const CUtensorMap& tk, const CUtensorMap& tv,
 }
 
 int launch_merge(int D, const MergeArgs& a, int B, cudaStream_t stream) {
-  dim3 grid(a.Hkv, B);
+  dim3 grid(B, a.Hkv);
   if (D == 128)
     phs_merge_kernel<128><<<grid, 128, 0, stream>>>(a);
   else if (D == 64)
