@@ -367,13 +367,18 @@ class HybridStackWorkload(Workload):
 
     kernel_launches_per_step = 0
 
-    def __init__(self, device, seed=3, distinct=4):
+    def __init__(self, device, seed=3, distinct=4, batch=256, swa_only=False):
         import paged_hybrid_sliding_gb300 as phs
         self.phs = phs
-        self.w = w = synth.hybrid_stack(seed=seed)
+        self.w = w = synth.hybrid_stack(seed=seed, B=batch)
         B, Hq, Hkv, D, W = w.B, w.Hq, w.Hkv, w.D, w.W
         lf = w.extra["layer_is_full"]
-        self.name = "hybrid_stack_70l_10full_60swa_w128_b256_hq32_hkv8_d128_seqlogU[4K,128K]"
+        if swa_only:
+            lf = np.zeros_like(lf)[:60]
+            distinct = 0
+        self.swa_only = swa_only
+        self.name = (f"hybrid_stack_70l_10full_60swa_w128_b{B}_hq32_hkv8_d128_seqlogU[4K,128K]"
+                     if not swa_only else f"swa_60l_w128_b{B}_hq32_hkv8_d128")
         g = seed * 1000
         self.pools = [phs.PagedPool(
             synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 10 * i + 1, device=device),
@@ -418,14 +423,17 @@ class HybridStackWorkload(Workload):
         self.full_layer_bytes = full_tok * tok_bytes + B * Hq * D * 2 + \
             int(synth.pages_needed(w.n_after).sum()) * 4
         self.swa_bytes = nswa * (swa_tok * tok_bytes + B * Hq * D * 2)
-        self.kernel_bytes = self.full_layer_bytes
-        self.launches_per_step = 2 + 1 + 2 * nfull
+        self.kernel_bytes = self.full_layer_bytes if nfull else self.swa_bytes
+        if not nfull:
+            self.kernel = "phs_swa_decode_kernel"
+        self.launches_per_step = (2 if nfull else 1) + 1 + 2 * nfull
         self.extra = {"batch": B, "layers": f"{nfull} Full + {nswa} SWA(W=128)",
                       "distinct_full_pools": distinct, "full_layers_aliased_onto": distinct,
                       "full_bytes_per_step": nfull * self.full_layer_bytes,
-                      "swa_bytes_per_step": self.swa_bytes,
-                      "kv_tokens_stored_ratio_vs_all_full":
-                          round((nfull * full_tok + nswa * swa_tok) / (len(lf) * full_tok), 4)}
+                      "swa_bytes_per_step": self.swa_bytes}
+        if nfull:
+            self.extra["kv_tokens_stored_ratio_vs_all_full"] = round(
+                (nfull * full_tok + nswa * swa_tok) / (len(lf) * full_tok), 4)
         self.h2d_bytes = nbytes(*self.host)
         self.d2h_bytes = nbytes(*self.h_outs)
 
@@ -447,6 +455,8 @@ class HybridStackWorkload(Workload):
         phs = self.phs
         w = self.w
         full = [L for L in self.layers if L.paged is not None]
+        if not full:
+            return None, self._swa_time(reps)
         ts = []
         for _ in range(reps):
             for L in full:
@@ -458,7 +468,12 @@ class HybridStackWorkload(Workload):
                 ts.append((a, b))
         torch.cuda.synchronize()
         split_s = statistics.fmean(a.elapsed_time(b) for a, b in ts) / 1e3
-        swa = [phs.Layer(q=L.q, out=L.out, ring=L.ring) for L in self.layers if L.ring is not None]
+        return split_s, self._swa_time(reps)
+
+    def _swa_time(self, reps):
+        w = self.w
+        swa = [self.phs.Layer(q=L.q, out=L.out, ring=L.ring) for L in self.layers
+               if L.ring is not None]
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         self.phs.attn_decode_hybrid_stack(swa, w.Hq, self.sl, self.max_seq, ring_pos=self.rp,
                                           do_append=False)
@@ -468,12 +483,13 @@ class HybridStackWorkload(Workload):
                                               do_append=False)
         b.record()
         torch.cuda.synchronize()
-        swa_s = a.elapsed_time(b) / 1e3 / reps
-        return split_s, swa_s
+        return a.elapsed_time(b) / 1e3 / reps
 
     def cpu_baseline(self, budget_s=12.0):
         import oracle
         w = self.w
+        if self.swa_only:
+            return self._cpu_baseline_swa()
         L = next(L for L in self.layers if L.paged is not None)
         order = [int(b) for b in np.argsort(w.n_after)]
         hk, bt = host_pages(L.paged.k, w.block_table, order[:1], w.n_after)
@@ -496,6 +512,21 @@ class HybridStackWorkload(Workload):
                           f"fp64 oracle, {t:.2f} s"}
 
 
+    def _cpu_baseline_swa(self):
+        import oracle
+        w = self.w
+        L = next(L for L in self.layers if L.ring is not None)
+        kr, vr, q = synth.bits(L.ring.k), synth.bits(L.ring.v), synth.bits(L.q)
+        t0 = time.perf_counter()
+        oracle.decode_swa_ring(q, kr, vr, None, w.ring_pos, w.n_after, w.softmax_scale)
+        t = time.perf_counter() - t0
+        toks = int(np.minimum(w.n_after, w.W).sum())
+        return {"value": toks * w.Hkv * w.D * 4 / t / 1e9, "unit": "GB/s",
+                "tokens_per_s": toks / t, "cores": oracle.max_threads(), "kind": "oracle",
+                "sample": f"one SWA layer, all {w.B} requests ({toks} tokens), fp64 oracle, "
+                          f"{t:.2f} s"}
+
+
 class Int8Workload(Workload):
     """Batch 32, 65,536 cached tokens: tokens [0, 64512) as INT8 (one fp32
     absmax/127 scale per 32 tokens per KV head, quantised on the GPU at set
@@ -504,12 +535,12 @@ class Int8Workload(Workload):
 
     kernel_launches_per_step = 1
 
-    def __init__(self, device, seed=4):
+    def __init__(self, device, seed=4, batch=32):
         import paged_hybrid_sliding_gb300 as phs
         self.phs = phs
-        self.w = w = synth.int8_block32(seed=seed)
+        self.w = w = synth.int8_block32(seed=seed, B=batch)
         B, Hq, Hkv, D = w.B, w.Hq, w.Hkv, w.D
-        self.name = "int8_block32_b32_n65536_hot1024_hq32_hkv8_d128"
+        self.name = f"int8_block32_b{B}_n65536_hot1024_hq32_hkv8_d128"
         g = seed * 100
         self.k = synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 1, device=device,
                                    outlier_p=0.01)
@@ -715,11 +746,12 @@ def make_workload(config, device, args):
     if config == 1:
         return TinyHybridWorkload(device)
     if config == 2:
-        return PagedFullWorkload(device, batch=args.batch)
+        return PagedFullWorkload(device, batch=args.batch or 64)
     if config == 3:
-        return HybridStackWorkload(device, distinct=args.distinct_pools)
+        return HybridStackWorkload(device, distinct=args.distinct_pools,
+                                   batch=args.batch or 256, swa_only=args.swa_only)
     if config == 4:
-        return Int8Workload(device)
+        return Int8Workload(device, batch=args.batch or 32)
     if config == 5:
         return SharedPrefixWorkload(device)
     raise ValueError(config)
@@ -777,9 +809,13 @@ def run_gpu(args, rank, world, local_rank):
     extra_kernels = {}
     if isinstance(wl, HybridStackWorkload):
         kernel_s, swa_s = wl.kernel_times()
-        extra_kernels["phs_swa_decode_kernel"] = {
-            "bytes_per_launch": wl.swa_bytes, "avg_launch_ms": round(swa_s * 1e3, 4),
-            "achieved_gbs": round(wl.swa_bytes / swa_s / 1e9, 1)}
+        if kernel_s is None:
+            kernel_s = swa_s
+        else:
+            extra_kernels["phs_swa_decode_kernel"] = {
+                "bytes_per_launch": wl.swa_bytes, "avg_launch_ms": round(swa_s * 1e3, 4),
+                "achieved_gbs": round(wl.swa_bytes / swa_s / 1e9, 1),
+                "frac": round(wl.swa_bytes / swa_s / 1e9 / peaks()[0], 4)}
 
     # end-to-end through the public API with host buffers
     for _ in range(3):
@@ -906,8 +942,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="phs", choices=["phs", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--batch", type=int, default=64,
-                    help="requests in the paged workload (64 = the benchmark case)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="requests (0 = the workload's own batch: 64 / 256 / 32 for configs "
+                         "2 / 3 / 4); smaller batches are for profiler captures")
+    ap.add_argument("--swa-only", action="store_true",
+                    help="config 3: only the 60 SWA layers (profiler captures)")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
                     help="1 tiny hybrid, 2 paged Full batch 64 (default), 3 70-layer hybrid "
                          "stack, 4 INT8 block-32, 5 shared 250K prefix")

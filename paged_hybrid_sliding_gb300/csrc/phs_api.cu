@@ -508,7 +508,7 @@ int phs_attn_decode_swa_ring(const void* q, int32_t num_q_heads, const phs_ring_
   p.W = ring->window;
   p.out_f32 = out_dtype == PHS_OUT_F32;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
-  return launch_swa_decode<1>(D, p, di.sms, reinterpret_cast<cudaStream_t>(stream));
+  return launch_swa_decode<1>(D, p, di.sms, di.smem_optin, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t phs_hybrid_stack_workspace_bytes(int32_t batch, int32_t num_q_heads,
@@ -628,11 +628,11 @@ int phs_attn_decode_hybrid_stack(const phs_layer* layers, int32_t num_layers,
       p->out[k] = L.out;
       p->num_rings[k] = L.ring.num_rings;
       if (++p->num_layers == kSwaMaxLayers) {
-        st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, s);
+        st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, di.smem_optin, s);
         p->num_layers = 0;
       }
     }
-    if (st == PHS_OK && p->num_layers) st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, s);
+    if (st == PHS_OK && p->num_layers) st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, di.smem_optin, s);
     delete p;
     if (st) return st;
   }

@@ -33,31 +33,69 @@ struct ChunkGeom {
   static constexpr int kI8RowBytes = D;           // INT8 row = D bytes
 };
 
+// Per-lane shared-memory offsets of the mma fragments inside a staged chunk,
+// computed once per warp.  Stage bases are 1024-byte aligned and the
+// swizzle only permutes 16-byte units inside 1024-byte blocks, so the
+// address of fragment step i is (stage + lane offset) ^ (constant of i) + an
+// immediate: one logic op per fragment load instead of the full swizzle.
+struct FragOffsets {
+  uint32_t bk, bv;        // bf16 chunk: K (ldmatrix) and V (ldmatrix.trans)
+  uint32_t ik, iv0, iv1;  // INT8 chunk: K (ldmatrix), V rows 2q+{0,8} and 2q+{1,9}
+
+  template <int D>
+  __device__ __forceinline__ void init(int lane) {
+    const int mi = lane >> 3, r = lane & 7, g = lane >> 2, qd = lane & 3;
+    // bf16 K: matrix mi = (tokens 8*(mi>>1).., 16-byte unit 2ks + (mi&1))
+    bk = (r + ((mi >> 1) << 3)) * 128 + ((((mi & 1) ^ r) & 7) << 4);
+    // bf16 V (transposed): (tokens 8*(mi&1).., unit 2np + (mi>>1))
+    bv = (r + ((mi & 1) << 3)) * 128 + ((((mi >> 1) ^ r) & 7) << 4);
+    const int gh = g >> 2, inner = (g & 3) * 4;
+    if constexpr (D == 128) {
+      // INT8 K rows of 128 bytes: row 8nt + r, unit 4hq + mi
+      ik = r * 128 + (((mi ^ r) & 7) << 4);
+      // INT8 V rows 2qd (+8) and 2qd+1 (+9), unit 2J + gh, byte 4*(g&3)
+      iv0 = (2 * qd) * 128 + (((gh ^ (2 * qd)) & 7) << 4) + inner;
+      iv1 = (2 * qd + 1) * 128 + (((gh ^ (2 * qd + 1)) & 7) << 4) + inner;
+    } else {
+      // 64-byte rows, 64-byte swizzle: unit ^= (row >> 1) & 3
+      ik = r * 64 + (((mi ^ (r >> 1)) & 3) << 4);
+      iv0 = (2 * qd) * 64 + (((gh ^ qd) & 3) << 4) + inner;
+      iv1 = (2 * qd + 1) * 64 + (((gh ^ qd) & 3) << 4) + inner;
+    }
+  }
+};
+
 // Running state of one warp's softmax reduction.  Rows g (and g+8 when the
 // group exceeds 8 heads) are this lane's query heads; the lane holds the
 // output columns of its accumulator fragments.
 template <int D, bool TWO>
 struct WarpState {
-  float o[D / 8][4];  // bf16-path layout: o[nt][0..1] = (row g, d 8nt+2q..+1)
+  static constexpr int R = TWO ? 4 : 2;  // accumulators kept per mma tile
+  float o[D / 8][R];  // bf16-path layout: o[nt][0..1] = (row g, d 8nt+2q..+1)
   float m[2];         // running max (log2 domain), rows g and g+8
   float l[2];         // this lane's partial sum of exp2 (quad-reduced at the end)
   float u;            // INT8 path: output is stored divided by this V scale
+  float lu;           // log2(u)
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+      for (int r = 0; r < R; ++r) o[i][r] = 0.f;
     m[0] = m[1] = -INFINITY;
     l[0] = l[1] = 0.f;
     u = 1.f;
+    lu = 0.f;
   }
 };
 
 // Q fragments of the group for the bf16 path (standard k order) and for the
 // INT8 path (f16, k order matching the ldmatrix layout of 8-bit rows, see
-// consume_i8).  Rows >= G are zero.
+// qk_i8).  Rows >= G are zero.
 template <int D, bool TWO>
 struct QFrags {
   uint32_t a[D / 16][4];
+  float qsum[2];  // INT8 path: sum over d of the f16 queries, rows g, g+8
 };
 
 template <int D, bool TWO>
@@ -105,26 +143,37 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 // INT8 path: A fragment for k-step ks holds physical columns
-// 16ks + 4q .. 16ks + 4q + 3 of each row (see consume_i8).
+// 16ks + 4q .. 16ks + 4q + 3 of each row (see qk_i8).  Also forms the
+// row sums of the f16 queries, which remove the code bias from the scores.
+__device__ __forceinline__ float f16x2_sum(uint32_t w) {
+  const float2 f = __half22float2(*reinterpret_cast<__half2*>(&w));
+  return f.x + f.y;
+}
+
 template <int D, bool TWO>
 __device__ __forceinline__ void load_q_f16_i8order(QFrags<D, TWO>& f, const __nv_bfloat16* q,
                                                    int G, int lane) {
   const int g = lane >> 2, qd = lane & 3;
   const uint2* q64 = reinterpret_cast<const uint2*>(q);
+  float s0 = 0.f, s1 = 0.f;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     const int c = 16 * ks + 4 * qd;  // 4 consecutive columns, 8 bytes
     uint2 w0 = g < G ? __ldg(q64 + (g * D + c) / 4) : make_uint2(0, 0);
     f.a[ks][0] = bf16x2_to_f16x2(w0.x);
     f.a[ks][2] = bf16x2_to_f16x2(w0.y);
+    s0 += f16x2_sum(f.a[ks][0]) + f16x2_sum(f.a[ks][2]);
     if (TWO) {
       uint2 w1 = g + 8 < G ? __ldg(q64 + ((g + 8) * D + c) / 4) : make_uint2(0, 0);
       f.a[ks][1] = bf16x2_to_f16x2(w1.x);
       f.a[ks][3] = bf16x2_to_f16x2(w1.y);
+      s1 += f16x2_sum(f.a[ks][1]) + f16x2_sum(f.a[ks][3]);
     } else {
       f.a[ks][1] = f.a[ks][3] = 0u;
     }
   }
+  f.qsum[0] = warp_sum_quad(s0);
+  f.qsum[1] = warp_sum_quad(s1);
 }
 
 // Zero the V rows of tokens whose bit in `valid` is clear, so that
@@ -145,59 +194,98 @@ __device__ __forceinline__ void zero_invalid_v_rows(uint8_t* sV, uint32_t valid,
   }
 }
 
-// Online-softmax update of one row given this lane's scores x[] (already in
-// the log2 domain, -inf where masked).  Returns the rescale factor for the
-// running output and writes p[] in place.
+// Online-softmax update of one row from this lane's raw scores s[] (-inf
+// where masked).  Log2-domain score: x = s * sl - off (sl > 0).  Writes
+// p = 2^(x - m_new + lr) into s[] (lr = log2 of a factor folded into P),
+// adds sum(p) * inv_ratio to the lane's running sum l and returns the
+// rescale factor 2^(m_old - m_new) of the running output.
 template <int N>
-__device__ __forceinline__ float softmax_row_update(float (&x)[N], float& m, float& l) {
-  float mx = x[0];
+__device__ __forceinline__ float softmax_row_update(float (&s)[N], float sl, float off, float lr,
+                                                    float inv_ratio, float& m, float& l) {
+  float mx = s[0];
 #pragma unroll
-  for (int i = 1; i < N; ++i) mx = fmaxf(mx, x[i]);
+  for (int i = 1; i < N; ++i) mx = fmaxf(mx, s[i]);
+  mx = mx == -INFINITY ? -INFINITY : mx * sl - off;
   mx = warp_max_quad(mx);
   const float m_new = fmaxf(m, mx);
   // all scores seen so far masked: keep the state, contribute nothing
   const float m_use = m_new == -INFINITY ? 0.f : m_new;
-  const float alpha = exp2f(m - m_use);
-  float s = 0.f;
+  const float alpha = ex2(m - m_use);
+  const float c = off + m_use - lr;
+  float sum = 0.f;
 #pragma unroll
   for (int i = 0; i < N; ++i) {
-    x[i] = exp2f(x[i] - m_use);
-    s += x[i];
+    s[i] = ex2(fmaf(s[i], sl, -c));
+    sum += s[i];
   }
-  l = l * alpha + s;
+  l = l * alpha + sum * inv_ratio;
   m = m_new;
   return alpha;
+}
+
+// Rescale the running output of row half rh by alpha, skipped when no row
+// of the warp changed its maximum (the common case once the row max has
+// settled).
+template <int D, int R>
+__device__ __forceinline__ void rescale_rows(float (&o)[D / 8][R], int rh, float alpha) {
+  if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      o[nt][2 * rh] *= alpha;
+      o[nt][2 * rh + 1] *= alpha;
+    }
+  }
 }
 
 // ----------------------------------------------------------------------
 // One 16-token bf16 chunk: K tile at sK, V tile at sV (each D/64 swizzled
 // 16 x 64 boxes of 2 KB).  valid: bit t set if token t of the chunk is part
-// of the sequence.
+// of the sequence.  Three phases so that a caller can overlap the score
+// contraction of the next chunk with the output update of the current one:
+//   qk_bf16 (S = Q K^T), softmax_bf16 (online softmax, returns P), pv_bf16.
 // ----------------------------------------------------------------------
 template <int D, bool TWO>
-__device__ __forceinline__ void consume_bf16(WarpState<D, TWO>& st, const QFrags<D, TWO>& qf,
-                                             uint32_t sK, uint32_t sV, uint32_t valid,
-                                             float scale_log2, int lane) {
-  const int qd = lane & 3;
-  const int mi = lane >> 3, r = lane & 7;
-  // ---- S = Q K^T : two n-tiles of 8 tokens, two accumulation chains
-  float s0[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  float s1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  {
-    const int tok = r + ((mi >> 1) << 3);  // matrices 2,3 -> tokens 8..15
+struct ScoresBf16 {
+  float s[2][WarpState<D, TWO>::R];  // n-tiles of 8 tokens
+};
+
+template <int D, bool TWO>
+__device__ __forceinline__ void qk_bf16(ScoresBf16<D, TWO>& sc, const QFrags<D, TWO>& qf,
+                                        const FragOffsets& fo, uint32_t sK) {
+  constexpr int R = WarpState<D, TWO>::R;
+  float s1[2][R];  // second accumulation chain (odd k-steps)
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      const int c16 = 2 * ks + (mi & 1);   // 16-byte column unit
-      const uint32_t addr = sK + (c16 >> 3) * 2048 + swz128(tok * 128 + (c16 & 7) * 16);
-      uint32_t b00, b01, b10, b11;
-      ldsm_x4(addr, b00, b01, b10, b11);
-      float(&acc)[2][4] = (ks & 1) ? s1 : s0;
-      mma_bf16(acc[0], qf.a[ks][0], qf.a[ks][1], qf.a[ks][2], qf.a[ks][3], b00, b01);
-      mma_bf16(acc[1], qf.a[ks][0], qf.a[ks][1], qf.a[ks][2], qf.a[ks][3], b10, b11);
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int r = 0; r < R; ++r) sc.s[i][r] = s1[i][r] = 0.f;
+  const uint32_t kbase = sK + fo.bk;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    // 16-byte unit 2ks + (mi&1) of the (ks/4)-th 64-column box
+    const uint32_t addr = (kbase ^ (((2 * ks) & 7) << 4)) + (ks >> 2) * 2048;
+    uint32_t b00, b01, b10, b11;
+    ldsm_x4(addr, b00, b01, b10, b11);
+    if (ks & 1) {
+      mma_bf16(s1[0], qf.a[ks][0], qf.a[ks][1], qf.a[ks][2], qf.a[ks][3], b00, b01);
+      mma_bf16(s1[1], qf.a[ks][0], qf.a[ks][1], qf.a[ks][2], qf.a[ks][3], b10, b11);
+    } else {
+      mma_bf16(sc.s[0], qf.a[ks][0], qf.a[ks][1], qf.a[ks][2], qf.a[ks][3], b00, b01);
+      mma_bf16(sc.s[1], qf.a[ks][0], qf.a[ks][1], qf.a[ks][2], qf.a[ks][3], b10, b11);
     }
   }
-  // ---- online softmax, rows g (and g+8)
-  uint32_t pa[2][2];  // P as bf16 A fragments: [row half][k half]
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int r = 0; r < R; ++r) sc.s[i][r] += s1[i][r];
+}
+
+// P as bf16 A fragments: pa[row half][k half]
+template <int D, bool TWO>
+__device__ __forceinline__ void softmax_bf16(WarpState<D, TWO>& st, ScoresBf16<D, TWO>& sc,
+                                             uint32_t (&pa)[2][2], uint32_t valid,
+                                             float scale_log2, int lane) {
+  constexpr int R = WarpState<D, TWO>::R;
+  const int qd = lane & 3;
 #pragma unroll
   for (int rh = 0; rh < (TWO ? 2 : 1); ++rh) {
     float x[4];
@@ -206,102 +294,130 @@ __device__ __forceinline__ void consume_bf16(WarpState<D, TWO>& st, const QFrags
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int t = 8 * nt + 2 * qd + e;
-        const float v = (s0[nt][2 * rh + e] + s1[nt][2 * rh + e]) * scale_log2;
-        x[2 * nt + e] = ((valid >> t) & 1u) ? v : -INFINITY;
+        x[2 * nt + e] = ((valid >> t) & 1u) ? sc.s[nt][2 * rh + e] : -INFINITY;
       }
-    const float alpha = softmax_row_update(x, st.m[rh], st.l[rh]);
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-      st.o[nt][2 * rh] *= alpha;
-      st.o[nt][2 * rh + 1] *= alpha;
-    }
+    const float alpha = softmax_row_update(x, scale_log2, 0.f, 0.f, 1.f, st.m[rh], st.l[rh]);
+    rescale_rows<D, R>(st.o, rh, alpha);
     pa[rh][0] = pack_bf16(x[0], x[1]);
     pa[rh][1] = pack_bf16(x[2], x[3]);
   }
   if (!TWO) pa[1][0] = pa[1][1] = 0u;
-  // ---- O += P V : V^T fragments through ldmatrix.trans
-  {
-    const int tok = r + ((mi & 1) << 3);
+}
+
+// O += P V : V^T fragments through ldmatrix.trans
+template <int D, bool TWO>
+__device__ __forceinline__ void pv_bf16(WarpState<D, TWO>& st, const uint32_t (&pa)[2][2],
+                                        const FragOffsets& fo, uint32_t sV) {
+  const uint32_t vbase = sV + fo.bv;
 #pragma unroll
-    for (int np = 0; np < D / 16; ++np) {
-      const int c16 = 2 * np + (mi >> 1);
-      const uint32_t addr = sV + (c16 >> 3) * 2048 + swz128(tok * 128 + (c16 & 7) * 16);
-      uint32_t v0, v1, v2, v3;
-      ldsm_x4_t(addr, v0, v1, v2, v3);
-      mma_bf16(st.o[2 * np], pa[0][0], pa[1][0], pa[0][1], pa[1][1], v0, v1);
-      mma_bf16(st.o[2 * np + 1], pa[0][0], pa[1][0], pa[0][1], pa[1][1], v2, v3);
-    }
+  for (int np = 0; np < D / 16; ++np) {
+    const uint32_t addr = (vbase ^ (((2 * np) & 7) << 4)) + (np >> 2) * 2048;
+    uint32_t v0, v1, v2, v3;
+    ldsm_x4_t(addr, v0, v1, v2, v3);
+    mma_bf16(st.o[2 * np], pa[0][0], pa[1][0], pa[0][1], pa[1][1], v0, v1);
+    mma_bf16(st.o[2 * np + 1], pa[0][0], pa[1][0], pa[0][1], pa[1][1], v2, v3);
   }
+}
+
+template <int D, bool TWO>
+__device__ __forceinline__ void consume_bf16(WarpState<D, TWO>& st, const QFrags<D, TWO>& qf,
+                                             const FragOffsets& fo, uint32_t sK, uint32_t sV,
+                                             uint32_t valid, float scale_log2, int lane) {
+  ScoresBf16<D, TWO> sc;
+  uint32_t pa[2][2];
+  qk_bf16(sc, qf, fo, sK);
+  softmax_bf16(st, sc, pa, valid, scale_log2, lane);
+  pv_bf16(st, pa, fo, sV);
 }
 
 // ----------------------------------------------------------------------
 // One 32-token INT8 chunk: K codes at sK, V codes at sV, each a 32 x D int8
 // tile (128-byte swizzle for D = 128, 64-byte swizzle for D = 64).  Scores
-// use f16 mma on the exact integer codes; the K scale is folded into the
-// score multiplier and the V scale into the output's storage scale st.u,
-// so the only rounding beyond the bf16 path is P in f16.
-// The output accumulator uses the INT8 column order: o[4J + e][0..1] hold
-// columns 32J + 8q + e and 32J + 8q + 4 + e of rows g (g+8).
+// use f16 mma on the integer codes (exact in f16); the K scale is folded
+// into the score multiplier and the V scale into P (see softmax_i8), so the
+// only rounding beyond the bf16 path is P in f16.  The output accumulator
+// uses the INT8 column order: o[4J + e][0..1] hold columns 32J + 8q + e and
+// 32J + 8q + 4 + e of rows g (g+8).  Phases as for bf16 chunks.
 // ----------------------------------------------------------------------
-template <int D>
-__device__ __forceinline__ uint32_t i8_off(int row, int c16) {
-  if constexpr (D == 128) {
-    return swz128(row * 128 + c16 * 16);
-  } else {
-    return swz64(row * 64 + c16 * 16);
-  }
-}
+template <int D, bool TWO>
+struct ScoresI8 {
+  float s[4][WarpState<D, TWO>::R];  // n-tiles of 8 tokens
+};
 
 template <int D, bool TWO>
-__device__ __forceinline__ void consume_i8(WarpState<D, TWO>& st, const QFrags<D, TWO>& qf,
-                                           uint32_t sK, uint32_t sV, float k_scale,
-                                           float v_scale, float scale_log2, int lane) {
-  const int g = lane >> 2, qd = lane & 3;
-  const int mi = lane >> 3, r = lane & 7;
+__device__ __forceinline__ void qk_i8(ScoresI8<D, TWO>& sc, const QFrags<D, TWO>& qf,
+                                      const FragOffsets& fo, uint32_t sK) {
   constexpr int KS = D / 16;  // k-steps over the head dim
-  // ---- S = Q K^T over 4 n-tiles of 8 tokens
-  float s[4][4];
+  constexpr int R = WarpState<D, TWO>::R;
+  // S = Q (K + 1152): the codes enter the mma biased (exact in f16, one
+  // fewer instruction per pair); softmax_i8 removes 1152 * sum(q)
+  const uint32_t kbase = sK + fo.ik;
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt) {
-    s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-    float s2[4] = {0.f, 0.f, 0.f, 0.f};
+    float s2[R];
+#pragma unroll
+    for (int e = 0; e < R; ++e) sc.s[nt][e] = s2[e] = 0.f;
 #pragma unroll
     for (int hq = 0; hq < KS / 4; ++hq) {
       // matrix mi = 16-byte column unit 4hq + mi of rows 8nt .. 8nt+7
-      const uint32_t addr = sK + i8_off<D>(8 * nt + r, 4 * hq + mi);
+      const uint32_t addr = (kbase ^ (hq << 6)) + nt * 8 * D;
       uint32_t w[4];
       ldsm_x4(addr, w[0], w[1], w[2], w[3]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int ks = 4 * hq + i;
         uint32_t b0, b1;
-        i8x4_to_f16x2x2(w[i], b0, b1);
-        float(&acc)[4] = (i & 1) ? s2 : s[nt];
-        mma_f16(acc, qf.a[ks][0], qf.a[ks][1], qf.a[ks][2], qf.a[ks][3], b0, b1);
+        i8x4_to_f16x2x2_biased(w[i], b0, b1);
+        if (i & 1)
+          mma_f16(s2, qf.a[ks][0], qf.a[ks][1], qf.a[ks][2], qf.a[ks][3], b0, b1);
+        else
+          mma_f16(sc.s[nt], qf.a[ks][0], qf.a[ks][1], qf.a[ks][2], qf.a[ks][3], b0, b1);
       }
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) s[nt][e] += s2[e];
+    for (int e = 0; e < R; ++e) sc.s[nt][e] += s2[e];
   }
-  // ---- online softmax; the V scale change is folded into the rescale
-  const float u_new = v_scale != 0.f ? v_scale : st.u;
-  const float ratio = st.u / u_new;
+}
+
+// Online softmax of an INT8 chunk.  The V scale enters through P: with the
+// output stored in units of st.u, a chunk scaled by v_scale contributes
+// P * (v_scale / st.u) * codes, so log2(v_scale / st.u) is added inside the
+// exponent; st.u moves (one rescale) only if that ratio leaves 2^+-8.
+// pa[row half][a0/a2 for k-step 0, a0/a2 for k-step 1] (f16).
+template <int D, bool TWO>
+__device__ __forceinline__ void softmax_i8(WarpState<D, TWO>& st, const QFrags<D, TWO>& qf,
+                                           ScoresI8<D, TWO>& sc, uint32_t (&pa)[2][4],
+                                           float k_scale, float v_scale, float scale_log2) {
+  constexpr int R = WarpState<D, TWO>::R;
+  float lr = 0.f, inv_ratio = 1.f;
+  if (v_scale > 0.f) {
+    const float lv = lg2(v_scale);
+    lr = lv - st.lu;
+    if (fabsf(lr) > 8.f) {
+      const float f = ex2(-lr);  // re-base the stored output on v_scale
+#pragma unroll
+      for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < R; ++e) st.o[nt][e] *= f;
+      st.u = v_scale;
+      st.lu = lv;
+      lr = 0.f;
+    }
+    inv_ratio = ex2(-lr);
+  }
   const float sl = scale_log2 * k_scale;
-  uint32_t pa[2][4];  // [row half][a0/a2 for k-step 0, a0/a2 for k-step 1]
 #pragma unroll
   for (int rh = 0; rh < (TWO ? 2 : 1); ++rh) {
     float x[8];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-      x[2 * nt] = s[nt][2 * rh] * sl;
-      x[2 * nt + 1] = s[nt][2 * rh + 1] * sl;
+      x[2 * nt] = sc.s[nt][2 * rh];
+      x[2 * nt + 1] = sc.s[nt][2 * rh + 1];
     }
-    const float alpha = softmax_row_update(x, st.m[rh], st.l[rh]) * ratio;
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-      st.o[nt][2 * rh] *= alpha;
-      st.o[nt][2 * rh + 1] *= alpha;
-    }
+    // scores carry the code bias: subtract 1152 * sum(q) (times sl)
+    const float alpha = softmax_row_update(x, sl, kI8Bias * qf.qsum[rh] * sl, lr, inv_ratio,
+                                           st.m[rh], st.l[rh]);
+    rescale_rows<D, R>(st.o, rh, alpha);
     // k-step kk covers tokens 16kk .. 16kk+15 = score n-tiles 2kk, 2kk+1
     pa[rh][0] = pack_f16(x[0], x[1]);
     pa[rh][1] = pack_f16(x[2], x[3]);
@@ -309,20 +425,26 @@ __device__ __forceinline__ void consume_i8(WarpState<D, TWO>& st, const QFrags<D
     pa[rh][3] = pack_f16(x[6], x[7]);
   }
   if (!TWO) pa[1][0] = pa[1][1] = pa[1][2] = pa[1][3] = 0u;
-  st.u = u_new;
-  // ---- O += P V over 2 k-steps of 16 tokens; V^T fragments built from
-  // 32-bit shared loads of 4 codes and byte interleaving
+}
+
+// O += P V over 2 k-steps of 16 tokens (exact codes: a bias here would cost
+// output precision); V^T fragments built from 32-bit shared loads of 4
+// codes and byte interleaving.
+template <int D, bool TWO>
+__device__ __forceinline__ void pv_i8(WarpState<D, TWO>& st, const uint32_t (&pa)[2][4],
+                                      const FragOffsets& fo, uint32_t sV) {
+  const uint32_t vb0 = sV + fo.iv0, vb1 = sV + fo.iv1;
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk) {
-    const int r0 = 16 * kk + 2 * qd;
 #pragma unroll
     for (int J = 0; J < D / 32; ++J) {
-      const int c16 = 2 * J + (g >> 2);
-      const uint32_t inner = (g & 3) * 4;
-      const uint32_t w0 = lds32(sV + i8_off<D>(r0, c16) + inner);
-      const uint32_t w1 = lds32(sV + i8_off<D>(r0 + 1, c16) + inner);
-      const uint32_t w2 = lds32(sV + i8_off<D>(r0 + 8, c16) + inner);
-      const uint32_t w3 = lds32(sV + i8_off<D>(r0 + 9, c16) + inner);
+      // rows 16kk + 2q + {0, 1, 8, 9}, 16-byte unit 2J + (g >> 2)
+      const uint32_t a0 = (vb0 ^ (J << 5)) + kk * 16 * D;
+      const uint32_t a1 = (vb1 ^ (J << 5)) + kk * 16 * D;
+      const uint32_t w0 = lds32(a0);
+      const uint32_t w1 = lds32(a1);
+      const uint32_t w2 = lds32(a0 + 8 * D);
+      const uint32_t w3 = lds32(a1 + 8 * D);
       uint32_t lo01, hi01, lo23, hi23;
       interleave_bytes(w0, w1, lo01, hi01);
       interleave_bytes(w2, w3, lo23, hi23);

@@ -157,6 +157,27 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Same contractions when only rows 0..7 of A are live (query groups of at
+// most 8 heads): rows 8..15 are fed as zero and their results discarded, so
+// the caller keeps only two accumulators per tile.
+__device__ __forceinline__ void mma_bf16(float (&d)[2], uint32_t a0, uint32_t /*a1*/, uint32_t a2,
+                                         uint32_t /*a3*/, uint32_t b0, uint32_t b1) {
+  float u0, u1;
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%6,%5,%6}, "
+      "{%7,%8}, {%0,%1,%9,%9};"
+      : "+f"(d[0]), "+f"(d[1]), "=f"(u0), "=f"(u1)
+      : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[2], uint32_t a0, uint32_t /*a1*/, uint32_t a2,
+                                        uint32_t /*a3*/, uint32_t b0, uint32_t b1) {
+  float u0, u1;
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%6,%5,%6}, "
+      "{%7,%8}, {%0,%1,%9,%9};"
+      : "+f"(d[0]), "+f"(d[1]), "=f"(u0), "=f"(u1)
+      : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -167,15 +188,24 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Four int8 codes (bytes 0..3 of w) -> two f16x2 holding the exact integer
-// values: (byte0, byte1) and (byte2, byte3).  Each biased byte u = x + 128 is
-// placed in the low mantissa bits of the f16 1024.0 (exponent 0x64), giving
-// 1024 + u exactly; subtracting 1152 = 1024 + 128 leaves x.
-__device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+// Four int8 codes x (bytes 0..3 of w) -> two f16x2 holding x + 1152 exactly:
+// (byte0, byte1) and (byte2, byte3).  The biased byte u = x + 128 (x XOR
+// 0x80) becomes the low mantissa byte of the f16 1024.0 (exponent byte
+// 0x64), i.e. the value 1024 + u.  The constant offset 1152 is removed once
+// per row by the caller (it contributes 1152 * sum(q) to a score and
+// 1152 * sum(p) to an output), not per element.
+__device__ __forceinline__ void i8x4_to_f16x2x2_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = w ^ 0x80808080u;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
+}
+
+constexpr float kI8Bias = 1152.f;  // 1024 (f16 exponent) + 128 (byte bias)
+
+// Exact variant: two f16x2 holding x itself (the bias subtracted per pair).
+__device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   uint32_t a, b;
-  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  i8x4_to_f16x2x2_biased(w, a, b);
   const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
   __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
   __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
@@ -188,6 +218,20 @@ __device__ __forceinline__ void interleave_bytes(uint32_t a, uint32_t b, uint32_
                                                  uint32_t& hi) {
   asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(lo) : "r"(a), "r"(b));
   asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(hi) : "r"(a), "r"(b));
+}
+
+// Hardware base-2 exponential and logarithm (PTX ex2/lg2.approx, flush to
+// zero).  Softmax arguments are <= 0 here, so results below 2^-126 flush to 0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ float warp_max_quad(float v) {

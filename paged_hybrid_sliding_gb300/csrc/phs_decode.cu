@@ -19,6 +19,8 @@
 // page, section 1 (KV in non-contiguous physical blocks through a page
 // table); "Kimi K2.5 architecture deep dive" page, sections 2.2-2.3 (INT8
 // block-wise warm zone, one scale per 32 tokens).
+#include <type_traits>
+
 #include "phs_attn.cuh"
 #include "phs_internal.h"
 
@@ -27,10 +29,20 @@ namespace phs {
 constexpr int kSplitWarps = 4;
 constexpr int kMaxChunksPerWarp = 64;  // tokens_per_split <= 4096
 
+// Compile-time tunables: TMA stages per warp and the CTAs per SM the
+// register allocation must allow (bytes in flight per SM = CTAs x 4 warps x
+// stages x 8 KB).
+#ifndef PHS_SPLIT_STAGES_128
+#define PHS_SPLIT_STAGES_128 3
+#endif
+#ifndef PHS_SPLIT_MIN_CTAS
+#define PHS_SPLIT_MIN_CTAS 2
+#endif
+
 template <int D>
 struct SplitLayout {
   static constexpr int kStage = ChunkGeom<D>::kStageBytes;
-  static constexpr int kStages = (D == 128) ? 3 : 4;
+  static constexpr int kStages = (D == 128) ? PHS_SPLIT_STAGES_128 : 4;
   static constexpr int kStagesBytes = kSplitWarps * kStages * kStage;
   static constexpr int kIdsOff = kStagesBytes;
   static constexpr int kIdsBytes = kSplitWarps * kMaxChunksPerWarp * 12;
@@ -57,8 +69,79 @@ __device__ __forceinline__ int request_splits(int n, int qlen, int T) {
   return (qlen + T - 1) / T + (n - qlen + T - 1) / T;
 }
 
+// One warp's walk over its chunks of a split.  Stage j is handed back to
+// TMA (chunk j + S) right after chunk j is folded into the warp state.
+// Returns the index of a chunk whose bounded wait gave up, or -1.
+template <bool I8, int D, bool TWO, int S, typename Issue>
+__device__ __forceinline__ int walk_chunks(WarpState<D, TWO>& st, const QFrags<D, TWO>& qf,
+                                           const FragOffsets& fo, int my_n, const int32_t* ids,
+                                           const float* kss, const float* vss, uint32_t bar0,
+                                           uint32_t sbase, uint8_t* smem, int t0, int t1,
+                                           int warp, float scale_log2, int lane, Issue&& issue) {
+  constexpr int kStage = ChunkGeom<D>::kStageBytes;
+  constexpr int NW = kSplitWarps;
+  using Scores = typename std::conditional<I8, ScoresI8<D, TWO>, ScoresBf16<D, TWO>>::type;
+  Scores sc;
+  uint32_t pa[2][I8 ? 4 : 2];
+  auto sK = [&](int j) { return sbase + (j % S) * kStage; };
+  auto wait = [&](int j) {
+    const bool done = mbar_wait(bar0 + 8 * (j % S), (j / S) & 1);
+    return __all_sync(0xffffffffu, done);
+  };
+  // valid-token mask of a bf16 chunk; zero the V rows of the others
+  auto prepare = [&](int j) -> uint32_t {
+    if constexpr (I8) {
+      return 0xFFFFFFFFu;
+    } else {
+      const int nv = t1 - (t0 + kPage * (warp + j * NW));
+      const uint32_t valid = nv >= kPage ? 0xFFFFu : ((1u << nv) - 1u);
+      if (valid != 0xFFFFu) {
+        zero_invalid_v_rows<D>(smem + (sK(j) + kStage / 2 - smem_u32(smem)), valid, lane);
+        __syncwarp();
+      }
+      return valid;
+    }
+  };
+  auto qk = [&](int j) {
+    if constexpr (I8)
+      qk_i8(sc, qf, fo, sK(j));
+    else
+      qk_bf16(sc, qf, fo, sK(j));
+  };
+  auto softmax = [&](int j, uint32_t valid) {
+    if constexpr (I8)
+      softmax_i8(st, qf, sc, pa, kss[j], vss[j], scale_log2);
+    else
+      softmax_bf16(st, sc, pa, valid, scale_log2, lane);
+  };
+  auto pv = [&](int j) {
+    if constexpr (I8)
+      pv_i8(st, pa, fo, sK(j) + kStage / 2);
+    else
+      pv_bf16(st, pa, fo, sK(j) + kStage / 2);
+  };
+  // In-order walk: each chunk is folded in completely before its stage is
+  // refilled.  (Issuing chunk j+1's scores ahead of chunk j's output update
+  // was measured slower: it delays the refill, so fewer bytes are in flight.)
+  for (int j = 0; j < my_n; ++j) {
+    if (!wait(j)) return j;
+    const uint32_t valid = prepare(j);
+    if (ids[j] >= 0) {
+      qk(j);
+      softmax(j, valid);
+      pv(j);
+    }
+    __syncwarp();
+    if (lane == 0 && j + S < my_n) {
+      fence_proxy_async_smem();
+      issue(j + S);
+    }
+  }
+  return -1;
+}
+
 template <int D, bool TWO>
-__global__ void __launch_bounds__(kSplitWarps * 32)
+__global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
     phs_split_decode_kernel(const __grid_constant__ CUtensorMap tk,
                             const __grid_constant__ CUtensorMap tv,
                             const __grid_constant__ CUtensorMap tk8,
@@ -192,40 +275,18 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
 
   WarpState<D, TWO> st;
   st.reset();
-  int j = 0;
-  for (; j < my_n; ++j) {
-    const uint32_t bar = bar0 + 8 * (j % S);
-    const bool done = mbar_wait(bar, (j / S) & 1);
-    if (!__all_sync(0xffffffffu, done)) {
-      if (lane == 0) set_status(a.status, PHS_ETIMEOUT);
-      break;
-    }
-    const int id = ids[j];
-    const uint32_t sK = sbase + (j % S) * L::kStage;
-    const uint32_t sV = sK + L::kStage / 2;
-    if (id >= 0) {
-      if (is_i8) {
-        consume_i8<D, TWO>(st, qf, sK, sV, kss[j], vss[j], a.scale_log2, lane);
-      } else {
-        const int tc = t0 + kPage * (warp + j * NW);
-        const int nv = t1 - tc;
-        const uint32_t valid = nv >= kPage ? 0xFFFFu : ((1u << nv) - 1u);
-        if (valid != 0xFFFFu) {
-          zero_invalid_v_rows<D>(smem + (sV - smem_u32(smem)), valid, lane);
-          __syncwarp();
-        }
-        consume_bf16<D, TWO>(st, qf, sK, sV, valid, a.scale_log2, lane);
-      }
-    }
-    __syncwarp();
-    if (lane == 0 && j + S < my_n) {
-      fence_proxy_async_smem();
-      issue(j + S);
-    }
-  }
-  if (j < my_n && lane == 0) {
-    // gave up: drain (bounded) the loads this warp still has in flight
-    for (int k = j; k < my_n && k < j + S; ++k) (void)mbar_wait(bar0 + 8 * (k % S), (k / S) & 1);
+  FragOffsets fo;
+  fo.init<D>(lane);
+  const int failed =
+      is_i8 ? walk_chunks<true, D, TWO, S>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem, t0,
+                                           t1, warp, a.scale_log2, lane, issue)
+            : walk_chunks<false, D, TWO, S>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem,
+                                            t0, t1, warp, a.scale_log2, lane, issue);
+  if (failed >= 0 && lane == 0) {
+    // gave up: record it and drain (bounded) the loads still in flight
+    set_status(a.status, PHS_ETIMEOUT);
+    for (int k = failed; k < my_n && k < failed + S; ++k)
+      (void)mbar_wait(bar0 + 8 * (k % S), (k / S) & 1);
   }
 
   // ---- warp result -> shared memory -> CTA merge

@@ -77,7 +77,8 @@ struct SwaParams {
 };
 
 template <int MAXL>
-int launch_swa_decode(int D, const SwaParams<MAXL>& p, int num_sms, cudaStream_t stream);
+int launch_swa_decode(int D, const SwaParams<MAXL>& p, int num_sms, int smem_optin,
+                      cudaStream_t stream);
 
 // -------------------------------------------------------------- append --
 constexpr int kAppendMaxLayers = 64;
