@@ -167,6 +167,8 @@ __device__ __forceinline__ void mma_bf16(float (&d)[2], uint32_t a0, uint32_t /*
       "{%7,%8}, {%0,%1,%9,%9};"
       : "+f"(d[0]), "+f"(d[1]), "=f"(u0), "=f"(u1)
       : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+  (void)u0;
+  (void)u1;
 }
 
 __device__ __forceinline__ void mma_f16(float (&d)[2], uint32_t a0, uint32_t /*a1*/, uint32_t a2,
@@ -176,6 +178,8 @@ __device__ __forceinline__ void mma_f16(float (&d)[2], uint32_t a0, uint32_t /*a
       "{%7,%8}, {%0,%1,%9,%9};"
       : "+f"(d[0]), "+f"(d[1]), "=f"(u0), "=f"(u1)
       : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+  (void)u0;
+  (void)u1;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {

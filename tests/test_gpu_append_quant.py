@@ -122,3 +122,34 @@ def test_copy_kernel():
     phs.copy_d2d(y, x)
     torch.cuda.synchronize()
     assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("scale_pow", [0, -1, 1, -20])
+def test_quant_int8_half_integer_quotients_bitexact(scale_pow):
+    """Groups whose absmax is 127 * 2^p, so s = 2^p exactly and x / s lands
+    on half-integers: every such element decides by round-half-even."""
+    D, Hkv = 128, 2
+    rng = np.random.default_rng(100 + scale_pow)
+    vals = np.empty((4, Hkv, 16, D), np.float32)
+    k = rng.integers(-63, 63, size=vals.shape)
+    vals[:] = (k + 0.5) * np.float32(2.0 ** scale_pow)
+    vals[:, :, 0, 0] = 127 * np.float32(2.0 ** scale_pow)   # absmax of each group
+    from paging import f32_to_bf16_bits
+    kp = f32_to_bf16_bits(vals)
+    vp = f32_to_bf16_bits(-vals)
+    bt = np.array([[0, 1, 2, 3]], np.int32)
+    qt = np.array([[1, 0]], np.int32)
+    kc = np.zeros((2, Hkv, 32, D), np.int8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros((2, Hkv), np.float32)
+    vs = np.zeros_like(ks)
+    assert oracle.quant_int8_block32(kp, vp, bt, kc, vc, ks, vs, qt, [0], [2]) == 0
+    assert np.all(ks == np.float32(2.0 ** scale_pow))
+    src = phs.PagedPool(bf16_dev(kp), bf16_dev(vp))
+    dst = phs.Int8Pool.empty(2, Hkv, D)
+    phs.kv_quant_int8_block32(src, dev(bt), dst, dev(qt), dev(np.zeros(1, np.int32)),
+                              dev(np.array([2], np.int32)), 2)
+    torch.cuda.synchronize()
+    assert np.array_equal(dst.k.cpu().numpy(), kc)
+    assert np.array_equal(dst.v.cpu().numpy(), vc)
+    assert np.array_equal(dst.k_scale.cpu().numpy(), ks)
