@@ -157,6 +157,8 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// (the discarded outputs u0, u1 of the next two helpers are intentional)
+#pragma nv_diag_suppress 550
 // Same contractions when only rows 0..7 of A are live (query groups of at
 // most 8 heads): rows 8..15 are fed as zero and their results discarded, so
 // the caller keeps only two accumulators per tile.
@@ -167,8 +169,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[2], uint32_t a0, uint32_t /*
       "{%7,%8}, {%0,%1,%9,%9};"
       : "+f"(d[0]), "+f"(d[1]), "=f"(u0), "=f"(u1)
       : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
-  (void)u0;
-  (void)u1;
 }
 
 __device__ __forceinline__ void mma_f16(float (&d)[2], uint32_t a0, uint32_t /*a1*/, uint32_t a2,
@@ -178,9 +178,9 @@ __device__ __forceinline__ void mma_f16(float (&d)[2], uint32_t a0, uint32_t /*a
       "{%7,%8}, {%0,%1,%9,%9};"
       : "+f"(d[0]), "+f"(d[1]), "=f"(u0), "=f"(u1)
       : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
-  (void)u0;
-  (void)u1;
 }
+
+#pragma nv_diag_default 550
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
