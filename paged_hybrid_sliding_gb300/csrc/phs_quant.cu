@@ -8,11 +8,11 @@
 // in IEEE single precision (division rounded to nearest even, rint rounding
 // half to even; a == 0 gives s = 0 and codes 0).
 //
-// One CTA of two warps per (request, block, KV head): warp 0 quantises K,
-// warp 1 V.  Each warp load covers two (D = 128) or four (D = 64) whole
-// token rows with 16-byte streaming loads, keeps the group in registers,
-// reduces the absmax in packed bf16 and with shuffles, and writes the codes
-// with 8-byte stores.
+// One CTA of four warps per (request, block, KV head): warps 0-1 quantise
+// K, warps 2-3 V, each warp one 16-token source page (a contiguous tile read
+// with 16-byte streaming loads and kept in registers).  The two halves of a
+// group combine their absmax through shared memory; codes go out with
+// 8-byte stores in the same piece order.
 #include "phs_common.cuh"
 #include "phs_internal.h"
 
@@ -24,12 +24,14 @@ namespace phs {
 constexpr float kRoundMagic = 12582912.0f;
 
 template <int D>
-__global__ void __launch_bounds__(64) phs_quant_kernel(const QuantArgs a) {
-  constexpr int kPieces = D / 8;          // 16-byte pieces per token row
-  constexpr int kRowsPerIt = 32 / kPieces;
-  constexpr int kIters = kQBlock / kRowsPerIt;
+__global__ void __launch_bounds__(128) phs_quant_kernel(const QuantArgs a) {
+  constexpr int kPieces = D / 8;              // 16-byte pieces per token row
+  constexpr int kIters = kPage * kPieces / 32;  // pieces of one page tile per lane
   const int jr = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int which = warp >> 1;  // 0 = K, 1 = V
+  const int half = warp & 1;    // tokens 16*half .. 16*half+15 = source page 2j+half
+  __shared__ float s_amax[4];
   if (jr >= a.num_qblocks[b]) return;
   const int j = a.first_qblock[b] + jr;
   if (j < 0 || j >= a.dst_max_qpages) {
@@ -41,32 +43,23 @@ __global__ void __launch_bounds__(64) phs_quant_kernel(const QuantArgs a) {
     if (threadIdx.x == 0) set_status(a.status, PHS_ERANGE);
     return;
   }
-  // the group's 32 tokens live in source pages 2j and 2j+1
-  int page = -1;
-  if (lane < 2) {
-    const int lp = 2 * j + lane;
-    page = lp < a.src_max_pages ? a.src_table[static_cast<size_t>(b) * a.src_max_pages + lp] : -1;
-  }
-  const int page0 = __shfl_sync(0xffffffffu, page, 0);
-  const int page1 = __shfl_sync(0xffffffffu, page, 1);
-  if (page0 < 0 || page0 >= a.num_pages || page1 < 0 || page1 >= a.num_pages) {
-    if (lane == 0) set_status(a.status, PHS_ERANGE);
+  const int lp = 2 * j + half;
+  const int page =
+      lp < a.src_max_pages ? a.src_table[static_cast<size_t>(b) * a.src_max_pages + lp] : -1;
+  const bool bad = page < 0 || page >= a.num_pages;  // uniform per warp
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) set_status(a.status, PHS_ERANGE);
     return;
   }
-  const __nv_bfloat16* src = warp ? a.v_src : a.k_src;
-  int8_t* codes = warp ? a.v_codes : a.k_codes;
-  float* scales = warp ? a.v_scale : a.k_scale;
-  const int piece = lane % kPieces;
-
+  const __nv_bfloat16* src = which ? a.v_src : a.k_src;
+  int8_t* codes = which ? a.v_codes : a.k_codes;
+  float* scales = which ? a.v_scale : a.k_scale;
+  // one contiguous 16 x D tile: lane takes 16-byte pieces lane, lane + 32, ...
+  const uint4* tile =
+      reinterpret_cast<const uint4*>(src + (static_cast<size_t>(page) * a.Hkv + h) * kPage * D);
   uint4 x[kIters];
 #pragma unroll
-  for (int it = 0; it < kIters; ++it) {
-    const int tt = it * kRowsPerIt + lane / kPieces;  // token within the group
-    const int pg = tt < kPage ? page0 : page1;
-    const size_t off = ((static_cast<size_t>(pg) * a.Hkv + h) * kPage + (tt % kPage)) * D +
-                       piece * 8;
-    x[it] = __ldcs(reinterpret_cast<const uint4*>(src + off));
-  }
+  for (int it = 0; it < kIters; ++it) x[it] = __ldcs(tile + it * 32 + lane);
   // absmax in packed bf16 (exact: the max of |x| is one of the inputs)
   __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
 #pragma unroll
@@ -78,6 +71,9 @@ __global__ void __launch_bounds__(64) phs_quant_kernel(const QuantArgs a) {
   float amax = fmaxf(__low2float(m2), __high2float(m2));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) s_amax[warp] = amax;
+  __syncthreads();
+  amax = fmaxf(s_amax[2 * which], s_amax[2 * which + 1]);  // whole 32-token group
   const float s = __fdiv_rn(amax, 127.0f);
   const float rs = s != 0.f ? __fdiv_rn(1.0f, s) : 0.f;
   // code = rint(x / s) with x / s the IEEE quotient.  y = x * fl(1/s) is
@@ -96,9 +92,11 @@ __global__ void __launch_bounds__(64) phs_quant_kernel(const QuantArgs a) {
       t = __fadd_rn(rintf(__fdiv_rn(v, s)), kRoundMagic);
     return __float_as_uint(t);  // code in the low byte
   };
+  // codes of this page tile: rows 16*half .. of INT8 page qp, same piece order
+  uint2* out = reinterpret_cast<uint2*>(codes + ((static_cast<size_t>(qp) * a.Hkv + h) * kQBlock +
+                                                 kPage * half) * D);
 #pragma unroll
   for (int it = 0; it < kIters; ++it) {
-    const int tt = it * kRowsPerIt + lane / kPieces;
     const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&x[it]);
     uint32_t w[2];
 #pragma unroll
@@ -109,19 +107,18 @@ __global__ void __launch_bounds__(64) phs_quant_kernel(const QuantArgs a) {
       const uint32_t hi = __byte_perm(code(f1.x), code(f1.y), 0x0040);
       w[k] = __byte_perm(lo, hi, 0x5410);
     }
-    const size_t off = ((static_cast<size_t>(qp) * a.Hkv + h) * kQBlock + tt) * D + piece * 8;
-    *reinterpret_cast<uint2*>(codes + off) = make_uint2(w[0], w[1]);
+    out[it * 32 + lane] = make_uint2(w[0], w[1]);
   }
-  if (lane == 0) scales[static_cast<size_t>(qp) * a.Hkv + h] = s;
+  if (threadIdx.x == 64 * which && half == 0) scales[static_cast<size_t>(qp) * a.Hkv + h] = s;
 }
 
 int launch_quant(const QuantArgs& a, int max_qblocks, int B, cudaStream_t stream) {
   if (max_qblocks <= 0 || B <= 0) return PHS_OK;
   dim3 grid(max_qblocks, B, a.Hkv);
   if (a.D == 128)
-    phs_quant_kernel<128><<<grid, 64, 0, stream>>>(a);
+    phs_quant_kernel<128><<<grid, 128, 0, stream>>>(a);
   else if (a.D == 64)
-    phs_quant_kernel<64><<<grid, 64, 0, stream>>>(a);
+    phs_quant_kernel<64><<<grid, 128, 0, stream>>>(a);
   else
     return PHS_EUNSUPPORTED;
   return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
