@@ -33,25 +33,32 @@ _lib = None
 ORC_OK, ORC_EINVAL, ORC_ERANGE, ORC_ESHARED = 0, -1, -3, -4
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (-O2 -fopenmp); returns the .so path."""
-    os.makedirs(_BUILD_DIR, exist_ok=True)
-    if (not force and os.path.exists(_SO)
-            and os.path.getmtime(_SO) >= os.path.getmtime(_SRC)):
-        return _SO
-    tmp = _SO + f".tmp{os.getpid()}"
+def build(force: bool = False, mutant: int = 0, out: str | None = None) -> str:
+    """Compile the oracle with gcc (-O2 -fopenmp); returns the .so path.
+    mutant > 0 builds a planted-mistake variant (for the pin tests only)
+    at `out`."""
+    so = out or _SO
+    os.makedirs(os.path.dirname(so), exist_ok=True)
+    if (not force and mutant == 0 and os.path.exists(so)
+            and os.path.getmtime(so) >= os.path.getmtime(_SRC)):
+        return so
+    tmp = so + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
-           "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+           "-fno-fast-math", "-ffp-contract=off", f"-DORC_MUTANT={int(mutant)}", "-o", tmp,
+           _SRC, "-lm"]
     subprocess.check_call(cmd)
-    os.replace(tmp, _SO)
-    return _SO
+    os.replace(tmp, so)
+    return so
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # PHS_ORACLE_MUTANT_LIB: a planted-mistake build, used only by the
+            # test that checks the pins catch such mistakes
+            path = os.environ.get("PHS_ORACLE_MUTANT_LIB") or build()
+            lib = ctypes.CDLL(path)
             P, I, L, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
             lib.phs_oracle_max_threads.restype = I
             lib.phs_oracle_append_paged.argtypes = [P, P, L, I, I, I, P, P, P, I, P, I, P]

@@ -54,6 +54,13 @@
 #include <omp.h>
 #endif
 
+/* Planted-mistake builds for the pin tests (ORC_MUTANT = 1..10): each turns
+ * on exactly one plausible bug, and the pin suite must catch every one.  The
+ * normal build is ORC_MUTANT = 0 and contains none of them. */
+#ifndef ORC_MUTANT
+#define ORC_MUTANT 0
+#endif
+
 #define ORC_OK 0
 #define ORC_EINVAL -1
 #define ORC_ERANGE -3
@@ -100,7 +107,7 @@ int phs_oracle_append_paged(uint16_t *k_pool, uint16_t *v_pool, int64_t num_page
     for (int b = 0; b < B; ++b) {
         int64_t n = seq_lens[b];
         if (n < 1) continue; /* nothing appended for an empty request */
-        int64_t t = n - 1;
+        int64_t t = ORC_MUTANT == 6 ? n : n - 1;
         int64_t lp = t / P;
         if (lp >= max_pages) { status = ORC_ERANGE; continue; }
         int64_t page = block_table[(int64_t)b * max_pages + lp];
@@ -109,7 +116,8 @@ int phs_oracle_append_paged(uint16_t *k_pool, uint16_t *v_pool, int64_t num_page
         int64_t slot = t % P;
         for (int h = 0; h < Hkv; ++h) {
             for (int d = 0; d < D; ++d) {
-                int64_t dst = ((page * Hkv + h) * P + slot) * D + d;
+                int64_t dst = ORC_MUTANT == 8 ? ((page * P + slot) * Hkv + h) * D + d
+                                              : ((page * Hkv + h) * P + slot) * D + d;
                 int64_t src = ((int64_t)b * Hkv + h) * D + d;
                 k_pool[dst] = k_new[src];
                 v_pool[dst] = v_new[src];
@@ -158,11 +166,11 @@ int phs_oracle_append_ring(uint16_t *k_ring, uint16_t *v_ring, int64_t num_rings
  * [num_qpages][Hkv] fp32, through dst_qtable[b][j] for 32-token block j.
  * Blocks j in [first_qblock[b], first_qblock[b] + num_qblocks[b]).
  * ---------------------------------------------------------------------- */
-static float quant_scale(float absmax) { return absmax / 127.0f; }
+static float quant_scale(float absmax) { return absmax / (ORC_MUTANT == 10 ? 128.0f : 127.0f); }
 
 static int8_t quant_code(float x, float s) {
     if (s == 0.0f) return 0;
-    float r = rintf(x / s);
+    float r = ORC_MUTANT == 5 ? roundf(x / s) : rintf(x / s);
     if (r > 127.0f) r = 127.0f;
     if (r < -127.0f) r = -127.0f;
     return (int8_t)r;
@@ -240,7 +248,7 @@ static void attend_one(const double *q, int D, int64_t t0, int64_t t1, double sc
         get_row(ctx, t, 0, row);
         double acc = 0.0;
         for (int d = 0; d < D; ++d) acc += q[d] * row[d];
-        s[t - t0] = acc * scale;
+        s[t - t0] = ORC_MUTANT == 3 ? acc : acc * scale;
         if (s[t - t0] > m) m = s[t - t0];
     }
     double l = 0.0;
@@ -250,7 +258,8 @@ static void attend_one(const double *q, int D, int64_t t0, int64_t t1, double sc
         get_row(ctx, t, 1, row);
         for (int d = 0; d < D; ++d) out[d] += p * row[d];
     }
-    for (int d = 0; d < D; ++d) out[d] /= l;
+    if (ORC_MUTANT != 9)
+        for (int d = 0; d < D; ++d) out[d] /= l;
     free(s);
 }
 
@@ -283,7 +292,7 @@ static void full_row(const void *vctx, int64_t t, int is_v, double *row) {
             return;
         }
         const int8_t *codes = is_v ? c->v_codes : c->k_codes;
-        float s = (is_v ? c->v_scale : c->k_scale)[qp * c->Hkv + c->h];
+        float s = ((is_v != (ORC_MUTANT == 7)) ? c->v_scale : c->k_scale)[qp * c->Hkv + c->h];
         const int8_t *r = codes + ((qp * c->Hkv + c->h) * 32 + t % 32) * c->D;
         for (int d = 0; d < c->D; ++d) row[d] = (double)((float)r[d] * s);
         return;
@@ -296,7 +305,8 @@ static void full_row(const void *vctx, int64_t t, int is_v, double *row) {
         return;
     }
     const uint16_t *pool = is_v ? c->v_pool : c->k_pool;
-    const uint16_t *r = pool + ((page * c->Hkv + c->h) * c->P + t % c->P) * c->D;
+    const uint16_t *r = pool + (ORC_MUTANT == 8 ? ((page * c->P + t % c->P) * c->Hkv + c->h)
+                                                : ((page * c->Hkv + c->h) * c->P + t % c->P)) * c->D;
     for (int d = 0; d < c->D; ++d) row[d] = bf16_to_double(r[d]);
 }
 
@@ -322,7 +332,7 @@ int phs_oracle_decode_full_paged(const uint16_t *q, int B, int Hq, int Hkv, int 
     for (int64_t w = 0; w < (int64_t)nsel * Hq; ++w) {
         int b = rows ? rows[w / Hq] : (int)(w / Hq);
         int i = (int)(w % Hq);
-        int h = i / G;
+        int h = ORC_MUTANT == 1 ? i % Hkv : i / G;
         int local_bad = 0;
         full_ctx c = {k_pool, v_pool, num_pages, P, Hkv, D,
                       block_table + (int64_t)b * max_pages, max_pages,
@@ -347,7 +357,8 @@ typedef struct {
 
 static void ring_row(const void *vctx, int64_t t, int is_v, double *row) {
     const ring_ctx *c = (const ring_ctx *)vctx;
-    int64_t slot = pos_mod(c->newest_slot - (c->n - 1 - t), c->W);
+    int64_t slot = ORC_MUTANT == 4 ? pos_mod(c->newest_slot + (c->n - 1 - t), c->W)
+                                   : pos_mod(c->newest_slot - (c->n - 1 - t), c->W);
     const uint16_t *base = is_v ? c->v_ring : c->k_ring;
     const uint16_t *r = base + ((c->ring * c->Hkv + c->h) * c->W + slot) * c->D;
     for (int d = 0; d < c->D; ++d) row[d] = bf16_to_double(r[d]);
@@ -377,10 +388,11 @@ int phs_oracle_decode_swa_ring(const uint16_t *q, int B, int Hq, int Hkv, int D,
             bad = 1;
             continue;
         }
-        ring_ctx c = {k_ring, v_ring, r, W, Hkv, D, i / G, ring_pos[b], n};
+        ring_ctx c = {k_ring, v_ring, r, W, Hkv, D, ORC_MUTANT == 1 ? i % Hkv : i / G,
+                      ring_pos[b], n};
         double qd[256];
         for (int d = 0; d < D; ++d) qd[d] = bf16_to_double(q[((int64_t)b * Hq + i) * D + d]);
-        int64_t t0 = n > W ? n - W : 0;
+        int64_t t0 = n > W ? n - W + (ORC_MUTANT == 2) : 0;
         attend_one(qd, D, t0, n, scale, ring_row, &c, out + ((int64_t)b * Hq + i) * D);
     }
     return bad ? ORC_ERANGE : ORC_OK;
