@@ -314,7 +314,7 @@ class TinyHybridWorkload(Workload):
         self.bytes_per_step = (full_tok + swa_tok) * tok_bytes + 2 * 2 * B * Hq * D * 2 + \
             2 * 2 * B * Hkv * D * 2
         self.kernel_bytes = None
-        self.launches_per_step = 5   # 2 appends, SWA decode, split, merge
+        self.launches_per_step = 4   # 2 appends, SWA decode, split (one split: no merge)
         self.extra = {"batch": B, "layers": "1 Full + 1 SWA(W=128)"}
         self.host = [pinned(t) for t in (self.qf, self.qs, self.kn, self.vn, self.sl, self.rp,
                                          self.bt)]
@@ -807,10 +807,22 @@ def run_gpu(args, rank, world, local_rank):
     import paged_hybrid_sliding_gb300 as phs
     phs.lib()
     wl = make_workload(args.config, device, args)
+    use_graph = args.graph if args.graph is not None else args.config == 1
+    if use_graph and isinstance(wl, SharedPrefixWorkload):
+        raise SystemExit("--graph: the shared-prefix steps change lengths every step")
     for _ in range(args.warmup):
         wl.step()
     torch.cuda.synchronize()
-    evs = wl.new_events(args.steps)
+    graph = None
+    if use_graph:
+        # one step recorded as a CUDA graph and replayed: the library's
+        # launches are captured as they are issued on the current stream
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            wl.step()
+        graph.replay()
+        torch.cuda.synchronize()
+    evs = [] if graph is not None else wl.new_events(args.steps)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
@@ -818,7 +830,10 @@ def run_gpu(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         start.record()
         for i in range(args.steps):
-            wl.step(evs[i] if evs else None)
+            if graph is not None:
+                graph.replay()
+            else:
+                wl.step(evs[i] if evs else None)
         stop.record()
         torch.cuda.synchronize()
     if world > 1:
@@ -879,6 +894,7 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    line["config"]["cuda_graph"] = graph is not None
     if isinstance(wl, TinyHybridWorkload):
         line["us_per_step"] = round(ms * 1e3, 2)
     if kernel_s is not None and wl.kernel_bytes:
@@ -966,6 +982,9 @@ def main():
     ap.add_argument("--batch", type=int, default=0,
                     help="requests (0 = the workload's own batch: 64 / 256 / 32 for configs "
                          "2 / 3 / 4); smaller batches are for profiler captures")
+    ap.add_argument("--graph", dest="graph", action="store_true", default=None,
+                    help="replay each step as a CUDA graph (default: only for config 1)")
+    ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--swa-only", action="store_true",
                     help="config 3: only the 60 SWA layers (profiler captures)")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],

@@ -5,13 +5,30 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "phs_internal.h"
 
 namespace phs {
 
 int swa_smem_bytes(int D, int G, int batch);
+
+int ensure_dynamic_smem(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;  // (kernel, device) -> bytes set
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PHS_ECUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find({kernel, dev});
+  if (it != done.end() && it->second >= bytes) return PHS_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return PHS_ECUDA;
+  done[{kernel, dev}] = bytes;
+  return PHS_OK;
+}
 
 namespace {
 
@@ -470,6 +487,7 @@ int phs_attn_decode_full_paged(const void* q, int32_t num_q_heads, const phs_pag
   if (st) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launch_split_decode(c.pl.D, c.tk, c.tv, c.tk8, c.tv8, c.a, batch, s))) return st;
+  if (c.pl.max_splits == 1) return PHS_OK;  // every request finished in its only split
   return launch_merge(c.pl.D, c.m, batch, s);
 }
 

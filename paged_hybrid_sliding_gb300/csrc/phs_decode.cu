@@ -413,8 +413,7 @@ static int launch_split_t(const CUtensorMap& tk, const CUtensorMap& tv, const CU
                           const CUtensorMap& tv8, const SplitArgs& a, int B, cudaStream_t stream) {
   auto kern = phs_split_decode_kernel<D, TWO>;
   const int smem = SplitLayout<D>::kAlloc;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return PHS_ECUDA;
+  if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
   dim3 grid(B, a.Hkv, a.max_splits);
   kern<<<grid, kSplitWarps * 32, smem, stream>>>(tk, tv, tk8, tv8, a);
   return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;

@@ -133,4 +133,9 @@ int launch_copy(void* dst, const void* src, size_t bytes, int num_sms, cudaStrea
 
 int swa_smem_bytes(int D, int G, int batch);
 
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device);
+// later calls are a lookup (no CUDA call, so launches stay cheap and safe to
+// record into a CUDA graph).
+int ensure_dynamic_smem(const void* kernel, int bytes);
+
 }  // namespace phs

@@ -229,8 +229,7 @@ template <int D, bool TWO, int MAXL, int NW>
 static int launch_swa_t(const SwaParams<MAXL>& p, int num_sms, cudaStream_t stream) {
   auto kern = phs_swa_decode_kernel<D, TWO, MAXL, NW>;
   const int smem = SwaLayout(D, p.G, NW, p.B).total;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return PHS_ECUDA;
+  if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
   const long long units = static_cast<long long>(p.num_layers) * p.B * p.Hkv;
   long long blocks = (units + NW - 1) / NW;
   if (blocks > num_sms) blocks = num_sms;
