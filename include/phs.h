@@ -71,8 +71,9 @@ typedef enum {
     PHS_EUNSUPPORTED = -7,  /* valid but unsupported shape */
     PHS_ETIMEOUT = -8,      /* (device) a bounded wait gave up */
     PHS_EALIGN = -9,        /* a pointer is not 16-byte aligned */
-    PHS_ESCRATCH = -10      /* request needs more than the built-in scratch of
+    PHS_ESCRATCH = -10,     /* request needs more than the built-in scratch of
                                phs_attn_decode_full_paged_noalloc */
+    PHS_ENOSPACE = -11      /* page allocator has fewer free pages than asked */
 } phs_status;
 
 enum { PHS_OUT_BF16 = 0, PHS_OUT_F32 = 1 };
@@ -321,6 +322,81 @@ int phs_hybrid_kv_tokens(const int32_t *layer_is_full_host, int32_t num_layers,
  * in-run HBM bandwidth yardstick.  dst and src 16-byte aligned, bytes a
  * multiple of 16. */
 int phs_copy_d2d(void *dst, const void *src, size_t bytes, void *stream);
+
+/* ========================================================================
+ * Host-side cache bookkeeping that produces the block tables and page
+ * reference counts the kernels consume.  Host memory in, host memory out;
+ * every object is thread-safe (one mutex per object).
+ * ====================================================================== */
+
+/* Refcounted page allocator over the pages of a Full pool.
+ * Source: "Kimi K3 context caching" page, section 1: requests that hit a
+ * shared prefix increment the reference count of its physical blocks in the
+ * page table (copy on write); only a request's own new tokens get new
+ * blocks. */
+typedef struct phs_page_allocator phs_page_allocator;
+phs_page_allocator *phs_page_allocator_create(int64_t num_pages); /* NULL on bad size */
+void phs_page_allocator_destroy(phs_page_allocator *a);
+/* n fresh pages with count 1 into out_pages (host); PHS_ENOSPACE if fewer free. */
+int phs_page_alloc(phs_page_allocator *a, int32_t n, int32_t *out_pages);
+/* +1 / -1 on each listed page (all must be live, else PHS_ERANGE and no
+ * change); pages reaching 0 return to the free list. */
+int phs_page_incref(phs_page_allocator *a, const int32_t *pages, int32_t n);
+int phs_page_decref(phs_page_allocator *a, const int32_t *pages, int32_t n);
+int64_t phs_page_free_count(phs_page_allocator *a);
+/* Snapshot of all counts into out (host int32 [num_pages]); copy it to the
+ * device for the refcount check of phs_kv_append_paged. */
+int phs_page_refcounts(phs_page_allocator *a, int32_t *out);
+/* Copy on write before appending into `page`: if its count is 1 the page is
+ * returned unchanged; otherwise a fresh page (count 1) is allocated, the
+ * shared page loses one reference, and the fresh id is returned -- the
+ * caller copies the contents with phs_copy_pages and updates its table. */
+int phs_page_cow(phs_page_allocator *a, int32_t page, int32_t *out_page);
+
+/* Device copy of whole pages (K and V, all heads): dst_pages[i] <- src_pages[i]
+ * (device int32 arrays).  Out-of-range ids record PHS_ERANGE. */
+int phs_copy_pages(const phs_paged_pool *pool, const int32_t *src_pages,
+                   const int32_t *dst_pages, int32_t n, int32_t *dev_status, void *stream);
+
+/* Radix prefix tree over whole pages.
+ * Source: "Kimi K3 context caching" page, sections 1 and 3 (global radix
+ * tree, longest-prefix match, insert of newly computed blocks).  Only whole
+ * pages are cached and shared.  The tree holds one reference on each page
+ * it caches. */
+typedef struct phs_radix_tree phs_radix_tree;
+phs_radix_tree *phs_radix_create(phs_page_allocator *alloc, int32_t page_size);
+void phs_radix_destroy(phs_radix_tree *t); /* drops the tree's page references */
+/* Longest cached whole-page prefix of tokens[0..n): its page ids go to
+ * out_pages (capacity max_pages, else PHS_ESHAPE), their number to
+ * *out_num_pages (matched tokens = that * page_size).  Each matched page
+ * gets one more reference (the caller's request); release with
+ * phs_page_decref when the request ends. */
+int phs_radix_match(phs_radix_tree *t, const int32_t *tokens, int64_t n, int32_t *out_pages,
+                    int32_t max_pages, int32_t *out_num_pages);
+/* Same, cut back to the window-safe length of a hybrid stack.  Source:
+ * "Xiaomi MiMo-V2.5 inference system" page, section 2 (prefix tree
+ * rebuild): a match is valid only where at least the last W tokens still
+ * have valid SWA slots.  Here: the longest page-aligned L <= match with
+ * every token of [max(0, L - window), L) marked SWA-valid at insert. */
+int phs_radix_match_window_safe(phs_radix_tree *t, const int32_t *tokens, int64_t n,
+                                int32_t window, int32_t *out_pages, int32_t max_pages,
+                                int32_t *out_num_pages);
+/* Cache the whole pages of tokens[0..n) with page ids pages[0..n/page_size).
+ * Positions already cached keep the tree's pages (the caller's ids for them
+ * are not referenced); new pages get a tree reference.  Token positions >=
+ * swa_from are marked SWA-valid (their SWA KV is kept with the sequence,
+ * e.g. n - W for a finished request; n for none). */
+int phs_radix_insert(phs_radix_tree *t, const int32_t *tokens, int64_t n, const int32_t *pages,
+                     int64_t swa_from);
+/* Evict least-recently-used leaves whose pages only the tree references
+ * until at least `pages` pages were freed or none is evictable. */
+int phs_radix_evict(phs_radix_tree *t, int64_t pages, int64_t *out_freed);
+int64_t phs_radix_cached_pages(phs_radix_tree *t);
+/* Window-safe length as a plain function: the largest L <= match_len, L a
+ * multiple of align, with swa_valid[t] != 0 (host uint8) for every t in
+ * [max(0, L - window), L); 0 if none. */
+int64_t phs_window_safe_len(const uint8_t *swa_valid, int64_t match_len, int32_t window,
+                            int32_t align);
 
 const char *phs_status_str(int status);
 int32_t phs_version(void);

@@ -25,7 +25,8 @@ __all__ = [
     "attn_decode_full_paged", "attn_decode_full_paged_split", "attn_merge_splits",
     "attn_decode_full_paged_noalloc", "NOALLOC_SCRATCH_BYTES",
     "attn_decode_swa_ring", "attn_decode_hybrid_stack", "hybrid_stack_workspace_bytes",
-    "hybrid_kv_tokens", "copy_d2d", "lib", "PAGE", "QBLOCK",
+    "hybrid_kv_tokens", "copy_d2d", "copy_pages", "PageAllocator", "RadixTree",
+    "window_safe_len", "lib", "PAGE", "QBLOCK",
 ]
 
 PAGE = 16
@@ -420,3 +421,135 @@ def copy_d2d(dst, src, stream=None):
         raise ValueError("copy_d2d size mismatch")
     _check(lib().phs_copy_d2d(_ptr(dst), _ptr(src), src.numel() * src.element_size(),
                               _stream(stream)), "copy_d2d")
+
+
+# ------------------------------------------------------- cache bookkeeping --
+def copy_pages(pool: PagedPool, src_pages, dst_pages, status=None, stream=None):
+    """Device copy of whole pages (K and V): dst_pages[i] <- src_pages[i]."""
+    pc = pool.c()
+    _need(src_pages, torch.int32, "src_pages", 1)
+    _need(dst_pages, torch.int32, "dst_pages", 1)
+    _opt(status, torch.int32, "status")
+    _check(lib().phs_copy_pages(ctypes.byref(pc), _ptr(src_pages), _ptr(dst_pages),
+                                src_pages.shape[0], _ptr(status), _stream(stream)), "copy_pages")
+
+
+def _i32(a):
+    import numpy as np
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+class PageAllocator:
+    """Refcounted page allocator (host object of the library)."""
+
+    def __init__(self, num_pages: int):
+        self.num_pages = int(num_pages)
+        self._h = lib().phs_page_allocator_create(self.num_pages)
+        if not self._h:
+            raise ValueError("bad number of pages")
+
+    def close(self):
+        if self._h:
+            lib().phs_page_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc(self, n: int):
+        import numpy as np
+        out = np.empty(max(int(n), 0), dtype=np.int32)
+        _check(lib().phs_page_alloc(self._h, int(n), out.ctypes.data), "page_alloc")
+        return out
+
+    def incref(self, pages):
+        p = _i32(pages)
+        _check(lib().phs_page_incref(self._h, p.ctypes.data, p.shape[0]), "page_incref")
+
+    def decref(self, pages):
+        p = _i32(pages)
+        _check(lib().phs_page_decref(self._h, p.ctypes.data, p.shape[0]), "page_decref")
+
+    def free_count(self) -> int:
+        return int(lib().phs_page_free_count(self._h))
+
+    def refcounts(self):
+        import numpy as np
+        out = np.empty(self.num_pages, dtype=np.int32)
+        _check(lib().phs_page_refcounts(self._h, out.ctypes.data), "page_refcounts")
+        return out
+
+    def cow(self, page: int) -> int:
+        out = ctypes.c_int32()
+        _check(lib().phs_page_cow(self._h, int(page), ctypes.byref(out)), "page_cow")
+        return out.value
+
+
+class RadixTree:
+    """Radix prefix tree over whole pages, holding references in `alloc`."""
+
+    def __init__(self, alloc: PageAllocator, page_size: int = PAGE):
+        self.alloc = alloc
+        self.page_size = int(page_size)
+        self._h = lib().phs_radix_create(alloc._h, self.page_size)
+        if not self._h:
+            raise ValueError("bad radix tree arguments")
+
+    def close(self):
+        if self._h:
+            lib().phs_radix_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _match(self, tokens, window=None):
+        import numpy as np
+        t = _i32(tokens)
+        cap = t.shape[0] // self.page_size + 1
+        out = np.empty(cap, dtype=np.int32)
+        n = ctypes.c_int32()
+        if window is None:
+            st = lib().phs_radix_match(self._h, t.ctypes.data, t.shape[0], out.ctypes.data, cap,
+                                       ctypes.byref(n))
+        else:
+            st = lib().phs_radix_match_window_safe(self._h, t.ctypes.data, t.shape[0],
+                                                   int(window), out.ctypes.data, cap,
+                                                   ctypes.byref(n))
+        _check(st, "radix_match")
+        return out[:n.value].copy()
+
+    def match(self, tokens):
+        """Matched page ids (each gets a reference for the caller)."""
+        return self._match(tokens)
+
+    def match_window_safe(self, tokens, window: int):
+        return self._match(tokens, window)
+
+    def insert(self, tokens, pages, swa_from=None):
+        t, p = _i32(tokens), _i32(pages)
+        sf = t.shape[0] if swa_from is None else int(swa_from)
+        _check(lib().phs_radix_insert(self._h, t.ctypes.data, t.shape[0], p.ctypes.data, sf),
+               "radix_insert")
+
+    def evict(self, pages: int) -> int:
+        freed = ctypes.c_int64()
+        _check(lib().phs_radix_evict(self._h, int(pages), ctypes.byref(freed)), "radix_evict")
+        return freed.value
+
+    def cached_pages(self) -> int:
+        return int(lib().phs_radix_cached_pages(self._h))
+
+
+def window_safe_len(swa_valid, match_len: int, window: int, align: int = 1) -> int:
+    import numpy as np
+    v = np.ascontiguousarray(swa_valid, dtype=np.uint8)
+    r = int(lib().phs_window_safe_len(v.ctypes.data, int(match_len), int(window), int(align)))
+    _check(min(r, 0), "window_safe_len")
+    return r

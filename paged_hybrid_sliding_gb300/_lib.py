@@ -73,6 +73,23 @@ _SIGS = {
     "phs_hybrid_stack_workspace_bytes": (c_size, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "phs_hybrid_kv_tokens": (ctypes.c_int, [c_vp, c_i32, c_vp, c_i32, c_i32, P_i64, P_i64]),
     "phs_copy_d2d": (ctypes.c_int, [c_vp, c_vp, c_size, c_vp]),
+    "phs_copy_pages": (ctypes.c_int, [_P(PagedPoolC), c_vp, c_vp, c_i32, c_vp, c_vp]),
+    "phs_page_allocator_create": (c_vp, [c_i64]),
+    "phs_page_allocator_destroy": (None, [c_vp]),
+    "phs_page_alloc": (ctypes.c_int, [c_vp, c_i32, c_vp]),
+    "phs_page_incref": (ctypes.c_int, [c_vp, c_vp, c_i32]),
+    "phs_page_decref": (ctypes.c_int, [c_vp, c_vp, c_i32]),
+    "phs_page_free_count": (c_i64, [c_vp]),
+    "phs_page_refcounts": (ctypes.c_int, [c_vp, c_vp]),
+    "phs_page_cow": (ctypes.c_int, [c_vp, c_i32, P_i32]),
+    "phs_radix_create": (c_vp, [c_vp, c_i32]),
+    "phs_radix_destroy": (None, [c_vp]),
+    "phs_radix_match": (ctypes.c_int, [c_vp, c_vp, c_i64, c_vp, c_i32, P_i32]),
+    "phs_radix_match_window_safe": (ctypes.c_int, [c_vp, c_vp, c_i64, c_i32, c_vp, c_i32, P_i32]),
+    "phs_radix_insert": (ctypes.c_int, [c_vp, c_vp, c_i64, c_vp, c_i64]),
+    "phs_radix_evict": (ctypes.c_int, [c_vp, c_i64, P_i64]),
+    "phs_radix_cached_pages": (c_i64, [c_vp]),
+    "phs_window_safe_len": (c_i64, [c_vp, c_i64, c_i32, c_i32]),
 }
 
 # every symbol include/phs.h declares

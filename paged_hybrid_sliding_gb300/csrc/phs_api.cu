@@ -311,6 +311,7 @@ const char* phs_status_str(int s) {
     case PHS_ETIMEOUT: return "device wait timed out";
     case PHS_EALIGN: return "pointer not aligned";
     case PHS_ESCRATCH: return "request exceeds the no-allocation entry point's built-in scratch";
+    case PHS_ENOSPACE: return "not enough free pages";
     default: return "unknown status";
   }
 }
@@ -685,6 +686,16 @@ int phs_hybrid_kv_tokens(const int32_t* layer_is_full_host, int32_t num_layers,
   *full_tokens = f;
   *swa_tokens = w;
   return PHS_OK;
+}
+
+int phs_copy_pages(const phs_paged_pool* pool, const int32_t* src_pages, const int32_t* dst_pages,
+                   int32_t n, int32_t* dev_status, void* stream) {
+  int st = check_paged(pool);
+  if (st) return st;
+  if (n < 0 || (n > 0 && (!src_pages || !dst_pages))) return PHS_EINVAL;
+  const int page_bytes = pool->num_kv_heads * kPage * pool->head_dim * 2;
+  return launch_copy_pages(pool->k, pool->v, src_pages, dst_pages, n, pool->num_pages,
+                           page_bytes, dev_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int phs_copy_d2d(void* dst, const void* src, size_t bytes, void* stream) {

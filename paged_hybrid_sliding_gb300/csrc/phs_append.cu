@@ -67,6 +67,34 @@ int launch_append(const AppendParams<MAXL>& p, cudaStream_t stream) {
 template int launch_append<1>(const AppendParams<1>&, cudaStream_t);
 template int launch_append<kAppendMaxLayers>(const AppendParams<kAppendMaxLayers>&, cudaStream_t);
 
+// ------------------------------------------------------------ page copy --
+// grid (n, 2): CTA (i, kv) copies page src[i] -> dst[i] of K (kv 0) or V.
+__global__ void __launch_bounds__(256) phs_copy_pages_kernel(uint4* k, uint4* v,
+                                                             const int32_t* src,
+                                                             const int32_t* dst, int64_t num_pages,
+                                                             int page_vecs, int32_t* status) {
+  const int i = blockIdx.x;
+  const int s = src[i], d = dst[i];
+  if (s < 0 || s >= num_pages || d < 0 || d >= num_pages) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) set_status(status, PHS_ERANGE);
+    return;
+  }
+  uint4* base = blockIdx.y ? v : k;
+  const uint4* from = base + static_cast<size_t>(s) * page_vecs;
+  uint4* to = base + static_cast<size_t>(d) * page_vecs;
+  for (int e = threadIdx.x; e < page_vecs; e += blockDim.x) to[e] = from[e];
+}
+
+int launch_copy_pages(void* k, void* v, const int32_t* src, const int32_t* dst, int32_t n,
+                      int64_t num_pages, int page_bytes, int32_t* status, cudaStream_t stream) {
+  if (n <= 0) return PHS_OK;
+  dim3 grid(n, 2);
+  phs_copy_pages_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<uint4*>(k),
+                                                  reinterpret_cast<uint4*>(v), src, dst,
+                                                  num_pages, page_bytes / 16, status);
+  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+}
+
 // ------------------------------------------------------------------ copy --
 __global__ void __launch_bounds__(512) phs_copy_kernel(uint4* __restrict__ dst,
                                                        const uint4* __restrict__ src, size_t n) {
