@@ -55,6 +55,15 @@ def peaks():
 SPLIT_KERNEL_SOURCES = ("phs_decode.cu", "phs_attn.cuh", "phs_common.cuh", "phs_internal.h")
 
 
+def peak_tflops():
+    """Measured dense bf16 tensor peak (burst), TFLOP/s."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 def kernel_source_hash(files=SPLIT_KERNEL_SOURCES):
     """Hash of the sources the split-KV decode kernel is compiled from."""
     h = hashlib.sha256()
@@ -663,12 +672,12 @@ class SharedPrefixWorkload(Workload):
     kernel_launches_per_step = 1
     l2 = "logical K/V bytes per step 65.7 GB >> L2; the shared prefix is reused through L2"
 
-    def __init__(self, device, seed=5):
+    def __init__(self, device, seed=5, prefix_kernel=True, prefix_len=250_000):
         import paged_hybrid_sliding_gb300 as phs
         self.phs = phs
-        self.w = w = synth.shared_prefix(seed=seed)
+        self.w = w = synth.shared_prefix(seed=seed, prefix=prefix_len)
         B, Hq, Hkv, D = w.B, w.Hq, w.Hkv, w.D
-        self.name = "shared_prefix_250000_b64_suffix512_128steps_hq32_hkv8_d128"
+        self.name = f"shared_prefix_{prefix_len}_b64_suffix512_128steps_hq32_hkv8_d128"
         g = seed * 100
         self.k = synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 1, device=device)
         self.v = synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 2, device=device)
@@ -687,6 +696,15 @@ class SharedPrefixWorkload(Workload):
         self.ws = torch.empty(phs.decode_workspace_bytes(B, Hq, Hkv, D, self.max_seq, self.tps),
                               dtype=torch.uint8, device=device)
         self.k_idx = 0
+        # tensor-core pass over the shared prefix (whole 64-token tiles)
+        self.prefix_kernel = prefix_kernel
+        self.shared_len = (w.extra["prefix_pages"] * 16 // 64) * 64
+        if prefix_kernel:
+            self.ws = torch.empty(phs.shared_prefix_workspace_bytes(B, Hq, Hkv, D, self.max_seq,
+                                                                    self.shared_len),
+                                  dtype=torch.uint8, device=device)
+            self.kernel = "phs_attn_decode_shared_prefix (prefix tcgen05 + suffix split + merge)"
+            self.l2 = "prefix read once per KV head for all 64 requests (tensor-core pass)"
         mean_n = float(w.n_pre.mean()) + (self.nsteps + 1) / 2
         tok_bytes = Hkv * D * 2 * 2
         self.tokens_per_step = int(round(B * mean_n))
@@ -696,10 +714,13 @@ class SharedPrefixWorkload(Workload):
         npref = w.extra["prefix_pages"]
         unique_tok = npref * 16 + B * (float(w.n_pre.mean()) - npref * 16 + (self.nsteps + 1) / 2)
         self.unique_bytes = int(unique_tok * tok_bytes)
-        self.launches_per_step = 3
+        self.launches_per_step = 4 if prefix_kernel else 3
+        # tensor work of the prefix pass: QK and PV over B*G rows x D per token
+        self.prefix_flops = 4 * B * Hq * D * self.shared_len
         self.extra = {"batch": B, "logical_bytes_per_step": self.bytes_per_step,
                       "unique_kv_bytes_per_step": self.unique_bytes,
-                      "tokens_per_split": self.tps}
+                      "tokens_per_split": self.tps, "shared_prefix_kernel": prefix_kernel,
+                      "shared_len_tensor_pass": self.shared_len if prefix_kernel else 0}
         self.h_q, self.h_kn, self.h_vn = pinned(self.q), pinned(self.kn), pinned(self.vn)
         self.h_sls = [pinned(s) for s in self.sls]
         self.sl_in = torch.empty_like(self.sls[0])
@@ -714,6 +735,12 @@ class SharedPrefixWorkload(Workload):
         phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, sl, page_refcount=self.rc)
         if ev is not None:
             ev[0][0].record()
+        if self.prefix_kernel:
+            phs.attn_decode_shared_prefix(self.q, self.pool, self.bt, sl, self.max_seq,
+                                          self.shared_len, out=self.out, workspace=self.ws)
+            if ev is not None:
+                ev[0][1].record()
+            return
         phs.attn_decode_full_paged_split(self.q, self.pool, self.bt, sl, self.max_seq, self.ws,
                                          self.out, tokens_per_split=self.tps)
         if ev is not None:
@@ -729,9 +756,14 @@ class SharedPrefixWorkload(Workload):
             d.copy_(h, non_blocking=True)
         self.phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl_in,
                                  page_refcount=self.rc)
-        self.phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl_in, self.max_seq,
-                                        out=self.out, tokens_per_split=self.tps,
-                                        workspace=self.ws)
+        if self.prefix_kernel:
+            self.phs.attn_decode_shared_prefix(self.q, self.pool, self.bt, self.sl_in,
+                                               self.max_seq, self.shared_len, out=self.out,
+                                               workspace=self.ws)
+        else:
+            self.phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl_in, self.max_seq,
+                                            out=self.out, tokens_per_split=self.tps,
+                                            workspace=self.ws)
         self.h_out.copy_(self.out, non_blocking=True)
 
     def cpu_baseline(self):
@@ -762,7 +794,8 @@ def make_workload(config, device, args):
     if config == 4:
         return Int8Workload(device, batch=args.batch or 32)
     if config == 5:
-        return SharedPrefixWorkload(device)
+        return SharedPrefixWorkload(device, prefix_kernel=not args.no_prefix_kernel,
+                                    prefix_len=args.prefix_len)
     raise ValueError(config)
 
 
@@ -905,8 +938,21 @@ def run_gpu(args, rank, world, local_rank):
             "bytes_per_launch": wl.kernel_bytes, "avg_launch_ms": round(kernel_s * 1e3, 4),
             "traffic": recorded_traffic(wl.kernel, wl.name)}
         if isinstance(wl, SharedPrefixWorkload):
-            line["roofline"]["bytes_are"] = "logical (prefix pages reused through L2)"
-            line["roofline"]["unique_kv_gbs"] = round(wl.unique_bytes / kernel_s / 1e9, 1)
+            if wl.prefix_kernel:
+                # the decode call reads each prefix page once: its HBM bound is
+                # the unique bytes; its tensor work is the prefix contraction
+                uniq = wl.unique_bytes / kernel_s / 1e9
+                tflops = wl.prefix_flops / kernel_s / 1e12
+                line["roofline"].update({
+                    "achieved": round(uniq, 1), "frac": round(uniq / peak, 4),
+                    "bytes_per_launch": wl.unique_bytes,
+                    "bytes_are": "unique K/V bytes (prefix read once per KV head)",
+                    "logical_gbs": round(achieved, 1),
+                    "tensor_tflops": round(tflops, 1),
+                    "tensor_frac_of_bf16_peak": round(tflops / peak_tflops()[0], 4)})
+            else:
+                line["roofline"]["bytes_are"] = "logical (prefix pages reused through L2)"
+                line["roofline"]["unique_kv_gbs"] = round(wl.unique_bytes / kernel_s / 1e9, 1)
     if extra_kernels:
         line["other_kernels"] = extra_kernels
     if rank == 0 and not args.no_cpu_baseline:
@@ -985,6 +1031,11 @@ def main():
     ap.add_argument("--graph", dest="graph", action="store_true", default=None,
                     help="replay each step as a CUDA graph (default: only for config 1)")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
+    ap.add_argument("--no-prefix-kernel", action="store_true",
+                    help="config 5: decode each request separately (no shared-prefix pass)")
+    ap.add_argument("--prefix-len", type=int, default=250_000,
+                    help="config 5: shared prefix tokens (a multiple of 16; smaller for "
+                         "profiler captures)")
     ap.add_argument("--swa-only", action="store_true",
                     help="config 3: only the 60 SWA layers (profiler captures)")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],

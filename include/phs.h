@@ -262,6 +262,34 @@ int phs_attn_decode_full_paged_noalloc(const void *q, int32_t num_q_heads,
                                        int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Full-attention decode of a batch that shares a prefix, on the tensor
+ * cores.  Source: "Kimi K3 context caching" page, sections 1 and 4 (requests
+ * hitting a cached prefix share its physical blocks; a 250,000-token shared
+ * prefix).  Computes exactly what phs_attn_decode_full_paged computes, for
+ * a batch whose block tables all begin with the same shared_len / 16 page
+ * ids (the caller guarantees it; row 0 of the table is read for them):
+ *   - tokens [0, shared_len) of every request are attended in one pass over
+ *     the prefix per KV head, with the B x G query rows of that head as one
+ *     dense tile (tcgen05.mma), so the prefix is read from HBM once;
+ *   - tokens [shared_len, n_b) by the split-KV kernel;
+ *   - a merge combines both by log-sum-exp.
+ * Limits: head_dim 128, batch x (Hq/Hkv) <= 256, shared_len a positive
+ * multiple of 64 with seq_lens[b] >= shared_len (else PHS_EUNSUPPORTED /
+ * PHS_EINVAL).  workspace: phs_shared_prefix_workspace_bytes(...) bytes,
+ * 256-byte aligned.
+ * ---------------------------------------------------------------------- */
+size_t phs_shared_prefix_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t max_seq_len, int32_t shared_len);
+
+int phs_attn_decode_shared_prefix(const void *q, int32_t num_q_heads, const phs_paged_pool *pool,
+                                  const int32_t *block_table, int32_t max_pages_per_seq,
+                                  const int32_t *seq_lens, int32_t max_seq_len, int32_t batch,
+                                  int32_t shared_len, float softmax_scale, void *out,
+                                  int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                                  int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
  * Sliding-window decode over the SWA ring.
  * Source: MiMo page, section 1 (SWA layers, window 128, attend to the most
  * recent tokens) and section 2 (ring buffer of capacity W).

@@ -24,6 +24,7 @@ __all__ = [
     "decode_workspace_bytes", "decode_tokens_per_split",
     "attn_decode_full_paged", "attn_decode_full_paged_split", "attn_merge_splits",
     "attn_decode_full_paged_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "attn_decode_shared_prefix", "shared_prefix_workspace_bytes",
     "attn_decode_swa_ring", "attn_decode_hybrid_stack", "hybrid_stack_workspace_bytes",
     "hybrid_kv_tokens", "copy_d2d", "copy_pages", "PageAllocator", "RadixTree",
     "window_safe_len", "lib", "PAGE", "QBLOCK",
@@ -289,6 +290,33 @@ def attn_decode_full_paged_noalloc(q, pool: PagedPool, block_table, seq_lens,
         0 if qtable is None else qtable.shape[1], _ptr(qlens), B, scale, int(tokens_per_split),
         _ptr(out), _out_code(out.dtype), _ptr(status), _stream(stream)),
         "attn_decode_full_paged_noalloc")
+    return out
+
+
+def shared_prefix_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                                  shared_len) -> int:
+    """Workspace bytes for attn_decode_shared_prefix; 0 if unsupported."""
+    return int(lib().phs_shared_prefix_workspace_bytes(batch, num_q_heads, num_kv_heads,
+                                                       head_dim, max_seq_len, shared_len))
+
+
+def attn_decode_shared_prefix(q, pool: PagedPool, block_table, seq_lens, max_seq_len: int,
+                              shared_len: int, softmax_scale=None, out=None,
+                              out_dtype=torch.bfloat16, workspace=None, status=None, stream=None):
+    """Decode for a batch whose block tables all start with the same
+    shared_len / 16 prefix pages: the prefix is attended once per KV head
+    for all requests on the tensor cores, each request's own tokens by the
+    split-KV kernel, then merged.  Same result as attn_decode_full_paged."""
+    pc, _, out = _decode_args(q, pool, block_table, seq_lens, None, None, None, out, out_dtype,
+                              status)
+    B, Hq, D = q.shape
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    need = shared_prefix_workspace_bytes(B, Hq, pool.k.shape[1], D, max_seq_len, shared_len)
+    ws = _workspace(workspace, need, q.device)
+    _check(lib().phs_attn_decode_shared_prefix(
+        _ptr(q), Hq, ctypes.byref(pc), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        int(max_seq_len), B, int(shared_len), scale, _ptr(out), _out_code(out.dtype), _ptr(ws),
+        ws.numel(), _ptr(status), _stream(stream)), "attn_decode_shared_prefix")
     return out
 
 

@@ -95,6 +95,23 @@ int map_bf16_rows(CUtensorMap* m, const void* base, int64_t rows, int D) {
   return r == CUDA_SUCCESS ? PHS_OK : PHS_ECUDA;
 }
 
+// bf16 pool (D = 128) viewed as a 3-D tensor {64 columns, rows, 2 column
+// halves} (strides 256 B, 128 B): one box of {64, 16, 2} fetches a whole
+// 16-row page block as [half][16 rows][128 B] with the 128-byte swizzle --
+// one 4 KB copy instead of two 2 KB ones (the copy engine's cost is per box).
+int map_bf16_pages3d(CUtensorMap* m, const void* base, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PHS_ECUDA;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), 2};
+  cuuint64_t strides[2] = {256, 128};
+  cuuint32_t box[3] = {64, 16, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PHS_OK : PHS_ECUDA;
+}
+
 // int8 codes, rows of D bytes; boxes of 32 rows x D with the 128-byte
 // (D = 128) or 64-byte (D = 64) swizzle.
 int map_i8_rows(CUtensorMap* m, const void* base, int64_t rows, int D) {
@@ -528,6 +545,142 @@ int phs_attn_decode_swa_ring(const void* q, int32_t num_q_heads, const phs_ring_
   p.out_f32 = out_dtype == PHS_OUT_F32;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   return launch_swa_decode<1>(D, p, di.sms, di.smem_optin, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------- shared-prefix decode --
+namespace {
+
+struct PrefixPlan {
+  int G = 0, rows = 0, T = 0, ms = 0, ntiles = 0, tps = 0, nsp = 0;
+  size_t off_ml = 0, off_po = 0, off_pml = 0, need = 0;
+};
+
+int make_prefix_plan(PrefixPlan& pl, int B, int Hq, int Hkv, int D, int max_seq, int shared_len) {
+  int st = check_dims(Hq, Hkv, D);
+  if (st) return st;
+  if (D != 128) return PHS_EUNSUPPORTED;
+  if (B <= 0 || shared_len <= 0 || max_seq < shared_len) return PHS_EINVAL;
+  if (shared_len % 64 != 0) return PHS_EUNSUPPORTED;
+  pl.G = Hq / Hkv;
+  pl.rows = B * pl.G;
+  if (pl.rows > 256) return PHS_EUNSUPPORTED;
+  DevInfo di;
+  if ((st = dev_info(di))) return st;
+  if (prefix_smem_bytes() > di.smem_optin) return PHS_EUNSUPPORTED;
+  const int suffix = std::max(1, max_seq - shared_len);
+  pl.T = plan_tokens_per_split(B, Hkv, suffix, 0, di.sms);
+  pl.ms = std::max(1, (suffix + pl.T - 1) / pl.T);
+  pl.ntiles = shared_len / 64;
+  // one CTA per SM: spread each KV head's prefix over sms / Hkv CTAs
+  const int target = std::max(1, di.sms / Hkv);
+  pl.tps = (pl.ntiles + target - 1) / target;
+  pl.nsp = (pl.ntiles + pl.tps - 1) / pl.tps;
+  if (pl.nsp > 65535) return PHS_EUNSUPPORTED;
+  pl.off_ml = ws_o_bytes(B, Hkv, pl.ms, pl.G, D);
+  pl.off_po = pl.off_ml + align256(static_cast<size_t>(B) * Hkv * pl.ms * pl.G * 2 * sizeof(float));
+  pl.off_pml = pl.off_po + align256(static_cast<size_t>(Hkv) * pl.nsp * 256 * D * sizeof(float));
+  pl.need = pl.off_pml + align256(static_cast<size_t>(Hkv) * pl.nsp * 256 * 2 * sizeof(float));
+  return PHS_OK;
+}
+
+}  // namespace
+
+size_t phs_shared_prefix_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t max_seq_len,
+                                         int32_t shared_len) {
+  PrefixPlan pl;
+  if (make_prefix_plan(pl, batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, shared_len))
+    return 0;
+  return pl.need;
+}
+
+int phs_attn_decode_shared_prefix(const void* q, int32_t num_q_heads, const phs_paged_pool* pool,
+                                  const int32_t* block_table, int32_t max_pages_per_seq,
+                                  const int32_t* seq_lens, int32_t max_seq_len, int32_t batch,
+                                  int32_t shared_len, float softmax_scale, void* out,
+                                  int32_t out_dtype, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, void* stream) {
+  int st = check_paged(pool);
+  if (st) return st;
+  if (!q || !block_table || !seq_lens || !out) return PHS_EINVAL;
+  if (max_pages_per_seq <= 0 || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
+    return PHS_EINVAL;
+  if (out_dtype != PHS_OUT_BF16 && out_dtype != PHS_OUT_F32) return PHS_EINVAL;
+  const int D = pool->head_dim, Hkv = pool->num_kv_heads;
+  PrefixPlan pl;
+  if ((st = make_prefix_plan(pl, batch, num_q_heads, Hkv, D, max_seq_len, shared_len))) return st;
+  if (shared_len / kPage > max_pages_per_seq) return PHS_ESHAPE;
+  if (!workspace || workspace_bytes < pl.need) return PHS_EWORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || !aligned16(q)) return PHS_EALIGN;
+  char* ws = reinterpret_cast<char*>(workspace);
+  CUtensorMap tk, tv;
+  const int64_t rows = pool->num_pages * Hkv * kPage;
+  if ((st = map_bf16_rows(&tk, pool->k, rows, D))) return st;
+  if ((st = map_bf16_rows(&tv, pool->v, rows, D))) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const float scale_log2 = softmax_scale * 1.4426950408889634f;
+  // 1. the shared prefix, all requests at once (tensor cores)
+  PrefixArgs pa;
+  std::memset(&pa, 0, sizeof(pa));
+  pa.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  pa.block_table = block_table;  // row 0 holds the shared prefix pages
+  pa.status = dev_status;
+  pa.ws_o = reinterpret_cast<float*>(ws + pl.off_po);
+  pa.ws_ml = reinterpret_cast<float*>(ws + pl.off_pml);
+  pa.num_pages = pool->num_pages;
+  pa.Hq = num_q_heads;
+  pa.Hkv = Hkv;
+  pa.G = pl.G;
+  pa.rows = pl.rows;
+  pa.shared_len = shared_len;
+  pa.tiles_per_split = pl.tps;
+  pa.num_splits = pl.nsp;
+  pa.scale_log2 = scale_log2;
+  CUtensorMap tv3;
+  if ((st = map_bf16_pages3d(&tv3, pool->v, rows))) return st;
+  if ((st = launch_prefix_decode(tk, tv3, pa, s))) return st;
+  // 2. each request's own tokens [shared_len, n) (split-KV, partials only)
+  SplitArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = pa.q;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.ws_o = reinterpret_cast<float*>(ws);
+  a.ws_ml = reinterpret_cast<float*>(ws + pl.off_ml);
+  a.status = dev_status;
+  a.num_pages = pool->num_pages;
+  a.Hq = num_q_heads;
+  a.Hkv = Hkv;
+  a.G = pl.G;
+  a.max_pages = max_pages_per_seq;
+  a.n_clamp = static_cast<int>(std::min<long long>(max_seq_len, 1LL * max_pages_per_seq * kPage));
+  a.T = pl.T;
+  a.max_splits = pl.ms;
+  a.out_f32 = out_dtype == PHS_OUT_F32;
+  a.scale_log2 = scale_log2;
+  a.skip_len = shared_len;
+  a.force_partial = 1;
+  if ((st = launch_split_decode(D, tk, tv, tk, tv, a, batch, s))) return st;
+  // 3. merge prefix and suffix partials
+  PrefixMergeArgs m;
+  std::memset(&m, 0, sizeof(m));
+  m.seq_lens = seq_lens;
+  m.ws_o = a.ws_o;
+  m.ws_ml = a.ws_ml;
+  m.ws_po = pa.ws_o;
+  m.ws_pml = pa.ws_ml;
+  m.out = out;
+  m.Hq = num_q_heads;
+  m.Hkv = Hkv;
+  m.G = pl.G;
+  m.n_clamp = a.n_clamp;
+  m.T = pl.T;
+  m.max_splits = pl.ms;
+  m.num_psplits = pl.nsp;
+  m.shared_len = shared_len;
+  m.out_f32 = a.out_f32;
+  return launch_merge_prefix(m, batch, s);
 }
 
 size_t phs_hybrid_stack_workspace_bytes(int32_t batch, int32_t num_q_heads,

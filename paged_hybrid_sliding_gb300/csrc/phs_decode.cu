@@ -64,9 +64,12 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v, int f3
 
 // Number of splits of a request and validation of its INT8 length.
 // Returns -1 if the request's lengths are invalid.
-__device__ __forceinline__ int request_splits(int n, int qlen, int T) {
-  if (n < 0 || qlen < 0 || qlen > n || (qlen % kQBlock) != 0) return -1;
-  return (qlen + T - 1) / T + (n - qlen + T - 1) / T;
+// The bf16 region starts at max(qlen, skip): tokens below `skip` (a shared
+// prefix) are attended by another kernel.
+__device__ __forceinline__ int request_splits(int n, int qlen, int T, int skip = 0) {
+  if (n < 0 || qlen < 0 || qlen > n || (qlen % kQBlock) != 0 || n < skip) return -1;
+  const int bf0 = max(qlen, skip);
+  return (qlen + T - 1) / T + (n - bf0 + T - 1) / T;
 }
 
 // One warp's walk over its chunks of a split.  Stage j is handed back to
@@ -166,14 +169,14 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
   }
   const int qlen = a.qlens ? a.qlens[b] : 0;
   const int T = a.T;
-  const int ns = min(request_splits(n, qlen, T), a.max_splits);
+  const int ns = min(request_splits(n, qlen, T, a.skip_len), a.max_splits);
   if (ns < 0) {
     if (s == 0 && h == 0 && threadIdx.x == 0) set_status(a.status, PHS_ERANGE);
     return;
   }
   const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
-  if (ns == 0) {  // empty request: zero output
-    if (s == 0)
+  if (ns == 0) {  // empty request: zero output (unless another kernel owns it)
+    if (s == 0 && !a.force_partial)
       for (int e = threadIdx.x; e < G * D; e += blockDim.x) store_out(a.out, out_row0 + e, 0.f, a.out_f32);
     return;
   }
@@ -187,7 +190,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
     t1 = min(t0 + T, qlen);
     nch = (t1 - t0) / kQBlock;
   } else {
-    t0 = qlen + (s - nsq) * T;
+    t0 = max(qlen, a.skip_len) + (s - nsq) * T;
     t1 = min(t0 + T, n);
     nch = (t1 - t0 + kPage - 1) / kPage;
   }
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
       Lsum += sL[w * GR + row] * f;
       O += sO[(w * GR + row) * D + d] * f;
     }
-    if (ns == 1) {
+    if (ns == 1 && !a.force_partial) {
       store_out(a.out, out_row0 + e, Lsum > 0.f ? O / Lsum : 0.f, a.out_f32);
     } else {
       a.ws_o[(part * G + row) * D + d] = O;

@@ -37,7 +37,46 @@ struct SplitArgs {
   int max_splits;
   int out_f32;
   float scale_log2;         // softmax_scale * log2(e)
+  int skip_len;             // tokens [0, skip_len) are attended elsewhere (shared prefix)
+  int force_partial;        // write partials even for single-split requests
 };
+
+// ------------------------------------------------- shared-prefix decode --
+struct PrefixArgs {
+  const __nv_bfloat16* q;   // [B][Hq][D]
+  const int32_t* block_table;  // page ids of the shared prefix (row 0 of the table)
+  int32_t* status;
+  float* ws_o;              // [Hkv][num_splits][256][D]
+  float* ws_ml;             // [Hkv][num_splits][256][2]
+  int64_t num_pages;
+  int Hq, Hkv, G;
+  int rows;                 // B * G <= 256
+  int shared_len;           // tokens, multiple of 64
+  int tiles_per_split;
+  int num_splits;
+  float scale_log2;
+};
+
+struct PrefixMergeArgs {
+  const int32_t* seq_lens;
+  const float* ws_o;        // suffix partials (split kernel layout)
+  const float* ws_ml;
+  const float* ws_po;       // prefix partials
+  const float* ws_pml;
+  void* out;
+  int Hq, Hkv, G;
+  int n_clamp;
+  int T;
+  int max_splits;           // suffix split slots
+  int num_psplits;
+  int shared_len;
+  int out_f32;
+};
+
+int launch_prefix_decode(const CUtensorMap& tk, const CUtensorMap& tv, const PrefixArgs& a,
+                         cudaStream_t stream);
+int launch_merge_prefix(const PrefixMergeArgs& a, int B, cudaStream_t stream);
+int prefix_smem_bytes();
 
 struct MergeArgs {
   const int32_t* seq_lens;

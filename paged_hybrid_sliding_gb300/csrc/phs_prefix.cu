@@ -1,0 +1,516 @@
+// phs_prefix.cu -- decode attention over a prefix shared by a batch of
+// requests, on the 5th-generation tensor cores.
+//
+// Source: "Kimi K3 context caching" page, section 1 (requests hitting the
+// same prefix share its physical KV blocks by reference count) and section 4
+// (a 250,000-token shared prefix).  When B requests share the prefix, the
+// queries of one KV head's group across all B requests (B x G rows) attend
+// to the same prefix K/V: one dense contraction per KV head instead of B
+// separate decodes that each stream the whole prefix.
+//
+// One CTA (persistent, one per SM) handles one (KV head, span of the
+// prefix) for all rows at once (up to 256 = 2 tiles of 128 rows):
+//   warp 8    : TMA producer of 64-token K tiles (four 16-token pages,
+//               128-byte swizzle), its copies issued by eight lanes at once
+//   warp 10   : the same for V (one 4 KB box per page); K and V stages are
+//               released separately (K after Q K^T, V after the P V product)
+//   warp 9    : MMA issuer (one lane); owns the tensor-memory allocation
+//   warps 0-7 : online softmax, one query row per thread
+// Tensor memory (512 columns): S [128 lanes = rows][2 x 64 tokens], Q
+// [128 lanes = rows][2 x 64 columns of bf16 pairs], O^T [128 lanes = d][256
+// rows].  Per 64-token tile j:
+//   S_j = Q K_j^T      tcgen05.mma, A = Q from tensor memory, B = K tile
+//                      (K-major), M = 128 per row tile, N = 64, K = 128;
+//   softmax            each thread reads its row of S_j (then S is free for
+//                      Q K_{j+1}^T), forms P_j = 2^(s * scale log2(e) - m)
+//                      in bf16 into shared memory ([row][token], K-major);
+//   O^T += V_j^T P_j^T A = V tile (MN-major), B = P_j, M = 128 (d),
+//                      N = 256 (rows), K = 64 tokens.
+// Putting the rows on N makes the P V product four N = 256 instructions per
+// tile instead of eight N = 128 ones, and Q in tensor memory takes the Q
+// operand off the shared-memory path; both keep the tensor pipe under the
+// HBM time of a tile.  The running max m of a row only moves when it grows
+// by more than 2^8 (so P <= 256); only then are the O^T columns rescaled,
+// CTA-wide: every row publishes its factor in shared memory and a barrier
+// reduction tells all softmax warps whether any row moved.  The CTA writes
+// (m, l, O) partials; a merge kernel combines them with the requests' own
+// suffix tokens (attended by the split-KV kernel).
+#include "phs_attn.cuh"
+#include "phs_internal.h"
+#include "phs_tc.cuh"
+
+namespace phs {
+
+#ifndef PHS_PFX_STAGES
+#define PHS_PFX_STAGES 4
+#endif
+#ifndef PHS_PFX_PBUFS
+#define PHS_PFX_PBUFS 2
+#endif
+constexpr int kPfxStages = PHS_PFX_STAGES;  // K/V tiles in shared memory
+constexpr int kPfxPBufs = PHS_PFX_PBUFS;    // P tiles in shared memory
+constexpr int kPfxTile = 64;     // tokens per tile (four pages)
+constexpr int kPfxRows = 256;    // query rows per KV head (two tiles of 128)
+constexpr int kPfxThreads = 352;  // 8 softmax warps, K producer, MMA, V producer
+
+// tensor-memory columns
+constexpr uint32_t kTmS = 0;     // S: row tile mt at kTmS + 64 mt
+constexpr uint32_t kTmQ = 128;   // Q: row tile mt at kTmQ + 64 mt
+constexpr uint32_t kTmO = 256;   // O^T: row r at column kTmO + r
+
+struct PfxLayout {
+  static constexpr int kP = 0;                           // [buf][256 rows][128 B]
+  static constexpr int kPBuf = 32 * 1024;
+  static constexpr int kKV = kPfxPBufs * kPBuf;          // [stage][K 16 KB | V 16 KB]
+  static constexpr int kStage = 32 * 1024;
+  static constexpr int kAlpha = kKV + kPfxStages * kStage;  // float [2][256]
+  static constexpr int kBar = kAlpha + 2 * kPfxRows * 4;
+  // full[2S], empty[2S], sfull, sfree, pfull[NP], odone[NP], drain
+  static constexpr int kNumBars = 4 * kPfxStages + 3 + 2 * kPfxPBufs;
+  static constexpr int kMisc = kBar + kNumBars * 8;      // tmem base, abort flag
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 227 * 1024, "prefix kernel shared memory above the per-CTA limit");
+};
+
+__device__ __forceinline__ uint8_t* pfx_align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Bounded mbarrier wait that also gives up when another role raised abort.
+__device__ __forceinline__ bool pfx_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+// OR of `pred` over the `count` threads of named barrier `id` (all of them
+// execute it; it also orders their shared-memory accesses).
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(kPfxThreads, 1)
+    phs_prefix_decode_kernel(const __grid_constant__ CUtensorMap tk,
+                             const __grid_constant__ CUtensorMap tv, const PrefixArgs a) {
+  using L = PfxLayout;
+  constexpr int D = 128;
+  constexpr int S = kPfxStages;
+  constexpr int NP = kPfxPBufs;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = pfx_align1024(smem_raw);
+  const uint32_t sb = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x, split = blockIdx.y;
+
+  // tiles of this CTA
+  const int ntiles_all = a.shared_len / kPfxTile;
+  const int t_begin = split * a.tiles_per_split;
+  const int t_end = min(ntiles_all, t_begin + a.tiles_per_split);
+  const int ntiles = max(0, t_end - t_begin);
+
+  const uint32_t bar_full = sb + L::kBar;                 // [2 (K, V)][S] stage loaded
+  const uint32_t bar_empty = bar_full + 16 * S;           // [2 (K, V)][S] stage consumed
+  const uint32_t bar_sfull = bar_empty + 16 * S;          // S_j in tensor memory
+  const uint32_t bar_sfree = bar_sfull + 8;               // S_j read by all rows
+  const uint32_t bar_pfull = bar_sfree + 8;               // [NP]: P buffer written
+  const uint32_t bar_odone = bar_pfull + 8 * NP;          // [NP]: P V of that buffer done
+  const uint32_t bar_drain = bar_odone + 8 * NP;          // every issued MMA done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  float* alpha_s = reinterpret_cast<float*>(smem + L::kAlpha);
+
+  if (warp == 9) {
+    tmem_alloc(sb + L::kMisc, 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 2 * S; ++i) {
+      mbar_init(bar_full + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, 1);
+    }
+    mbar_init(bar_sfull, 1);
+    mbar_init(bar_sfree, 256);
+    for (int i = 0; i < NP; ++i) {
+      mbar_init(bar_pfull + 8 * i, 256);
+      mbar_init(bar_odone + 8 * i, 1);
+    }
+    mbar_init(bar_drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // ---- queries: thread r puts row r (request r / G, head h*G + r % G) into
+  // tensor-memory lane r % 128 of row tile r / 128, as 64 columns of bf16
+  // pairs (element 2c in the low half of column c); rows past B*G are zero
+  if (warp < 8) {
+    const int r = tid;
+    const int mt = r >> 7;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const bool live = r < a.rows;
+    const uint4* src = live ? reinterpret_cast<const uint4*>(
+                                  a.q + (static_cast<size_t>(r / a.G) * a.Hq + h * a.G + r % a.G) * D)
+                            : nullptr;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t qv[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = live ? __ldg(src + half * 8 + c) : make_uint4(0, 0, 0, 0);
+        qv[4 * c] = v.x;
+        qv[4 * c + 1] = v.y;
+        qv[4 * c + 2] = v.z;
+        qv[4 * c + 3] = v.w;
+      }
+      tmem_st32(tmem + lane_base + kTmQ + mt * 64 + half * 32, qv);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == 8 || warp == 10) {
+    // ------------------------------------------- TMA producers (K, V)
+    // The copy engine's cost is per box, so a tile's boxes are issued by
+    // several lanes at once: K as eight 2 KB boxes (page i, column half) into
+    // [half][64 rows], V as four 4 KB 3-D boxes (one per page) into
+    // [page][half][16 rows].  Lane 0 owns the stage barriers.
+    if (ntiles > 0) {
+      const int kv = warp == 10;  // 0: K, 1: V
+      const CUtensorMap* map = kv ? &tv : &tk;
+      const uint32_t full = bar_full + 8 * S * kv, empty = bar_empty + 8 * S * kv;
+      const int nl = kv ? kPfxTile / kPage : 2 * kPfxTile / kPage;  // issuing lanes
+      const int pg = kv ? lane : (lane >> 1), half = kv ? 0 : (lane & 1);
+      const bool issuer = lane < nl;
+      const uint64_t pol = policy_evict_first();
+      if (lane == 0) prefetch_tmap(map);
+      int issued = 0;
+      bool ok = true;
+      // page ids are read two tiles ahead, so their latency overlaps the
+      // wait for a free stage instead of delaying the copies
+      auto page_id = [&](int jt) {
+        return issuer ? a.block_table[(t_begin + min(jt, ntiles - 1)) * (kPfxTile / kPage) + pg] : 0;
+      };
+      int id0 = page_id(0), id1 = page_id(1);
+      for (int j = 0; j < ntiles; ++j) {
+        const int st = j % S;
+        int page = id0;
+        id0 = id1;
+        id1 = page_id(j + 2);
+        if (lane == 0 && j >= S) ok = pfx_wait(empty + 8 * st, ((j / S) - 1) & 1, abort);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          if (lane == 0) {
+            set_status(a.status, PHS_ETIMEOUT);
+            *abort = 1;
+          }
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(full + 8 * st, L::kStage / 2);
+        __syncwarp();
+        if (issuer) {
+          if (page < 0 || page >= a.num_pages) {
+            set_status(a.status, PHS_ERANGE);
+            page = 0;  // keep the byte count: read a valid page, result flagged
+          }
+          const int row = (page * a.Hkv + h) * kPage;
+          const uint32_t stage = sb + L::kKV + st * L::kStage + kv * 16384;
+          if (kv)
+            tma_load_3d(stage + pg * 4096, map, 0, row, 0, full + 8 * st, pol);
+          else
+            tma_load_2d(stage + half * 8192 + pg * 2048, map, half * 64, row, full + 8 * st, pol);
+        }
+        issued = j + 1;
+      }
+      // copies still in flight land before the CTA exits (all have landed
+      // already unless another role gave up)
+      if (lane == 0)
+        for (int t = max(0, issued - S); t < issued; ++t) mbar_wait(full + 8 * (t % S), (t / S) & 1);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kPfxTile, false, false);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kPfxRows, true, false);
+      auto issue_qk = [&](int j) -> bool {
+        const int st = j % S;
+        if (!pfx_wait(bar_full + 8 * st, (j / S) & 1, abort)) return false;    // K_j
+        if (j >= 1 && !pfx_wait(bar_sfree, (j - 1) & 1, abort)) return false;  // S_{j-1} read
+        tc_fence_after();
+        const uint32_t kst = sb + L::kKV + st * L::kStage;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            umma_bf16_ts(tmem + kTmS + mt * kPfxTile, tmem + kTmQ + mt * 64 + ks * 8,
+                         sdesc_sw128(kst + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), kIdescQK,
+                         ks > 0);
+        }
+        umma_commit(bar_sfull);
+        umma_commit(bar_empty + 8 * st);  // K stage free once Q K_j^T completes
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int st = j % S, pb = j % NP;
+        if (!pfx_wait(bar_full + 8 * (S + st), (j / S) & 1, abort)) return false;  // V_j
+        if (!pfx_wait(bar_pfull + 8 * pb, (j / NP) & 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t vst = sb + L::kKV + st * L::kStage + 16384;
+        const uint32_t pst = sb + L::kP + pb * L::kPBuf;
+#pragma unroll
+        for (int kk = 0; kk < kPfxTile / 16; ++kk)
+          umma_bf16(tmem + kTmO, sdesc_sw128(vst + kk * 4096, 2048, 1024),
+                    sdesc_sw128(pst + kk * 32, 16, 1024), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar_odone + 8 * pb);
+        umma_commit(bar_empty + 8 * (S + st));  // V stage free once the product completes
+        return true;
+      };
+      bool ok = issue_qk(0);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (j + 1 < ntiles) ok = issue_qk(j + 1);
+        if (ok) ok = issue_pv(j);
+      }
+      if (!ok) {
+        set_status(a.status, PHS_ETIMEOUT);
+        *abort = 1;
+      }
+      // every MMA issued above completes before tensor memory is released
+      umma_commit(bar_drain);
+      mbar_wait(bar_drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------ softmax rows
+    const int mt = warp >> 2;
+    const int rr = 32 * (warp & 3) + lane;
+    const int r = mt * 128 + rr;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const bool got = pfx_wait(bar_sfull, j & 1, abort);
+      uint32_t sv0[32], sv1[32];  // scores of tokens 0..31 and 32..63 of the tile
+      if (got) {
+        tc_fence_after();
+        tmem_ld32(tmem + lane_base + kTmS + mt * kPfxTile, sv0);
+        tmem_ld32(tmem + lane_base + kTmS + mt * kPfxTile + 32, sv1);
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar_sfree);
+      // every softmax thread takes part in the same barrier reductions, so
+      // a failed wait ends the loop for all of them together
+      if (bar_red_or(1, 256, !got)) {
+        ok = false;
+        break;
+      }
+      auto sv = [&](int i) { return __uint_as_float(i < 32 ? sv0[i] : sv1[i - 32]); };
+      float m8[8];  // tree reduction: eight independent chains
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m8[k] = sv(k);
+#pragma unroll
+      for (int i = 8; i < kPfxTile; i += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], sv(i + k));
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      mx *= a.scale_log2;
+      float alpha = 1.f;
+      if (j == 0) {
+        m_used = mx;
+      } else if (mx > m_used + 8.f) {
+        alpha = ex2(m_used - mx);
+        m_used = mx;
+      }
+      float* al = alpha_s + (j & 1) * kPfxRows;
+      al[r] = alpha;
+      const bool resc = bar_red_or(1, 256, alpha != 1.f);
+      // P buffer j % NP was last read by P V_{j-NP}; a rescale of O needs P V_{j-1}
+      if (j >= NP || (resc && j >= 1)) {
+        const int jj = resc ? j - 1 : j - NP;
+        if (!pfx_wait(bar_odone + 8 * (jj % NP), (jj / NP) & 1, abort)) {
+          ok = false;  // the next tile's reduction ends the loop
+          *abort = 1;
+        }
+        tc_fence_after();
+      }
+      l *= alpha;
+      // P row: 64 bf16 = eight 16-byte units, K-major 128-byte swizzle
+      const float c0 = m_used;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint8_t* prow = smem + L::kP + (j % NP) * L::kPBuf + r * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float p0 = ex2(fmaf(sv(8 * u + 2 * k), a.scale_log2, -c0));
+          const float p1 = ex2(fmaf(sv(8 * u + 2 * k + 1), a.scale_log2, -c0));
+          sum4[k] += p0 + p1;
+          w[k] = pack_bf16(p0, p1);
+        }
+        *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      fence_proxy_async_smem();
+      if (resc) {
+        // this warp rescales O^T lanes d = 32 (warp & 3) .. +31, row columns
+        // 128 mt .. +127, by the factors every row published above
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          const int col0 = 128 * mt + 32 * c;
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + kTmO + col0, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * al[col0 + i]);
+          tmem_st32(tmem + lane_base + kTmO + col0, ov);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar_pfull + 8 * (j % NP));
+    }
+    // ---- partial result: O^T columns of this warp's rows, lanes = d
+    if (ok && ntiles > 0) {
+      const int jl = ntiles - 1;  // the last P V completes after all earlier ones
+      ok = pfx_wait(bar_odone + 8 * (jl % NP), (jl / NP) & 1, abort);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    const size_t part0 = (static_cast<size_t>(h) * a.num_splits + split) * kPfxRows;
+    if (ok) {
+      tc_fence_after();
+      const int d = 32 * (warp & 3) + lane;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        const int col0 = 128 * mt + 32 * c;
+        uint32_t ov[32];
+        if (ntiles > 0) {
+          tmem_ld32(tmem + lane_base + kTmO + col0, ov);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col0 + i < a.rows) a.ws_o[(part0 + col0 + i) * D + d] = __uint_as_float(ov[i]);
+      }
+      if (r < a.rows)
+        reinterpret_cast<float2*>(a.ws_ml)[part0 + r] =
+            make_float2(ntiles > 0 ? m_used : -INFINITY, ntiles > 0 ? l : 0.f);
+    } else if (lane == 0) {
+      set_status(a.status, PHS_ETIMEOUT);
+      *abort = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge of the shared-prefix partials with each request's suffix partials.
+// One CTA per (request, KV head); warp w merges query rows w, w+4, ...
+__global__ void __launch_bounds__(128) phs_merge_prefix_kernel(const PrefixMergeArgs a) {
+  constexpr int D = 128;
+  constexpr int V = D / 32;
+  const int b = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.G;
+  const int n = min(a.seq_lens[b], a.n_clamp);
+  const int ns = n > a.shared_len ? min((n - a.shared_len + a.T - 1) / a.T, a.max_splits) : 0;
+  const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
+  for (int g = warp; g < G; g += 4) {
+    const int r = b * G + g;
+    // sources: prefix splits then suffix splits
+    const int total = a.num_psplits + ns;
+    auto ml_of = [&](int s) -> float2 {
+      if (s < a.num_psplits)
+        return reinterpret_cast<const float2*>(
+            a.ws_pml)[(static_cast<size_t>(h) * a.num_psplits + s) * kPfxRows + r];
+      const size_t part = (static_cast<size_t>(b) * a.Hkv + h) * a.max_splits + (s - a.num_psplits);
+      return reinterpret_cast<const float2*>(a.ws_ml)[part * G + g];
+    };
+    auto o_of = [&](int s) -> const float* {
+      if (s < a.num_psplits)
+        return a.ws_po + ((static_cast<size_t>(h) * a.num_psplits + s) * kPfxRows + r) * D;
+      const size_t part = (static_cast<size_t>(b) * a.Hkv + h) * a.max_splits + (s - a.num_psplits);
+      return a.ws_o + (part * G + g) * D;
+    };
+    float M = -INFINITY;
+    for (int s = lane; s < total; s += 32) M = fmaxf(M, ml_of(s).x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float Lsum = 0.f;
+    float acc[V] = {0.f, 0.f, 0.f, 0.f};
+    for (int s0 = 0; s0 < total; s0 += 32) {
+      float wl = 0.f;
+      if (s0 + lane < total) {
+        const float2 v = ml_of(s0 + lane);
+        wl = v.x == -INFINITY ? 0.f : exp2f(v.x - M);
+        Lsum += v.y * wl;
+      }
+      const int cnt = min(32, total - s0);
+      for (int k = 0; k < cnt; ++k) {
+        const float w = __shfl_sync(0xffffffffu, wl, k);
+        const float4 o = *reinterpret_cast<const float4*>(o_of(s0 + k) + lane * V);
+        acc[0] += w * o.x;
+        acc[1] += w * o.y;
+        acc[2] += w * o.z;
+        acc[3] += w * o.w;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const size_t idx = out_row0 + static_cast<size_t>(g) * D + lane * V + i;
+      if (a.out_f32)
+        reinterpret_cast<float*>(a.out)[idx] = acc[i] * inv;
+      else
+        reinterpret_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(acc[i] * inv);
+    }
+  }
+}
+
+int launch_prefix_decode(const CUtensorMap& tk, const CUtensorMap& tv, const PrefixArgs& a,
+                         cudaStream_t stream) {
+  auto kern = phs_prefix_decode_kernel;
+  if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), PfxLayout::kAlloc) != PHS_OK)
+    return PHS_ECUDA;
+  dim3 grid(a.Hkv, a.num_splits);
+  kern<<<grid, kPfxThreads, PfxLayout::kAlloc, stream>>>(tk, tv, a);
+  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+}
+
+int launch_merge_prefix(const PrefixMergeArgs& a, int B, cudaStream_t stream) {
+  dim3 grid(B, a.Hkv);
+  phs_merge_prefix_kernel<<<grid, 128, 0, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+}
+
+int prefix_smem_bytes() { return PfxLayout::kAlloc; }
+
+}  // namespace phs
