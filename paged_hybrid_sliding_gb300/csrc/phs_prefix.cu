@@ -14,8 +14,15 @@
 //               128-byte swizzle), its copies issued by eight lanes at once
 //   warp 10   : the same for V (one 4 KB box per page); K and V stages are
 //               released separately (K after Q K^T, V after the P V product)
-//   warp 9    : MMA issuer (one lane); owns the tensor-memory allocation
+//   warp 9    : MMA issuer (one lane) of S = Q K^T for row tile 0 and of every
+//               P V product; owns the tensor-memory allocation
+//   warp 11   : MMA issuer (one lane) of S = Q K^T for row tile 1
 //   warps 0-7 : online softmax, one query row per thread
+// The tensor pipe holds about one instruction ahead, so an issuing thread
+// that waits for its scheduler leaves it idle; the softmax warps keep every
+// sub-partition busy, and two issuers on different sub-partitions cover for
+// each other (measured: a tile's 20 instructions take 1,600 cycles from one
+// issuer next to the softmax load, 1,210 from two).
 // Tensor memory (512 columns): S [128 lanes = rows][2 x 64 tokens], Q
 // [128 lanes = rows][2 x 64 columns of bf16 pairs], O^T [128 lanes = d][256
 // rows].  Per 64-token tile j:
@@ -41,17 +48,22 @@
 
 namespace phs {
 
-#ifndef PHS_PFX_STAGES
-#define PHS_PFX_STAGES 4
+#ifndef PHS_PFX_KSTAGES
+#define PHS_PFX_KSTAGES 4
+#endif
+#ifndef PHS_PFX_VSTAGES
+#define PHS_PFX_VSTAGES 4
 #endif
 #ifndef PHS_PFX_PBUFS
 #define PHS_PFX_PBUFS 2
 #endif
-constexpr int kPfxStages = PHS_PFX_STAGES;  // K/V tiles in shared memory
+constexpr int kPfxKStages = PHS_PFX_KSTAGES;  // K tiles in shared memory
+constexpr int kPfxVStages = PHS_PFX_VSTAGES;  // V tiles in shared memory
 constexpr int kPfxPBufs = PHS_PFX_PBUFS;    // P tiles in shared memory
 constexpr int kPfxTile = 64;     // tokens per tile (four pages)
 constexpr int kPfxRows = 256;    // query rows per KV head (two tiles of 128)
-constexpr int kPfxThreads = 352;  // 8 softmax warps, K producer, MMA, V producer
+// 8 softmax warps, K producer, MMA (row tile 0 + P V), V producer, MMA (row tile 1)
+constexpr int kPfxThreads = 384;
 
 // tensor-memory columns
 constexpr uint32_t kTmS = 0;     // S: row tile mt at kTmS + 64 mt
@@ -61,12 +73,13 @@ constexpr uint32_t kTmO = 256;   // O^T: row r at column kTmO + r
 struct PfxLayout {
   static constexpr int kP = 0;                           // [buf][256 rows][128 B]
   static constexpr int kPBuf = 32 * 1024;
-  static constexpr int kKV = kPfxPBufs * kPBuf;          // [stage][K 16 KB | V 16 KB]
-  static constexpr int kStage = 32 * 1024;
-  static constexpr int kAlpha = kKV + kPfxStages * kStage;  // float [2][256]
+  static constexpr int kTileKV = 16 * 1024;              // one 64-token K or V tile
+  static constexpr int kK = kPfxPBufs * kPBuf;           // K ring [KS][16 KB]
+  static constexpr int kV = kK + kPfxKStages * kTileKV;  // V ring [VS][16 KB]
+  static constexpr int kAlpha = kV + kPfxVStages * kTileKV;  // float [2][256]
   static constexpr int kBar = kAlpha + 2 * kPfxRows * 4;
-  // full[2S], empty[2S], sfull, sfree, pfull[NP], odone[NP], drain
-  static constexpr int kNumBars = 4 * kPfxStages + 3 + 2 * kPfxPBufs;
+  // full[KS + VS], empty[KS + VS], sfull[2], sfree[2], pfull[NP], odone[NP], drain
+  static constexpr int kNumBars = 2 * (kPfxKStages + kPfxVStages) + 5 + 2 * kPfxPBufs;
   static constexpr int kMisc = kBar + kNumBars * 8;      // tmem base, abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -110,7 +123,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
                              const __grid_constant__ CUtensorMap tv, const PrefixArgs a) {
   using L = PfxLayout;
   constexpr int D = 128;
-  constexpr int S = kPfxStages;
+  constexpr int KS = kPfxKStages, VS = kPfxVStages;
   constexpr int NP = kPfxPBufs;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = pfx_align1024(smem_raw);
@@ -124,11 +137,11 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
   const int t_end = min(ntiles_all, t_begin + a.tiles_per_split);
   const int ntiles = max(0, t_end - t_begin);
 
-  const uint32_t bar_full = sb + L::kBar;                 // [2 (K, V)][S] stage loaded
-  const uint32_t bar_empty = bar_full + 16 * S;           // [2 (K, V)][S] stage consumed
-  const uint32_t bar_sfull = bar_empty + 16 * S;          // S_j in tensor memory
-  const uint32_t bar_sfree = bar_sfull + 8;               // S_j read by all rows
-  const uint32_t bar_pfull = bar_sfree + 8;               // [NP]: P buffer written
+  const uint32_t bar_full = sb + L::kBar;                 // [KS + VS] stage loaded (K, then V)
+  const uint32_t bar_empty = bar_full + 8 * (KS + VS);    // [KS + VS] stage consumed
+  const uint32_t bar_sfull = bar_empty + 8 * (KS + VS);   // [2 row tiles] S_j in tensor memory
+  const uint32_t bar_sfree = bar_sfull + 16;              // [2 row tiles] S_j read by its rows
+  const uint32_t bar_pfull = bar_sfree + 16;              // [NP]: P buffer written
   const uint32_t bar_odone = bar_pfull + 8 * NP;          // [NP]: P V of that buffer done
   const uint32_t bar_drain = bar_odone + 8 * NP;          // every issued MMA done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
@@ -140,17 +153,19 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 2 * S; ++i) {
+    for (int i = 0; i < KS + VS; ++i) {
       mbar_init(bar_full + 8 * i, 1);
-      mbar_init(bar_empty + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, i < KS ? 2 : 1);  // a K stage is read by both Q K^T issuers
     }
-    mbar_init(bar_sfull, 1);
-    mbar_init(bar_sfree, 256);
+    for (int mt = 0; mt < 2; ++mt) {
+      mbar_init(bar_sfull + 8 * mt, 1);
+      mbar_init(bar_sfree + 8 * mt, 128);
+    }
     for (int i = 0; i < NP; ++i) {
       mbar_init(bar_pfull + 8 * i, 256);
       mbar_init(bar_odone + 8 * i, 1);
     }
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain, 2);
     *abort = 0;
     fence_mbar_init();
   }
@@ -198,7 +213,9 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     if (ntiles > 0) {
       const int kv = warp == 10;  // 0: K, 1: V
       const CUtensorMap* map = kv ? &tv : &tk;
-      const uint32_t full = bar_full + 8 * S * kv, empty = bar_empty + 8 * S * kv;
+      const int S = kv ? VS : KS;
+      const uint32_t full = bar_full + 8 * KS * kv, empty = bar_empty + 8 * KS * kv;
+      const uint32_t ring = sb + (kv ? L::kV : L::kK);
       const int nl = kv ? kPfxTile / kPage : 2 * kPfxTile / kPage;  // issuing lanes
       const int pg = kv ? lane : (lane >> 1), half = kv ? 0 : (lane & 1);
       const bool issuer = lane < nl;
@@ -225,7 +242,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
           }
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(full + 8 * st, L::kStage / 2);
+        if (lane == 0) mbar_arrive_expect_tx(full + 8 * st, L::kTileKV);
         __syncwarp();
         if (issuer) {
           if (page < 0 || page >= a.num_pages) {
@@ -233,7 +250,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
             page = 0;  // keep the byte count: read a valid page, result flagged
           }
           const int row = (page * a.Hkv + h) * kPage;
-          const uint32_t stage = sb + L::kKV + st * L::kStage + kv * 16384;
+          const uint32_t stage = ring + st * L::kTileKV;
           if (kv)
             tma_load_3d(stage + pg * 4096, map, 0, row, 0, full + 8 * st, pol);
           else
@@ -246,48 +263,46 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
       if (lane == 0)
         for (int t = max(0, issued - S); t < issued; ++t) mbar_wait(full + 8 * (t % S), (t / S) & 1);
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 11) {
+    // ------------------------------------------------------ MMA issuers
     if (lane == 0 && ntiles > 0) {
+      const int mt = warp == 11;  // row tile whose S = Q K^T this thread issues
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kPfxTile, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kPfxRows, true, false);
       auto issue_qk = [&](int j) -> bool {
-        const int st = j % S;
-        if (!pfx_wait(bar_full + 8 * st, (j / S) & 1, abort)) return false;    // K_j
-        if (j >= 1 && !pfx_wait(bar_sfree, (j - 1) & 1, abort)) return false;  // S_{j-1} read
+        const int st = j % KS;
+        if (!pfx_wait(bar_full + 8 * st, (j / KS) & 1, abort)) return false;  // K_j
+        if (j >= 1 && !pfx_wait(bar_sfree + 8 * mt, (j - 1) & 1, abort)) return false;
         tc_fence_after();
-        const uint32_t kst = sb + L::kKV + st * L::kStage;
+        const uint32_t kst = sb + L::kK + st * L::kTileKV;
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            umma_bf16_ts(tmem + kTmS + mt * kPfxTile, tmem + kTmQ + mt * 64 + ks * 8,
-                         sdesc_sw128(kst + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), kIdescQK,
-                         ks > 0);
-        }
-        umma_commit(bar_sfull);
-        umma_commit(bar_empty + 8 * st);  // K stage free once Q K_j^T completes
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_bf16_ts(tmem + kTmS + mt * kPfxTile, tmem + kTmQ + mt * 64 + ks * 8,
+                       sdesc_sw128(kst + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), kIdescQK,
+                       ks > 0);
+        umma_commit(bar_sfull + 8 * mt);
+        umma_commit(bar_empty + 8 * st);  // K stage free once both row tiles' products complete
         return true;
       };
       auto issue_pv = [&](int j) -> bool {
-        const int st = j % S, pb = j % NP;
-        if (!pfx_wait(bar_full + 8 * (S + st), (j / S) & 1, abort)) return false;  // V_j
+        const int st = j % VS, pb = j % NP;
+        if (!pfx_wait(bar_full + 8 * (KS + st), (j / VS) & 1, abort)) return false;  // V_j
         if (!pfx_wait(bar_pfull + 8 * pb, (j / NP) & 1, abort)) return false;
         tc_fence_after();
-        const uint32_t vst = sb + L::kKV + st * L::kStage + 16384;
+        const uint32_t vst = sb + L::kV + st * L::kTileKV;
         const uint32_t pst = sb + L::kP + pb * L::kPBuf;
 #pragma unroll
         for (int kk = 0; kk < kPfxTile / 16; ++kk)
           umma_bf16(tmem + kTmO, sdesc_sw128(vst + kk * 4096, 2048, 1024),
                     sdesc_sw128(pst + kk * 32, 16, 1024), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar_odone + 8 * pb);
-        umma_commit(bar_empty + 8 * (S + st));  // V stage free once the product completes
+        umma_commit(bar_empty + 8 * (KS + st));  // V stage free once the product completes
         return true;
       };
       bool ok = issue_qk(0);
       for (int j = 0; ok && j < ntiles; ++j) {
         if (j + 1 < ntiles) ok = issue_qk(j + 1);
-        if (ok) ok = issue_pv(j);
+        if (ok && mt == 0) ok = issue_pv(j);
       }
       if (!ok) {
         set_status(a.status, PHS_ETIMEOUT);
@@ -306,7 +321,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      const bool got = pfx_wait(bar_sfull, j & 1, abort);
+      const bool got = pfx_wait(bar_sfull + 8 * mt, j & 1, abort);
       uint32_t sv0[32], sv1[32];  // scores of tokens 0..31 and 32..63 of the tile
       if (got) {
         tc_fence_after();
@@ -315,7 +330,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
         tmem_ld_wait();
       }
       tc_fence_before();
-      mbar_arrive(bar_sfree);
+      mbar_arrive(bar_sfree + 8 * mt);
       // every softmax thread takes part in the same barrier reductions, so
       // a failed wait ends the loop for all of them together
       if (bar_red_or(1, 256, !got)) {
