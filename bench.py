@@ -65,7 +65,7 @@ def peak_tflops():
 
 
 def kernel_source_hash(files=SPLIT_KERNEL_SOURCES):
-    """Hash of the sources the split-KV decode kernel is compiled from."""
+    """Hash of the kernel sources a traffic record was taken on."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "paged_hybrid_sliding_gb300", "csrc")
     for name in files:
@@ -75,17 +75,20 @@ def kernel_source_hash(files=SPLIT_KERNEL_SOURCES):
 
 
 def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    """DRAM bytes per launch from the committed ncu records (profiles/
+    traffic.json), if one was taken for this kernel and workload on the
+    current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
-    e = rec.get(kernel, {})
-    if e.get("workload") != workload or e.get("source_hash") != kernel_source_hash():
-        return None
-    return e.get("dram_bytes_per_launch")
+    for e in rec.get("entries", []):
+        if e.get("kernel") == kernel and e.get("workload") == workload:
+            if e.get("source_hash") != kernel_source_hash(e.get("sources", SPLIT_KERNEL_SOURCES)):
+                return None
+            return e.get("dram_bytes_per_launch")
+    return None
 
 
 class ClockSampler:

@@ -112,6 +112,13 @@ int map_bf16_pages3d(CUtensorMap* m, const void* base, int64_t rows) {
   return r == CUDA_SUCCESS ? PHS_OK : PHS_ECUDA;
 }
 
+// Map for the per-page K/V copies of the decode kernels: one 3-D box per
+// 16-row block when D = 128, two 2-D boxes of 64 columns otherwise (D = 64:
+// one box).  Both land as [column half][16 rows][128 B] in shared memory.
+int map_bf16_kv(CUtensorMap* m, const void* base, int64_t rows, int D) {
+  return D == 128 ? map_bf16_pages3d(m, base, rows) : map_bf16_rows(m, base, rows, D);
+}
+
 // int8 codes, rows of D bytes; boxes of 32 rows x D with the 128-byte
 // (D = 128) or 64-byte (D = 64) swizzle.
 int map_i8_rows(CUtensorMap* m, const void* base, int64_t rows, int D) {
@@ -293,8 +300,8 @@ int prepare_decode(DecodeCall& c, const void* q, int Hq, const phs_paged_pool* p
   c.m.out_f32 = c.a.out_f32;
 
   const int64_t rows = pool->num_pages * Hkv * kPage;
-  if ((st = map_bf16_rows(&c.tk, pool->k, rows, D))) return st;
-  if ((st = map_bf16_rows(&c.tv, pool->v, rows, D))) return st;
+  if ((st = map_bf16_kv(&c.tk, pool->k, rows, D))) return st;
+  if ((st = map_bf16_kv(&c.tv, pool->v, rows, D))) return st;
   if (int8) {
     const int64_t qrows = int8->num_qpages * Hkv * kQBlock;
     if ((st = map_i8_rows(&c.tk8, int8->k, qrows, D))) return st;
@@ -527,8 +534,8 @@ int phs_attn_decode_swa_ring(const void* q, int32_t num_q_heads, const phs_ring_
   if (swa_smem_bytes(D, num_q_heads / Hkv, batch) > di.smem_optin) return PHS_EUNSUPPORTED;
   SwaParams<1> p;
   std::memset(&p, 0, sizeof(p));
-  if ((st = map_bf16_rows(&p.tk[0], ring->k, ring->num_rings * Hkv * ring->window, D))) return st;
-  if ((st = map_bf16_rows(&p.tv[0], ring->v, ring->num_rings * Hkv * ring->window, D))) return st;
+  if ((st = map_bf16_kv(&p.tk[0], ring->k, ring->num_rings * Hkv * ring->window, D))) return st;
+  if ((st = map_bf16_kv(&p.tv[0], ring->v, ring->num_rings * Hkv * ring->window, D))) return st;
   p.q[0] = reinterpret_cast<const __nv_bfloat16*>(q);
   p.out[0] = out;
   p.num_rings[0] = ring->num_rings;
@@ -613,10 +620,9 @@ int phs_attn_decode_shared_prefix(const void* q, int32_t num_q_heads, const phs_
   if (!workspace || workspace_bytes < pl.need) return PHS_EWORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || !aligned16(q)) return PHS_EALIGN;
   char* ws = reinterpret_cast<char*>(workspace);
-  CUtensorMap tk, tv;
+  CUtensorMap tk;  // 64-column boxes: the prefix kernel's K tile is [half][64 rows]
   const int64_t rows = pool->num_pages * Hkv * kPage;
   if ((st = map_bf16_rows(&tk, pool->k, rows, D))) return st;
-  if ((st = map_bf16_rows(&tv, pool->v, rows, D))) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   // 1. the shared prefix, all requests at once (tensor cores)
@@ -636,7 +642,8 @@ int phs_attn_decode_shared_prefix(const void* q, int32_t num_q_heads, const phs_
   pa.tiles_per_split = pl.tps;
   pa.num_splits = pl.nsp;
   pa.scale_log2 = scale_log2;
-  CUtensorMap tv3;
+  CUtensorMap tk3, tv3;  // per-page boxes (split kernel K/V, prefix kernel V)
+  if ((st = map_bf16_pages3d(&tk3, pool->k, rows))) return st;
   if ((st = map_bf16_pages3d(&tv3, pool->v, rows))) return st;
   if ((st = launch_prefix_decode(tk, tv3, pa, s))) return st;
   // 2. each request's own tokens [shared_len, n) (split-KV, partials only)
@@ -661,7 +668,7 @@ int phs_attn_decode_shared_prefix(const void* q, int32_t num_q_heads, const phs_
   a.scale_log2 = scale_log2;
   a.skip_len = shared_len;
   a.force_partial = 1;
-  if ((st = launch_split_decode(D, tk, tv, tk, tv, a, batch, s))) return st;
+  if ((st = launch_split_decode(D, tk3, tv3, tk3, tv3, a, batch, s))) return st;
   // 3. merge prefix and suffix partials
   PrefixMergeArgs m;
   std::memset(&m, 0, sizeof(m));
@@ -794,8 +801,8 @@ int phs_attn_decode_hybrid_stack(const phs_layer* layers, int32_t num_layers,
       if (L.is_full) continue;
       const int k = p->num_layers;
       const int64_t rows = L.ring.num_rings * Hkv * W;
-      if ((st = map_bf16_rows(&p->tk[k], L.ring.k, rows, D))) break;
-      if ((st = map_bf16_rows(&p->tv[k], L.ring.v, rows, D))) break;
+      if ((st = map_bf16_kv(&p->tk[k], L.ring.k, rows, D))) break;
+      if ((st = map_bf16_kv(&p->tv[k], L.ring.v, rows, D))) break;
       p->q[k] = reinterpret_cast<const __nv_bfloat16*>(L.q);
       p->out[k] = L.out;
       p->num_rings[k] = L.ring.num_rings;

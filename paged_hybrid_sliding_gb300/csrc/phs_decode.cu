@@ -250,10 +250,12 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
       tma_load_2d(dst + L::kStage / 2, &tv8, 0, row, bar, pol);
     } else {
       const int row = (id * a.Hkv + h) * kPage;
-#pragma unroll
-      for (int sub = 0; sub < D / 64; ++sub) {
-        tma_load_2d(dst + sub * 2048, &tk, sub * 64, row, bar, pol);
-        tma_load_2d(dst + L::kStage / 2 + sub * 2048, &tv, sub * 64, row, bar, pol);
+      if constexpr (D == 128) {  // one 4 KB box per page: [half][16 rows]
+        tma_load_3d(dst, &tk, 0, row, 0, bar, pol);
+        tma_load_3d(dst + L::kStage / 2, &tv, 0, row, 0, bar, pol);
+      } else {
+        tma_load_2d(dst, &tk, 0, row, bar, pol);
+        tma_load_2d(dst + L::kStage / 2, &tv, 0, row, bar, pol);
       }
     }
   };

@@ -110,10 +110,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
       const uint32_t qbytes = ic == 0 ? static_cast<uint32_t>(G * D * 2) : 0u;
       mbar_arrive_expect_tx(bar, L.kv + qbytes);
       const int row = (iu.ring * Hkv + iu.h) * W + kPage * ic;
-#pragma unroll
-      for (int sub = 0; sub < D / 64; ++sub) {
-        tma_load_2d(dst + sub * 2048, &p.tk[iu.l], sub * 64, row, bar, pol);
-        tma_load_2d(dst + L.kv / 2 + sub * 2048, &p.tv[iu.l], sub * 64, row, bar, pol);
+      if constexpr (D == 128) {  // one 4 KB box per 16-row block: [half][16 rows]
+        tma_load_3d(dst, &p.tk[iu.l], 0, row, 0, bar, pol);
+        tma_load_3d(dst + L.kv / 2, &p.tv[iu.l], 0, row, 0, bar, pol);
+      } else {
+        tma_load_2d(dst, &p.tk[iu.l], 0, row, bar, pol);
+        tma_load_2d(dst + L.kv / 2, &p.tv[iu.l], 0, row, bar, pol);
       }
       if (ic == 0) {
         const __nv_bfloat16* q =
