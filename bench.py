@@ -291,9 +291,10 @@ class TinyHybridWorkload(Workload):
     kernel_launches_per_step = 0
     l2 = "latency-bound case: ~0.2 MB per step, resident in L2"
 
-    def __init__(self, device, seed=1):
+    def __init__(self, device, seed=1, fused=True):
         import paged_hybrid_sliding_gb300 as phs
         self.phs = phs
+        self.fused = fused
         self.w = w = synth.tiny_hybrid(seed=seed)
         self.name = "tiny_hybrid_b2_hq4_hkv2_d64_full+swa_w128"
         B, Hq, Hkv, D, W = w.B, w.Hq, w.Hkv, w.D, w.W
@@ -317,8 +318,9 @@ class TinyHybridWorkload(Workload):
             phs.Layer(q=self.qs, out=self.os, ring=phs.RingPool(self.kr, self.vr),
                       k_new=self.kn, v_new=self.vn)]
         self.max_seq = int(w.n_after.max())
-        self.ws = torch.empty(phs.hybrid_stack_workspace_bytes(B, Hq, Hkv, D, self.max_seq),
-                              dtype=torch.uint8, device=device)
+        ws_bytes = (phs.hybrid_stack_fused_workspace_bytes(B, Hq, Hkv, D, self.max_seq, 1)
+                    if fused else phs.hybrid_stack_workspace_bytes(B, Hq, Hkv, D, self.max_seq))
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
         full_tok = int(w.n_after.sum())
         swa_tok = int(np.minimum(w.n_after, W).sum())
         self.tokens_per_step = full_tok + swa_tok
@@ -326,8 +328,11 @@ class TinyHybridWorkload(Workload):
         self.bytes_per_step = (full_tok + swa_tok) * tok_bytes + 2 * 2 * B * Hq * D * 2 + \
             2 * 2 * B * Hkv * D * 2
         self.kernel_bytes = None
-        self.launches_per_step = 4   # 2 appends, SWA decode, split (one split: no merge)
-        self.extra = {"batch": B, "layers": "1 Full + 1 SWA(W=128)"}
+        # fused: Full split (append fused, one split: no merge) + SWA decode;
+        # else 2 appends, SWA decode, split
+        self.launches_per_step = 2 if fused else 4
+        self.extra = {"batch": B, "layers": "1 Full + 1 SWA(W=128)",
+                      "append_fused_into_attention": fused}
         self.host = [pinned(t) for t in (self.qf, self.qs, self.kn, self.vn, self.sl, self.rp,
                                          self.bt)]
         self.dev_in = [self.qf, self.qs, self.kn, self.vn, self.sl, self.rp, self.bt]
@@ -337,6 +342,11 @@ class TinyHybridWorkload(Workload):
         self.d2h_bytes = nbytes(self.h_of, self.h_os)
 
     def step(self, ev=None):
+        if self.fused:
+            self.phs.attn_decode_hybrid_stack_fused(self.layers, self.w.Hq, self.sl, self.max_seq,
+                                                    block_table=self.bt, ring_pos=self.rp,
+                                                    workspace=self.ws)
+            return
         self.phs.attn_decode_hybrid_stack(self.layers, self.w.Hq, self.sl, self.max_seq,
                                           block_table=self.bt, ring_pos=self.rp,
                                           workspace=self.ws)
@@ -379,9 +389,10 @@ class HybridStackWorkload(Workload):
 
     kernel_launches_per_step = 0
 
-    def __init__(self, device, seed=3, distinct=4, batch=256, swa_only=False):
+    def __init__(self, device, seed=3, distinct=4, batch=256, swa_only=False, fused=True):
         import paged_hybrid_sliding_gb300 as phs
         self.phs = phs
+        self.fused = fused
         self.w = w = synth.hybrid_stack(seed=seed, B=batch)
         B, Hq, Hkv, D, W = w.B, w.Hq, w.Hkv, w.D, w.W
         lf = w.extra["layer_is_full"]
@@ -422,9 +433,10 @@ class HybridStackWorkload(Workload):
         self.host = [pinned(t) for t in self.dev_in]
         self.h_outs = [torch.empty_like(o, device="cpu").pin_memory() for o in self.outs]
         self.max_seq = int(w.n_after.max())
-        self.ws = torch.empty(phs.hybrid_stack_workspace_bytes(B, Hq, Hkv, D, self.max_seq),
-                              dtype=torch.uint8, device=device)
         nfull, nswa = int(lf.sum()), int(len(lf) - lf.sum())
+        ws_bytes = (phs.hybrid_stack_fused_workspace_bytes(B, Hq, Hkv, D, self.max_seq, nfull)
+                    if fused else phs.hybrid_stack_workspace_bytes(B, Hq, Hkv, D, self.max_seq))
+        self.ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
         full_tok = int(w.n_after.sum())
         swa_tok = int(np.minimum(w.n_after, W).sum())
         tok_bytes = Hkv * D * 2 * 2
@@ -438,11 +450,18 @@ class HybridStackWorkload(Workload):
         self.kernel_bytes = self.full_layer_bytes if nfull else self.swa_bytes
         if not nfull:
             self.kernel = "phs_swa_decode_kernel"
-        self.launches_per_step = (2 if nfull else 1) + 1 + 2 * nfull
+        elif fused:
+            self.kernel = ("phs_stack_full_kernel + phs_stack_merge_kernel (all Full layers in one "
+                           "launch each, append fused; per-layer average)")
+        if fused:
+            self.launches_per_step = (2 if nfull else 0) + (1 if nswa else 0)
+        else:
+            self.launches_per_step = (2 if nfull else 1) + 1 + 2 * nfull
         self.extra = {"batch": B, "layers": f"{nfull} Full + {nswa} SWA(W=128)",
                       "distinct_full_pools": distinct, "full_layers_aliased_onto": distinct,
                       "full_bytes_per_step": nfull * self.full_layer_bytes,
-                      "swa_bytes_per_step": self.swa_bytes}
+                      "swa_bytes_per_step": self.swa_bytes,
+                      "append_fused_into_attention": fused}
         if nfull:
             self.extra["kv_tokens_stored_ratio_vs_all_full"] = round(
                 (nfull * full_tok + nswa * swa_tok) / (len(lf) * full_tok), 4)
@@ -450,6 +469,11 @@ class HybridStackWorkload(Workload):
         self.d2h_bytes = nbytes(*self.h_outs)
 
     def step(self, ev=None):
+        if self.fused:
+            self.phs.attn_decode_hybrid_stack_fused(self.layers, self.w.Hq, self.sl, self.max_seq,
+                                                    block_table=self.bt, ring_pos=self.rp,
+                                                    workspace=self.ws)
+            return
         self.phs.attn_decode_hybrid_stack(self.layers, self.w.Hq, self.sl, self.max_seq,
                                           block_table=self.bt, ring_pos=self.rp,
                                           workspace=self.ws)
@@ -469,6 +493,20 @@ class HybridStackWorkload(Workload):
         full = [L for L in self.layers if L.paged is not None]
         if not full:
             return None, self._swa_time(reps)
+        if self.fused:
+            # the step's Full part: one multi-layer split launch (append fused)
+            # plus one merge launch; per-layer average reported
+            def run():
+                phs.attn_decode_hybrid_stack_fused(full, w.Hq, self.sl, self.max_seq,
+                                                   block_table=self.bt, workspace=self.ws)
+            run()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                run()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / 1e3 / reps / len(full), self._swa_time(reps)
         ts = []
         for _ in range(reps):
             for L in full:
@@ -788,12 +826,13 @@ class SharedPrefixWorkload(Workload):
 
 def make_workload(config, device, args):
     if config == 1:
-        return TinyHybridWorkload(device)
+        return TinyHybridWorkload(device, fused=not args.no_fused)
     if config == 2:
         return PagedFullWorkload(device, batch=args.batch or 64)
     if config == 3:
         return HybridStackWorkload(device, distinct=args.distinct_pools,
-                                   batch=args.batch or 256, swa_only=args.swa_only)
+                                   batch=args.batch or 256, swa_only=args.swa_only,
+                                   fused=not args.no_fused)
     if config == 4:
         return Int8Workload(device, batch=args.batch or 32)
     if config == 5:
@@ -1041,6 +1080,10 @@ def main():
                          "profiler captures)")
     ap.add_argument("--swa-only", action="store_true",
                     help="config 3: only the 60 SWA layers (profiler captures)")
+    ap.add_argument("--no-fused", action="store_true",
+                    help="configs 1 and 3: separate append launches and one split + merge per "
+                         "Full layer instead of the fused step (appends inside the attention "
+                         "launches, all Full layers in one launch)")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
                     help="1 tiny hybrid, 2 paged Full batch 64 (default), 3 70-layer hybrid "
                          "stack, 4 INT8 block-32, 5 shared 250K prefix")

@@ -338,6 +338,39 @@ size_t phs_hybrid_stack_workspace_bytes(int32_t batch, int32_t num_q_heads,
                                         int32_t num_kv_heads, int32_t head_dim,
                                         int32_t max_seq_len);
 
+/* ------------------------------------------------------------------------
+ * One decode step of a hybrid layer stack, appends fused into the attention
+ * launches.  Source: MiMo page, section 1 (10 Full + 60 SWA layers) and
+ * section 2 (layer-wise overlap of a step; the whole step replayed as a
+ * graph).  Same contract as phs_attn_decode_hybrid_stack with do_append = 1:
+ * every layer's k_new/v_new ([batch][Hkv][D] bf16, 16-byte aligned,
+ * required) is written into slot seq_lens[b]-1 of its page (Full, through
+ * the shared block_table) or into ring slot ring_pos[b] (SWA), and attended
+ * as the newest token -- the kernels take it from k_new/v_new instead of
+ * reading it back.  Launches: one split-KV launch and one merge launch for
+ * up to 16 Full layers at once, one persistent launch for up to 64 SWA
+ * layers (config 3, 10 Full + 60 SWA: three launches per step instead of
+ * twenty-three).  The Full layers' partials live side by side, so the
+ * workspace is phs_hybrid_stack_fused_workspace_bytes (256-byte aligned).
+ * Outputs and pool contents equal those of the unfused call.
+ * Errors as phs_attn_decode_hybrid_stack (PHS_EINVAL also for a missing
+ * k_new/v_new); block-table ids must be valid for every Full pool.
+ * ---------------------------------------------------------------------- */
+int phs_attn_decode_hybrid_stack_fused(const phs_layer *layers, int32_t num_layers,
+                                       int32_t num_q_heads, int32_t batch,
+                                       const int32_t *block_table, int32_t max_pages_per_seq,
+                                       const int32_t *seq_lens, int32_t max_seq_len,
+                                       const int32_t *ring_ids, const int32_t *ring_pos,
+                                       float softmax_scale, int32_t out_dtype, void *workspace,
+                                       size_t workspace_bytes, int32_t *dev_status,
+                                       void *stream);
+
+/* Workspace of phs_attn_decode_hybrid_stack_fused: one split-partials area
+ * per Full layer (0 when num_full_layers <= 0). */
+size_t phs_hybrid_stack_fused_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                              int32_t num_kv_heads, int32_t head_dim,
+                                              int32_t max_seq_len, int32_t num_full_layers);
+
 /* KV tokens held by a hybrid stack (host arrays in, host results out):
  * Full layers hold seq_lens[b] tokens per request, SWA layers
  * min(seq_lens[b], window).  Source: MiMo page, section 1 (the 10/60 stack

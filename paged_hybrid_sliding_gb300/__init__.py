@@ -26,6 +26,7 @@ __all__ = [
     "attn_decode_full_paged_noalloc", "NOALLOC_SCRATCH_BYTES",
     "attn_decode_shared_prefix", "shared_prefix_workspace_bytes",
     "attn_decode_swa_ring", "attn_decode_hybrid_stack", "hybrid_stack_workspace_bytes",
+    "attn_decode_hybrid_stack_fused", "hybrid_stack_fused_workspace_bytes",
     "hybrid_kv_tokens", "copy_d2d", "copy_pages", "PageAllocator", "RadixTree",
     "window_safe_len", "lib", "PAGE", "QBLOCK",
 ]
@@ -429,6 +430,43 @@ def attn_decode_hybrid_stack(layers, num_q_heads, seq_lens, max_seq_len, block_t
         _ptr(ring_ids), _ptr(ring_pos), scale, int(bool(do_append)), out_code, _ptr(workspace),
         0 if workspace is None else workspace.numel(), _ptr(status), _stream(stream)),
         "attn_decode_hybrid_stack")
+
+
+def hybrid_stack_fused_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                                       num_full_layers):
+    return int(lib().phs_hybrid_stack_fused_workspace_bytes(batch, num_q_heads, num_kv_heads,
+                                                            head_dim, max_seq_len,
+                                                            num_full_layers))
+
+
+def attn_decode_hybrid_stack_fused(layers, num_q_heads, seq_lens, max_seq_len, block_table=None,
+                                   ring_pos=None, ring_ids=None, softmax_scale=None,
+                                   workspace=None, status=None, stream=None):
+    """One decode step over every layer of a hybrid stack with the appends
+    fused into the attention launches (every layer needs k_new / v_new)."""
+    arr = (_lib.LayerC * len(layers))(*[L.c() for L in layers])
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _opt(block_table, torch.int32, "block_table", 2)
+    _opt(ring_pos, torch.int32, "ring_pos", 1)
+    _opt(ring_ids, torch.int32, "ring_ids", 1)
+    _opt(status, torch.int32, "status")
+    B = seq_lens.shape[0]
+    q0 = layers[0].q
+    D = q0.shape[2]
+    out_code = _out_code(layers[0].out.dtype)
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    nfull = sum(1 for L in layers if L.paged is not None)
+    if workspace is None and nfull:
+        hkv = next(L.paged.k.shape[1] for L in layers if L.paged is not None)
+        workspace = torch.empty(hybrid_stack_fused_workspace_bytes(B, num_q_heads, hkv, D,
+                                                                   max_seq_len, nfull),
+                                dtype=torch.uint8, device=q0.device)
+    _check(lib().phs_attn_decode_hybrid_stack_fused(
+        arr, len(layers), num_q_heads, B, _ptr(block_table),
+        0 if block_table is None else block_table.shape[1], _ptr(seq_lens), int(max_seq_len),
+        _ptr(ring_ids), _ptr(ring_pos), scale, out_code, _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _ptr(status), _stream(stream)),
+        "attn_decode_hybrid_stack_fused")
 
 
 def hybrid_kv_tokens(layer_is_full, seq_lens_host, window):

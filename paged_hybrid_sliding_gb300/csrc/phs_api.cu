@@ -829,6 +829,184 @@ int phs_attn_decode_hybrid_stack(const phs_layer* layers, int32_t num_layers,
   return PHS_OK;
 }
 
+size_t phs_hybrid_stack_fused_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                              int32_t num_kv_heads, int32_t head_dim,
+                                              int32_t max_seq_len, int32_t num_full_layers) {
+  if (num_full_layers <= 0) return 0;
+  const size_t one =
+      phs_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, 0, 0);
+  return one * static_cast<size_t>(num_full_layers);
+}
+
+int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_layers,
+                                       int32_t num_q_heads, int32_t batch,
+                                       const int32_t* block_table, int32_t max_pages_per_seq,
+                                       const int32_t* seq_lens, int32_t max_seq_len,
+                                       const int32_t* ring_ids, const int32_t* ring_pos,
+                                       float softmax_scale, int32_t out_dtype, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_status,
+                                       void* stream) {
+  if (!layers || num_layers <= 0 || batch < 0 || !seq_lens) return PHS_EINVAL;
+  if (out_dtype != PHS_OUT_BF16 && out_dtype != PHS_OUT_F32) return PHS_EINVAL;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return PHS_EINVAL;
+  if (batch == 0) return PHS_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int st;
+  // ---- validate every layer before launching anything
+  int D = -1, Hkv = -1, W = -1, nfull = 0, nswa = 0;
+  int64_t min_pages = 0;  // the Full pools share the block table: ids must fit all of them
+  for (int i = 0; i < num_layers; ++i) {
+    const phs_layer& L = layers[i];
+    if (!L.q || !L.out || !L.k_new || !L.v_new) return PHS_EINVAL;
+    int d, h;
+    if (L.is_full) {
+      if ((st = check_paged(&L.paged))) return st;
+      d = L.paged.head_dim;
+      h = L.paged.num_kv_heads;
+      min_pages = nfull == 0 ? L.paged.num_pages : std::min(min_pages, L.paged.num_pages);
+      ++nfull;
+    } else {
+      if ((st = check_ring(&L.ring))) return st;
+      d = L.ring.head_dim;
+      h = L.ring.num_kv_heads;
+      if (W < 0) W = L.ring.window;
+      if (L.ring.window != W) return PHS_ESHAPE;
+      ++nswa;
+    }
+    if (D < 0) {
+      D = d;
+      Hkv = h;
+    }
+    if (d != D || h != Hkv) return PHS_ESHAPE;
+    if (!aligned16(L.q) || !aligned16(L.k_new) || !aligned16(L.v_new)) return PHS_EALIGN;
+  }
+  if ((st = check_dims(num_q_heads, Hkv, D))) return st;
+  if (nfull && (!block_table || max_pages_per_seq <= 0)) return PHS_EINVAL;
+  if (nswa && !ring_pos) return PHS_EINVAL;
+  DevInfo di;
+  if ((st = dev_info(di))) return st;
+  if (nswa && swa_smem_bytes(D, num_q_heads / Hkv, batch) > di.smem_optin) return PHS_EUNSUPPORTED;
+  DecodePlan pl;
+  if (nfull) {
+    if ((st = make_plan(pl, batch, num_q_heads, Hkv, D, max_seq_len, 0, false))) return st;
+    if (!workspace || workspace_bytes < pl.need * static_cast<size_t>(nfull))
+      return PHS_EWORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PHS_EALIGN;
+  }
+  const float scale_log2 = softmax_scale * 1.4426950408889634f;
+
+  // ---- launch 1 (per 16 Full layers): split-KV decode of every Full layer,
+  // each CTA holding a request's newest token also appends it
+  if (nfull) {
+    StackFullParams* p = new StackFullParams();
+    std::memset(p, 0, sizeof(*p));
+    StackMergeParams* m = new StackMergeParams();
+    std::memset(m, 0, sizeof(*m));
+    SplitArgs& a = p->a;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.status = dev_status;
+    a.num_pages = min_pages;
+    a.Hq = num_q_heads;
+    a.Hkv = Hkv;
+    a.G = pl.G;
+    a.max_pages = max_pages_per_seq;
+    a.n_clamp = static_cast<int>(std::min<long long>(max_seq_len, 1LL * max_pages_per_seq * kPage));
+    a.T = pl.T;
+    a.max_splits = pl.max_splits;
+    a.out_f32 = out_dtype == PHS_OUT_F32;
+    a.scale_log2 = scale_log2;
+    MergeArgs& ma = m->a;
+    ma.seq_lens = seq_lens;
+    ma.Hq = num_q_heads;
+    ma.Hkv = Hkv;
+    ma.G = pl.G;
+    ma.n_clamp = a.n_clamp;
+    ma.T = pl.T;
+    ma.max_splits = pl.max_splits;
+    ma.out_f32 = a.out_f32;
+    const size_t off_ml = ws_o_bytes(batch, Hkv, pl.max_splits, pl.G, D);
+    char* ws = reinterpret_cast<char*>(workspace);
+    int k = 0, done = 0;
+    st = PHS_OK;
+    for (int i = 0; i < num_layers && st == PHS_OK; ++i) {
+      const phs_layer& L = layers[i];
+      if (!L.is_full) continue;
+      StackFullLayer& F = p->layer[k];
+      const int64_t rows = L.paged.num_pages * Hkv * kPage;
+      if ((st = map_bf16_kv(&F.tk, L.paged.k, rows, D))) break;
+      if ((st = map_bf16_kv(&F.tv, L.paged.v, rows, D))) break;
+      char* lw = ws + pl.need * static_cast<size_t>(done + k);
+      F.q = reinterpret_cast<const __nv_bfloat16*>(L.q);
+      F.out = L.out;
+      F.ws_o = reinterpret_cast<float*>(lw);
+      F.ws_ml = reinterpret_cast<float*>(lw + off_ml);
+      F.app = FusedAppend{reinterpret_cast<const __nv_bfloat16*>(L.k_new),
+                          reinterpret_cast<const __nv_bfloat16*>(L.v_new),
+                          reinterpret_cast<__nv_bfloat16*>(L.paged.k),
+                          reinterpret_cast<__nv_bfloat16*>(L.paged.v)};
+      m->layer[k] = StackMergeLayer{F.ws_o, F.ws_ml, L.out};
+      if (++k == kStackMaxFull) {
+        p->num_layers = k;
+        if ((st = launch_stack_full(D, *p, batch, s))) break;
+        if (pl.max_splits > 1 && (st = launch_stack_merge(D, *m, batch, k, s))) break;
+        done += k;
+        k = 0;
+      }
+    }
+    if (st == PHS_OK && k) {
+      p->num_layers = k;
+      st = launch_stack_full(D, *p, batch, s);
+      if (st == PHS_OK && pl.max_splits > 1) st = launch_stack_merge(D, *m, batch, k, s);
+    }
+    delete p;
+    delete m;
+    if (st) return st;
+  }
+
+  // ---- launch 2: every SWA layer (one persistent launch per 64 layers),
+  // each unit holding a request's newest slot also appends it
+  if (nswa) {
+    SwaParams<kSwaMaxLayers>* p = new SwaParams<kSwaMaxLayers>();
+    std::memset(p, 0, sizeof(*p));
+    p->ring_ids = ring_ids;
+    p->ring_pos = ring_pos;
+    p->seq_lens = seq_lens;
+    p->status = dev_status;
+    p->B = batch;
+    p->Hq = num_q_heads;
+    p->Hkv = Hkv;
+    p->G = num_q_heads / Hkv;
+    p->W = W;
+    p->out_f32 = out_dtype == PHS_OUT_F32;
+    p->scale_log2 = scale_log2;
+    st = PHS_OK;
+    for (int i = 0; i < num_layers && st == PHS_OK; ++i) {
+      const phs_layer& L = layers[i];
+      if (L.is_full) continue;
+      const int k = p->num_layers;
+      const int64_t rows = L.ring.num_rings * Hkv * W;
+      if ((st = map_bf16_kv(&p->tk[k], L.ring.k, rows, D))) break;
+      if ((st = map_bf16_kv(&p->tv[k], L.ring.v, rows, D))) break;
+      p->q[k] = reinterpret_cast<const __nv_bfloat16*>(L.q);
+      p->out[k] = L.out;
+      p->num_rings[k] = L.ring.num_rings;
+      p->app[k] = FusedAppend{reinterpret_cast<const __nv_bfloat16*>(L.k_new),
+                              reinterpret_cast<const __nv_bfloat16*>(L.v_new),
+                              reinterpret_cast<__nv_bfloat16*>(L.ring.k),
+                              reinterpret_cast<__nv_bfloat16*>(L.ring.v)};
+      if (++p->num_layers == kSwaMaxLayers) {
+        st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, di.smem_optin, s);
+        p->num_layers = 0;
+      }
+    }
+    if (st == PHS_OK && p->num_layers) st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, di.smem_optin, s);
+    delete p;
+    if (st) return st;
+  }
+  return PHS_OK;
+}
+
 int phs_hybrid_kv_tokens(const int32_t* layer_is_full_host, int32_t num_layers,
                          const int32_t* seq_lens_host, int32_t batch, int32_t window,
                          int64_t* full_tokens, int64_t* swa_tokens) {

@@ -75,12 +75,13 @@ __device__ __forceinline__ int request_splits(int n, int qlen, int T, int skip =
 // One warp's walk over its chunks of a split.  Stage j is handed back to
 // TMA (chunk j + S) right after chunk j is folded into the warp state.
 // Returns the index of a chunk whose bounded wait gave up, or -1.
-template <bool I8, int D, bool TWO, int S, typename Issue>
+template <bool I8, int D, bool TWO, int S, typename Issue, typename Patch>
 __device__ __forceinline__ int walk_chunks(WarpState<D, TWO>& st, const QFrags<D, TWO>& qf,
                                            const FragOffsets& fo, int my_n, const int32_t* ids,
                                            const float* kss, const float* vss, uint32_t bar0,
                                            uint32_t sbase, uint8_t* smem, int t0, int t1,
-                                           int warp, float scale_log2, int lane, Issue&& issue) {
+                                           int warp, float scale_log2, int lane, Issue&& issue,
+                                           Patch&& patch) {
   constexpr int kStage = ChunkGeom<D>::kStageBytes;
   constexpr int NW = kSplitWarps;
   using Scores = typename std::conditional<I8, ScoresI8<D, TWO>, ScoresBf16<D, TWO>>::type;
@@ -130,6 +131,7 @@ __device__ __forceinline__ int walk_chunks(WarpState<D, TWO>& st, const QFrags<D
     if (!wait(j)) return j;
     const uint32_t valid = prepare(j);
     if (ids[j] >= 0) {
+      patch(j, sK(j));  // a fused append's new token, taken from the input
       qk(j);
       softmax(j, valid);
       pv(j);
@@ -143,12 +145,16 @@ __device__ __forceinline__ int walk_chunks(WarpState<D, TWO>& st, const QFrags<D
   return -1;
 }
 
+// The work of one CTA: request b, KV head h, split s.  q/out/ws_o/ws_ml are
+// the layer's; `app` (k_new null: none) is an append fused into this
+// launch: the CTA holding token n-1 writes it into its page and patches its
+// staged copy from the input before using it.
 template <int D, bool TWO>
-__global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
-    phs_split_decode_kernel(const __grid_constant__ CUtensorMap tk,
-                            const __grid_constant__ CUtensorMap tv,
-                            const __grid_constant__ CUtensorMap tk8,
-                            const __grid_constant__ CUtensorMap tv8, const SplitArgs a) {
+__device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensorMap* tv,
+                                           const CUtensorMap* tk8, const CUtensorMap* tv8,
+                                           const SplitArgs& a, const __nv_bfloat16* q,
+                                           void* out, float* ws_o, float* ws_ml,
+                                           const FusedAppend& app, int b, int h, int s) {
   using L = SplitLayout<D>;
   constexpr int S = L::kStages;
   constexpr int NW = kSplitWarps;
@@ -156,9 +162,6 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
 
-  // request index fastest: CTAs that read the same shared-prefix pages for
-  // different requests run close together in time and share them through L2
-  const int b = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
 
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
   const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
   if (ns == 0) {  // empty request: zero output (unless another kernel owns it)
     if (s == 0 && !a.force_partial)
-      for (int e = threadIdx.x; e < G * D; e += blockDim.x) store_out(a.out, out_row0 + e, 0.f, a.out_f32);
+      for (int e = threadIdx.x; e < G * D; e += blockDim.x) store_out(out, out_row0 + e, 0.f, a.out_f32);
     return;
   }
   if (s >= ns) return;
@@ -246,33 +249,33 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
     mbar_arrive_expect_tx(bar, L::kStage);
     if (is_i8) {
       const int row = (id * a.Hkv + h) * kQBlock;
-      tma_load_2d(dst, &tk8, 0, row, bar, pol);
-      tma_load_2d(dst + L::kStage / 2, &tv8, 0, row, bar, pol);
+      tma_load_2d(dst, tk8, 0, row, bar, pol);
+      tma_load_2d(dst + L::kStage / 2, tv8, 0, row, bar, pol);
     } else {
       const int row = (id * a.Hkv + h) * kPage;
       if constexpr (D == 128) {  // one 4 KB box per page: [half][16 rows]
-        tma_load_3d(dst, &tk, 0, row, 0, bar, pol);
-        tma_load_3d(dst + L::kStage / 2, &tv, 0, row, 0, bar, pol);
+        tma_load_3d(dst, tk, 0, row, 0, bar, pol);
+        tma_load_3d(dst + L::kStage / 2, tv, 0, row, 0, bar, pol);
       } else {
-        tma_load_2d(dst, &tk, 0, row, bar, pol);
-        tma_load_2d(dst + L::kStage / 2, &tv, 0, row, bar, pol);
+        tma_load_2d(dst, tk, 0, row, bar, pol);
+        tma_load_2d(dst + L::kStage / 2, tv, 0, row, bar, pol);
       }
     }
   };
   if (lane == 0) {
     if (is_i8) {
-      prefetch_tmap(&tk8);
-      prefetch_tmap(&tv8);
+      prefetch_tmap(tk8);
+      prefetch_tmap(tv8);
     } else {
-      prefetch_tmap(&tk);
-      prefetch_tmap(&tv);
+      prefetch_tmap(tk);
+      prefetch_tmap(tv);
     }
     for (int j = 0; j < S && j < my_n; ++j) issue(j);
   }
 
   // ---- queries of the group (overlaps the first loads)
   QFrags<D, TWO> qf;
-  const __nv_bfloat16* qg = a.q + out_row0;
+  const __nv_bfloat16* qg = q + out_row0;
   if (is_i8)
     load_q_f16_i8order(qf, qg, G, lane);
   else
@@ -282,11 +285,32 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
   st.reset();
   FragOffsets fo;
   fo.init<D>(lane);
+  auto no_patch = [](int, uint32_t) {};
+  // fused append: row (n-1) % 16 of the chunk holding token n-1; lanes 0-15
+  // carry K, 16-31 V, 16 bytes each (the staged tile is [half][16 rows][128 B]
+  // with the 128-byte swizzle)
+  auto patch = [&](int j, uint32_t stage) {
+    if (app.k_new == nullptr) return;
+    const int r = n - 1 - (t0 + kPage * (warp + j * NW));
+    if (r < 0 || r >= kPage) return;
+    const int op = lane >> 4, c = lane & 15;
+    if (c < D / 8) {
+      const size_t src = (static_cast<size_t>(b) * a.Hkv + h) * D + c * 8;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>((op ? app.v_new : app.k_new) + src));
+      const uint32_t dst = stage + op * (L::kStage / 2) + (c >> 3) * 2048 + r * 128 +
+                           (((c & 7) ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(smem + (dst - smem_u32(smem))) = v;
+      __nv_bfloat16* pool = op ? app.v_pool : app.k_pool;
+      *reinterpret_cast<uint4*>(
+          pool + ((static_cast<size_t>(ids[j]) * a.Hkv + h) * kPage + r) * D + c * 8) = v;
+    }
+    __syncwarp();
+  };
   const int failed =
       is_i8 ? walk_chunks<true, D, TWO, S>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem, t0,
-                                           t1, warp, a.scale_log2, lane, issue)
+                                           t1, warp, a.scale_log2, lane, issue, no_patch)
             : walk_chunks<false, D, TWO, S>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem,
-                                            t0, t1, warp, a.scale_log2, lane, issue);
+                                            t0, t1, warp, a.scale_log2, lane, issue, patch);
   if (failed >= 0 && lane == 0) {
     // gave up: record it and drain (bounded) the loads still in flight
     set_status(a.status, PHS_ETIMEOUT);
@@ -337,15 +361,41 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
       O += sO[(w * GR + row) * D + d] * f;
     }
     if (ns == 1 && !a.force_partial) {
-      store_out(a.out, out_row0 + e, Lsum > 0.f ? O / Lsum : 0.f, a.out_f32);
+      store_out(out, out_row0 + e, Lsum > 0.f ? O / Lsum : 0.f, a.out_f32);
     } else {
-      a.ws_o[(part * G + row) * D + d] = O;
+      ws_o[(part * G + row) * D + d] = O;
       if (d == 0) {
-        a.ws_ml[(part * G + row) * 2] = M;
-        a.ws_ml[(part * G + row) * 2 + 1] = Lsum;
+        ws_ml[(part * G + row) * 2] = M;
+        ws_ml[(part * G + row) * 2 + 1] = Lsum;
       }
     }
   }
+}
+
+// request index fastest: CTAs that read the same shared-prefix pages for
+// different requests run close together in time and share them through L2
+template <int D, bool TWO>
+__global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
+    phs_split_decode_kernel(const __grid_constant__ CUtensorMap tk,
+                            const __grid_constant__ CUtensorMap tv,
+                            const __grid_constant__ CUtensorMap tk8,
+                            const __grid_constant__ CUtensorMap tv8, const SplitArgs a) {
+  const FusedAppend none{nullptr, nullptr, nullptr, nullptr};
+  split_body<D, TWO>(&tk, &tv, &tk8, &tv8, a, a.q, a.out, a.ws_o, a.ws_ml, none, blockIdx.x,
+                     blockIdx.y, blockIdx.z);
+}
+
+// Every Full layer of a hybrid stack in one launch: blockIdx.z = layer *
+// max_splits + split; each layer brings its own pool maps, queries, output,
+// partials and new token.  Source: "Xiaomi MiMo-V2.5 inference system" page,
+// section 2 (layer-wise overlap of the step; whole-step replay).
+template <int D, bool TWO>
+__global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
+    phs_stack_full_kernel(const __grid_constant__ StackFullParams p) {
+  const int l = blockIdx.z / p.a.max_splits, s = blockIdx.z - l * p.a.max_splits;
+  const StackFullLayer& L = p.layer[l];
+  split_body<D, TWO>(&L.tk, &L.tv, &L.tk, &L.tv, p.a, L.q, L.out, L.ws_o, L.ws_ml, L.app,
+                     blockIdx.x, blockIdx.y, s);
 }
 
 // Cross-split log-sum-exp merge for requests with more than one split.
@@ -354,9 +404,9 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
 // lane accumulates D/32 output columns over the splits with independent
 // vector loads.
 template <int D>
-__global__ void __launch_bounds__(128) phs_merge_kernel(const MergeArgs a) {
+__device__ __forceinline__ void merge_body(const MergeArgs& a, const float* ws_o,
+                                           const float* ws_ml, void* out, int b, int h) {
   constexpr int V = D / 32;  // columns per lane (4 or 2)
-  const int h = blockIdx.y, b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
   const int n = min(a.seq_lens[b], a.n_clamp);
@@ -366,7 +416,7 @@ __global__ void __launch_bounds__(128) phs_merge_kernel(const MergeArgs a) {
   const size_t part0 = (static_cast<size_t>(b) * a.Hkv + h) * a.max_splits;
   const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
   for (int row = warp; row < G; row += 4) {
-    const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + part0 * G + row;
+    const float2* ml = reinterpret_cast<const float2*>(ws_ml) + part0 * G + row;
     float M = -INFINITY;
     for (int s = lane; s < ns; s += 32) M = fmaxf(M, ml[static_cast<size_t>(s) * G].x);
 #pragma unroll
@@ -375,7 +425,7 @@ __global__ void __launch_bounds__(128) phs_merge_kernel(const MergeArgs a) {
     float acc[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0.f;
-    const float* ob = a.ws_o + (part0 * G + row) * D + lane * V;
+    const float* ob = ws_o + (part0 * G + row) * D + lane * V;
     for (int s0 = 0; s0 < ns; s0 += 32) {
       // weight of split s0 + lane, then broadcast one split at a time
       float wl = 0.f;
@@ -407,9 +457,21 @@ __global__ void __launch_bounds__(128) phs_merge_kernel(const MergeArgs a) {
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
 #pragma unroll
     for (int i = 0; i < V; ++i)
-      store_out(a.out, out_row0 + static_cast<size_t>(row) * D + lane * V + i, acc[i] * inv,
+      store_out(out, out_row0 + static_cast<size_t>(row) * D + lane * V + i, acc[i] * inv,
                 a.out_f32);
   }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) phs_merge_kernel(const MergeArgs a) {
+  merge_body<D>(a, a.ws_o, a.ws_ml, a.out, blockIdx.x, blockIdx.y);
+}
+
+// The merges of every Full layer of a hybrid stack in one launch (z = layer).
+template <int D>
+__global__ void __launch_bounds__(128) phs_stack_merge_kernel(const __grid_constant__ StackMergeParams p) {
+  const StackMergeLayer& L = p.layer[blockIdx.z];
+  merge_body<D>(p.a, L.ws_o, L.ws_ml, L.out, blockIdx.x, blockIdx.y);
 }
 
 // ------------------------------------------------------------ launchers --
@@ -437,6 +499,42 @@ int launch_split_decode(int D, const CUtensorMap& tk, const CUtensorMap& tv,
                : launch_split_t<64, false>(tk, tv, tk8, tv8, a, B, stream);
   }
   return PHS_EUNSUPPORTED;
+}
+
+template <int D, bool TWO>
+static int launch_stack_full_t(const StackFullParams& p, int B, cudaStream_t stream) {
+  auto kern = phs_stack_full_kernel<D, TWO>;
+  const int smem = SplitLayout<D>::kAlloc;
+  if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
+  dim3 grid(B, p.a.Hkv, p.a.max_splits * p.num_layers);
+  kern<<<grid, kSplitWarps * 32, smem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+}
+
+int launch_stack_full(int D, const StackFullParams& p, int B, cudaStream_t stream) {
+  if (p.num_layers <= 0 || p.num_layers > kStackMaxFull) return PHS_EINVAL;
+  if (static_cast<long long>(p.a.max_splits) * p.num_layers > 65535) return PHS_EUNSUPPORTED;
+  const bool two = p.a.G > 8;
+  if (D == 128)
+    return two ? launch_stack_full_t<128, true>(p, B, stream)
+               : launch_stack_full_t<128, false>(p, B, stream);
+  if (D == 64)
+    return two ? launch_stack_full_t<64, true>(p, B, stream)
+               : launch_stack_full_t<64, false>(p, B, stream);
+  return PHS_EUNSUPPORTED;
+}
+
+int launch_stack_merge(int D, const StackMergeParams& p, int B, int num_layers,
+                       cudaStream_t stream) {
+  if (num_layers <= 0 || num_layers > kStackMaxFull) return PHS_EINVAL;
+  dim3 grid(B, p.a.Hkv, num_layers);
+  if (D == 128)
+    phs_stack_merge_kernel<128><<<grid, 128, 0, stream>>>(p);
+  else if (D == 64)
+    phs_stack_merge_kernel<64><<<grid, 128, 0, stream>>>(p);
+  else
+    return PHS_EUNSUPPORTED;
+  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
 }
 
 int launch_merge(int D, const MergeArgs& a, int B, cudaStream_t stream) {

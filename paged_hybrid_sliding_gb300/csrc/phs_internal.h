@@ -41,6 +41,40 @@ struct SplitArgs {
   int force_partial;        // write partials even for single-split requests
 };
 
+// New token of each request for an append fused into a decode kernel: the
+// kernel writes it to its page (or ring slot) and attends to it from these
+// inputs instead of reading it back.  k_new null: no append.
+struct FusedAppend {
+  const __nv_bfloat16* k_new;  // [B][Hkv][D]
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* k_pool;       // paged [num_pages][Hkv][16][D] / ring [rings][Hkv][W][D]
+  __nv_bfloat16* v_pool;
+};
+
+// ------------------------------------- hybrid stack: Full layers at once --
+constexpr int kStackMaxFull = 16;  // Full layers per launch
+
+struct StackFullLayer {
+  CUtensorMap tk, tv;        // per-page K / V boxes of this layer's pool
+  const __nv_bfloat16* q;    // [B][Hq][D]
+  void* out;
+  float* ws_o;               // this layer's partials (split kernel layout)
+  float* ws_ml;
+  FusedAppend app;
+};
+
+struct StackFullParams {
+  StackFullLayer layer[kStackMaxFull];
+  SplitArgs a;               // fields shared by the layers (q/out/ws_* unused)
+  int num_layers;
+};
+
+struct StackMergeLayer {
+  const float* ws_o;
+  const float* ws_ml;
+  void* out;
+};
+
 // ------------------------------------------------- shared-prefix decode --
 struct PrefixArgs {
   const __nv_bfloat16* q;   // [B][Hq][D]
@@ -96,6 +130,16 @@ int launch_split_decode(int D, const CUtensorMap& tk, const CUtensorMap& tv,
                         int B, cudaStream_t stream);
 int launch_merge(int D, const MergeArgs& a, int B, cudaStream_t stream);
 
+// Every Full layer of a hybrid stack in one split launch (fused append) and
+// one merge launch.
+struct StackMergeParams {
+  StackMergeLayer layer[kStackMaxFull];
+  MergeArgs a;               // fields shared by the layers (ws_*/out unused)
+};
+int launch_stack_full(int D, const StackFullParams& p, int B, cudaStream_t stream);
+int launch_stack_merge(int D, const StackMergeParams& p, int B, int num_layers,
+                       cudaStream_t stream);
+
 // ------------------------------------------------------------ SWA ring --
 constexpr int kSwaMaxLayers = 64;
 
@@ -106,6 +150,7 @@ struct SwaParams {
   const __nv_bfloat16* q[MAXL];
   void* out[MAXL];
   int64_t num_rings[MAXL];
+  FusedAppend app[MAXL];    // per layer; k_new null: no fused append
   const int32_t* ring_ids;  // null = identity
   const int32_t* ring_pos;
   const int32_t* seq_lens;

@@ -159,6 +159,25 @@ __global__ void __launch_bounds__(NW * 32, 1)
       else if (lane == 0)
         set_status(p.status, PHS_ERANGE);
     }
+    if (u.ok && p.app[u.l].k_new != nullptr && u.n > 0) {
+      // fused append: the new token sits in slot u.pos; write it into the
+      // ring and patch the staged row from the input (lanes 0-15 K, 16-31 V)
+      const int r = u.pos - kPage * c;
+      if (r >= 0 && r < kPage) {
+        const FusedAppend& app = p.app[u.l];
+        const int op = lane >> 4, cc = lane & 15;
+        if (cc < D / 8) {
+          const size_t src = (static_cast<size_t>(u.b) * Hkv + u.h) * D + cc * 8;
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>((op ? app.v_new : app.k_new) + src));
+          const uint32_t dst = (op ? sV : sK) + (cc >> 3) * 2048 + r * 128 + (((cc & 7) ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(smem + (dst - smem_u32(smem))) = v;
+          __nv_bfloat16* ring = op ? app.v_pool : app.k_pool;
+          *reinterpret_cast<uint4*>(
+              ring + ((static_cast<size_t>(u.ring) * Hkv + u.h) * W + u.pos) * D + cc * 8) = v;
+        }
+        __syncwarp();
+      }
+    }
     if (u.ok) {
       const int nv = min(u.n, W);  // valid slots: the last nv tokens
       uint32_t valid = 0xFFFFu;

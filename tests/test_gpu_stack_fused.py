@@ -1,0 +1,170 @@
+"""GPU tests of the hybrid-stack step with the appends fused into the
+attention launches (phs_attn_decode_hybrid_stack_fused): outputs against the
+oracle, pools bit-exact against the oracle's append, and outputs and pools
+bit-identical to the unfused call on the same inputs.  Lengths are chosen so
+the newest token lands on the first, a middle and the last slot of a page,
+in single- and multi-split requests, with rings partly and fully filled."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_hybrid_sliding_gb300 as phs
+import synth
+from gpu_util import assert_close, bf16_dev, dev, out_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _stack(n_after, Hq, Hkv, D, layer_is_full, seed, W=128, out_dtype=torch.float32):
+    """Host copies and device layers of a stack; every layer has its own
+    pool and new token, the Full layers share one block table."""
+    B = len(n_after)
+    bt, num_pages = synth.block_tables_from_permutation(synth.pages_needed(n_after), seed + 1,
+                                                        num_pages=int(synth.pages_needed(
+                                                            n_after).sum()) + 7)
+    ring_pos = synth.ring_positions(B, W, seed + 2)
+    host, layers = [], []
+    for l, full in enumerate(layer_is_full):
+        s = seed * 1000 + 10 * l
+        q = synth.bits(synth.normal_bf16((B, Hq, D), s))
+        kn = synth.bits(synth.normal_bf16((B, Hkv, D), s + 1))
+        vn = synth.bits(synth.normal_bf16((B, Hkv, D), s + 2))
+        shape = (num_pages, Hkv, 16, D) if full else (B, Hkv, W, D)
+        k = synth.bits(synth.normal_bf16(shape, s + 3))
+        v = synth.bits(synth.normal_bf16(shape, s + 4))
+        host.append((bool(full), q, kn, vn, k, v))
+    return bt, ring_pos, host
+
+
+def _device_layers(host, out_dtype):
+    layers = []
+    for full, q, kn, vn, k, v in host:
+        B, Hq, D = q.shape
+        kw = dict(q=bf16_dev(q), out=torch.empty((B, Hq, D), dtype=out_dtype, device="cuda"),
+                  k_new=bf16_dev(kn), v_new=bf16_dev(vn))
+        if full:
+            kw["paged"] = phs.PagedPool(bf16_dev(k), bf16_dev(v))
+        else:
+            kw["ring"] = phs.RingPool(bf16_dev(k), bf16_dev(v))
+        layers.append(phs.Layer(**kw))
+    return layers
+
+
+def _pools(L):
+    p = L.paged if L.paged is not None else L.ring
+    return p.k, p.v
+
+
+CASES = [
+    # (n_after per request, Hq, Hkv, D, layers)
+    ([1, 16, 17, 130, 1025, 2048, 3001, 4096], 32, 8, 128, [0, 1, 0, 0, 1, 0, 1]),
+    ([5, 128, 129, 700, 1040], 4, 2, 64, [1, 0, 1, 0]),
+    ([33, 2049, 4000], 32, 2, 128, [1, 0]),  # G = 16: two row tiles per warp
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_fused_stack_matches_oracle(case):
+    n, Hq, Hkv, D, lf = CASES[case]
+    n_after = np.array(n, dtype=np.int32)
+    bt, rp, host = _stack(n_after, Hq, Hkv, D, lf, seed=40 + case)
+    layers = _device_layers(host, torch.float32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    phs.attn_decode_hybrid_stack_fused(layers, Hq, dev(n_after), int(n_after.max()),
+                                       block_table=dev(bt), ring_pos=dev(rp), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    scale = 1.0 / np.sqrt(D)
+    for l, (L, (full, q, kn, vn, k, v)) in enumerate(zip(layers, host)):
+        k, v = k.copy(), v.copy()
+        if full:
+            oracle.append_paged(k, v, kn, vn, bt, n_after)
+            ref, s = oracle.decode_full_paged(q, k, v, bt, n_after, scale)
+        else:
+            oracle.append_ring(k, v, kn, vn, None, rp)
+            ref, s = oracle.decode_swa_ring(q, k, v, None, rp, n_after, scale)
+        assert s == 0
+        pk, pv = _pools(L)
+        assert np.array_equal(synth.bits(pk), k) and np.array_equal(synth.bits(pv), v), l
+        assert_close(out_np(L.out), ref, f"case {case} layer {l} ({'Full' if full else 'SWA'})")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_fused_equals_unfused_bitexact(out_dtype):
+    n, Hq, Hkv, D, lf = CASES[0]
+    n_after = np.array(n, dtype=np.int32)
+    bt, rp, host = _stack(n_after, Hq, Hkv, D, lf, seed=77)
+    a = _device_layers(host, out_dtype)
+    b = _device_layers(host, out_dtype)
+    common = dict(block_table=dev(bt), ring_pos=dev(rp))
+    phs.attn_decode_hybrid_stack(a, Hq, dev(n_after), int(n_after.max()), do_append=True, **common)
+    phs.attn_decode_hybrid_stack_fused(b, Hq, dev(n_after), int(n_after.max()), **common)
+    torch.cuda.synchronize()
+    for l, (La, Lb) in enumerate(zip(a, b)):
+        assert torch.equal(La.out, Lb.out), l
+        for x, y in zip(_pools(La), _pools(Lb)):
+            assert torch.equal(x, y), l
+
+
+def test_fused_stack_two_steps():
+    """Two consecutive steps: the second attends to the token the first
+    appended (read back from the pool) plus its own new token."""
+    n, Hq, Hkv, D, lf = CASES[1]
+    n1 = np.array(n, dtype=np.int32)
+    bt, rp, host = _stack(n1 + 1, Hq, Hkv, D, lf, seed=91)  # table covers both steps
+    layers = _device_layers(host, torch.float32)
+    scale = 1.0 / np.sqrt(D)
+    rp2 = ((rp.astype(np.int64) + 1) % 128).astype(np.int32)
+    for step, (nn, pos) in enumerate([(n1, rp), (n1 + 1, rp2)]):
+        if step == 1:  # fresh new tokens and queries for the second step
+            for L, hst in zip(layers, host):
+                kn2 = synth.bits(synth.normal_bf16(hst[2].shape, 500 + step))
+                vn2 = synth.bits(synth.normal_bf16(hst[3].shape, 600 + step))
+                q2 = synth.bits(synth.normal_bf16(hst[1].shape, 700 + step))
+                L.k_new.copy_(bf16_dev(kn2))
+                L.v_new.copy_(bf16_dev(vn2))
+                L.q.copy_(bf16_dev(q2))
+        phs.attn_decode_hybrid_stack_fused(layers, Hq, dev(nn), int(nn.max()),
+                                           block_table=dev(bt), ring_pos=dev(pos))
+    torch.cuda.synchronize()
+    for l, (L, (full, q, kn, vn, k, v)) in enumerate(zip(layers, host)):
+        k, v = k.copy(), v.copy()
+        kn2 = synth.bits(L.k_new)
+        vn2 = synth.bits(L.v_new)
+        q2 = synth.bits(L.q)
+        if full:
+            oracle.append_paged(k, v, kn, vn, bt, n1)
+            oracle.append_paged(k, v, kn2, vn2, bt, n1 + 1)
+            ref, _ = oracle.decode_full_paged(q2, k, v, bt, n1 + 1, scale)
+        else:
+            oracle.append_ring(k, v, kn, vn, None, rp)
+            oracle.append_ring(k, v, kn2, vn2, None, rp2)
+            ref, _ = oracle.decode_swa_ring(q2, k, v, None, rp2, n1 + 1, scale)
+        pk, pv = _pools(L)
+        assert np.array_equal(synth.bits(pk), k) and np.array_equal(synth.bits(pv), v), l
+        assert_close(out_np(L.out), ref, f"second step, layer {l}")
+
+
+def test_fused_stack_errors():
+    n, Hq, Hkv, D, lf = CASES[1]
+    n_after = np.array(n, dtype=np.int32)
+    bt, rp, host = _stack(n_after, Hq, Hkv, D, lf, seed=5)
+    layers = _device_layers(host, torch.float32)
+    args = (layers, Hq, dev(n_after), int(n_after.max()))
+    kw = dict(block_table=dev(bt), ring_pos=dev(rp))
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(phs.PhsError) as e:
+        phs.attn_decode_hybrid_stack_fused(*args, workspace=small, **kw)
+    assert e.value.code == -5  # PHS_EWORKSPACE
+    layers[0].k_new = None
+    with pytest.raises(phs.PhsError) as e:
+        phs.attn_decode_hybrid_stack_fused(*args, **kw)
+    assert e.value.code == -1  # PHS_EINVAL: every layer needs its new token
+    with pytest.raises(phs.PhsError) as e:
+        phs.attn_decode_hybrid_stack_fused(_device_layers(host, torch.float32), Hq, dev(n_after),
+                                           int(n_after.max()), block_table=dev(bt))
+    assert e.value.code == -1  # SWA layers without ring positions
+    assert phs.hybrid_stack_fused_workspace_bytes(8, 32, 8, 128, 4096, 0) == 0
+    one = phs.hybrid_stack_fused_workspace_bytes(8, 32, 8, 128, 4096, 1)
+    assert phs.hybrid_stack_fused_workspace_bytes(8, 32, 8, 128, 4096, 10) == 10 * one
