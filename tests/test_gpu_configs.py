@@ -221,3 +221,60 @@ def test_config5_shared_prefix_steps_sampled():
                                       w.softmax_scale)
     assert s == 0
     assert_close(out_np(out)[rows], ref, "config 5 sampled")
+
+
+@pytest.mark.slow
+def test_config3_full_size_fused_sampled():
+    """The 70-layer stack at full size (batch 256, lengths log-uniform in
+    [4K, 128K]) through the fused step the bench times; the 10 Full layers
+    share one pool, as the bench aliases them (each layer still attends to
+    its own new token, taken from its input).  Sampled requests of two Full
+    and two SWA layers against the oracle."""
+    w = synth.hybrid_stack()
+    B, Hq, Hkv, D, W = w.B, w.Hq, w.Hkv, w.D, w.W
+    lf = w.extra["layer_is_full"]
+    kp = synth.normal_bf16((w.num_pages, Hkv, 16, D), 71, device="cuda")
+    vp = synth.normal_bf16((w.num_pages, Hkv, 16, D), 72, device="cuda")
+    pool = phs.PagedPool(kp, vp)
+    rows = [0, int(np.argmax(w.n_after)), int(np.argmin(w.n_after)), B - 1]
+    check = {6, 69, 0, 35}  # Full, Full, SWA, SWA
+    hk, bt_s = sub_pool(kp, w.block_table, rows, w.n_after)
+    hv, _ = sub_pool(vp, w.block_table, rows, w.n_after)
+    layers, host = [], {}
+    for l, full in enumerate(lf):
+        q = synth.normal_bf16((B, Hq, D), 3000 + 3 * l, device="cuda")
+        kn = synth.normal_bf16((B, Hkv, D), 3001 + 3 * l, device="cuda")
+        vn = synth.normal_bf16((B, Hkv, D), 3002 + 3 * l, device="cuda")
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+        if full:
+            L = phs.Layer(q=q, out=out, paged=pool, k_new=kn, v_new=vn)
+        else:
+            ring = phs.RingPool(synth.normal_bf16((B, Hkv, W, D), 4000 + 2 * l, device="cuda"),
+                                synth.normal_bf16((B, Hkv, W, D), 4001 + 2 * l, device="cuda"))
+            L = phs.Layer(q=q, out=out, ring=ring, k_new=kn, v_new=vn)
+            if l in check:
+                host[l] = (synth.bits(ring.k)[rows], synth.bits(ring.v)[rows])
+        layers.append(L)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    phs.attn_decode_hybrid_stack_fused(layers, Hq, dev(w.n_after), int(w.n_after.max()),
+                                       block_table=dev(w.block_table), ring_pos=dev(w.ring_pos),
+                                       status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    n_s, rp_s = w.n_after[rows], w.ring_pos[rows]
+    for l in sorted(check):
+        L = layers[l]
+        qh = synth.bits(L.q)[rows]
+        knh, vnh = synth.bits(L.k_new)[rows], synth.bits(L.v_new)[rows]
+        if lf[l]:
+            k, v = hk.copy(), hv.copy()
+            oracle.append_paged(k, v, knh, vnh, bt_s, n_s)
+            ref, s = oracle.decode_full_paged(qh, k, v, bt_s, n_s, w.softmax_scale)
+        else:
+            k, v = (x.copy() for x in host[l])
+            oracle.append_ring(k, v, knh, vnh, None, rp_s)
+            ref, s = oracle.decode_swa_ring(qh, k, v, None, rp_s, n_s, w.softmax_scale)
+            # the ring now holds the new token (bit-exact)
+            assert np.array_equal(synth.bits(L.ring.k)[rows], k), l
+        assert s == 0
+        assert_close(out_np(L.out)[rows], ref, f"config 3 fused, layer {l}")
