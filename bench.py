@@ -451,10 +451,12 @@ class HybridStackWorkload(Workload):
         if not nfull:
             self.kernel = "phs_swa_decode_kernel"
         elif fused:
-            self.kernel = ("phs_stack_full_kernel + phs_stack_merge_kernel (all Full layers in one "
-                           "launch each, append fused; per-layer average)")
+            self.kernel = ("phs_stack_full_kernel + merges (all Full layers in one launch, "
+                           "append fused; per-layer average)")
         if fused:
-            self.launches_per_step = (2 if nfull else 0) + (1 if nswa else 0)
+            # Full split launch + SWA launch (which also runs the Full merges)
+            self.launches_per_step = (1 if nfull else 0) + (1 if nswa else 0) + \
+                (1 if nfull and not nswa else 0)
         else:
             self.launches_per_step = (2 if nfull else 1) + 1 + 2 * nfull
         self.extra = {"batch": B, "layers": f"{nfull} Full + {nswa} SWA(W=128)",

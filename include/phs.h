@@ -347,10 +347,11 @@ size_t phs_hybrid_stack_workspace_bytes(int32_t batch, int32_t num_q_heads,
  * required) is written into slot seq_lens[b]-1 of its page (Full, through
  * the shared block_table) or into ring slot ring_pos[b] (SWA), and attended
  * as the newest token -- the kernels take it from k_new/v_new instead of
- * reading it back.  Launches: one split-KV launch and one merge launch for
- * up to 16 Full layers at once, one persistent launch for up to 64 SWA
- * layers (config 3, 10 Full + 60 SWA: three launches per step instead of
- * twenty-three).  The Full layers' partials live side by side, so the
+ * reading it back.  Launches: one split-KV launch for up to 16 Full layers
+ * at once and one persistent launch for up to 64 SWA layers, whose warps
+ * also run the Full layers' cross-split merges after their SWA work (a
+ * stack without SWA layers gets a merge launch instead).  Config 3, 10
+ * Full + 60 SWA: two launches per step instead of twenty-three.  The Full layers' partials live side by side, so the
  * workspace is phs_hybrid_stack_fused_workspace_bytes (256-byte aligned).
  * Outputs and pool contents equal those of the unfused call.
  * Errors as phs_attn_decode_hybrid_stack (PHS_EINVAL also for a missing

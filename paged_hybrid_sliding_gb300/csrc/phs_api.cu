@@ -894,6 +894,9 @@ int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_laye
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PHS_EALIGN;
   }
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
+  StackMergeParams fold_merges;  // Full-layer merges handed to the SWA launch
+  std::memset(&fold_merges, 0, sizeof(fold_merges));
+  int fold_layers = 0;
 
   // ---- launch 1 (per 16 Full layers): split-KV decode of every Full layer,
   // each CTA holding a request's newest token also appends it
@@ -957,7 +960,16 @@ int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_laye
     if (st == PHS_OK && k) {
       p->num_layers = k;
       st = launch_stack_full(D, *p, batch, s);
-      if (st == PHS_OK && pl.max_splits > 1) st = launch_stack_merge(D, *m, batch, k, s);
+      // the last batch of Full layers is merged by the SWA launch when there
+      // is one (two launches per step); otherwise by a merge launch
+      if (st == PHS_OK && pl.max_splits > 1) {
+        if (nswa) {
+          fold_merges = *m;
+          fold_layers = k;
+        } else {
+          st = launch_stack_merge(D, *m, batch, k, s);
+        }
+      }
     }
     delete p;
     delete m;
@@ -980,6 +992,11 @@ int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_laye
     p->W = W;
     p->out_f32 = out_dtype == PHS_OUT_F32;
     p->scale_log2 = scale_log2;
+    if (fold_layers) {  // the Full layers' merges ride on the first SWA launch
+      for (int i = 0; i < fold_layers; ++i) p->merge_layer[i] = fold_merges.layer[i];
+      p->merge = fold_merges.a;
+      p->num_merge_layers = fold_layers;
+    }
     st = PHS_OK;
     for (int i = 0; i < num_layers && st == PHS_OK; ++i) {
       const phs_layer& L = layers[i];
@@ -998,6 +1015,7 @@ int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_laye
       if (++p->num_layers == kSwaMaxLayers) {
         st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, di.smem_optin, s);
         p->num_layers = 0;
+        p->num_merge_layers = 0;
       }
     }
     if (st == PHS_OK && p->num_layers) st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, di.smem_optin, s);

@@ -23,6 +23,7 @@
 
 #include "phs_attn.cuh"
 #include "phs_internal.h"
+#include "phs_merge.cuh"
 
 namespace phs {
 
@@ -53,23 +54,6 @@ struct SplitLayout {
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-__device__ __forceinline__ void store_out(void* out, size_t idx, float v, int f32) {
-  if (f32)
-    reinterpret_cast<float*>(out)[idx] = v;
-  else
-    reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
-}
-
-// Number of splits of a request and validation of its INT8 length.
-// Returns -1 if the request's lengths are invalid.
-// The bf16 region starts at max(qlen, skip): tokens below `skip` (a shared
-// prefix) are attended by another kernel.
-__device__ __forceinline__ int request_splits(int n, int qlen, int T, int skip = 0) {
-  if (n < 0 || qlen < 0 || qlen > n || (qlen % kQBlock) != 0 || n < skip) return -1;
-  const int bf0 = max(qlen, skip);
-  return (qlen + T - 1) / T + (n - bf0 + T - 1) / T;
 }
 
 // One warp's walk over its chunks of a split.  Stage j is handed back to
@@ -398,68 +382,12 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
                      blockIdx.x, blockIdx.y, s);
 }
 
-// Cross-split log-sum-exp merge for requests with more than one split.
-// One CTA per (request, KV head); warp w merges query rows w, w+4, ...  The
-// lanes first reduce (max m, sum l) over the splits in parallel, then each
-// lane accumulates D/32 output columns over the splits with independent
-// vector loads.
+// Cross-split merge of one (request, KV head): warp w of the CTA merges
+// query rows w, w+4, ...
 template <int D>
 __device__ __forceinline__ void merge_body(const MergeArgs& a, const float* ws_o,
                                            const float* ws_ml, void* out, int b, int h) {
-  constexpr int V = D / 32;  // columns per lane (4 or 2)
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = a.G;
-  const int n = min(a.seq_lens[b], a.n_clamp);
-  const int qlen = a.qlens ? a.qlens[b] : 0;
-  const int ns = min(request_splits(n, qlen, a.T), a.max_splits);
-  if (ns <= 1) return;
-  const size_t part0 = (static_cast<size_t>(b) * a.Hkv + h) * a.max_splits;
-  const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
-  for (int row = warp; row < G; row += 4) {
-    const float2* ml = reinterpret_cast<const float2*>(ws_ml) + part0 * G + row;
-    float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, ml[static_cast<size_t>(s) * G].x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Lsum = 0.f;
-    float acc[V];
-#pragma unroll
-    for (int i = 0; i < V; ++i) acc[i] = 0.f;
-    const float* ob = ws_o + (part0 * G + row) * D + lane * V;
-    for (int s0 = 0; s0 < ns; s0 += 32) {
-      // weight of split s0 + lane, then broadcast one split at a time
-      float wl = 0.f;
-      if (s0 + lane < ns) {
-        const float2 v = ml[static_cast<size_t>(s0 + lane) * G];
-        wl = v.x == -INFINITY ? 0.f : exp2f(v.x - M);
-        Lsum += v.y * wl;
-      }
-      const int cnt = min(32, ns - s0);
-#pragma unroll 4
-      for (int k = 0; k < cnt; ++k) {
-        const float w = __shfl_sync(0xffffffffu, wl, k);
-        const float* src = ob + static_cast<size_t>(s0 + k) * G * D;
-        if constexpr (V == 4) {
-          const float4 o = *reinterpret_cast<const float4*>(src);
-          acc[0] += w * o.x;
-          acc[1] += w * o.y;
-          acc[2] += w * o.z;
-          acc[3] += w * o.w;
-        } else {
-          const float2 o = *reinterpret_cast<const float2*>(src);
-          acc[0] += w * o.x;
-          acc[1] += w * o.y;
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-#pragma unroll
-    for (int i = 0; i < V; ++i)
-      store_out(out, out_row0 + static_cast<size_t>(row) * D + lane * V + i, acc[i] * inv,
-                a.out_f32);
-  }
+  merge_request<D>(a, ws_o, ws_ml, out, b, h, threadIdx.x >> 5, blockDim.x >> 5);
 }
 
 template <int D>

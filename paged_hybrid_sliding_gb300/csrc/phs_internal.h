@@ -158,6 +158,12 @@ struct SwaParams {
   int num_layers, B, Hq, Hkv, G, W;
   int out_f32;
   float scale_log2;
+  // The Full layers' cross-split merges of a hybrid-stack step, taken as
+  // extra work after the SWA units (the split launch ran before this one on
+  // the stream): layer l's partials and output, shared merge fields.
+  StackMergeLayer merge_layer[kStackMaxFull];
+  MergeArgs merge;
+  int num_merge_layers;     // 0: none
 };
 
 template <int MAXL>

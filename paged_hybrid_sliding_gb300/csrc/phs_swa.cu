@@ -16,6 +16,7 @@
 // by layer).
 #include "phs_attn.cuh"
 #include "phs_internal.h"
+#include "phs_merge.cuh"
 
 namespace phs {
 
@@ -244,6 +245,17 @@ __global__ void __launch_bounds__(NW * 32, 1)
       }
     }
   }
+  // ---- a hybrid-stack step's Full-layer merges: one warp per (layer,
+  // request, KV head), after this warp's SWA units
+  if (p.num_merge_layers > 0) {
+    const int mu = p.num_merge_layers * BH;
+    for (int id = gw; id < mu; id += tw) {
+      const int l = id / BH, rem = id - l * BH;
+      const int b = rem / Hkv, h = rem - (rem / Hkv) * Hkv;
+      const StackMergeLayer& M = p.merge_layer[l];
+      merge_request<D>(p.merge, M.ws_o, M.ws_ml, M.out, b, h, 0, 1);
+    }
+  }
 }
 
 template <int D, bool TWO, int MAXL, int NW>
@@ -251,7 +263,9 @@ static int launch_swa_t(const SwaParams<MAXL>& p, int num_sms, cudaStream_t stre
   auto kern = phs_swa_decode_kernel<D, TWO, MAXL, NW>;
   const int smem = SwaLayout(D, p.G, NW, p.B).total;
   if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
-  const long long units = static_cast<long long>(p.num_layers) * p.B * p.Hkv;
+  const long long units = std::max(static_cast<long long>(p.num_layers),
+                                   static_cast<long long>(p.num_merge_layers)) *
+                          p.B * p.Hkv;  // SWA units, or merge units if more
   long long blocks = (units + NW - 1) / NW;
   if (blocks > num_sms) blocks = num_sms;
   if (blocks < 1) blocks = 1;
