@@ -1013,12 +1013,13 @@ int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_laye
                               reinterpret_cast<__nv_bfloat16*>(L.ring.k),
                               reinterpret_cast<__nv_bfloat16*>(L.ring.v)};
       if (++p->num_layers == kSwaMaxLayers) {
-        st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, di.smem_optin, s);
+        st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, di.smem_optin, s, nfull > 0);
         p->num_layers = 0;
         p->num_merge_layers = 0;
       }
     }
-    if (st == PHS_OK && p->num_layers) st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, di.smem_optin, s);
+    if (st == PHS_OK && p->num_layers)
+      st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, di.smem_optin, s, nfull > 0);
     delete p;
     if (st) return st;
   }

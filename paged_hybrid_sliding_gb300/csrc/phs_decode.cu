@@ -145,6 +145,9 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
   constexpr int GR = TWO ? 16 : 8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
+  // a dependent launch (merge, or the next layers' SWA work) may start as
+  // soon as every CTA of this grid is running; it waits for our results
+  pdl_launch_dependents();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
@@ -387,6 +390,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
 template <int D>
 __device__ __forceinline__ void merge_body(const MergeArgs& a, const float* ws_o,
                                            const float* ws_ml, void* out, int b, int h) {
+  pdl_wait_prior_grid();  // launched as a dependent of the split launch
   merge_request<D>(a, ws_o, ws_ml, out, b, h, threadIdx.x >> 5, blockDim.x >> 5);
 }
 
@@ -452,28 +456,38 @@ int launch_stack_full(int D, const StackFullParams& p, int B, cudaStream_t strea
   return PHS_EUNSUPPORTED;
 }
 
+// Launch as a programmatic dependent of the previous launch on the stream
+// (the kernel waits for that grid before reading its results).
+template <typename Kern, typename Arg>
+static int launch_dependent(Kern kern, dim3 grid, dim3 block, int smem, cudaStream_t stream,
+                            const Arg& arg) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, arg) == cudaSuccess ? PHS_OK : PHS_ECUDA;
+}
+
 int launch_stack_merge(int D, const StackMergeParams& p, int B, int num_layers,
                        cudaStream_t stream) {
   if (num_layers <= 0 || num_layers > kStackMaxFull) return PHS_EINVAL;
   dim3 grid(B, p.a.Hkv, num_layers);
-  if (D == 128)
-    phs_stack_merge_kernel<128><<<grid, 128, 0, stream>>>(p);
-  else if (D == 64)
-    phs_stack_merge_kernel<64><<<grid, 128, 0, stream>>>(p);
-  else
-    return PHS_EUNSUPPORTED;
-  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+  if (D == 128) return launch_dependent(phs_stack_merge_kernel<128>, grid, 128, 0, stream, p);
+  if (D == 64) return launch_dependent(phs_stack_merge_kernel<64>, grid, 128, 0, stream, p);
+  return PHS_EUNSUPPORTED;
 }
 
 int launch_merge(int D, const MergeArgs& a, int B, cudaStream_t stream) {
   dim3 grid(B, a.Hkv);
-  if (D == 128)
-    phs_merge_kernel<128><<<grid, 128, 0, stream>>>(a);
-  else if (D == 64)
-    phs_merge_kernel<64><<<grid, 128, 0, stream>>>(a);
-  else
-    return PHS_EUNSUPPORTED;
-  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+  if (D == 128) return launch_dependent(phs_merge_kernel<128>, grid, 128, 0, stream, a);
+  if (D == 64) return launch_dependent(phs_merge_kernel<64>, grid, 128, 0, stream, a);
+  return PHS_EUNSUPPORTED;
 }
 
 }  // namespace phs

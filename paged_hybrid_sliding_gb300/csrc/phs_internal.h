@@ -168,7 +168,7 @@ struct SwaParams {
 
 template <int MAXL>
 int launch_swa_decode(int D, const SwaParams<MAXL>& p, int num_sms, int smem_optin,
-                      cudaStream_t stream);
+                      cudaStream_t stream, bool dependent = false);
 
 // -------------------------------------------------------------- append --
 constexpr int kAppendMaxLayers = 64;

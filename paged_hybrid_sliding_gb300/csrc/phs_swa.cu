@@ -248,6 +248,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
   // ---- a hybrid-stack step's Full-layer merges: one warp per (layer,
   // request, KV head), after this warp's SWA units
   if (p.num_merge_layers > 0) {
+    // the split launch before this one (this grid may start while it runs)
+    pdl_wait_prior_grid();
     const int mu = p.num_merge_layers * BH;
     for (int id = gw; id < mu; id += tw) {
       const int l = id / BH, rem = id - l * BH;
@@ -259,7 +261,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
 }
 
 template <int D, bool TWO, int MAXL, int NW>
-static int launch_swa_t(const SwaParams<MAXL>& p, int num_sms, cudaStream_t stream) {
+static int launch_swa_t(const SwaParams<MAXL>& p, int num_sms, cudaStream_t stream,
+                        bool dependent) {
   auto kern = phs_swa_decode_kernel<D, TWO, MAXL, NW>;
   const int smem = SwaLayout(D, p.G, NW, p.B).total;
   if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
@@ -269,8 +272,24 @@ static int launch_swa_t(const SwaParams<MAXL>& p, int num_sms, cudaStream_t stre
   long long blocks = (units + NW - 1) / NW;
   if (blocks > num_sms) blocks = num_sms;
   if (blocks < 1) blocks = 1;
-  kern<<<static_cast<int>(blocks), NW * 32, smem, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+  if (!dependent) {
+    kern<<<static_cast<int>(blocks), NW * 32, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+  }
+  // programmatic dependent of the previous launch (a hybrid-stack step's
+  // Full split): the SWA units need nothing from it and overlap its last
+  // wave; the folded merges wait for it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? PHS_OK : PHS_ECUDA;
 }
 
 // 8 warps per CTA when their stages fit in shared memory, else 4.
@@ -284,14 +303,14 @@ int swa_smem_bytes(int D, int G, int batch) { return SwaLayout(D, G, 4, batch).t
 
 template <int MAXL>
 int launch_swa_decode(int D, const SwaParams<MAXL>& p, int num_sms, int smem_optin,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool dependent) {
   if (static_cast<long long>(p.num_layers) * p.B * p.Hkv > INT32_MAX / 2) return PHS_EUNSUPPORTED;
   const int nw = swa_warps(D, p.G, p.B, smem_optin);
   if (nw == 0) return PHS_EUNSUPPORTED;
   const bool two = p.G > 8;
 #define PHS_SWA_LAUNCH(DD, TT)                                                    \
-  return nw == 8 ? launch_swa_t<DD, TT, MAXL, 8>(p, num_sms, stream) \
-                 : launch_swa_t<DD, TT, MAXL, 4>(p, num_sms, stream)
+  return nw == 8 ? launch_swa_t<DD, TT, MAXL, 8>(p, num_sms, stream, dependent) \
+                 : launch_swa_t<DD, TT, MAXL, 4>(p, num_sms, stream, dependent)
   if (D == 128) {
     if (two) PHS_SWA_LAUNCH(128, true);
     PHS_SWA_LAUNCH(128, false);
@@ -304,8 +323,8 @@ int launch_swa_decode(int D, const SwaParams<MAXL>& p, int num_sms, int smem_opt
   return PHS_EUNSUPPORTED;
 }
 
-template int launch_swa_decode<1>(int, const SwaParams<1>&, int, int, cudaStream_t);
+template int launch_swa_decode<1>(int, const SwaParams<1>&, int, int, cudaStream_t, bool);
 template int launch_swa_decode<kSwaMaxLayers>(int, const SwaParams<kSwaMaxLayers>&, int, int,
-                                              cudaStream_t);
+                                              cudaStream_t, bool);
 
 }  // namespace phs
