@@ -171,6 +171,31 @@ def nbytes(*ts):
     return sum(t.numel() * t.element_size() for t in ts)
 
 
+class Arena:
+    """Tensors carved from one device buffer (256-byte aligned slots) and
+    mirrored by one pinned host buffer, so that a step's inputs (or outputs)
+    cross the host link in a single copy instead of one per tensor."""
+
+    def __init__(self, device, tensors):
+        offs, off = [], 0
+        for t in tensors:
+            offs.append(off)
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.nbytes = off
+        self.dev = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+        self.host = torch.empty(max(off, 256), dtype=torch.uint8).pin_memory()
+
+        def view(buf, o, t):
+            n = t.numel() * t.element_size()
+            return buf[o:o + n].view(t.dtype).view(t.shape)
+        self.views = [view(self.dev, o, t) for o, t in zip(offs, tensors)]
+        self.host_views = [view(self.host, o, t) for o, t in zip(offs, tensors)]
+        for v, t in zip(self.views, tensors):
+            v.copy_(t)
+        self.host.copy_(self.dev)
+
+
+
 def rows_for_budget(n_after, order, per_token_s, budget_s):
     rows, acc = [], 0.0
     for b in order:
@@ -184,9 +209,11 @@ def rows_for_budget(n_after, order, per_token_s, budget_s):
 class Workload:
     """One decode step of a synthetic workload on the device.  Subclasses
     set the byte / token accounting and implement step() (inputs resident),
-    e2e_step() (public API from pinned host buffers) and cpu_baseline()."""
+    e2e_io() / e2e_compute() (public API from pinned host buffers) and
+    cpu_baseline()."""
     kernel = "phs_split_decode_kernel"
     l2 = "inputs larger than L2 (K/V read per step >> 129 MB)"
+    e2e_pipelined = True
 
     def kernel_seconds(self, evs):
         return statistics.fmean(a.elapsed_time(b) for a, b in evs) / 1e3 if evs else None
@@ -194,6 +221,67 @@ class Workload:
     def new_events(self, steps):
         return [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                  for _ in range(self.kernel_launches_per_step)] for _ in range(steps)]
+
+    # ---- end to end through the public API, from and to pinned host memory.
+    # Subclasses give e2e_io(k) -> (inputs [(host, device)], outputs
+    # [(device, host)]) and e2e_compute(k) (the API calls of step k, inputs
+    # resident in the device tensors).
+    def e2e_run(self, steps):
+        """Serving-style loop: step k+1's inputs go up on one copy stream and
+        step k's outputs come down on another while step k computes.  The
+        host copies land in double-buffered device staging; a step moves its
+        staged inputs onto its working tensors (device copy) before its API
+        calls and its outputs onto a staging slot after them.  Every step's
+        host copies happen inside the loop.  A latency-bound step (where the
+        staging would cost more than it hides) copies in and out directly."""
+        if not self.e2e_pipelined:
+            for k in range(steps):
+                ins, outs = self.e2e_io(k)
+                for h, d in ins:
+                    d.copy_(h, non_blocking=True)
+                self.e2e_compute(k)
+                for src, h in outs:
+                    h.copy_(src, non_blocking=True)
+            return
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        comp = torch.cuda.current_stream()
+        ins0, outs0 = self.e2e_io(0)
+        st_in = [[torch.empty_like(d) for _, d in ins0] for _ in range(2)]
+        st_out = [[torch.empty_like(src) for src, _ in outs0] for _ in range(2)]
+        ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]  # noqa: E731
+        h2d_done, in_free, out_ready, out_free = ev(), ev(), ev(), ev()
+
+        def upload(k):
+            b = k % 2
+            ins, _ = self.e2e_io(k)
+            with torch.cuda.stream(up):
+                if k >= 2:
+                    up.wait_event(in_free[b])  # step k-2 has taken its inputs off slot b
+                for (h, _), sbuf in zip(ins, st_in[b]):
+                    sbuf.copy_(h, non_blocking=True)
+                h2d_done[b].record(up)
+
+        upload(0)
+        for k in range(steps):
+            b = k % 2
+            if k + 1 < steps:
+                upload(k + 1)
+            ins, outs = self.e2e_io(k)
+            comp.wait_event(h2d_done[b])
+            for sbuf, (_, d) in zip(st_in[b], ins):
+                d.copy_(sbuf, non_blocking=True)
+            in_free[b].record(comp)
+            self.e2e_compute(k)
+            if k >= 2:
+                comp.wait_event(out_free[b])  # step k-2's outputs have left slot b
+            for (src, _), obuf in zip(outs, st_out[b]):
+                obuf.copy_(src, non_blocking=True)
+            out_ready[b].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(out_ready[b])
+                for obuf, (_, h) in zip(st_out[b], outs):
+                    h.copy_(obuf, non_blocking=True)
+                out_free[b].record(down)
 
 
 class PagedFullWorkload(Workload):
@@ -231,10 +319,11 @@ class PagedFullWorkload(Workload):
         self.kernel_bytes = kv + B * Hq * D * 2 + tables
         self.launches_per_step = 3
         self.extra = {"batch": B, "tokens_per_split": self.tps}
-        self.h_q, self.h_kn, self.h_vn = pinned(self.q), pinned(self.kn), pinned(self.vn)
-        self.h_bt, self.h_sl = pinned(self.bt), pinned(self.sl)
+        # the step's inputs in one staged buffer: one host->device copy per step
+        self.inp = Arena(device, [self.q, self.kn, self.vn, self.bt, self.sl])
+        self.q, self.kn, self.vn, self.bt, self.sl = self.inp.views
         self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
-        self.h2d_bytes = nbytes(self.h_q, self.h_kn, self.h_vn, self.h_bt, self.h_sl)
+        self.h2d_bytes = self.inp.nbytes
         self.d2h_bytes = nbytes(self.h_out)
 
     def step(self, ev=None):
@@ -249,15 +338,14 @@ class PagedFullWorkload(Workload):
         phs.attn_merge_splits(self.out, self.w.Hkv, self.sl, self.max_seq, self.ws,
                               tokens_per_split=self.tps)
 
-    def e2e_step(self):
+    def e2e_io(self, k):
+        return [(self.inp.host, self.inp.dev)], [(self.out, self.h_out)]
+
+    def e2e_compute(self, k):
         phs = self.phs
-        for d, h in ((self.q, self.h_q), (self.kn, self.h_kn), (self.vn, self.h_vn),
-                     (self.bt, self.h_bt), (self.sl, self.h_sl)):
-            d.copy_(h, non_blocking=True)
         phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl)
         phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl, self.max_seq,
                                    out=self.out, tokens_per_split=self.tps, workspace=self.ws)
-        self.h_out.copy_(self.out, non_blocking=True)
 
     def cpu_baseline(self, budget_s=12.0):
         """The oracle as it stands on a sample of requests of this step."""
@@ -290,6 +378,7 @@ class TinyHybridWorkload(Workload):
 
     kernel_launches_per_step = 0
     l2 = "latency-bound case: ~0.2 MB per step, resident in L2"
+    e2e_pipelined = False  # 13 us steps: staging costs more than it hides
 
     def __init__(self, device, seed=1, fused=True):
         import paged_hybrid_sliding_gb300 as phs
@@ -312,6 +401,11 @@ class TinyHybridWorkload(Workload):
         self.bt = torch.from_numpy(w.block_table).to(device)
         self.sl = torch.from_numpy(w.n_after).to(device)
         self.rp = torch.from_numpy(w.ring_pos).to(device)
+        # the step's inputs and outputs each in one staged buffer
+        self.inp = Arena(device, [self.qf, self.qs, self.kn, self.vn, self.sl, self.rp, self.bt])
+        self.qf, self.qs, self.kn, self.vn, self.sl, self.rp, self.bt = self.inp.views
+        self.outp = Arena(device, [self.of, self.os])
+        self.of, self.os = self.outp.views
         self.layers = [
             phs.Layer(q=self.qf, out=self.of, paged=phs.PagedPool(self.kp, self.vp),
                       k_new=self.kn, v_new=self.vn),
@@ -333,13 +427,8 @@ class TinyHybridWorkload(Workload):
         self.launches_per_step = 2 if fused else 4
         self.extra = {"batch": B, "layers": "1 Full + 1 SWA(W=128)",
                       "append_fused_into_attention": fused}
-        self.host = [pinned(t) for t in (self.qf, self.qs, self.kn, self.vn, self.sl, self.rp,
-                                         self.bt)]
-        self.dev_in = [self.qf, self.qs, self.kn, self.vn, self.sl, self.rp, self.bt]
-        self.h_of = torch.empty_like(self.of, device="cpu").pin_memory()
-        self.h_os = torch.empty_like(self.os, device="cpu").pin_memory()
-        self.h2d_bytes = nbytes(*self.host)
-        self.d2h_bytes = nbytes(self.h_of, self.h_os)
+        self.h2d_bytes = self.inp.nbytes
+        self.d2h_bytes = self.outp.nbytes
 
     def step(self, ev=None):
         if self.fused:
@@ -351,12 +440,11 @@ class TinyHybridWorkload(Workload):
                                           block_table=self.bt, ring_pos=self.rp,
                                           workspace=self.ws)
 
-    def e2e_step(self):
-        for d, h in zip(self.dev_in, self.host):
-            d.copy_(h, non_blocking=True)
+    def e2e_io(self, k):
+        return [(self.inp.host, self.inp.dev)], [(self.outp.dev, self.outp.host)]
+
+    def e2e_compute(self, k):
         self.step()
-        self.h_of.copy_(self.of, non_blocking=True)
-        self.h_os.copy_(self.os, non_blocking=True)
 
     def cpu_baseline(self):
         import oracle
@@ -408,7 +496,7 @@ class HybridStackWorkload(Workload):
             synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 10 * i + 2, device=device))
             for i in range(distinct)]
         self.layers, nf = [], 0
-        self.dev_in, self.host, self.outs, self.h_outs = [], [], [], []
+        self.dev_in, self.outs = [], []
         for l, full in enumerate(lf):
             q = synth.normal_bf16((B, Hq, D), g + 500 + 3 * l, device=device)
             kn = synth.normal_bf16((B, Hkv, D), g + 501 + 3 * l, device=device)
@@ -430,8 +518,18 @@ class HybridStackWorkload(Workload):
         self.sl = torch.from_numpy(w.n_after).to(device)
         self.rp = torch.from_numpy(w.ring_pos).to(device)
         self.dev_in += [self.bt, self.sl, self.rp]
-        self.host = [pinned(t) for t in self.dev_in]
-        self.h_outs = [torch.empty_like(o, device="cpu").pin_memory() for o in self.outs]
+        # every layer's q / k_new / v_new and the tables in one staged buffer,
+        # every layer's output in another: one copy each way per step
+        self.inp = Arena(device, self.dev_in)
+        v = self.inp.views
+        for l, L in enumerate(self.layers):
+            L.q, L.k_new, L.v_new = v[3 * l], v[3 * l + 1], v[3 * l + 2]
+        self.bt, self.sl, self.rp = v[-3], v[-2], v[-1]
+        self.outp = Arena(device, self.outs)
+        for L, o in zip(self.layers, self.outp.views):
+            L.out = o
+        self.outs = self.outp.views
+        del self.dev_in
         self.max_seq = int(w.n_after.max())
         nfull, nswa = int(lf.sum()), int(len(lf) - lf.sum())
         ws_bytes = (phs.hybrid_stack_fused_workspace_bytes(B, Hq, Hkv, D, self.max_seq, nfull)
@@ -467,8 +565,8 @@ class HybridStackWorkload(Workload):
         if nfull:
             self.extra["kv_tokens_stored_ratio_vs_all_full"] = round(
                 (nfull * full_tok + nswa * swa_tok) / (len(lf) * full_tok), 4)
-        self.h2d_bytes = nbytes(*self.host)
-        self.d2h_bytes = nbytes(*self.h_outs)
+        self.h2d_bytes = self.inp.nbytes
+        self.d2h_bytes = self.outp.nbytes
 
     def step(self, ev=None):
         if self.fused:
@@ -480,12 +578,11 @@ class HybridStackWorkload(Workload):
                                           block_table=self.bt, ring_pos=self.rp,
                                           workspace=self.ws)
 
-    def e2e_step(self):
-        for d, h in zip(self.dev_in, self.host):
-            d.copy_(h, non_blocking=True)
+    def e2e_io(self, k):
+        return [(self.inp.host, self.inp.dev)], [(self.outp.dev, self.outp.host)]
+
+    def e2e_compute(self, k):
         self.step()
-        for h, o in zip(self.h_outs, self.outs):
-            h.copy_(o, non_blocking=True)
 
     def kernel_times(self, reps=3):
         """Average launch time of the split kernel on the Full layers and of
@@ -648,10 +745,10 @@ class Int8Workload(Workload):
         self.extra = {"batch": B, "int8_tokens": i8_tok, "bf16_tokens": bf_tok,
                       "codes_bytes": codes, "scale_bytes": scales, "bf16_tail_bytes": tail,
                       "tokens_per_split": self.tps, "quantiser_setup": self.quant_setup}
-        self.host = [pinned(t) for t in (self.q, self.kn, self.vn, self.sl)]
-        self.dev_in = [self.q, self.kn, self.vn, self.sl]
+        self.inp = Arena(device, [self.q, self.kn, self.vn, self.sl])
+        self.q, self.kn, self.vn, self.sl = self.inp.views
         self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
-        self.h2d_bytes = nbytes(*self.host)
+        self.h2d_bytes = self.inp.nbytes
         self.d2h_bytes = nbytes(self.h_out)
 
     def _decode(self, split_only=False):
@@ -676,12 +773,12 @@ class Int8Workload(Workload):
         self.phs.attn_merge_splits(self.out, self.w.Hkv, self.sl, self.max_seq, self.ws,
                                    qlens=self.ql, has_int8=True, tokens_per_split=self.tps)
 
-    def e2e_step(self):
-        for d, h in zip(self.dev_in, self.host):
-            d.copy_(h, non_blocking=True)
+    def e2e_io(self, k):
+        return [(self.inp.host, self.inp.dev)], [(self.out, self.h_out)]
+
+    def e2e_compute(self, k):
         self.phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl)
         self._decode()
-        self.h_out.copy_(self.out, non_blocking=True)
 
     def cpu_baseline(self):
         import oracle
@@ -764,11 +861,14 @@ class SharedPrefixWorkload(Workload):
                       "unique_kv_bytes_per_step": self.unique_bytes,
                       "tokens_per_split": self.tps, "shared_prefix_kernel": prefix_kernel,
                       "shared_len_tensor_pass": self.shared_len if prefix_kernel else 0}
-        self.h_q, self.h_kn, self.h_vn = pinned(self.q), pinned(self.kn), pinned(self.vn)
+        # q / k_new / v_new in one staged buffer; the step's lengths (a
+        # different vector every step) travel in a second copy
+        self.inp = Arena(device, [self.q, self.kn, self.vn])
+        self.q, self.kn, self.vn = self.inp.views
         self.h_sls = [pinned(s) for s in self.sls]
         self.sl_in = torch.empty_like(self.sls[0])
         self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
-        self.h2d_bytes = nbytes(self.h_q, self.h_kn, self.h_vn, self.h_sls[0])
+        self.h2d_bytes = self.inp.nbytes + nbytes(self.h_sls[0])
         self.d2h_bytes = nbytes(self.h_out)
 
     def step(self, ev=None):
@@ -791,12 +891,11 @@ class SharedPrefixWorkload(Workload):
         phs.attn_merge_splits(self.out, self.w.Hkv, sl, self.max_seq, self.ws,
                               tokens_per_split=self.tps)
 
-    def e2e_step(self):
-        k = self.k_idx % self.nsteps
-        self.k_idx += 1
-        for d, h in ((self.q, self.h_q), (self.kn, self.h_kn), (self.vn, self.h_vn),
-                     (self.sl_in, self.h_sls[k])):
-            d.copy_(h, non_blocking=True)
+    def e2e_io(self, k):
+        return ([(self.inp.host, self.inp.dev), (self.h_sls[k % self.nsteps], self.sl_in)],
+                [(self.out, self.h_out)])
+
+    def e2e_compute(self, k):
         self.phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl_in,
                                  page_refcount=self.rc)
         if self.prefix_kernel:
@@ -807,7 +906,6 @@ class SharedPrefixWorkload(Workload):
             self.phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl_in, self.max_seq,
                                             out=self.out, tokens_per_split=self.tps,
                                             workspace=self.ws)
-        self.h_out.copy_(self.out, non_blocking=True)
 
     def cpu_baseline(self):
         import oracle
@@ -930,14 +1028,13 @@ def run_gpu(args, rank, world, local_rank):
                 "achieved_gbs": round(wl.swa_bytes / swa_s / 1e9, 1),
                 "frac": round(wl.swa_bytes / swa_s / 1e9 / peaks()[0], 4)}
 
-    # end-to-end through the public API with host buffers
-    for _ in range(3):
-        wl.e2e_step()
+    # end-to-end through the public API with host buffers (copies overlapped
+    # with compute, as a serving loop would)
+    wl.e2e_run(3)
     torch.cuda.synchronize()
     e2e_steps = max(3, args.steps // 4)
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        wl.e2e_step()
+    wl.e2e_run(e2e_steps)
     torch.cuda.synchronize()
     t_e2e = time.perf_counter() - t0
     copy_gbs = time_copy(device)
@@ -967,7 +1064,13 @@ def run_gpu(args, rank, world, local_rank):
         "pct_of_copy": round(100 * value / world / copy_gbs, 2),
         "e2e": {"value": round(wl.bytes_per_step * e2e_steps * world / t_e2e / 1e9, 1),
                 "unit": "GB/s", "h2d_bytes_per_step": wl.h2d_bytes,
-                "d2h_bytes_per_step": wl.d2h_bytes, "steps": e2e_steps},
+                "d2h_bytes_per_step": wl.d2h_bytes, "steps": e2e_steps,
+                "copies": ("every step's inputs up and outputs down through pinned host "
+                           "buffers, overlapped with the previous/next step's compute (two "
+                           "copy streams, double-buffered device staging)"
+                           if wl.e2e_pipelined else
+                           "every step's inputs up and outputs down through pinned host "
+                           "buffers, in line with the step")},
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
