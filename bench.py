@@ -52,7 +52,8 @@ def peaks():
     return 6800.0, "fallback"
 
 
-SPLIT_KERNEL_SOURCES = ("phs_decode.cu", "phs_attn.cuh", "phs_common.cuh", "phs_internal.h")
+SPLIT_KERNEL_SOURCES = ("phs_decode.cu", "phs_attn.cuh", "phs_common.cuh", "phs_internal.h",
+                        "phs_merge.cuh")
 
 
 def peak_tflops():
