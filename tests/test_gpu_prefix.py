@@ -49,16 +49,18 @@ def _oracle_rows(pool, q, bt, lens, rows, D=128):
     return ref
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,shared_len,seed", [
-    (2, 32, 8, 64, 1),        # one tile, 8 rows per head
-    (8, 32, 8, 1024, 2),      # 16 tiles, 32 rows
-    (64, 32, 8, 4096, 3),     # 256 rows: both 128-row tiles full
-    (5, 16, 2, 2048, 4),      # G = 8, 40 rows
-    (33, 32, 8, 640, 5),      # rows 132: second tile partly used
+@pytest.mark.parametrize("B,Hq,Hkv,shared_len,seed,max_suffix", [
+    (2, 32, 8, 64, 1, 700),        # one tile, 8 rows per head
+    (8, 32, 8, 1024, 2, 700),      # 16 tiles, 32 rows
+    (64, 32, 8, 4096, 3, 700),     # 256 rows: both 128-row tiles full
+    (5, 16, 2, 2048, 4, 700),      # G = 8, 40 rows
+    (33, 32, 8, 640, 5, 700),      # rows 132: second tile partly used
+    (16, 32, 2, 512, 6, 700),      # G = 16, 256 rows
+    (6, 32, 8, 256, 7, 5000),      # own tokens over several splits: merged with the prefix
 ])
-def test_shared_prefix_matches_oracle_and_paged_path(B, Hq, Hkv, shared_len, seed):
+def test_shared_prefix_matches_oracle_and_paged_path(B, Hq, Hkv, shared_len, seed, max_suffix):
     rng = np.random.default_rng(seed)
-    suffixes = [int(x) for x in rng.integers(0, 700, size=B)]
+    suffixes = [int(x) for x in rng.integers(0, max_suffix, size=B)]
     suffixes[0] = 0                  # a request with no tokens of its own
     pool, q, bt, lens = _shared_case(B, Hq, Hkv, shared_len, suffixes, seed)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
