@@ -595,7 +595,8 @@ class HybridStackWorkload(Workload):
             return None, self._swa_time(reps)
         if self.fused:
             # the step's Full part: one multi-layer split launch (append fused)
-            # plus one merge launch; per-layer average reported
+            # plus its merges (a merge launch, as the layers run without the
+            # SWA launch here); per-layer average reported
             def run():
                 phs.attn_decode_hybrid_stack_fused(full, w.Hq, self.sl, self.max_seq,
                                                    block_table=self.bt, workspace=self.ws)

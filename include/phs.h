@@ -311,8 +311,8 @@ int phs_attn_decode_swa_ring(const void *q, int32_t num_q_heads, const phs_ring_
  * shared block_table, ring slot ring_pos for SWA layers), then attend:
  * Full layers through phs_attn_decode_full_paged, SWA layers through the
  * ring.  All SWA layers go into one launch; each Full layer is one split
- * launch plus one merge launch, all reusing `workspace`
- * (phs_hybrid_stack_workspace_bytes).  Layers are independent: the step
+ * launch plus one merge launch when a request has several splits, all
+ * reusing `workspace` (phs_hybrid_stack_workspace_bytes).  Layers are independent: the step
  * runs each layer on its own q (no model weights are involved).
  * ---------------------------------------------------------------------- */
 typedef struct {

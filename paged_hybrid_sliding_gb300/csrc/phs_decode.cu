@@ -6,12 +6,16 @@
 // bf16 region [qlen, n) are split separately so that every CTA handles one
 // chunk kind.  The CTA's 4 warps take the split's chunks round-robin; each
 // warp streams its chunks through its own ring of S shared-memory stages
-// filled by TMA (two 2-D tiled loads per 16-token bf16 page: K and V, each
-// D/64 boxes of 16 x 64 with the 128-byte swizzle; or one 32 x D box each
-// for a 32-token INT8 page), and reduces them with the GQA-packed mma
-// kernels of phs_attn.cuh.  The 4 warp states are merged through shared
-// memory; a request with a single split writes its output directly, others
-// write (m, l, o) partials that phs_merge_kernel combines.
+// filled by TMA (per 16-token bf16 page: K and V, each one 4 KB box of
+// {64 columns, 16 rows, 2 column halves} for D = 128 or one 16 x 64 box for
+// D = 64, 128-byte swizzle; or one 32 x D box each for a 32-token INT8
+// page), and reduces them with the GQA-packed mma kernels of phs_attn.cuh.
+// The 4 warp states are merged through shared memory; a request with a
+// single split writes its output directly, others write (m, l, o) partials
+// that phs_merge_kernel (phs_merge.cuh) combines.  The same body serves
+// phs_stack_full_kernel (every Full layer of a hybrid-stack step in one
+// launch, the append fused in).  Each split CTA signals dependent launches
+// at its start (programmatic dependent launch; the merge waits for it).
 //
 // Sources: "Xiaomi MiMo-V2.5 inference system" page, sections 1-2 (Full
 // layers attend over the whole sequence through the authoritative Full

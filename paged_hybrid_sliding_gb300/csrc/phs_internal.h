@@ -130,8 +130,8 @@ int launch_split_decode(int D, const CUtensorMap& tk, const CUtensorMap& tv,
                         int B, cudaStream_t stream);
 int launch_merge(int D, const MergeArgs& a, int B, cudaStream_t stream);
 
-// Every Full layer of a hybrid stack in one split launch (fused append) and
-// one merge launch.
+// The cross-split merges of every Full layer of a hybrid stack: one launch
+// for a stack without SWA layers, else extra work of the SWA launch.
 struct StackMergeParams {
   StackMergeLayer layer[kStackMaxFull];
   MergeArgs a;               // fields shared by the layers (ws_*/out unused)

@@ -8,7 +8,12 @@
 // tail of the current one.  A stage holds a 16-slot K tile and V tile (TMA,
 // 128-byte swizzle); the stage that carries a unit's first chunk also gets
 // the group's queries in a slot of its own (1-D bulk copy).  A unit's output
-// is written straight from the accumulators: no split, no workspace.
+// is written straight from the accumulators: no split, no workspace.  In a
+// hybrid-stack step (phs_attn_decode_hybrid_stack_fused) the warp holding a
+// request's newest slot also appends the new token (ring write + patch of
+// the staged row from the input), and the warps take the Full layers'
+// cross-split merges after their SWA units, once the split launch before
+// them has finished (programmatic dependent launch).
 //
 // Sources: "Xiaomi MiMo-V2.5 inference system" page, section 1 (SWA layers
 // keep and attend to the most recent 128 tokens) and section 2 (ring
