@@ -668,7 +668,8 @@ int phs_attn_decode_shared_prefix(const void* q, int32_t num_q_heads, const phs_
   a.scale_log2 = scale_log2;
   a.skip_len = shared_len;
   a.force_partial = 1;
-  if ((st = launch_split_decode(D, tk3, tv3, tk3, tv3, a, batch, s))) return st;
+  a.wait_prior_at_exit = 1;  // started beside the prefix pass (independent tokens)
+  if ((st = launch_split_decode(D, tk3, tv3, tk3, tv3, a, batch, s, true))) return st;
   // 3. merge prefix and suffix partials
   PrefixMergeArgs m;
   std::memset(&m, 0, sizeof(m));

@@ -374,6 +374,11 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
   const FusedAppend none{nullptr, nullptr, nullptr, nullptr};
   split_body<D, TWO>(&tk, &tv, &tk8, &tv8, a, a.q, a.out, a.ws_o, a.ws_ml, none, blockIdx.x,
                      blockIdx.y, blockIdx.z);
+  // started early beside an independent grid: one CTA holds this grid open
+  // until that grid has finished, so a launch that waits for this grid also
+  // sees the other's results
+  if (a.wait_prior_at_exit && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+    pdl_wait_prior_grid();
 }
 
 // Every Full layer of a hybrid stack in one launch: blockIdx.z = layer *
@@ -413,26 +418,40 @@ __global__ void __launch_bounds__(128) phs_stack_merge_kernel(const __grid_const
 // ------------------------------------------------------------ launchers --
 template <int D, bool TWO>
 static int launch_split_t(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tk8,
-                          const CUtensorMap& tv8, const SplitArgs& a, int B, cudaStream_t stream) {
+                          const CUtensorMap& tv8, const SplitArgs& a, int B, cudaStream_t stream,
+                          bool dependent) {
   auto kern = phs_split_decode_kernel<D, TWO>;
   const int smem = SplitLayout<D>::kAlloc;
   if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
   dim3 grid(B, a.Hkv, a.max_splits);
-  kern<<<grid, kSplitWarps * 32, smem, stream>>>(tk, tv, tk8, tv8, a);
-  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+  if (!dependent) {
+    kern<<<grid, kSplitWarps * 32, smem, stream>>>(tk, tv, tk8, tv8, a);
+    return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kSplitWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, tk8, tv8, a) == cudaSuccess ? PHS_OK : PHS_ECUDA;
 }
 
 int launch_split_decode(int D, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tk8, const CUtensorMap& tv8, const SplitArgs& a,
-                        int B, cudaStream_t stream) {
+                        int B, cudaStream_t stream, bool dependent) {
   const bool two = a.G > 8;
   if (D == 128) {
-    return two ? launch_split_t<128, true>(tk, tv, tk8, tv8, a, B, stream)
-               : launch_split_t<128, false>(tk, tv, tk8, tv8, a, B, stream);
+    return two ? launch_split_t<128, true>(tk, tv, tk8, tv8, a, B, stream, dependent)
+               : launch_split_t<128, false>(tk, tv, tk8, tv8, a, B, stream, dependent);
   }
   if (D == 64) {
-    return two ? launch_split_t<64, true>(tk, tv, tk8, tv8, a, B, stream)
-               : launch_split_t<64, false>(tk, tv, tk8, tv8, a, B, stream);
+    return two ? launch_split_t<64, true>(tk, tv, tk8, tv8, a, B, stream, dependent)
+               : launch_split_t<64, false>(tk, tv, tk8, tv8, a, B, stream, dependent);
   }
   return PHS_EUNSUPPORTED;
 }

@@ -30,6 +30,8 @@ struct SplitArgs {
   int64_t num_pages;
   int64_t num_qpages;
   int Hq, Hkv, G;
+  int wait_prior_at_exit;   // launched beside an independent grid (programmatic
+                            // dependent): do not complete before it has
   int max_pages;            // block table row length
   int max_qpages;           // INT8 table row length
   int n_clamp;              // lengths above this are an error and clamped
@@ -127,7 +129,7 @@ struct MergeArgs {
 
 int launch_split_decode(int D, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tk8, const CUtensorMap& tv8, const SplitArgs& a,
-                        int B, cudaStream_t stream);
+                        int B, cudaStream_t stream, bool dependent = false);
 int launch_merge(int D, const MergeArgs& a, int B, cudaStream_t stream);
 
 // The cross-split merges of every Full layer of a hybrid stack: one launch

@@ -130,6 +130,9 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
   const uint32_t sb = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, split = blockIdx.y;
+  // the own-token split launch after this one does not depend on it: it may
+  // start in this grid's tail (programmatic dependent launch)
+  pdl_launch_dependents();
 
   // tiles of this CTA
   const int ntiles_all = a.shared_len / kPfxTile;
@@ -452,6 +455,9 @@ __global__ void __launch_bounds__(128) phs_merge_prefix_kernel(const PrefixMerge
   constexpr int V = D / 32;
   const int b = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // launched as a dependent of the own-token split, which does not complete
+  // before the prefix pass has: both grids' partials are in place after this
+  pdl_wait_prior_grid();
   const int G = a.G;
   const int n = min(a.seq_lens[b], a.n_clamp);
   const int ns = n > a.shared_len ? min((n - a.shared_len + a.T - 1) / a.T, a.max_splits) : 0;
@@ -521,9 +527,16 @@ int launch_prefix_decode(const CUtensorMap& tk, const CUtensorMap& tv, const Pre
 }
 
 int launch_merge_prefix(const PrefixMergeArgs& a, int B, cudaStream_t stream) {
-  dim3 grid(B, a.Hkv);
-  phs_merge_prefix_kernel<<<grid, 128, 0, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B, a.Hkv);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, phs_merge_prefix_kernel, a) == cudaSuccess ? PHS_OK : PHS_ECUDA;
 }
 
 int prefix_smem_bytes() { return PfxLayout::kAlloc; }
