@@ -66,8 +66,8 @@ __device__ __forceinline__ void merge_request(const MergeArgs& a, const float* w
         Lsum += v.y * wl;
       }
       const int cnt = min(32, ns - s0);
-#pragma unroll 4
-      for (int k = 0; k < cnt; ++k) {
+#pragma unroll 16
+      for (int k = 0; k < cnt; ++k) {  // up to 16 split loads in flight per lane
         const float w = __shfl_sync(0xffffffffu, wl, k);
         const float* src = ob + static_cast<size_t>(s0 + k) * G * D;
         if constexpr (V == 4) {
