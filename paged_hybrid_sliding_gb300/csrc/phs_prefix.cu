@@ -37,9 +37,10 @@
 // tile instead of eight N = 128 ones, and Q in tensor memory takes the Q
 // operand off the shared-memory path; both keep the tensor pipe under the
 // HBM time of a tile.  The running max m of a row only moves when it grows
-// by more than 2^8 (so P <= 256); only then are the O^T columns rescaled,
-// CTA-wide: every row publishes its factor in shared memory and a barrier
-// reduction tells all softmax warps whether any row moved.  The CTA writes
+// by more than 2^8 (so P <= 256); only then are the O^T columns of its row
+// tile rescaled: every row publishes its factor in shared memory and a
+// barrier reduction over the tile's four softmax warps tells them whether
+// any row moved.  The CTA writes
 // (m, l, O) partials; a merge kernel combines them with the requests' own
 // suffix tokens (attended by the split-KV kernel).
 #include "phs_attn.cuh"
@@ -80,8 +81,9 @@ struct PfxLayout {
   static constexpr int kBar = kAlpha + 2 * kPfxRows * 4;
   // full[KS + VS], empty[KS + VS], sfull[2], sfree[2], pfull[NP], odone[NP], drain
   static constexpr int kNumBars = 2 * (kPfxKStages + kPfxVStages) + 5 + 2 * kPfxPBufs;
-  static constexpr int kMisc = kBar + kNumBars * 8;      // tmem base, abort flag
-  static constexpr int kBytes = kMisc + 16;
+  // tmem base, abort flag, softmax failure flags [row tile][tile parity]
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 32;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 227 * 1024, "prefix kernel shared memory above the per-CTA limit");
 };
@@ -101,6 +103,36 @@ __device__ __forceinline__ bool pfx_wait(uint32_t bar, uint32_t parity, volatile
       if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
   }
+}
+
+// Packed fp32 pairs (two lanes of work per instruction on the FMA pipe) and
+// the three-input maximum: they halve the instruction count of the softmax
+// rows' scale, sum and max steps, which share their issue slots with the
+// exponentials and the P stores.
+__device__ __forceinline__ uint64_t f2_make(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_split(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // OR of `pred` over the `count` threads of named barrier `id` (all of them
@@ -149,6 +181,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
   const uint32_t bar_drain = bar_odone + 8 * NP;          // every issued MMA done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  volatile int* sm_fail = reinterpret_cast<volatile int*>(smem + L::kMisc + 8);
   float* alpha_s = reinterpret_cast<float*>(smem + L::kAlpha);
 
   if (warp == 9) {
@@ -170,6 +203,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
     }
     mbar_init(bar_drain, 2);
     *abort = 0;
+    for (int i = 0; i < 4; ++i) sm_fail[i] = 0;
     fence_mbar_init();
   }
   tc_fence_before();
@@ -331,25 +365,21 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
         tmem_ld32(tmem + lane_base + kTmS + mt * kPfxTile, sv0);
         tmem_ld32(tmem + lane_base + kTmS + mt * kPfxTile + 32, sv1);
         tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv0[i] = sv1[i] = 0u;
       }
       tc_fence_before();
       mbar_arrive(bar_sfree + 8 * mt);
-      // every softmax thread takes part in the same barrier reductions, so
-      // a failed wait ends the loop for all of them together
-      if (bar_red_or(1, 256, !got)) {
-        ok = false;
-        break;
-      }
       auto sv = [&](int i) { return __uint_as_float(i < 32 ? sv0[i] : sv1[i - 32]); };
-      float m8[8];  // tree reduction: eight independent chains
+      float m4[4];  // four independent chains, two scores per step
 #pragma unroll
-      for (int k = 0; k < 8; ++k) m8[k] = sv(k);
+      for (int k = 0; k < 4; ++k) m4[k] = fmaxf(sv(k), sv(4 + k));
 #pragma unroll
       for (int i = 8; i < kPfxTile; i += 8)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], sv(i + k));
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], sv(i + k), sv(i + 4 + k));
+      float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
       mx *= a.scale_log2;
       float alpha = 1.f;
       if (j == 0) {
@@ -360,7 +390,18 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
       }
       float* al = alpha_s + (j & 1) * kPfxRows;
       al[r] = alpha;
-      const bool resc = bar_red_or(1, 256, alpha != 1.f);
+      // The 128 threads of this row tile take part in one barrier reduction
+      // per tile: whether any row's max moved or any wait failed.  A failed
+      // wait is recorded in a flag of this tile's parity before the barrier
+      // (a thread cannot write the same flag again before every thread has
+      // read it: that would take it past the next tile's barrier), so all of
+      // them leave the loop together.
+      if (!got) sm_fail[2 * mt + (j & 1)] = 1;
+      const bool resc = bar_red_or(1 + mt, 128, !got || alpha != 1.f);
+      if (resc && sm_fail[2 * mt + (j & 1)]) {
+        ok = false;
+        break;
+      }
       // P buffer j % NP was last read by P V_{j-NP}; a rescale of O needs P V_{j-1}
       if (j >= NP || (resc && j >= 1)) {
         const int jj = resc ? j - 1 : j - NP;
@@ -373,21 +414,28 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
       l *= alpha;
       // P row: 64 bf16 = eight 16-byte units, K-major 128-byte swizzle
       const float c0 = m_used;
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
       uint8_t* prow = smem + L::kP + (j % NP) * L::kPBuf + r * 128;
+      // x = s * scale log2(e) - m for two scores per instruction; the row
+      // sum runs as four packed pairs
+      const uint64_t scale2 = f2_make(a.scale_log2, a.scale_log2), negm2 = f2_make(-c0, -c0);
+      uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         uint32_t w[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float p0 = ex2(fmaf(sv(8 * u + 2 * k), a.scale_log2, -c0));
-          const float p1 = ex2(fmaf(sv(8 * u + 2 * k + 1), a.scale_log2, -c0));
-          sum4[k] += p0 + p1;
+          const float2 x = f2_split(ffma2(f2_make(sv(8 * u + 2 * k), sv(8 * u + 2 * k + 1)),
+                                          scale2, negm2));
+          const float p0 = ex2(x.x), p1 = ex2(x.y);
+          sum2[k] = fadd2(sum2[k], f2_make(p0, p1));
           w[k] = pack_bf16(p0, p1);
         }
         *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      {
+        const float2 s0 = f2_split(fadd2(sum2[0], sum2[1])), s1 = f2_split(fadd2(sum2[2], sum2[3]));
+        l += (s0.x + s0.y) + (s1.x + s1.y);
+      }
       fence_proxy_async_smem();
       if (resc) {
         // this warp rescales O^T lanes d = 32 (warp & 3) .. +31, row columns
