@@ -524,11 +524,14 @@ __global__ void __launch_bounds__(128) phs_merge_prefix_kernel(const PrefixMerge
       const size_t part = (static_cast<size_t>(b) * a.Hkv + h) * a.max_splits + (s - a.num_psplits);
       return reinterpret_cast<const float2*>(a.ws_ml)[part * G + g];
     };
+    // split s's output row: prefix splits kPfxRows rows apart, then the
+    // suffix splits G rows apart (a select, so the loads can be hoisted)
+    const float* po = a.ws_po + ((static_cast<size_t>(h) * a.num_psplits) * kPfxRows + r) * D;
+    const float* so = a.ws_o + (((static_cast<size_t>(b) * a.Hkv + h) * a.max_splits) * G + g) * D -
+                      static_cast<ptrdiff_t>(a.num_psplits) * G * D;
     auto o_of = [&](int s) -> const float* {
-      if (s < a.num_psplits)
-        return a.ws_po + ((static_cast<size_t>(h) * a.num_psplits + s) * kPfxRows + r) * D;
-      const size_t part = (static_cast<size_t>(b) * a.Hkv + h) * a.max_splits + (s - a.num_psplits);
-      return a.ws_o + (part * G + g) * D;
+      return s < a.num_psplits ? po + static_cast<size_t>(s) * kPfxRows * D
+                               : so + static_cast<ptrdiff_t>(s) * G * D;
     };
     float M = -INFINITY;
     for (int s = lane; s < total; s += 32) M = fmaxf(M, ml_of(s).x);
@@ -544,7 +547,8 @@ __global__ void __launch_bounds__(128) phs_merge_prefix_kernel(const PrefixMerge
         Lsum += v.y * wl;
       }
       const int cnt = min(32, total - s0);
-      for (int k = 0; k < cnt; ++k) {
+#pragma unroll 16
+      for (int k = 0; k < cnt; ++k) {  // up to 16 split loads in flight per lane
         const float w = __shfl_sync(0xffffffffu, wl, k);
         const float4 o = *reinterpret_cast<const float4*>(o_of(s0 + k) + lane * V);
         acc[0] += w * o.x;
