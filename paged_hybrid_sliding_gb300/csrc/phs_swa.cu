@@ -25,7 +25,13 @@
 
 namespace phs {
 
-constexpr int kSwaStages = 3;
+// Shared-memory stages per warp.  Measured on 60 layers x batch 256: 2
+// stages 6,845 GB/s, 3 stages 6,471, 4 (4 warps per CTA) 5,990 -- fewer
+// copies in flight per SM run faster here.
+#ifndef PHS_SWA_STAGES
+#define PHS_SWA_STAGES 2
+#endif
+constexpr int kSwaStages = PHS_SWA_STAGES;
 
 // Shared-memory layout for NW warps: [stages][bars][query slots][info].
 struct SwaLayout {
