@@ -16,14 +16,6 @@
 
 namespace phs {
 
-// swizzled byte offset inside a tile written by TMA with
-// CU_TENSOR_MAP_SWIZZLE_128B (tile base 1024-byte aligned)
-__device__ __forceinline__ uint32_t swz128(uint32_t off) {
-  return off ^ (((off >> 7) & 7u) << 4);
-}
-// ... and with CU_TENSOR_MAP_SWIZZLE_64B (tile base 512-byte aligned)
-__device__ __forceinline__ uint32_t swz64(uint32_t off) { return off ^ (((off >> 7) & 3u) << 4); }
-
 // Bytes of one staged chunk: K + V of 16 bf16 tokens, or of 32 INT8 tokens.
 template <int D>
 struct ChunkGeom {
@@ -34,7 +26,9 @@ struct ChunkGeom {
 };
 
 // Per-lane shared-memory offsets of the mma fragments inside a staged chunk,
-// computed once per warp.  Stage bases are 1024-byte aligned and the
+// computed once per warp.  TMA's 128-byte swizzle stores byte offset o of a
+// tile at o ^ (((o >> 7) & 7) << 4) (the 64-byte swizzle: & 3 instead of
+// & 7).  Stage bases are 1024-byte aligned and the
 // swizzle only permutes 16-byte units inside 1024-byte blocks, so the
 // address of fragment step i is (stage + lane offset) ^ (constant of i) + an
 // immediate: one logic op per fragment load instead of the full swizzle.
