@@ -290,7 +290,7 @@ class PagedFullWorkload(Workload):
 
     kernel_launches_per_step = 1
 
-    def __init__(self, device, seed=2, batch=64):
+    def __init__(self, device, seed=2, batch=64, tokens_per_split=0):
         import paged_hybrid_sliding_gb300 as phs
         self.phs = phs
         self.w = w = synth.paged_full(seed=seed, B=batch)
@@ -307,7 +307,7 @@ class PagedFullWorkload(Workload):
         self.sl = torch.from_numpy(w.n_after).to(device)
         self.max_seq = int(w.n_after.max())
         self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
-        self.tps = phs.decode_tokens_per_split(B, Hkv, self.max_seq)
+        self.tps = phs.decode_tokens_per_split(B, Hkv, self.max_seq, tokens_per_split)
         self.ws = torch.empty(phs.decode_workspace_bytes(B, Hq, Hkv, D, self.max_seq, self.tps),
                               dtype=torch.uint8, device=device)
         tokens = int(w.n_after.sum())
@@ -686,7 +686,7 @@ class Int8Workload(Workload):
 
     kernel_launches_per_step = 1
 
-    def __init__(self, device, seed=4, batch=32):
+    def __init__(self, device, seed=4, batch=32, tokens_per_split=0):
         import paged_hybrid_sliding_gb300 as phs
         self.phs = phs
         self.w = w = synth.int8_block32(seed=seed, B=batch)
@@ -730,7 +730,7 @@ class Int8Workload(Workload):
         self.ql = torch.from_numpy(self.qlen).to(device)
         self.max_seq = int(w.n_after.max())
         self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
-        self.tps = phs.decode_tokens_per_split(B, Hkv, self.max_seq)
+        self.tps = phs.decode_tokens_per_split(B, Hkv, self.max_seq, tokens_per_split)
         self.ws = torch.empty(phs.decode_workspace_bytes(B, Hq, Hkv, D, self.max_seq, self.tps,
                                                          has_int8=True),
                               dtype=torch.uint8, device=device)
@@ -834,7 +834,7 @@ class SharedPrefixWorkload(Workload):
         self.vn = synth.normal_bf16((B, Hkv, D), g + 5, device=device)
         self.max_seq = int(w.n_pre.max()) + self.nsteps
         self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
-        self.tps = phs.decode_tokens_per_split(B, Hkv, self.max_seq)
+        self.tps = phs.decode_tokens_per_split(B, Hkv, self.max_seq, tokens_per_split)
         self.ws = torch.empty(phs.decode_workspace_bytes(B, Hq, Hkv, D, self.max_seq, self.tps),
                               dtype=torch.uint8, device=device)
         self.k_idx = 0
@@ -930,13 +930,15 @@ def make_workload(config, device, args):
     if config == 1:
         return TinyHybridWorkload(device, fused=not args.no_fused)
     if config == 2:
-        return PagedFullWorkload(device, batch=args.batch or 64)
+        return PagedFullWorkload(device, batch=args.batch or 64,
+                                 tokens_per_split=args.tokens_per_split)
     if config == 3:
         return HybridStackWorkload(device, distinct=args.distinct_pools,
                                    batch=args.batch or 256, swa_only=args.swa_only,
                                    fused=not args.no_fused)
     if config == 4:
-        return Int8Workload(device, batch=args.batch or 32)
+        return Int8Workload(device, batch=args.batch or 32,
+                            tokens_per_split=args.tokens_per_split)
     if config == 5:
         return SharedPrefixWorkload(device, prefix_kernel=not args.no_prefix_kernel,
                                     prefix_len=args.prefix_len)
@@ -1186,6 +1188,9 @@ def main():
     ap.add_argument("--batch", type=int, default=0,
                     help="requests (0 = the workload's own batch: 64 / 256 / 32 for configs "
                          "2 / 3 / 4); smaller batches are for profiler captures")
+    ap.add_argument("--tokens-per-split", type=int, default=0,
+                    help="configs 2 and 4: split length (0 = the library's choice for the "
+                         "batch); profiler captures of a smaller batch pass the full-size one")
     ap.add_argument("--graph", dest="graph", action="store_true", default=None,
                     help="replay each step as a CUDA graph (default: only for config 1)")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
