@@ -42,22 +42,25 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 
 def test_noalloc_lengthens_splits_to_fit_and_rejects_beyond_scratch():
-    # 32 requests with a stated bound of 128K tokens: at the default split
-    # length the partials would need 68 MB, more than the 32 MiB scratch, so
-    # the call must lengthen its splits and still match the workspace path
-    lens = synth.seq_lens_uniform(32, 1, 8000, 74)
-    pool, q, bt, sl, _ = _case(73, lens)
-    bound = 131072
-    out = torch.empty((32, 32, 128), dtype=torch.float32, device="cuda")
+    # two requests of one KV head with 16 query heads and a stated bound of
+    # 600,000 tokens: for so small a grid the library's split length is short
+    # (256 tokens on 152 SMs) and its partials (39 MB) do not fit the 32 MiB
+    # scratch, so the call must lengthen its splits and still match the
+    # workspace path
+    Hq, Hkv, D, bound = 16, 1, 128, 600_000
+    pool, q, bt, sl, _ = _case(73, [3000, 7001], Hq=Hq, Hkv=Hkv, D=D)
+    assert phs.decode_workspace_bytes(2, Hq, Hkv, D, bound) > phs.NOALLOC_SCRATCH_BYTES
+    out = torch.empty((2, Hq, D), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     phs.attn_decode_full_paged_noalloc(q, pool, bt, sl, bound, out, status=st)
     ref = phs.attn_decode_full_paged(q, pool, bt, sl, bound, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    assert phs.decode_workspace_bytes(32, 32, 8, 128, bound) > phs.NOALLOC_SCRATCH_BYTES
     assert_close(out_np(out), out_np(ref), "lengthened splits")
     # a request that cannot fit even with 4096-token splits is refused on
     # the host, before anything is launched
+    bound = 131072
+    pool, *_ = _case(75, [16])
     big_b = 512
     qb = torch.zeros((big_b, 32, 128), dtype=torch.bfloat16, device="cuda")
     btb = torch.zeros((big_b, 64), dtype=torch.int32, device="cuda")
