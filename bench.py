@@ -834,7 +834,7 @@ class SharedPrefixWorkload(Workload):
         self.vn = synth.normal_bf16((B, Hkv, D), g + 5, device=device)
         self.max_seq = int(w.n_pre.max()) + self.nsteps
         self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
-        self.tps = phs.decode_tokens_per_split(B, Hkv, self.max_seq, tokens_per_split)
+        self.tps = phs.decode_tokens_per_split(B, Hkv, self.max_seq)
         self.ws = torch.empty(phs.decode_workspace_bytes(B, Hq, Hkv, D, self.max_seq, self.tps),
                               dtype=torch.uint8, device=device)
         self.k_idx = 0
