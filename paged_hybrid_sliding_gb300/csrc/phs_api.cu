@@ -1004,6 +1004,7 @@ int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_laye
     p->W = W;
     p->out_f32 = out_dtype == PHS_OUT_F32;
     p->scale_log2 = scale_log2;
+    p->wait_prior_at_exit = nfull > 0;  // every SWA launch here is a dependent launch
     if (fold_layers) {  // the Full layers' merges ride on the first SWA launch
       for (int i = 0; i < fold_layers; ++i) p->merge_layer[i] = fold_merges.layer[i];
       p->merge = fold_merges.a;

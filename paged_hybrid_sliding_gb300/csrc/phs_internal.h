@@ -166,6 +166,9 @@ struct SwaParams {
   StackMergeLayer merge_layer[kStackMaxFull];
   MergeArgs merge;
   int num_merge_layers;     // 0: none
+  int wait_prior_at_exit;   // launched beside the split launch before it
+                            // (programmatic dependent): do not complete
+                            // before it has
 };
 
 template <int MAXL>

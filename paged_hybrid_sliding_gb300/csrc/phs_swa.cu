@@ -264,7 +264,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
   }
   // ---- a hybrid-stack step's Full-layer merges: one warp per (layer,
-  // request, KV head), after this warp's SWA units
+  // request, KV head), after this warp's SWA units.  Without merges, one
+  // thread still waits for the split grid this launch started beside, so
+  // that this grid's completion (which later launches are ordered after)
+  // implies that one's.
+  if (p.num_merge_layers == 0 && p.wait_prior_at_exit && blockIdx.x == 0 && threadIdx.x == 0)
+    pdl_wait_prior_grid();
   if (p.num_merge_layers > 0) {
     // the split launch before this one (this grid may start while it runs)
     pdl_wait_prior_grid();
