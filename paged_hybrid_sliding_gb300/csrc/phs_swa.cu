@@ -40,16 +40,17 @@ constexpr int kSwaStages = PHS_SWA_STAGES;
 #endif
 constexpr int kSwaWarps = PHS_SWA_WARPS;
 
-// Shared-memory layout for NW warps: [stages][bars][query slots][info].
+// Shared-memory layout for NW warps of S stages: [stages][bars][query
+// slots][info].
 struct SwaLayout {
   int kv, qslot, stages_bytes, bar_off, q_off, info_off, total;
-  __host__ __device__ SwaLayout(int D, int G, int NW, int B) {
+  __host__ __device__ SwaLayout(int D, int G, int NW, int S, int B) {
     kv = 64 * D;                                   // K + V tile of 16 tokens
     qslot = (G * D * 2 + 127) / 128 * 128;         // one group's queries
-    stages_bytes = NW * kSwaStages * kv;
+    stages_bytes = NW * S * kv;
     bar_off = stages_bytes;
-    q_off = bar_off + NW * kSwaStages * 8;
-    info_off = q_off + NW * kSwaStages * qslot;
+    q_off = bar_off + NW * S * 8;
+    info_off = q_off + NW * S * qslot;
     total = info_off + 12 * B + 1024;              // + base alignment slack
   }
 };
@@ -63,15 +64,14 @@ struct SwaUnit {
   bool ok;
 };
 
-template <int D, bool TWO, int MAXL, int NW>
+template <int D, bool TWO, int MAXL, int NW, int S>
 __global__ void __launch_bounds__(NW * 32, 1)
     phs_swa_decode_kernel(const __grid_constant__ SwaParams<MAXL> p) {
-  constexpr int S = kSwaStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = swa_align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = p.B, Hkv = p.Hkv, G = p.G, W = p.W;
-  const SwaLayout L(D, G, NW, B);
+  const SwaLayout L(D, G, NW, S, B);
 
   // ---- per-request ring id, newest slot and length, cached in smem
   int32_t* s_ring = reinterpret_cast<int32_t*>(smem + L.info_off);
@@ -283,11 +283,11 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
 }
 
-template <int D, bool TWO, int MAXL, int NW>
+template <int D, bool TWO, int MAXL, int NW, int S>
 static int launch_swa_t(const SwaParams<MAXL>& p, int num_sms, cudaStream_t stream,
                         bool dependent) {
-  auto kern = phs_swa_decode_kernel<D, TWO, MAXL, NW>;
-  const int smem = SwaLayout(D, p.G, NW, p.B).total;
+  auto kern = phs_swa_decode_kernel<D, TWO, MAXL, NW, S>;
+  const int smem = SwaLayout(D, p.G, NW, S, p.B).total;
   if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
   const long long units = std::max(static_cast<long long>(p.num_layers),
                                    static_cast<long long>(p.num_merge_layers)) *
@@ -315,25 +315,43 @@ static int launch_swa_t(const SwaParams<MAXL>& p, int num_sms, cudaStream_t stre
   return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? PHS_OK : PHS_ECUDA;
 }
 
-// kSwaWarps warps per CTA when their stages fit in shared memory, else 4.
-int swa_warps(int D, int G, int batch, int smem_optin) {
-  if (SwaLayout(D, G, kSwaWarps, batch).total <= smem_optin) return kSwaWarps;
-  if (SwaLayout(D, G, 4, batch).total <= smem_optin) return 4;
-  return 0;
+// Launch shapes (warps per CTA x stages per warp):
+//   latency  4 x 4: when every unit gets a warp of its own in one wave, a
+//            unit's W/16 chunks are the whole chain, and 4 stages take it in
+//            half the round trips of 2 (one SWA layer of a batch-2 hybrid
+//            step: 13.5 -> 12.3 us per step; 8 stages for D = 64 gave the
+//            same);
+//   stream   kSwaWarps x kSwaStages: many units per warp, the copies of the
+//            next unit overlap the current one;
+//   small    4 x kSwaStages: when the stream shape's shared memory does not fit.
+enum SwaMode { kSwaNone = 0, kSwaLatency, kSwaStream, kSwaSmall };
+
+SwaMode swa_mode(int D, int G, int batch, long long units, int num_sms, int smem_optin) {
+  if (units <= 4LL * num_sms &&
+      SwaLayout(D, G, 4, 4, batch).total <= smem_optin)
+    return kSwaLatency;
+  if (SwaLayout(D, G, kSwaWarps, kSwaStages, batch).total <= smem_optin) return kSwaStream;
+  if (SwaLayout(D, G, 4, kSwaStages, batch).total <= smem_optin) return kSwaSmall;
+  return kSwaNone;
 }
 
-int swa_smem_bytes(int D, int G, int batch) { return SwaLayout(D, G, 4, batch).total; }
+int swa_smem_bytes(int D, int G, int batch) { return SwaLayout(D, G, 4, kSwaStages, batch).total; }
 
 template <int MAXL>
 int launch_swa_decode(int D, const SwaParams<MAXL>& p, int num_sms, int smem_optin,
                       cudaStream_t stream, bool dependent) {
   if (static_cast<long long>(p.num_layers) * p.B * p.Hkv > INT32_MAX / 2) return PHS_EUNSUPPORTED;
-  const int nw = swa_warps(D, p.G, p.B, smem_optin);
-  if (nw == 0) return PHS_EUNSUPPORTED;
+  const SwaMode mode = swa_mode(D, p.G, p.B, static_cast<long long>(p.num_layers) * p.B * p.Hkv,
+                                num_sms, smem_optin);
+  if (mode == kSwaNone) return PHS_EUNSUPPORTED;
   const bool two = p.G > 8;
-#define PHS_SWA_LAUNCH(DD, TT)                                                    \
-  return nw == kSwaWarps ? launch_swa_t<DD, TT, MAXL, kSwaWarps>(p, num_sms, stream, dependent) \
-                         : launch_swa_t<DD, TT, MAXL, 4>(p, num_sms, stream, dependent)
+#define PHS_SWA_LAUNCH(DD, TT)                                                               \
+  switch (mode) {                                                                            \
+    case kSwaLatency: return launch_swa_t<DD, TT, MAXL, 4, 4>(p, num_sms, stream, dependent); \
+    case kSwaStream:                                                                         \
+      return launch_swa_t<DD, TT, MAXL, kSwaWarps, kSwaStages>(p, num_sms, stream, dependent); \
+    default: return launch_swa_t<DD, TT, MAXL, 4, kSwaStages>(p, num_sms, stream, dependent);  \
+  }
   if (D == 128) {
     if (two) PHS_SWA_LAUNCH(128, true);
     PHS_SWA_LAUNCH(128, false);
