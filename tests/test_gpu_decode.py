@@ -146,6 +146,29 @@ def test_swa_ring_decode(W, D, Hq, Hkv):
     assert_close(out_np(out), ref, f"W={W} D={D}")
 
 
+@pytest.mark.parametrize("B", [4, 700, 7200])
+def test_swa_ring_decode_launch_shapes(B):
+    # the SWA launch picks its shape from the work and shared memory: 4 warps
+    # x 4 stages when every (request, KV head) unit has a warp of its own (4
+    # units), 8 warps x 2 stages for many units (700), and 4 warps x 2 stages
+    # when the per-request table of a very large batch leaves too little
+    # shared memory for 8 warps (7200)
+    W, D, Hq, Hkv = 16, 128, 4, 1
+    lens = np.random.default_rng(B).integers(1, 3 * W, B).astype(np.int32)
+    c = ring_case(lens, W, Hq, Hkv, D, seed=B)
+    ring = phs.RingPool(bf16_dev(c["kr"]), bf16_dev(c["vr"]))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = phs.attn_decode_swa_ring(bf16_dev(c["q"]), ring, dev(c["pos"]), dev(c["lens"]),
+                                   ring_ids=dev(c["ids"]), softmax_scale=1 / math.sqrt(D),
+                                   out_dtype=torch.float32, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref, s = oracle.decode_swa_ring(c["q"], c["kr"], c["vr"], c["ids"], c["pos"], c["lens"],
+                                    1 / math.sqrt(D))
+    assert s == 0
+    assert_close(out_np(out), ref, f"B={B}")
+
+
 # ------------------------------------------------------------------ INT8 --
 def int8_case(lens, qlens, Hq, Hkv, D, seed):
     """bf16 pages over the whole sequence; INT8 pages for tokens < qlen,
