@@ -23,8 +23,47 @@ namespace phs {
 // low mantissa bits, so the code byte is the low byte of the sum's bits.
 constexpr float kRoundMagic = 12582912.0f;
 
+// Packed fp32 pairs (two lanes of work per instruction on the FMA pipe,
+// each rounded to nearest as the scalar instruction would) and the
+// three-input min / max.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 template <int D>
-__global__ void __launch_bounds__(128) phs_quant_kernel(const QuantArgs a) {
+__global__ void __launch_bounds__(128, 8) phs_quant_kernel(const QuantArgs a) {
   constexpr int kPieces = D / 8;              // 16-byte pieces per token row
   constexpr int kIters = kPage * kPieces / 32;  // pieces of one page tile per lane
   const int jr = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
@@ -60,15 +99,18 @@ __global__ void __launch_bounds__(128) phs_quant_kernel(const QuantArgs a) {
   uint4 x[kIters];
 #pragma unroll
   for (int it = 0; it < kIters; ++it) x[it] = __ldcs(tile + it * 32 + lane);
-  // absmax in packed bf16 (exact: the max of |x| is one of the inputs)
-  __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
+  // absmax in packed bf16 (exact: the max of |x| is one of the inputs).
+  // max.xorsign.abs keeps max(|a|, |b|) as the magnitude (its sign is
+  // dropped below): one instruction per pair
+  uint32_t m2 = 0u;
 #pragma unroll
   for (int it = 0; it < kIters; ++it) {
-    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&x[it]);
+    const uint32_t* v = reinterpret_cast<const uint32_t*>(&x[it]);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) m2 = __hmax2(m2, __habs2(v[k]));
+    for (int k = 0; k < 4; ++k) asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v[k]));
   }
-  float amax = fmaxf(__low2float(m2), __high2float(m2));
+  m2 &= 0x7FFF7FFFu;
+  float amax = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if (lane == 0) s_amax[warp] = amax;
@@ -79,32 +121,46 @@ __global__ void __launch_bounds__(128) phs_quant_kernel(const QuantArgs a) {
   // code = rint(x / s) with x / s the IEEE quotient.  y = x * fl(1/s) is
   // within |x/s| * (2^-23 + 2^-48) + ulp/2 <= 1.9e-5 of that quotient (|x/s|
   // <= 127.5), so rint(y) equals rint(x / s) unless y lies within 1.9e-5 of
-  // a half-integer; those rare elements take the IEEE division itself.  A
-  // scale so small that 1/s overflows (subnormal groups) always divides.
-  // |rint(x / s)| <= 127 by construction, so no clamp is needed.  s == 0
-  // gives rs == 0 and every code 0.
+  // a half-integer: a group of 8 codes holding such an element takes the
+  // IEEE division for all 8 (rare).  A scale so small that 1/s overflows
+  // (subnormal groups) always divides.  |rint(x / s)| <= 127 by
+  // construction, so no clamp is needed.  s == 0 gives rs == 0 and every
+  // code 0.  The rounding steps run on packed pairs (two elements per
+  // instruction, each rounded as the scalar operation would be).
   const bool always_divide = !(rs < INFINITY);
-  auto code = [s, rs, always_divide](float v) -> uint32_t {
-    const float y = __fmul_rn(v, rs);
-    float t = __fadd_rn(y, kRoundMagic);
-    const float r = __fsub_rn(t, kRoundMagic);
-    if (always_divide || fabsf(__fsub_rn(y, r)) > 0.4999f)
-      t = __fadd_rn(rintf(__fdiv_rn(v, s)), kRoundMagic);
-    return __float_as_uint(t);  // code in the low byte
-  };
-  // codes of this page tile: rows 16*half .. of INT8 page qp, same piece order
+  const uint64_t rs2 = f2_pack(rs, rs), magic2 = f2_pack(kRoundMagic, kRoundMagic);
   uint2* out = reinterpret_cast<uint2*>(codes + ((static_cast<size_t>(qp) * a.Hkv + h) * kQBlock +
                                                  kPage * half) * D);
 #pragma unroll
   for (int it = 0; it < kIters; ++it) {
-    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&x[it]);
+    const uint32_t* v = reinterpret_cast<const uint32_t*>(&x[it]);
+    uint32_t t[8];  // fl(rint(code) + 1.5 * 2^23): the code in the low byte
+    float dmax = 0.f, dmin = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      // bf16 pair -> fp32 pair: the bf16 bits are the high half of the fp32
+      const uint64_t f = f2_pack(__uint_as_float(v[k] << 16), __uint_as_float(v[k] & 0xFFFF0000u));
+      const uint64_t y = f2_mul(f, rs2);
+      const uint64_t tt = f2_add(y, magic2);
+      const uint64_t d = f2_sub(y, f2_sub(tt, magic2));  // y - rint(y), in [-1/2, 1/2]
+      const float2 dd = f2_unpack(d), tf = f2_unpack(tt);
+      dmax = fmax3(dmax, dd.x, dd.y);
+      dmin = fmin3(dmin, dd.x, dd.y);
+      t[2 * k] = __float_as_uint(tf.x);
+      t[2 * k + 1] = __float_as_uint(tf.y);
+    }
+    if (always_divide || dmax > 0.4999f || dmin < -0.4999f) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float xv = __uint_as_float(e & 1 ? v[e >> 1] & 0xFFFF0000u : v[e >> 1] << 16);
+        t[e] = __float_as_uint(__fadd_rn(rintf(__fdiv_rn(xv, s)), kRoundMagic));
+      }
+    }
     uint32_t w[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const float2 f0 = __bfloat1622float2(v[2 * k]);
-      const float2 f1 = __bfloat1622float2(v[2 * k + 1]);
-      const uint32_t lo = __byte_perm(code(f0.x), code(f0.y), 0x0040);
-      const uint32_t hi = __byte_perm(code(f1.x), code(f1.y), 0x0040);
+      const uint32_t lo = __byte_perm(t[4 * k], t[4 * k + 1], 0x0040);
+      const uint32_t hi = __byte_perm(t[4 * k + 2], t[4 * k + 3], 0x0040);
       w[k] = __byte_perm(lo, hi, 0x5410);
     }
     out[it * 32 + lane] = make_uint2(w[0], w[1]);
