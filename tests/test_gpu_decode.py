@@ -245,3 +245,26 @@ def test_split_and_merge_entry_points_match_composed_call():
     torch.cuda.synchronize()
     assert torch.equal(out1, out2)
     assert_close(out_np(out1), ref_full(c), "split+merge")
+
+
+# ------------------------------------------------------------ split plan --
+def test_split_length_planner():
+    # the longest of 4096, 2048, ..., 128 tokens whose grid (batch x KV heads
+    # x splits of the longest request) still has 16 CTAs per SM, else 128;
+    # an explicit length is kept; the workspace follows the chosen length
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+
+    def rule(B, Hkv, n):
+        t = 4096
+        while t > 128 and B * Hkv * -(-n // t) < 16 * sms:
+            t //= 2
+        return t
+
+    for B, Hkv, n in [(64, 8, 32769), (32, 8, 65537), (256, 8, 131073), (2, 1, 600_000),
+                      (1, 1, 100), (8, 8, 8000)]:
+        t = phs.decode_tokens_per_split(B, Hkv, n)
+        assert t == rule(B, Hkv, n), (B, Hkv, n)
+        ws = phs.decode_workspace_bytes(B, 4 * Hkv, Hkv, 128, n)
+        assert ws == phs.decode_workspace_bytes(B, 4 * Hkv, Hkv, 128, n, t)
+    assert phs.decode_tokens_per_split(64, 8, 32769, 512) == 512
+    assert phs.decode_tokens_per_split(64, 8, 32769) == 4096  # the paged batch-64 workload
