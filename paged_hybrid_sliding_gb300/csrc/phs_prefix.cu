@@ -52,14 +52,15 @@
 
 namespace phs {
 
-// Stage counts measured on the 250,000-token prefix (decode call, ms):
-// 3 K / 2 V 0.253, 2/2 0.256, 3/3 0.257, 4/2 0.262, 4/4 0.263, 5/4 0.265 --
+// Stage counts measured on the 250,000-token prefix (decode call, ms, with
+// the separate P V issuer): 3 K / 3 V 0.2467, 4/2 0.2477, 4/4 0.2493,
+// 4/3 0.2497, 3/4 0.2499, 3/2 0.2505, 5/3 0.2506, 2/2 0.2528 -- past 3 + 3
 // a deeper ring only adds requests in flight, not rate.
 #ifndef PHS_PFX_KSTAGES
 #define PHS_PFX_KSTAGES 3
 #endif
 #ifndef PHS_PFX_VSTAGES
-#define PHS_PFX_VSTAGES 2
+#define PHS_PFX_VSTAGES 3
 #endif
 #ifndef PHS_PFX_PBUFS
 #define PHS_PFX_PBUFS 2
