@@ -174,13 +174,15 @@ int check_int8(const phs_int8_pool* p) {
   return PHS_OK;
 }
 
-// Default split length: the longest of 4096, 2048, ... 128 tokens whose
-// grid (B x Hkv x splits of the longest request) still has 16 CTAs per SM.
-// Long splits amortise each CTA's set-up (queries, page ids, the first
-// copies) and keep the partial results small.  Measured (GB/s, whole step;
-// 1024 / 2048 / 4096 tokens): paged batch 64 7,028 / 7,089 / 7,037; INT8
-// batch 32 6,033 / 6,557 / 6,753; 70-layer stack batch 256 7,042 / 7,206 /
-// 7,306.
+// Default split length: the longest of 4096, 2048, ... 128 tokens that
+// gives the longest request at least 8 splits and whose grid (B x Hkv x
+// splits of the longest request) still has 16 CTAs per SM.  Long splits
+// amortise each CTA's set-up (queries, page ids, the first copies) and keep
+// the partial results small; 8 splits of the longest request keep the last
+// wave fine-grained.  Measured (GB/s, whole step, each set on one box; 1024
+// / 2048 / 4096 tokens): paged batch 64, lengths to 32K, 7,114 / 7,170 /
+// 7,134; INT8 batch 32 at 65K 6,033 / 6,557 / 6,753; 70-layer stack batch
+// 256, lengths to 128K, 7,042 / 7,206 / 7,306.
 #ifndef PHS_SPLIT_T_MAX
 #define PHS_SPLIT_T_MAX 4096
 #endif
@@ -191,6 +193,7 @@ int check_int8(const phs_int8_pool* p) {
 int32_t plan_tokens_per_split(int B, int Hkv, int max_seq, int requested, int sms) {
   if (requested > 0) return requested;
   int t = PHS_SPLIT_T_MAX;
+  while (t > 128 && 8LL * t > max_seq) t /= 2;
   const long long target = static_cast<long long>(PHS_SPLIT_CTAS_PER_SM) * std::max(sms, 1);
   while (t > 128) {
     const long long ctas = static_cast<long long>(B) * Hkv * ((max_seq + t - 1) / t);

@@ -249,13 +249,16 @@ def test_split_and_merge_entry_points_match_composed_call():
 
 # ------------------------------------------------------------ split plan --
 def test_split_length_planner():
-    # the longest of 4096, 2048, ..., 128 tokens whose grid (batch x KV heads
-    # x splits of the longest request) still has 16 CTAs per SM, else 128;
-    # an explicit length is kept; the workspace follows the chosen length
+    # the longest of 4096, 2048, ..., 128 tokens that gives the longest
+    # request at least 8 splits and whose grid (batch x KV heads x splits of
+    # the longest request) still has 16 CTAs per SM, else 128; an explicit
+    # length is kept; the workspace follows the chosen length
     sms = torch.cuda.get_device_properties(0).multi_processor_count
 
     def rule(B, Hkv, n):
         t = 4096
+        while t > 128 and 8 * t > n:
+            t //= 2
         while t > 128 and B * Hkv * -(-n // t) < 16 * sms:
             t //= 2
         return t
@@ -267,4 +270,5 @@ def test_split_length_planner():
         ws = phs.decode_workspace_bytes(B, 4 * Hkv, Hkv, 128, n)
         assert ws == phs.decode_workspace_bytes(B, 4 * Hkv, Hkv, 128, n, t)
     assert phs.decode_tokens_per_split(64, 8, 32769, 512) == 512
-    assert phs.decode_tokens_per_split(64, 8, 32769) == 4096  # the paged batch-64 workload
+    assert phs.decode_tokens_per_split(64, 8, 32700) == 2048  # the paged batch-64 workload
+    assert phs.decode_tokens_per_split(32, 8, 65537) == 4096  # the INT8 workload
