@@ -168,3 +168,38 @@ def test_fused_stack_errors():
     assert phs.hybrid_stack_fused_workspace_bytes(8, 32, 8, 128, 4096, 0) == 0
     one = phs.hybrid_stack_fused_workspace_bytes(8, 32, 8, 128, 4096, 1)
     assert phs.hybrid_stack_fused_workspace_bytes(8, 32, 8, 128, 4096, 10) == 10 * one
+
+
+@pytest.mark.parametrize("nfull,nswa", [(1, 66), (18, 2)])
+def test_fused_stack_many_layers_equals_unfused(nfull, nswa):
+    # more SWA layers than one launch carries (64: a second SWA launch, a
+    # dependent of the first) and more Full layers than one split launch
+    # carries (16: a second multi-layer launch, the first batch merged by a
+    # merge launch, the last by the SWA launch); multi-split requests
+    n = [40, 700, 3001, 5100]
+    n_after = np.array(n, dtype=np.int32)
+    Hq, Hkv, D = 4, 1, 64
+    lf = [1] * nfull + [0] * nswa
+    bt, rp, host = _stack(n_after, Hq, Hkv, D, lf, seed=130 + nfull, W=16)
+    a = _device_layers(host, torch.float32)
+    b = _device_layers(host, torch.float32)
+    common = dict(block_table=dev(bt), ring_pos=dev(rp))
+    phs.attn_decode_hybrid_stack(a, Hq, dev(n_after), int(n_after.max()), do_append=True, **common)
+    phs.attn_decode_hybrid_stack_fused(b, Hq, dev(n_after), int(n_after.max()), **common)
+    torch.cuda.synchronize()
+    for l, (La, Lb) in enumerate(zip(a, b)):
+        assert torch.equal(La.out, Lb.out), l
+        for x, y in zip(_pools(La), _pools(Lb)):
+            assert torch.equal(x, y), l
+    # and the last layer of each kind against the oracle
+    scale = 1.0 / np.sqrt(D)
+    for l in (nfull - 1, nfull + nswa - 1):
+        full, q, kn, vn, k, v = host[l]
+        k, v = k.copy(), v.copy()
+        if full:
+            oracle.append_paged(k, v, kn, vn, bt, n_after)
+            ref, _ = oracle.decode_full_paged(q, k, v, bt, n_after, scale)
+        else:
+            oracle.append_ring(k, v, kn, vn, None, rp)
+            ref, _ = oracle.decode_swa_ring(q, k, v, None, rp, n_after, scale)
+        assert_close(out_np(b[l].out), ref, f"layer {l}")
