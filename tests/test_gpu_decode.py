@@ -49,7 +49,7 @@ RAGGED = [1, 15, 16, 17, 100, 1000, 2049, 5000]
 
 
 @pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 4, 2), (128, 8, 1), (128, 16, 2),
-                                      (64, 32, 2)])
+                                      (64, 32, 2), (128, 8, 8), (64, 2, 2)])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_full_decode_ragged(D, Hq, Hkv, out_dtype):
     c = paged_case(RAGGED, Hq, Hkv, D, seed=100 + D + Hq)
@@ -129,7 +129,7 @@ def ring_case(lens, W, Hq, Hkv, D, seed):
 
 
 @pytest.mark.parametrize("W", [16, 128, 1024])
-@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 4, 2), (128, 32, 2)])
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 4, 2), (128, 32, 2), (128, 8, 8)])
 def test_swa_ring_decode(W, D, Hq, Hkv):
     lens = [1, 5, W - 1, W, W + 1, 3 * W + 7, 40000]
     c = ring_case(lens, W, Hq, Hkv, D, seed=W + D)
@@ -192,7 +192,7 @@ def int8_case(lens, qlens, Hq, Hkv, D, seed):
     return c
 
 
-@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 8, 2), (128, 32, 2)])
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 8, 2), (128, 32, 2), (128, 8, 8)])
 @pytest.mark.parametrize("tps", [0, 64, 256])
 def test_int8_decode(D, Hq, Hkv, tps):
     lens = [33, 1100, 2100, 1056, 5000, 40]
