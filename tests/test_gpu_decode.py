@@ -169,6 +169,24 @@ def test_swa_ring_decode_launch_shapes(B):
     assert_close(out_np(out), ref, f"B={B}")
 
 
+def test_swa_ring_empty_request_gives_zero():
+    W, D, Hq, Hkv = 16, 128, 8, 2
+    c = ring_case([0, 1, 17, 0], W, Hq, Hkv, D, seed=55)
+    ring = phs.RingPool(bf16_dev(c["kr"]), bf16_dev(c["vr"]))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = phs.attn_decode_swa_ring(bf16_dev(c["q"]), ring, dev(c["pos"]), dev(c["lens"]),
+                                   ring_ids=dev(c["ids"]), softmax_scale=1 / math.sqrt(D),
+                                   out_dtype=torch.float32, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = out_np(out)
+    assert not got[0].any() and not got[3].any()
+    ref, s = oracle.decode_swa_ring(c["q"], c["kr"], c["vr"], c["ids"], c["pos"], c["lens"],
+                                    1 / math.sqrt(D))
+    assert s == 0
+    assert_close(got, ref, "empty SWA requests")
+
+
 # ------------------------------------------------------------------ INT8 --
 def int8_case(lens, qlens, Hq, Hkv, D, seed):
     """bf16 pages over the whole sequence; INT8 pages for tokens < qlen,
