@@ -314,7 +314,7 @@ int phs_attn_decode_swa_ring(const void *q, int32_t num_q_heads, const phs_ring_
  * k_new/v_new into the layer's pool (paged for Full layers through the
  * shared block_table, ring slot ring_pos for SWA layers), then attend:
  * Full layers through phs_attn_decode_full_paged, SWA layers through the
- * ring.  All SWA layers go into one launch; each Full layer is one split
+ * ring.  All SWA layers go into one launch per 64 layers; each Full layer is one split
  * launch plus one merge launch when a request has several splits, all
  * reusing `workspace` (phs_hybrid_stack_workspace_bytes).  Layers are independent: the step
  * runs each layer on its own q (no model weights are involved).
@@ -338,6 +338,9 @@ int phs_attn_decode_hybrid_stack(const phs_layer *layers, int32_t num_layers,
                                  void *workspace, size_t workspace_bytes,
                                  int32_t *dev_status, void *stream);
 
+/* Workspace bytes for phs_attn_decode_hybrid_stack with these shapes (the
+ * split partials of one Full layer at a time: the layers reuse it); 0 if the
+ * shape is not supported.  Host call, no device work. */
 size_t phs_hybrid_stack_workspace_bytes(int32_t batch, int32_t num_q_heads,
                                         int32_t num_kv_heads, int32_t head_dim,
                                         int32_t max_seq_len);
