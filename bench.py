@@ -1,14 +1,20 @@
 """Benchmark of the decode hot path on synthetic workloads.
 
-Default workload (N = 1): paged Full-attention decode, batch 64, 32 query /
-8 KV heads, head_dim 128, pages of 16 tokens, lengths uniform in [1K, 32K]
-(about 1.08 M cached tokens, 4.43 GB of K/V per step).  One step = append of
-the new token of every request + split-KV decode + cross-split merge,
-through the C ABI of libphs.so.
+Default run (no --config): every workload in one invocation.  The headline
+line is the 70-layer hybrid stack (10 Full paged layers + 60 SWA ring layers
+of W = 128, batch 256, 32 query / 8 KV heads, head_dim 128, lengths
+log-uniform in [4K, 128K]): one step appends every layer's new token and
+attends every layer, through the fused hybrid-stack call (two launches).
+The tiny hybrid case, the batch-64 paged Full decode, the INT8 block-32
+decode (with the rolling hot-to-warm hand-off) and the shared 250K-token
+prefix decode are measured in the same run, each with its own roofline,
+end-to-end number and CPU-oracle baseline, under the line's "configs" key.
+--config N measures one workload alone.
 
-Prints one JSON line with the throughput in algorithmic HBM GB/s (the K/V
-bytes the step must read, plus query, output and append bytes), attended KV
-tokens/s, the roofline of the dominant kernel, an end-to-end number through
+Each line gives the throughput in algorithmic HBM GB/s (the K/V bytes the
+step must read, plus query, output, table and append bytes), attended KV
+tokens/s, the roofline of the dominant kernel (CUDA events around its
+launch on its stream inside the timed loop), an end-to-end number through
 the public API with host buffers, and the CPU oracle timed on a bounded
 sample on the host cores.  --impl reference times the CPU oracle alone.
 
@@ -19,6 +25,7 @@ the slowest rank's time is used.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import math
@@ -207,21 +214,35 @@ def rows_for_budget(n_after, order, per_token_s, budget_s):
     return rows
 
 
+
 class Workload:
     """One decode step of a synthetic workload on the device.  Subclasses
     set the byte / token accounting and implement step() (inputs resident),
     e2e_io() / e2e_compute() (public API from pinned host buffers) and
-    cpu_baseline()."""
+    cpu_baseline().  A workload whose steps differ (a walk of `cycle`
+    steps: lengths that grow, INT8 blocks that age out) keeps the index of
+    its next step in `idx` and accounts bytes per step index."""
     kernel = "phs_split_decode_kernel"
     l2 = "inputs larger than L2 (K/V read per step >> 129 MB)"
     e2e_pipelined = True
+    graphable = True
+    cycle = 1
+    idx = 0
+    us_per_step = False
 
-    def kernel_seconds(self, evs):
-        return statistics.fmean(a.elapsed_time(b) for a, b in evs) / 1e3 if evs else None
+    def step_bytes(self, i):
+        return self.bytes_per_step
 
-    def new_events(self, steps):
-        return [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(self.kernel_launches_per_step)] for _ in range(steps)]
+    def step_tokens(self, i):
+        return self.tokens_per_step
+
+    def step_kernel_bytes(self, i):
+        return self.kernel_bytes
+
+    def advance(self):
+        i = self.idx
+        self.idx = (self.idx + 1) % self.cycle
+        return i
 
     # ---- end to end through the public API, from and to pinned host memory.
     # Subclasses give e2e_io(k) -> (inputs [(host, device)], outputs
@@ -288,8 +309,6 @@ class Workload:
 class PagedFullWorkload(Workload):
     """Paged Full-attention decode, batch 64 (one step = append + decode)."""
 
-    kernel_launches_per_step = 1
-
     def __init__(self, device, seed=2, batch=64, tokens_per_split=0):
         import paged_hybrid_sliding_gb300 as phs
         self.phs = phs
@@ -329,13 +348,14 @@ class PagedFullWorkload(Workload):
 
     def step(self, ev=None):
         phs = self.phs
+        self.advance()
         phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl)
         if ev is not None:
-            ev[0][0].record()
+            ev[0].record()
         phs.attn_decode_full_paged_split(self.q, self.pool, self.bt, self.sl, self.max_seq,
                                          self.ws, self.out, tokens_per_split=self.tps)
         if ev is not None:
-            ev[0][1].record()
+            ev[1].record()
         phs.attn_merge_splits(self.out, self.w.Hkv, self.sl, self.max_seq, self.ws,
                               tokens_per_split=self.tps)
 
@@ -348,7 +368,7 @@ class PagedFullWorkload(Workload):
         phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl, self.max_seq,
                                    out=self.out, tokens_per_split=self.tps, workspace=self.ws)
 
-    def cpu_baseline(self, budget_s=12.0):
+    def cpu_baseline(self, budget_s=8.0):
         """The oracle as it stands on a sample of requests of this step."""
         import oracle
         w = self.w
@@ -375,11 +395,12 @@ class PagedFullWorkload(Workload):
 
 class TinyHybridWorkload(Workload):
     """Batch 2, 4 q / 2 KV heads, D 64: one Full (paged) + one SWA (ring)
-    layer, append + attend through the hybrid-stack call.  Latency-bound."""
+    layer, append + attend through the hybrid-stack call.  Latency-bound:
+    replayed as a CUDA graph, the whole step timed."""
 
-    kernel_launches_per_step = 0
     l2 = "latency-bound case: ~0.2 MB per step, resident in L2"
     e2e_pipelined = False  # 13 us steps: staging costs more than it hides
+    us_per_step = True
 
     def __init__(self, device, seed=1, fused=True):
         import paged_hybrid_sliding_gb300 as phs
@@ -422,7 +443,9 @@ class TinyHybridWorkload(Workload):
         tok_bytes = Hkv * D * 2 * 2
         self.bytes_per_step = (full_tok + swa_tok) * tok_bytes + 2 * 2 * B * Hq * D * 2 + \
             2 * 2 * B * Hkv * D * 2
-        self.kernel_bytes = None
+        self.kernel_bytes = self.bytes_per_step
+        self.kernel = ("the whole step (" + ("Full split + SWA launch, append fused"
+                                             if fused else "2 appends, SWA, split") + ")")
         # fused: Full split (append fused, one split: no merge) + SWA decode;
         # else 2 appends, SWA decode, split
         self.launches_per_step = 2 if fused else 4
@@ -432,14 +455,19 @@ class TinyHybridWorkload(Workload):
         self.d2h_bytes = self.outp.nbytes
 
     def step(self, ev=None):
+        self.advance()
+        if ev is not None:
+            ev[0].record()
         if self.fused:
             self.phs.attn_decode_hybrid_stack_fused(self.layers, self.w.Hq, self.sl, self.max_seq,
                                                     block_table=self.bt, ring_pos=self.rp,
                                                     workspace=self.ws)
-            return
-        self.phs.attn_decode_hybrid_stack(self.layers, self.w.Hq, self.sl, self.max_seq,
-                                          block_table=self.bt, ring_pos=self.rp,
-                                          workspace=self.ws)
+        else:
+            self.phs.attn_decode_hybrid_stack(self.layers, self.w.Hq, self.sl, self.max_seq,
+                                              block_table=self.bt, ring_pos=self.rp,
+                                              workspace=self.ws)
+        if ev is not None:
+            ev[1].record()
 
     def e2e_io(self, k):
         return [(self.inp.host, self.inp.dev)], [(self.outp.dev, self.outp.host)]
@@ -471,12 +499,10 @@ class HybridStackWorkload(Workload):
     """70 layers (Full iff layer % 7 == 6: 10 Full, 60 SWA W=128), batch 256,
     32 q / 8 KV heads, D 128, lengths log-uniform in [4K, 128K]; one step =
     append into every layer + attend every layer, one hybrid-stack call.
-    Ten distinct 37.6 GB Full pools do not fit one GPU: `distinct` pools are
+    Ten distinct 44 GB Full pools do not fit one GPU: `distinct` pools are
     allocated and the Full layers use them round-robin (each layer still
     streams its whole pool, far above L2, so no layer reads another's data
     from cache)."""
-
-    kernel_launches_per_step = 0
 
     def __init__(self, device, seed=3, distinct=4, batch=256, swa_only=False, fused=True):
         import paged_hybrid_sliding_gb300 as phs
@@ -546,12 +572,19 @@ class HybridStackWorkload(Workload):
         self.full_layer_bytes = full_tok * tok_bytes + B * Hq * D * 2 + \
             int(synth.pages_needed(w.n_after).sum()) * 4
         self.swa_bytes = nswa * (swa_tok * tok_bytes + B * Hq * D * 2)
-        self.kernel_bytes = self.full_layer_bytes if nfull else self.swa_bytes
+        self.nfull, self.nswa = nfull, nswa
+        # the step is the two launches of the fused call (the Full layers'
+        # split launch and the SWA launch that also runs their merges), timed
+        # together by events around the call; separately timed parts are
+        # reported as a breakdown
+        self.kernel_bytes = self.bytes_per_step
         if not nfull:
             self.kernel = "phs_swa_decode_kernel"
         elif fused:
-            self.kernel = ("phs_stack_full_kernel + merges (all Full layers in one launch, "
-                           "append fused; per-layer average)")
+            self.kernel = ("phs_stack_full_kernel + phs_swa_decode_kernel (the fused step's two "
+                           "launches: all Full layers, then all SWA layers and the Full merges)")
+        else:
+            self.kernel = "the whole unfused step (appends, SWA launch, split + merge per layer)"
         if fused:
             # Full split launch + SWA launch (which also runs the Full merges)
             self.launches_per_step = (1 if nfull else 0) + (1 if nswa else 0) + \
@@ -569,127 +602,130 @@ class HybridStackWorkload(Workload):
         self.h2d_bytes = self.inp.nbytes
         self.d2h_bytes = self.outp.nbytes
 
-    def step(self, ev=None):
+    def _call(self, layers, **kw):
         if self.fused:
-            self.phs.attn_decode_hybrid_stack_fused(self.layers, self.w.Hq, self.sl, self.max_seq,
+            self.phs.attn_decode_hybrid_stack_fused(layers, self.w.Hq, self.sl, self.max_seq,
                                                     block_table=self.bt, ring_pos=self.rp,
-                                                    workspace=self.ws)
-            return
-        self.phs.attn_decode_hybrid_stack(self.layers, self.w.Hq, self.sl, self.max_seq,
-                                          block_table=self.bt, ring_pos=self.rp,
-                                          workspace=self.ws)
+                                                    workspace=self.ws, **kw)
+        else:
+            self.phs.attn_decode_hybrid_stack(layers, self.w.Hq, self.sl, self.max_seq,
+                                              block_table=self.bt, ring_pos=self.rp,
+                                              workspace=self.ws, **kw)
+
+    def step(self, ev=None):
+        self.advance()
+        if ev is not None:
+            ev[0].record()
+        self._call(self.layers)
+        if ev is not None:
+            ev[1].record()
 
     def e2e_io(self, k):
         return [(self.inp.host, self.inp.dev)], [(self.outp.dev, self.outp.host)]
 
     def e2e_compute(self, k):
-        self.step()
+        self._call(self.layers)
 
-    def kernel_times(self, reps=3):
-        """Average launch time of the split kernel on the Full layers and of
-        the SWA kernel on all SWA layers (separate timed loops)."""
-        phs = self.phs
-        w = self.w
-        full = [L for L in self.layers if L.paged is not None]
-        if not full:
-            return None, self._swa_time(reps)
-        if self.fused:
-            # the step's Full part: one multi-layer split launch (append fused)
-            # plus its merges (a merge launch, as the layers run without the
-            # SWA launch here); per-layer average reported
-            def run():
-                phs.attn_decode_hybrid_stack_fused(full, w.Hq, self.sl, self.max_seq,
-                                                   block_table=self.bt, workspace=self.ws)
-            run()
+    def breakdown(self, reps=3):
+        """The step's two parts timed in loops of their own (after the timed
+        region): the Full layers alone (their split launch, append fused, and
+        a merge launch) and the SWA layers alone (one launch, no append)."""
+        out = {}
+        peak = peaks()[0]
+
+        def timed(fn):
+            fn()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             for _ in range(reps):
-                run()
+                fn()
             b.record()
             torch.cuda.synchronize()
-            return a.elapsed_time(b) / 1e3 / reps / len(full), self._swa_time(reps)
-        ts = []
-        for _ in range(reps):
-            for L in full:
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                phs.attn_decode_full_paged_split(L.q, L.paged, self.bt, self.sl, self.max_seq,
-                                                 self.ws, L.out)
-                b.record()
-                ts.append((a, b))
-        torch.cuda.synchronize()
-        split_s = statistics.fmean(a.elapsed_time(b) for a, b in ts) / 1e3
-        return split_s, self._swa_time(reps)
+            return a.elapsed_time(b) / 1e3 / reps
 
-    def _swa_time(self, reps):
-        w = self.w
+        full = [L for L in self.layers if L.paged is not None]
         swa = [self.phs.Layer(q=L.q, out=L.out, ring=L.ring) for L in self.layers
                if L.ring is not None]
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        self.phs.attn_decode_hybrid_stack(swa, w.Hq, self.sl, self.max_seq, ring_pos=self.rp,
-                                          do_append=False)
-        a.record()
-        for _ in range(reps):
-            self.phs.attn_decode_hybrid_stack(swa, w.Hq, self.sl, self.max_seq, ring_pos=self.rp,
-                                              do_append=False)
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / 1e3 / reps
+        if full and self.fused:
+            t = timed(lambda: self._call(full))
+            b = self.nfull * self.full_layer_bytes
+            out["phs_stack_full_kernel + merge (10 Full layers)"] = {
+                "bytes": b, "ms": round(t * 1e3, 4), "achieved_gbs": round(b / t / 1e9, 1),
+                "frac": round(b / t / 1e9 / peak, 4)}
+        if swa:
+            t = timed(lambda: self.phs.attn_decode_hybrid_stack(
+                swa, self.w.Hq, self.sl, self.max_seq, ring_pos=self.rp, do_append=False))
+            out["phs_swa_decode_kernel (60 SWA layers)"] = {
+                "bytes": self.swa_bytes, "ms": round(t * 1e3, 4),
+                "achieved_gbs": round(self.swa_bytes / t / 1e9, 1),
+                "frac": round(self.swa_bytes / t / 1e9 / peak, 4)}
+        return out
 
     def cpu_baseline(self, budget_s=12.0):
+        """The oracle on a sample of the step: requests of one Full layer and
+        the same requests in six SWA layers (the stack's 1 : 6 mix)."""
         import oracle
         w = self.w
-        if self.swa_only:
-            return self._cpu_baseline_swa()
-        L = next(L for L in self.layers if L.paged is not None)
-        order = [int(b) for b in np.argsort(w.n_after)]
-        hk, bt = host_pages(L.paged.k, w.block_table, order[:1], w.n_after)
-        hv, _ = host_pages(L.paged.v, w.block_table, order[:1], w.n_after)
-        t0 = time.perf_counter()
-        oracle.decode_full_paged(synth.bits(L.q)[order[:1]], hk, hv, bt, w.n_after[order[:1]],
-                                 w.softmax_scale)
-        per_tok = (time.perf_counter() - t0) / float(w.n_after[order[0]])
-        rows = rows_for_budget(w.n_after, order, per_tok, budget_s)
-        hk, bt = host_pages(L.paged.k, w.block_table, rows, w.n_after)
-        hv, _ = host_pages(L.paged.v, w.block_table, rows, w.n_after)
-        t0 = time.perf_counter()
-        oracle.decode_full_paged(synth.bits(L.q)[rows], hk, hv, bt, w.n_after[rows],
-                                 w.softmax_scale)
-        t = time.perf_counter() - t0
-        toks = int(w.n_after[rows].sum())
+        full = [L for L in self.layers if L.paged is not None]
+        swa = [L for L in self.layers if L.ring is not None][:6]
+        order = [int(b) for b in np.random.default_rng(11).permutation(w.B)]
+
+        def run(rows):
+            t, fb, sb = 0.0, 0, 0
+            if full:
+                L = full[0]
+                hk, bt = host_pages(L.paged.k, w.block_table, rows, w.n_after)
+                hv, _ = host_pages(L.paged.v, w.block_table, rows, w.n_after)
+                qh = synth.bits(L.q)[rows]
+                t0 = time.perf_counter()
+                oracle.decode_full_paged(qh, hk, hv, bt, w.n_after[rows], w.softmax_scale)
+                t += time.perf_counter() - t0
+                fb = int(w.n_after[rows].sum())
+            for L in swa:
+                kr, vr = synth.bits(L.ring.k[rows]), synth.bits(L.ring.v[rows])
+                qh = synth.bits(L.q)[rows]
+                t0 = time.perf_counter()
+                oracle.decode_swa_ring(qh, kr, vr, None, w.ring_pos[rows], w.n_after[rows],
+                                       w.softmax_scale)
+                t += time.perf_counter() - t0
+                sb += int(np.minimum(w.n_after[rows], w.W).sum())
+            return t, fb, sb
+
+        t1, fb1, sb1 = run(order[:1])
+        per_tok = t1 / max(1, fb1 + sb1)
+        est = [float(w.n_after[b]) + len(swa) * min(float(w.n_after[b]), w.W) for b in order]
+        rows, acc = [], 0.0
+        for b, e in zip(order, est):
+            if rows and acc + per_tok * e > budget_s:
+                break
+            rows.append(b)
+            acc += per_tok * e
+        t, fb, sb = run(rows)
+        toks = fb + sb
         return {"value": toks * w.Hkv * w.D * 4 / t / 1e9, "unit": "GB/s",
                 "tokens_per_s": toks / t, "cores": oracle.max_threads(), "kind": "oracle",
-                "sample": f"{len(rows)} of {w.B} requests of one Full layer ({toks} tokens), "
-                          f"fp64 oracle, {t:.2f} s"}
-
-
-    def _cpu_baseline_swa(self):
-        import oracle
-        w = self.w
-        L = next(L for L in self.layers if L.ring is not None)
-        kr, vr, q = synth.bits(L.ring.k), synth.bits(L.ring.v), synth.bits(L.q)
-        t0 = time.perf_counter()
-        oracle.decode_swa_ring(q, kr, vr, None, w.ring_pos, w.n_after, w.softmax_scale)
-        t = time.perf_counter() - t0
-        toks = int(np.minimum(w.n_after, w.W).sum())
-        return {"value": toks * w.Hkv * w.D * 4 / t / 1e9, "unit": "GB/s",
-                "tokens_per_s": toks / t, "cores": oracle.max_threads(), "kind": "oracle",
-                "sample": f"one SWA layer, all {w.B} requests ({toks} tokens), fp64 oracle, "
+                "sample": f"{len(rows)} of {w.B} requests in {1 if full else 0} Full and "
+                          f"{len(swa)} SWA layers ({fb} + {sb} attended tokens), fp64 oracle, "
                           f"{t:.2f} s"}
 
 
 class Int8Workload(Workload):
-    """Batch 32, 65,536 cached tokens: tokens [0, 64512) as INT8 (one fp32
+    """Batch 32, 65,536 cached tokens: tokens [0, qlen) as INT8 (one fp32
     absmax/127 scale per 32 tokens per KV head, quantised on the GPU at set
-    up), the last 1025 in bf16; K/V N(0,1) with 1% N(0, 8^2) outliers.  One
-    step = append into the bf16 tail + split-KV decode + merge."""
+    up), the rest bf16; K/V N(0,1) with 1% N(0, 8^2) outliers.  One step =
+    append into the bf16 tail + (when a tail reaches 1056 tokens) the
+    quantisation of its oldest bf16 block + split-KV decode + merge.  The
+    steps walk 64 decode positions (lengths 65,537 .. 65,600, each request's
+    INT8 length growing by 32 at steps 31 and 63), then start over."""
 
-    kernel_launches_per_step = 1
+    cycle = 64
+    hot = 1024
+    graphable = False  # each step decodes other lengths
 
     def __init__(self, device, seed=4, batch=32, tokens_per_split=0):
         import paged_hybrid_sliding_gb300 as phs
         self.phs = phs
-        self.w = w = synth.int8_block32(seed=seed, B=batch)
+        self.w = w = synth.int8_block32(seed=seed, B=batch, steps=self.cycle)
         B, Hq, Hkv, D = w.B, w.Hq, w.Hkv, w.D
         self.name = f"int8_block32_b{B}_n65536_hot1024_hq32_hkv8_d128"
         g = seed * 100
@@ -698,11 +734,11 @@ class Int8Workload(Workload):
         self.v = synth.normal_bf16((w.num_pages, Hkv, 16, D), g + 2, device=device,
                                    outlier_p=0.01)
         self.pool = phs.PagedPool(self.k, self.v)
-        self.qlen = w.extra["qlen"]
+        self.qlen0 = w.extra["qlen"]
         self.qt = torch.from_numpy(w.extra["qtable"]).to(device)
         self.i8 = phs.Int8Pool.empty(w.extra["num_qpages"], Hkv, D, device=device)
         self.bt = torch.from_numpy(w.block_table).to(device)
-        nqb = (self.qlen // 32).astype(np.int32)
+        nqb = (self.qlen0 // 32).astype(np.int32)
         zeros = torch.zeros(B, dtype=torch.int32, device=device)
         nqb_d = torch.from_numpy(nqb).to(device)
 
@@ -720,99 +756,141 @@ class Int8Workload(Workload):
         torch.cuda.synchronize()
         q_s = a.elapsed_time(b) / 1e3 / reps
         # algorithmic bytes: read the bf16 group, write codes + one scale
-        qbytes = int(nqb.sum()) * Hkv * 2 * (32 * D * 2 + 32 * D + 4)
+        self.group_bytes = Hkv * 2 * (32 * D * 2 + 32 * D + 4)
+        qbytes = int(nqb.sum()) * self.group_bytes
         self.quant_setup = {"kernel": "phs_quant_kernel", "ms": round(q_s * 1e3, 3),
                             "GB/s": round(qbytes / q_s / 1e9, 1), "bytes": qbytes}
         self.q = synth.normal_bf16((B, Hq, D), g + 3, device=device)
         self.kn = synth.normal_bf16((B, Hkv, D), g + 4, device=device)
         self.vn = synth.normal_bf16((B, Hkv, D), g + 5, device=device)
-        self.sl = torch.from_numpy(w.n_after).to(device)
-        self.ql = torch.from_numpy(self.qlen).to(device)
-        self.max_seq = int(w.n_after.max())
+        # the walk: lengths after each step's append, the INT8 length each
+        # step decodes with, and the blocks that age out at that step
+        n0 = w.n_after.astype(np.int64)
+        self.n_walk = [(n0 + k).astype(np.int32) for k in range(self.cycle)]
+        self.q_walk = [(((n - self.hot) // 32) * 32).astype(np.int32) for n in self.n_walk]
+        assert np.array_equal(self.q_walk[0], self.qlen0)
+        self.sls = [torch.from_numpy(n).to(device) for n in self.n_walk]
+        self.qls = [torch.from_numpy(q).to(device) for q in self.q_walk]
+        self.ages = {}
+        for k in range(1, self.cycle):
+            grown = (self.q_walk[k] > self.q_walk[k - 1]).astype(np.int32)
+            if grown.any():
+                first = (self.q_walk[k - 1] // 32).astype(np.int32)
+                self.ages[k] = (torch.from_numpy(first).to(device),
+                                torch.from_numpy(grown).to(device), int(grown.sum()))
+        self.max_seq = int(self.n_walk[-1].max())
         self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
         self.tps = phs.decode_tokens_per_split(B, Hkv, self.max_seq, tokens_per_split)
         self.ws = torch.empty(phs.decode_workspace_bytes(B, Hq, Hkv, D, self.max_seq, self.tps,
                                                          has_int8=True),
                               dtype=torch.uint8, device=device)
-        i8_tok = int(self.qlen.sum())
-        bf_tok = int((w.n_after - self.qlen).sum())
-        self.tokens_per_step = i8_tok + bf_tok
-        codes = i8_tok * Hkv * D * 2
-        scales = i8_tok // 32 * Hkv * 4 * 2
-        tail = bf_tok * Hkv * D * 2 * 2
-        tables = int(synth.pages_needed(w.n_after - self.qlen).sum()) * 4 + i8_tok // 32 * 4
-        self.kernel_bytes = codes + scales + tail + B * Hq * D * 2 + tables
-        self.bytes_per_step = self.kernel_bytes + B * Hq * D * 2 + 2 * B * Hkv * D * 2 * 2
-        self.launches_per_step = 3
-        self.extra = {"batch": B, "int8_tokens": i8_tok, "bf16_tokens": bf_tok,
-                      "codes_bytes": codes, "scale_bytes": scales, "bf16_tail_bytes": tail,
+        self.tokens_per_step = int(self.n_walk[0].sum())
+        self.kernel_bytes = self.step_kernel_bytes(0)
+        self.bytes_per_step = self.step_bytes(0)
+        self.launches_per_step = 3  # + one quantiser launch at steps 31 and 63
+        i8_tok = int(self.qlen0.sum())
+        bf_tok = int((w.n_after - self.qlen0).sum())
+        self.extra = {"batch": B, "int8_tokens_step0": i8_tok, "bf16_tokens_step0": bf_tok,
+                      "walk": f"{self.cycle} steps, lengths {int(n0.min())}..{self.max_seq}; "
+                              f"one 32-token block per request quantised at steps "
+                              f"{sorted(self.ages)} of the walk",
                       "tokens_per_split": self.tps, "quantiser_setup": self.quant_setup}
-        self.inp = Arena(device, [self.q, self.kn, self.vn, self.sl])
-        self.q, self.kn, self.vn, self.sl = self.inp.views
+        self.inp = Arena(device, [self.q, self.kn, self.vn])
+        self.q, self.kn, self.vn = self.inp.views
+        self.h_sls = [pinned(s) for s in self.sls]
+        self.h_qls = [pinned(s) for s in self.qls]
+        self.sl_in = torch.empty_like(self.sls[0])
+        self.ql_in = torch.empty_like(self.qls[0])
         self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
-        self.h2d_bytes = self.inp.nbytes
+        self.h2d_bytes = self.inp.nbytes + nbytes(self.h_sls[0]) + nbytes(self.h_qls[0])
         self.d2h_bytes = nbytes(self.h_out)
 
-    def _decode(self, split_only=False):
-        phs = self.phs
-        if split_only:
-            phs.attn_decode_full_paged_split(self.q, self.pool, self.bt, self.sl, self.max_seq,
-                                             self.ws, self.out, int8=self.i8, qtable=self.qt,
-                                             qlens=self.ql, tokens_per_split=self.tps)
-        else:
-            phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl, self.max_seq,
-                                       int8=self.i8, qtable=self.qt, qlens=self.ql,
-                                       tokens_per_split=self.tps, out=self.out,
-                                       workspace=self.ws)
+    def step_tokens(self, i):
+        return int(self.n_walk[i % self.cycle].sum())
+
+    def step_kernel_bytes(self, i):
+        w = self.w
+        n, ql = self.n_walk[i % self.cycle].astype(np.int64), self.q_walk[i % self.cycle]
+        i8_tok, bf_tok = int(ql.sum()), int((n - ql).sum())
+        codes = i8_tok * w.Hkv * w.D * 2
+        scales = i8_tok // 32 * w.Hkv * 4 * 2
+        tail = bf_tok * w.Hkv * w.D * 2 * 2
+        tables = int(synth.pages_needed(n - ql).sum()) * 4 + i8_tok // 32 * 4
+        return codes + scales + tail + w.B * w.Hq * w.D * 2 + tables
+
+    def step_bytes(self, i):
+        w = self.w
+        k = i % self.cycle
+        aged = self.ages[k][2] if k in self.ages else 0
+        return (self.step_kernel_bytes(i) + w.B * w.Hq * w.D * 2 + 2 * w.B * w.Hkv * w.D * 2 * 2
+                + aged * self.group_bytes)
+
+    def _age(self, k):
+        if k in self.ages:
+            first, num, _ = self.ages[k]
+            self.phs.kv_quant_int8_block32(self.pool, self.bt, self.i8, self.qt, first, num, 1)
 
     def step(self, ev=None):
-        self.phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl)
+        k = self.advance()
+        phs = self.phs
+        sl, ql = self.sls[k], self.qls[k]
+        phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, sl)
+        self._age(k)
         if ev is not None:
-            ev[0][0].record()
-        self._decode(split_only=True)
+            ev[0].record()
+        phs.attn_decode_full_paged_split(self.q, self.pool, self.bt, sl, self.max_seq,
+                                         self.ws, self.out, int8=self.i8, qtable=self.qt,
+                                         qlens=ql, tokens_per_split=self.tps)
         if ev is not None:
-            ev[0][1].record()
-        self.phs.attn_merge_splits(self.out, self.w.Hkv, self.sl, self.max_seq, self.ws,
-                                   qlens=self.ql, has_int8=True, tokens_per_split=self.tps)
+            ev[1].record()
+        phs.attn_merge_splits(self.out, self.w.Hkv, sl, self.max_seq, self.ws, qlens=ql,
+                              has_int8=True, tokens_per_split=self.tps)
 
     def e2e_io(self, k):
-        return [(self.inp.host, self.inp.dev)], [(self.out, self.h_out)]
+        c = k % self.cycle
+        return ([(self.inp.host, self.inp.dev), (self.h_sls[c], self.sl_in),
+                 (self.h_qls[c], self.ql_in)], [(self.out, self.h_out)])
 
     def e2e_compute(self, k):
-        self.phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl)
-        self._decode()
+        phs = self.phs
+        phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl_in)
+        self._age(k % self.cycle)
+        phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl_in, self.max_seq,
+                                   int8=self.i8, qtable=self.qt, qlens=self.ql_in,
+                                   tokens_per_split=self.tps, out=self.out, workspace=self.ws)
 
     def cpu_baseline(self):
         import oracle
         w = self.w
         rows = [0]
-        hk, bt = host_pages(self.k, w.block_table, rows, w.n_after)
-        hv, _ = host_pages(self.v, w.block_table, rows, w.n_after)
-        nq = int(self.qlen[0] // 32)
+        n = self.n_walk[0]
+        hk, bt = host_pages(self.k, w.block_table, rows, n)
+        hv, _ = host_pages(self.v, w.block_table, rows, n)
+        nq = int(self.qlen0[0] // 32)
         ids = self.qt[0, :nq].long()
         i8 = dict(k_codes=self.i8.k.index_select(0, ids).cpu().numpy(),
                   v_codes=self.i8.v.index_select(0, ids).cpu().numpy(),
                   k_scale=self.i8.k_scale.index_select(0, ids).cpu().numpy(),
                   v_scale=self.i8.v_scale.index_select(0, ids).cpu().numpy(),
-                  qtable=np.arange(nq, dtype=np.int32)[None], qlens=self.qlen[rows])
+                  qtable=np.arange(nq, dtype=np.int32)[None], qlens=self.qlen0[rows])
         t0 = time.perf_counter()
-        oracle.decode_full_paged(synth.bits(self.q)[rows], hk, hv, bt, w.n_after[rows],
+        oracle.decode_full_paged(synth.bits(self.q)[rows], hk, hv, bt, n[rows],
                                  w.softmax_scale, int8=i8)
         t = time.perf_counter() - t0
-        b = self.kernel_bytes / w.B
-        return {"value": b / t / 1e9, "unit": "GB/s", "tokens_per_s": float(w.n_after[0]) / t,
+        b = self.step_kernel_bytes(0) / w.B
+        return {"value": b / t / 1e9, "unit": "GB/s", "tokens_per_s": float(n[0]) / t,
                 "cores": oracle.max_threads(), "kind": "oracle",
-                "sample": f"1 of {w.B} requests ({int(w.n_after[0])} tokens, INT8 + bf16 tail),"
+                "sample": f"1 of {w.B} requests ({int(n[0])} tokens, INT8 + bf16 tail),"
                           f" fp64 oracle, {t:.2f} s"}
 
 
 class SharedPrefixWorkload(Workload):
     """64 requests sharing one 250,000-token prefix (15,625 pages, refcount
     64) + a unique 512-token suffix each; 128 decode steps with append.  One
-    bench step = one decode step; the timed loop walks the 128 steps."""
+    bench step = one decode step; the steps walk the 128 positions."""
 
-    kernel_launches_per_step = 1
     l2 = "logical K/V bytes per step 65.7 GB >> L2; the shared prefix is reused through L2"
+    graphable = False  # each step decodes other lengths
 
     def __init__(self, device, seed=5, prefix_kernel=True, prefix_len=250_000):
         import paged_hybrid_sliding_gb300 as phs
@@ -826,41 +904,38 @@ class SharedPrefixWorkload(Workload):
         self.pool = phs.PagedPool(self.k, self.v)
         self.bt = torch.from_numpy(w.block_table).to(device)
         self.rc = torch.from_numpy(w.extra["refcount"]).to(device)
-        self.nsteps = w.extra["steps"]
+        self.cycle = w.extra["steps"]
         self.sls = [torch.from_numpy((w.n_pre + 1 + k).astype(np.int32)).to(device)
-                    for k in range(self.nsteps)]
+                    for k in range(self.cycle)]
         self.q = synth.normal_bf16((B, Hq, D), g + 3, device=device)
         self.kn = synth.normal_bf16((B, Hkv, D), g + 4, device=device)
         self.vn = synth.normal_bf16((B, Hkv, D), g + 5, device=device)
-        self.max_seq = int(w.n_pre.max()) + self.nsteps
+        self.max_seq = int(w.n_pre.max()) + self.cycle
         self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
         self.tps = phs.decode_tokens_per_split(B, Hkv, self.max_seq)
         self.ws = torch.empty(phs.decode_workspace_bytes(B, Hq, Hkv, D, self.max_seq, self.tps),
                               dtype=torch.uint8, device=device)
-        self.k_idx = 0
         # tensor-core pass over the shared prefix (whole 64-token tiles)
         self.prefix_kernel = prefix_kernel
-        self.shared_len = (w.extra["prefix_pages"] * 16 // 64) * 64
+        self.npref = w.extra["prefix_pages"]
+        self.shared_len = (self.npref * 16 // 64) * 64
         if prefix_kernel:
             self.ws = torch.empty(phs.shared_prefix_workspace_bytes(B, Hq, Hkv, D, self.max_seq,
                                                                     self.shared_len),
                                   dtype=torch.uint8, device=device)
             self.kernel = "phs_attn_decode_shared_prefix (prefix tcgen05 + suffix split + merge)"
             self.l2 = "prefix read once per KV head for all 64 requests (tensor-core pass)"
-        mean_n = float(w.n_pre.mean()) + (self.nsteps + 1) / 2
-        tok_bytes = Hkv * D * 2 * 2
-        self.tokens_per_step = int(round(B * mean_n))
-        self.bytes_per_step = self.tokens_per_step * tok_bytes + 2 * B * Hq * D * 2 + \
-            2 * B * Hkv * D * 2 * 2
-        self.kernel_bytes = self.tokens_per_step * tok_bytes + B * Hq * D * 2
-        npref = w.extra["prefix_pages"]
-        unique_tok = npref * 16 + B * (float(w.n_pre.mean()) - npref * 16 + (self.nsteps + 1) / 2)
-        self.unique_bytes = int(unique_tok * tok_bytes)
+        self.tok_bytes = Hkv * D * 2 * 2
+        self.tokens_per_step = self.step_tokens(0)
+        self.bytes_per_step = self.step_bytes(0)
+        self.kernel_bytes = self.step_kernel_bytes(0)
         self.launches_per_step = 4 if prefix_kernel else 3
         # tensor work of the prefix pass: QK and PV over B*G rows x D per token
         self.prefix_flops = 4 * B * Hq * D * self.shared_len
-        self.extra = {"batch": B, "logical_bytes_per_step": self.bytes_per_step,
-                      "unique_kv_bytes_per_step": self.unique_bytes,
+        self.extra = {"batch": B, "logical_bytes_step0": self.bytes_per_step,
+                      "unique_kv_bytes_step0": self.step_unique_bytes(0),
+                      "walk": f"{self.cycle} decode steps (lengths {int(w.n_pre[0]) + 1}.."
+                              f"{self.max_seq})",
                       "tokens_per_split": self.tps, "shared_prefix_kernel": prefix_kernel,
                       "shared_len_tensor_pass": self.shared_len if prefix_kernel else 0}
         # q / k_new / v_new in one staged buffer; the step's lengths (a
@@ -873,28 +948,44 @@ class SharedPrefixWorkload(Workload):
         self.h2d_bytes = self.inp.nbytes + nbytes(self.h_sls[0])
         self.d2h_bytes = nbytes(self.h_out)
 
+    def step_tokens(self, i):
+        return int((self.w.n_pre + 1 + i % self.cycle).sum())
+
+    def step_unique_bytes(self, i):
+        w = self.w
+        own = int((w.n_pre + 1 + i % self.cycle - self.npref * 16).sum())
+        return (self.npref * 16 + own) * self.tok_bytes + w.B * w.Hq * w.D * 2
+
+    def step_kernel_bytes(self, i):
+        w = self.w
+        return self.step_tokens(i) * self.tok_bytes + w.B * w.Hq * w.D * 2
+
+    def step_bytes(self, i):
+        w = self.w
+        return (self.step_tokens(i) * self.tok_bytes + 2 * w.B * w.Hq * w.D * 2
+                + 2 * w.B * w.Hkv * w.D * 2 * 2)
+
     def step(self, ev=None):
         phs = self.phs
-        sl = self.sls[self.k_idx % self.nsteps]
-        self.k_idx += 1
+        sl = self.sls[self.advance()]
         phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, sl, page_refcount=self.rc)
         if ev is not None:
-            ev[0][0].record()
+            ev[0].record()
         if self.prefix_kernel:
             phs.attn_decode_shared_prefix(self.q, self.pool, self.bt, sl, self.max_seq,
                                           self.shared_len, out=self.out, workspace=self.ws)
             if ev is not None:
-                ev[0][1].record()
+                ev[1].record()
             return
         phs.attn_decode_full_paged_split(self.q, self.pool, self.bt, sl, self.max_seq, self.ws,
                                          self.out, tokens_per_split=self.tps)
         if ev is not None:
-            ev[0][1].record()
+            ev[1].record()
         phs.attn_merge_splits(self.out, self.w.Hkv, sl, self.max_seq, self.ws,
                               tokens_per_split=self.tps)
 
     def e2e_io(self, k):
-        return ([(self.inp.host, self.inp.dev), (self.h_sls[k % self.nsteps], self.sl_in)],
+        return ([(self.inp.host, self.inp.dev), (self.h_sls[k % self.cycle], self.sl_in)],
                 [(self.out, self.h_out)])
 
     def e2e_compute(self, k):
@@ -980,16 +1071,13 @@ def job_throughput(bytes_per_step, steps, world, t):
     return bytes_per_step * steps * world / t / 1e9
 
 
-def run_gpu(args, rank, world, local_rank):
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    import paged_hybrid_sliding_gb300 as phs
-    phs.lib()
-    wl = make_workload(args.config, device, args)
-    use_graph = args.graph if args.graph is not None else args.config == 1
-    if use_graph and isinstance(wl, SharedPrefixWorkload):
-        raise SystemExit("--graph: the shared-prefix steps change lengths every step")
-    for _ in range(args.warmup):
+def measure(wl, steps, warmup, world, device, use_graph, copy_gbs, with_cpu):
+    """Warm-up, then exactly `steps` steps timed with CUDA events between
+    barriers (max over ranks); the dominant kernel timed by events around
+    its launch on its stream on every `stride`-th step; then the same number
+    of steps end to end through the public API from pinned host buffers."""
+    warmup = max(3, warmup)
+    for _ in range(warmup):
         wl.step()
     torch.cuda.synchronize()
     graph = None
@@ -1001,188 +1089,260 @@ def run_gpu(args, rank, world, local_rank):
             wl.step()
         graph.replay()
         torch.cuda.synchronize()
-    # the dominant kernel is timed with CUDA events around its launch on every
-    # `stride`-th step of the timed loop: an event between two launches ends
-    # the programmatic overlap of the second with the first, so events on
-    # every step would slow the step they measure
-    stride = max(1, args.steps // 200)
-    evs = [] if graph is not None else wl.new_events((args.steps + stride - 1) // stride)
+    # an event between two launches ends the programmatic overlap of the
+    # second with the first, so the events go on every `stride`-th step only
+    stride = max(1, steps // 200)
+    evs = []
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    idx0 = wl.idx
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(device.index or 0) as clk:
         start.record()
-        for i in range(args.steps):
+        for i in range(steps):
+            pair = None
+            if i % stride == 0:
+                pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                evs.append((pair, (idx0 + i) % wl.cycle))
             if graph is not None:
+                if pair is not None:
+                    pair[0].record()
                 graph.replay()
+                if pair is not None:
+                    pair[1].record()
             else:
-                wl.step(evs[i // stride] if evs and i % stride == 0 else None)
+                wl.step(pair)
         stop.record()
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    t = start.elapsed_time(stop) / 1e3
-    flat = [p for e in evs for p in e]
-    kernel_s = wl.kernel_seconds(flat)
-    t = slowest_rank_time(t, world, device)
-    extra_kernels = {}
-    if isinstance(wl, HybridStackWorkload):
-        kernel_s, swa_s = wl.kernel_times()
-        if kernel_s is None:
-            kernel_s = swa_s
-        else:
-            extra_kernels["phs_swa_decode_kernel"] = {
-                "bytes_per_launch": wl.swa_bytes, "avg_launch_ms": round(swa_s * 1e3, 4),
-                "achieved_gbs": round(wl.swa_bytes / swa_s / 1e9, 1),
-                "frac": round(wl.swa_bytes / swa_s / 1e9 / peaks()[0], 4)}
+    t = slowest_rank_time(start.elapsed_time(stop) / 1e3, world, device)
+    step_ids = [(idx0 + i) % wl.cycle for i in range(steps)] if graph is None else [0] * steps
+    total_bytes = sum(wl.step_bytes(i) for i in step_ids)
+    total_tokens = sum(wl.step_tokens(i) for i in step_ids)
+    k_time = sum(a.elapsed_time(b) for (a, b), _ in evs) / 1e3
+    k_bytes = sum(wl.step_kernel_bytes(i) for _, i in evs)
+    breakdown = wl.breakdown() if hasattr(wl, "breakdown") else None
 
-    # end-to-end through the public API with host buffers (copies overlapped
-    # with compute, as a serving loop would)
+    # end to end through the public API with host buffers, the same number
+    # of steps as the timed loop (copies overlapped with compute, as a
+    # serving loop would)
     wl.e2e_run(3)
     torch.cuda.synchronize()
-    e2e_steps = max(3, args.steps // 4)
+    if world > 1:
+        torch.distributed.barrier()
     t0 = time.perf_counter()
-    wl.e2e_run(e2e_steps)
+    wl.e2e_run(steps)
     torch.cuda.synchronize()
-    t_e2e = time.perf_counter() - t0
-    copy_gbs = time_copy(device)
+    t_e2e = slowest_rank_time(time.perf_counter() - t0, world, device)
+    e2e_bytes = sum(wl.step_bytes(k % wl.cycle) for k in range(steps))
 
     peak, peak_kind = peaks()
-    ms = t / args.steps * 1e3
-    value = job_throughput(wl.bytes_per_step, args.steps, world, t)
+    ms = t / steps * 1e3
+    value = total_bytes * world / t / 1e9
     line = {
         "metric": METRIC,
         "value": round(value, 1),
         "unit": "GB/s",
         "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
+        "steps": steps,
+        "warmup": warmup,
         "ms_per_step": round(ms, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": wl.name, "kv_tokens_per_step": wl.tokens_per_step,
-                   "bytes_per_step": wl.bytes_per_step, "l2": wl.l2,
-                   "parallelism": "replicas" if world > 1 else "single", **wl.extra},
-        "tokens_per_s": round(wl.tokens_per_step * args.steps * world / t, 1),
+        "config": {"workload": wl.name, "kv_tokens_per_step": round(total_tokens / steps),
+                   "bytes_per_step": round(total_bytes / steps), "l2": wl.l2,
+                   "parallelism": "replicas" if world > 1 else "single", **wl.extra,
+                   "cuda_graph": graph is not None},
+        "tokens_per_s": round(total_tokens * world / t, 1),
         "pct_of_peak": round(100 * value / world / peak, 2),
         "copy_gbs": round(copy_gbs, 1),
         "pct_of_copy": round(100 * value / world / copy_gbs, 2),
-        "e2e": {"value": round(wl.bytes_per_step * e2e_steps * world / t_e2e / 1e9, 1),
+        "e2e": {"value": round(e2e_bytes * world / t_e2e / 1e9, 1),
                 "unit": "GB/s", "h2d_bytes_per_step": wl.h2d_bytes,
-                "d2h_bytes_per_step": wl.d2h_bytes, "steps": e2e_steps,
+                "d2h_bytes_per_step": wl.d2h_bytes, "steps": steps,
                 "copies": ("every step's inputs up and outputs down through pinned host "
                            "buffers, overlapped with the previous/next step's compute (two "
                            "copy streams, double-buffered device staging)"
                            if wl.e2e_pipelined else
                            "every step's inputs up and outputs down through pinned host "
                            "buffers, in line with the step")},
-        "gpu_launches": wl.launches_per_step * args.steps,
+        "gpu_launches": wl.launches_per_step * steps + sum(
+            1 for i in step_ids if i in getattr(wl, "ages", {})),
         "clocks": clk.summary(),
     }
-    line["config"]["cuda_graph"] = graph is not None
-    if isinstance(wl, TinyHybridWorkload):
+    if wl.us_per_step:
         line["us_per_step"] = round(ms * 1e3, 2)
-    if kernel_s is not None and wl.kernel_bytes:
-        achieved = wl.kernel_bytes / kernel_s / 1e9
+    if evs and k_time > 0:
+        achieved = k_bytes / k_time / 1e9
         line["roofline"] = {
             "bound": "hbm", "kernel": wl.kernel, "achieved": round(achieved, 1), "peak": peak,
             "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-            "bytes_per_launch": wl.kernel_bytes, "avg_launch_ms": round(kernel_s * 1e3, 4),
-            "traffic": recorded_traffic(wl.kernel, wl.name)}
-        if flat:
-            line["roofline"]["timed_launches"] = (
-                f"{len(flat)} launches inside the timed loop (CUDA events around the launch, "
-                f"on its stream, in 1 of every {stride} steps)")
+            "bytes_per_launch": round(k_bytes / len(evs)),
+            "avg_launch_ms": round(k_time / len(evs) * 1e3, 4),
+            "traffic": recorded_traffic(wl.kernel, wl.name),
+            "timed_launches": (f"{len(evs)} launches inside the timed loop (CUDA events around "
+                               f"the launch, on its stream, in 1 of every {stride} steps)")}
+        if wl.us_per_step:
+            line["roofline"]["note"] = ("latency-bound: the step moves ~0.2 MB, so its launch "
+                                        "latency, not HBM bandwidth, sets its time")
         if isinstance(wl, SharedPrefixWorkload):
             if wl.prefix_kernel:
                 # the decode call reads each prefix page once: its HBM bound is
                 # the unique bytes; its tensor work is the prefix contraction
-                uniq = wl.unique_bytes / kernel_s / 1e9
-                tflops = wl.prefix_flops / kernel_s / 1e12
+                ub = sum(wl.step_unique_bytes(i) for _, i in evs)
+                uniq = ub / k_time / 1e9
+                tflops = wl.prefix_flops * len(evs) / k_time / 1e12
                 line["roofline"].update({
                     "achieved": round(uniq, 1), "frac": round(uniq / peak, 4),
-                    "bytes_per_launch": wl.unique_bytes,
+                    "bytes_per_launch": round(ub / len(evs)),
                     "bytes_are": "unique K/V bytes (prefix read once per KV head)",
                     "logical_gbs": round(achieved, 1),
                     "tensor_tflops": round(tflops, 1),
                     "tensor_frac_of_bf16_peak": round(tflops / peak_tflops()[0], 4)})
             else:
+                ub = sum(wl.step_unique_bytes(i) for _, i in evs)
                 line["roofline"]["bytes_are"] = "logical (prefix pages reused through L2)"
-                line["roofline"]["unique_kv_gbs"] = round(wl.unique_bytes / kernel_s / 1e9, 1)
-    if extra_kernels:
-        line["other_kernels"] = extra_kernels
-    if rank == 0 and not args.no_cpu_baseline:
+                line["roofline"]["unique_kv_gbs"] = round(ub / k_time / 1e9, 1)
+    if breakdown:
+        line["breakdown"] = breakdown
+    if with_cpu:
         line["cpu_baseline"] = wl.cpu_baseline()
     return line
 
 
+SUITE = (3, 1, 2, 4, 5)          # headline first (the largest workload)
+SUITE_MIN_STEPS = {1: 2000, 2: 200, 3: 0, 4: 200, 5: 128}
+
+
+def run_gpu(args, rank, world, local_rank):
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    import paged_hybrid_sliding_gb300 as phs
+    phs.lib()
+    copy_gbs = time_copy(device)
+    configs = [args.config] if args.config else list(SUITE)
+    lines = {}
+    for c in configs:
+        wl = make_workload(c, device, args)
+        use_graph = args.graph if args.graph is not None else c == 1
+        if use_graph and not wl.graphable:
+            raise SystemExit("--graph: this workload's steps differ")
+        steps = args.steps if (args.config or c == SUITE[0]) else max(args.steps,
+                                                                      SUITE_MIN_STEPS[c])
+        lines[c] = measure(wl, steps, args.warmup, world, device, use_graph, copy_gbs,
+                           with_cpu=rank == 0 and not args.no_cpu_baseline)
+        del wl
+        gc.collect()
+        torch.cuda.empty_cache()
+    head = lines[configs[0]]
+    if len(configs) > 1:
+        head["configs"] = {str(c): lines[c] for c in configs[1:]}
+        head["suite"] = ("the headline is the 70-layer hybrid stack (the largest workload); "
+                         "the other workloads were measured in the same run, each line with "
+                         "its own steps, roofline, e2e and CPU-oracle baseline")
+    return head
+
+
 def run_reference(args, rank, budget_s=40.0):
-    """The CPU oracle as the reference arm: each step is the oracle over a
-    bounded sample of the same workload's requests, sized so that all
-    warm-up and timed steps together take about budget_s seconds."""
+    """The CPU oracle as the reference arm, on the headline workload (the
+    70-layer hybrid stack): each step is the oracle over a bounded sample
+    of the step -- a few requests, appended and attended in one Full layer
+    and in six SWA layers (the stack's 1 : 6 mix) -- sized so that all
+    warm-up and timed steps together take about budget_s seconds.  Inputs
+    are drawn on the host; nothing runs on the GPU."""
     if rank != 0:
         return None
     import oracle
-    w = synth.paged_full()
-    order = [int(b) for b in np.argsort(w.n_after)]  # shortest first
+    if args.config not in (None, 3):
+        raise SystemExit("--impl reference times the hybrid-stack workload (config 3)")
+    w = synth.hybrid_stack()
+    name = HYBRID_STACK_NAME
+    W, Hkv, D, Hq = w.W, w.Hkv, w.D, w.Hq
+    order = [int(b) for b in np.random.default_rng(11).permutation(w.B)]
+    n_swa = 6
 
     def inputs(rows):
         pages = [int(synth.pages_needed(w.n_after[b])) for b in rows]
         npg = sum(pages)
-        kp = synth.bits(synth.normal_bf16((npg, w.Hkv, 16, w.D), 201))
-        vp = synth.bits(synth.normal_bf16((npg, w.Hkv, 16, w.D), 202))
-        q = synth.bits(synth.normal_bf16((len(rows), w.Hq, w.D), 203))
+        kp = synth.bits(synth.normal_bf16((npg, Hkv, 16, D), 201))
+        vp = synth.bits(synth.normal_bf16((npg, Hkv, 16, D), 202))
         bt = np.full((len(rows), max(pages)), -1, np.int32)
         o = 0
         for i, p in enumerate(pages):
             bt[i, :p] = np.arange(o, o + p)
             o += p
-        return q, kp, vp, bt, w.n_after[rows]
+        nr = len(rows)
+        rings = [(synth.bits(synth.normal_bf16((nr, Hkv, W, D), 300 + 2 * l)),
+                  synth.bits(synth.normal_bf16((nr, Hkv, W, D), 301 + 2 * l)))
+                 for l in range(n_swa)]
+        qs = [synth.bits(synth.normal_bf16((nr, Hq, D), 400 + l)) for l in range(1 + n_swa)]
+        kn = synth.bits(synth.normal_bf16((nr, Hkv, D), 500))
+        vn = synth.bits(synth.normal_bf16((nr, Hkv, D), 501))
+        return kp, vp, bt, rings, qs, kn, vn, w.n_after[rows], w.ring_pos[rows]
 
-    q, kp, vp, bt, sl = inputs(order[:1])
+    def step(x):
+        kp, vp, bt, rings, qs, kn, vn, sl, rp = x
+        oracle.append_paged(kp, vp, kn, vn, bt, sl)
+        oracle.decode_full_paged(qs[0], kp, vp, bt, sl, w.softmax_scale)
+        for l, (kr, vr) in enumerate(rings):
+            oracle.append_ring(kr, vr, kn, vn, None, rp)
+            oracle.decode_swa_ring(qs[1 + l], kr, vr, None, rp, sl, w.softmax_scale)
+
+    def tokens(rows):
+        sl = w.n_after[rows]
+        return int(sl.sum()), int(np.minimum(sl, W).sum()) * n_swa
+
+    x = inputs(order[:1])
     t0 = time.perf_counter()
-    oracle.decode_full_paged(q, kp, vp, bt, sl, w.softmax_scale)
-    per_tok = (time.perf_counter() - t0) / float(sl.sum())
+    step(x)
+    f1, s1 = tokens(order[:1])
+    per_tok = (time.perf_counter() - t0) / (f1 + s1)
     per_step = budget_s / max(1, args.steps + args.warmup)
     rows, acc = [], 0.0
     for b in order:
-        if rows and acc + per_tok * float(w.n_after[b]) > per_step:
+        e = per_tok * (float(w.n_after[b]) + n_swa * min(float(w.n_after[b]), W))
+        if rows and acc + e > per_step:
             break
         rows.append(b)
-        acc += per_tok * float(w.n_after[b])
-    q, kp, vp, bt, sl = inputs(rows)
-    toks = int(sl.sum())
+        acc += e
+    x = inputs(rows)
+    ft, st = tokens(rows)
+    step_bytes = (ft + st) * Hkv * D * 4
     for _ in range(args.warmup):
-        oracle.decode_full_paged(q, kp, vp, bt, sl, w.softmax_scale)
+        step(x)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.decode_full_paged(q, kp, vp, bt, sl, w.softmax_scale)
+        step(x)
     t = time.perf_counter() - t0
-    gbs = toks * w.Hkv * w.D * 4 * args.steps / t / 1e9
-    sample = (f"{len(rows)} of {w.B} requests ({toks} tokens, all 32 query heads) of the "
-              f"batch-64 paged workload per step, fp64 oracle")
+    gbs = step_bytes * args.steps / t / 1e9
+    sample = (f"{len(rows)} of {w.B} requests of the 70-layer stack step, appended and attended "
+              f"in 1 Full and {n_swa} SWA layers ({ft} + {st} attended tokens, all {Hq} query "
+              f"heads), fp64 oracle")
     return {"impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "paged_full_b64_hq32_hkv8_d128_p16_seqU[1K,32K]",
-                       "sample": sample},
-            "tokens_per_s": round(toks * args.steps / t, 1),
+            "config": {"workload": name, "sample": sample},
+            "tokens_per_s": round((ft + st) * args.steps / t, 1),
             "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "kind": "oracle",
                              "cores": oracle.max_threads(), "sample": sample},
             "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
 
+HYBRID_STACK_NAME = "hybrid_stack_70l_10full_60swa_w128_b256_hq32_hkv8_d128_seqlogU[4K,128K]"
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="phs", choices=["phs", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
@@ -1205,11 +1365,12 @@ def main():
                     help="configs 1 and 3: separate append launches and one split + merge per "
                          "Full layer instead of the fused step (appends inside the attention "
                          "launches, all Full layers in one launch)")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
-                    help="1 tiny hybrid, 2 paged Full batch 64 (default), 3 70-layer hybrid "
-                         "stack, 4 INT8 block-32, 5 shared 250K prefix")
+    ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5],
+                    help="one workload alone: 1 tiny hybrid, 2 paged Full batch 64, 3 70-layer "
+                         "hybrid stack, 4 INT8 block-32, 5 shared 250K prefix (default: all, "
+                         "config 3 as the headline)")
     ap.add_argument("--distinct-pools", type=int, default=4,
-                    help="config 3: distinct 37.6 GB Full pools allocated (layers alias them)")
+                    help="config 3: distinct 44 GB Full pools allocated (layers alias them)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

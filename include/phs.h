@@ -47,7 +47,8 @@
  *     NULL: a device int32 the caller zeroes; the first error code written
  *     wins.  The offending item is skipped; nothing traps.
  *   - Supported shapes: page_size 16, head_dim 64 or 128, Hq a multiple of Hkv
- *     with group size Hq/Hkv <= 16, window a multiple of 16 (<= 4096).
+ *     with group size Hq/Hkv <= 16, window a multiple of 16 (<= 4096),
+ *     Hkv * head_dim <= 8192 (Hkv <= 64 at head_dim 128).
  *     Anything else returns PHS_EUNSUPPORTED.
  */
 #ifndef PHS_H_
@@ -244,7 +245,9 @@ int phs_attn_merge_splits(int32_t batch, int32_t num_q_heads, int32_t num_kv_hea
  * PHS_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU which loads the library
  * holds until the process exits.  The library's first call of this entry
  * point on a device looks up the array's device address (no allocation);
- * make that first call before any stream capture.  All calls share the one
+ * make that first call before any stream capture.  The address is cached
+ * per CUDA context: after a device reset the first call in the new context
+ * looks it up again (make that call outside a capture too).  All calls share the one
  * array and keep no state in it between calls, so calls that overlap on
  * the GPU (on different streams, or from several threads) race: serialise
  * them.  When tokens_per_split is 0 the library picks the split length as
@@ -271,16 +274,20 @@ int phs_attn_decode_full_paged_noalloc(const void *q, int32_t num_q_heads,
  * hitting a cached prefix share its physical blocks; a 250,000-token shared
  * prefix).  Computes exactly what phs_attn_decode_full_paged computes, for
  * a batch whose block tables all begin with the same shared_len / 16 page
- * ids (the caller guarantees it; row 0 of the table is read for them):
+ * ids (row 0 of the table is read for them):
  *   - tokens [0, shared_len) of every request are attended in one pass over
  *     the prefix per KV head, with the B x G query rows of that head as one
  *     dense tile (tcgen05.mma), so the prefix is read from HBM once;
  *   - tokens [shared_len, n_b) by the split-KV kernel;
  *   - a merge combines both by log-sum-exp.
  * Limits: head_dim 128, batch x (Hq/Hkv) <= 256, shared_len a positive
- * multiple of 64 with seq_lens[b] >= shared_len (else PHS_EUNSUPPORTED /
+ * multiple of 64 with max_seq_len >= shared_len (else PHS_EUNSUPPORTED /
  * PHS_EINVAL).  workspace: phs_shared_prefix_workspace_bytes(...) bytes,
  * 256-byte aligned.
+ * Checked on the device: a request whose first shared_len / 16 page ids
+ * differ from row 0's, or whose seq_lens[b] < shared_len, records
+ * PHS_ESHAPE in *dev_status and gets an all-zero output row; the other
+ * requests are unaffected.
  * ---------------------------------------------------------------------- */
 size_t phs_shared_prefix_workspace_bytes(int32_t batch, int32_t num_q_heads,
                                          int32_t num_kv_heads, int32_t head_dim,
@@ -318,6 +325,12 @@ int phs_attn_decode_swa_ring(const void *q, int32_t num_q_heads, const phs_ring_
  * launch plus one merge launch when a request has several splits, all
  * reusing `workspace` (phs_hybrid_stack_workspace_bytes).  Layers are independent: the step
  * runs each layer on its own q (no model weights are involved).
+ * page_refcount (device, int32 [num_pages], may be NULL) is checked as by
+ * phs_kv_append_paged: a Full layer's new token whose page count is not 1
+ * is not written (PHS_ESHARED in *dev_status); the Full pools share the
+ * block table, so one count per page id serves every Full layer.
+ * Every argument is checked before anything is launched (softmax_scale
+ * must be positive and finite).
  * ---------------------------------------------------------------------- */
 typedef struct {
     int32_t is_full;      /* 1 = Full-attention layer, 0 = SWA layer */
@@ -332,6 +345,7 @@ typedef struct {
 int phs_attn_decode_hybrid_stack(const phs_layer *layers, int32_t num_layers,
                                  int32_t num_q_heads, int32_t batch,
                                  const int32_t *block_table, int32_t max_pages_per_seq,
+                                 const int32_t *page_refcount,
                                  const int32_t *seq_lens, int32_t max_seq_len,
                                  const int32_t *ring_ids, const int32_t *ring_pos,
                                  float softmax_scale, int32_t do_append, int32_t out_dtype,
@@ -362,11 +376,16 @@ size_t phs_hybrid_stack_workspace_bytes(int32_t batch, int32_t num_q_heads,
  * workspace is phs_hybrid_stack_fused_workspace_bytes (256-byte aligned).
  * Outputs and pool contents equal those of the unfused call.
  * Errors as phs_attn_decode_hybrid_stack (PHS_EINVAL also for a missing
- * k_new/v_new); block-table ids must be valid for every Full pool.
+ * k_new/v_new); block-table ids must be valid for every Full pool.  With
+ * page_refcount, a new token whose page is shared is neither written nor
+ * attended from k_new/v_new (the layer attends to the page as it stands,
+ * as the unfused call does after its refused append) and PHS_ESHARED is
+ * recorded.
  * ---------------------------------------------------------------------- */
 int phs_attn_decode_hybrid_stack_fused(const phs_layer *layers, int32_t num_layers,
                                        int32_t num_q_heads, int32_t batch,
                                        const int32_t *block_table, int32_t max_pages_per_seq,
+                                       const int32_t *page_refcount,
                                        const int32_t *seq_lens, int32_t max_seq_len,
                                        const int32_t *ring_ids, const int32_t *ring_pos,
                                        float softmax_scale, int32_t out_dtype, void *workspace,

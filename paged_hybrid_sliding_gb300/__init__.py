@@ -406,11 +406,14 @@ def hybrid_stack_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max
 
 def attn_decode_hybrid_stack(layers, num_q_heads, seq_lens, max_seq_len, block_table=None,
                              ring_pos=None, ring_ids=None, softmax_scale=None, do_append=True,
-                             workspace=None, status=None, stream=None):
-    """One decode step (append + attend) over every layer of a hybrid stack."""
+                             workspace=None, status=None, stream=None, page_refcount=None):
+    """One decode step (append + attend) over every layer of a hybrid stack.
+    page_refcount: optional device int32 [num_pages]; a Full layer's new token
+    is not written into a page whose count is not 1."""
     arr = (_lib.LayerC * len(layers))(*[L.c() for L in layers])
     _need(seq_lens, torch.int32, "seq_lens", 1)
     _opt(block_table, torch.int32, "block_table", 2)
+    _opt(page_refcount, torch.int32, "page_refcount", 1)
     _opt(ring_pos, torch.int32, "ring_pos", 1)
     _opt(ring_ids, torch.int32, "ring_ids", 1)
     _opt(status, torch.int32, "status")
@@ -426,7 +429,8 @@ def attn_decode_hybrid_stack(layers, num_q_heads, seq_lens, max_seq_len, block_t
                                 dtype=torch.uint8, device=q0.device)
     _check(lib().phs_attn_decode_hybrid_stack(
         arr, len(layers), num_q_heads, B, _ptr(block_table),
-        0 if block_table is None else block_table.shape[1], _ptr(seq_lens), int(max_seq_len),
+        0 if block_table is None else block_table.shape[1], _ptr(page_refcount),
+        _ptr(seq_lens), int(max_seq_len),
         _ptr(ring_ids), _ptr(ring_pos), scale, int(bool(do_append)), out_code, _ptr(workspace),
         0 if workspace is None else workspace.numel(), _ptr(status), _stream(stream)),
         "attn_decode_hybrid_stack")
@@ -441,12 +445,14 @@ def hybrid_stack_fused_workspace_bytes(batch, num_q_heads, num_kv_heads, head_di
 
 def attn_decode_hybrid_stack_fused(layers, num_q_heads, seq_lens, max_seq_len, block_table=None,
                                    ring_pos=None, ring_ids=None, softmax_scale=None,
-                                   workspace=None, status=None, stream=None):
+                                   workspace=None, status=None, stream=None, page_refcount=None):
     """One decode step over every layer of a hybrid stack with the appends
-    fused into the attention launches (every layer needs k_new / v_new)."""
+    fused into the attention launches (every layer needs k_new / v_new).
+    page_refcount as for attn_decode_hybrid_stack."""
     arr = (_lib.LayerC * len(layers))(*[L.c() for L in layers])
     _need(seq_lens, torch.int32, "seq_lens", 1)
     _opt(block_table, torch.int32, "block_table", 2)
+    _opt(page_refcount, torch.int32, "page_refcount", 1)
     _opt(ring_pos, torch.int32, "ring_pos", 1)
     _opt(ring_ids, torch.int32, "ring_ids", 1)
     _opt(status, torch.int32, "status")
@@ -463,7 +469,8 @@ def attn_decode_hybrid_stack_fused(layers, num_q_heads, seq_lens, max_seq_len, b
                                 dtype=torch.uint8, device=q0.device)
     _check(lib().phs_attn_decode_hybrid_stack_fused(
         arr, len(layers), num_q_heads, B, _ptr(block_table),
-        0 if block_table is None else block_table.shape[1], _ptr(seq_lens), int(max_seq_len),
+        0 if block_table is None else block_table.shape[1], _ptr(page_refcount),
+        _ptr(seq_lens), int(max_seq_len),
         _ptr(ring_ids), _ptr(ring_pos), scale, out_code, _ptr(workspace),
         0 if workspace is None else workspace.numel(), _ptr(status), _stream(stream)),
         "attn_decode_hybrid_stack_fused")

@@ -72,12 +72,12 @@ _SIGS = {
     "phs_attn_decode_swa_ring": (ctypes.c_int, [c_vp, c_i32, _P(RingPoolC), c_vp, c_vp, c_vp,
                                                 c_i32, c_f32, c_vp, c_i32, c_vp, c_vp]),
     "phs_attn_decode_hybrid_stack": (ctypes.c_int, [_P(LayerC), c_i32, c_i32, c_i32, c_vp, c_i32,
-                                                    c_vp, c_i32, c_vp, c_vp, c_f32, c_i32, c_i32,
-                                                    c_vp, c_size, c_vp, c_vp]),
+                                                    c_vp, c_vp, c_i32, c_vp, c_vp, c_f32, c_i32,
+                                                    c_i32, c_vp, c_size, c_vp, c_vp]),
     "phs_hybrid_stack_workspace_bytes": (c_size, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "phs_attn_decode_hybrid_stack_fused": (ctypes.c_int, [_P(LayerC), c_i32, c_i32, c_i32, c_vp,
-                                                          c_i32, c_vp, c_i32, c_vp, c_vp, c_f32,
-                                                          c_i32, c_vp, c_size, c_vp, c_vp]),
+                                                          c_i32, c_vp, c_vp, c_i32, c_vp, c_vp,
+                                                          c_f32, c_i32, c_vp, c_size, c_vp, c_vp]),
     "phs_hybrid_stack_fused_workspace_bytes": (c_size, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32]),
     "phs_hybrid_kv_tokens": (ctypes.c_int, [c_vp, c_i32, c_vp, c_i32, c_i32, P_i64, P_i64]),
     "phs_copy_d2d": (ctypes.c_int, [c_vp, c_vp, c_size, c_vp]),

@@ -13,7 +13,7 @@
 
 namespace phs {
 
-int swa_smem_bytes(int D, int G, int batch);
+int swa_smem_bytes(int D, int G);
 
 int ensure_dynamic_smem(const void* kernel, int bytes) {
   static std::mutex mu;
@@ -34,6 +34,9 @@ namespace {
 
 constexpr int kMaxSplitTokens = 4096;
 constexpr int kMaxWindow = 4096;
+// The append kernel gives one thread to each 16-byte piece of a token's K
+// (and V) row over all KV heads, in one CTA.
+constexpr int kMaxAppendThreads = 1024;
 
 // ---------------------------------------------------------- device info --
 struct DevInfo {
@@ -151,6 +154,7 @@ int check_paged(const phs_paged_pool* pool) {
   if (pool->page_size != kPage) return PHS_EUNSUPPORTED;
   if (pool->head_dim != 64 && pool->head_dim != 128) return PHS_EUNSUPPORTED;
   if (pool->num_pages * pool->num_kv_heads * kPage > INT32_MAX) return PHS_EUNSUPPORTED;
+  if (int64_t{pool->num_kv_heads} * pool->head_dim / 8 > kMaxAppendThreads) return PHS_EUNSUPPORTED;
   if (!aligned16(pool->k) || !aligned16(pool->v)) return PHS_EALIGN;
   return PHS_OK;
 }
@@ -161,6 +165,7 @@ int check_ring(const phs_ring_pool* ring) {
   if (ring->window % kPage != 0 || ring->window > kMaxWindow) return PHS_EUNSUPPORTED;
   if (ring->head_dim != 64 && ring->head_dim != 128) return PHS_EUNSUPPORTED;
   if (ring->num_rings * ring->num_kv_heads * ring->window > INT32_MAX) return PHS_EUNSUPPORTED;
+  if (int64_t{ring->num_kv_heads} * ring->head_dim / 8 > kMaxAppendThreads) return PHS_EUNSUPPORTED;
   if (!aligned16(ring->k) || !aligned16(ring->v)) return PHS_EALIGN;
   return PHS_OK;
 }
@@ -545,7 +550,7 @@ int phs_attn_decode_swa_ring(const void* q, int32_t num_q_heads, const phs_ring_
   if (batch == 0) return PHS_OK;
   DevInfo di;
   if ((st = dev_info(di))) return st;
-  if (swa_smem_bytes(D, num_q_heads / Hkv, batch) > di.smem_optin) return PHS_EUNSUPPORTED;
+  if (swa_smem_bytes(D, num_q_heads / Hkv) > di.smem_optin) return PHS_EUNSUPPORTED;
   SwaParams<1> p;
   std::memset(&p, 0, sizeof(p));
   if ((st = map_bf16_kv(&p.tk[0], ring->k, ring->num_rings * Hkv * ring->window, D))) return st;
@@ -573,7 +578,7 @@ namespace {
 
 struct PrefixPlan {
   int G = 0, rows = 0, T = 0, ms = 0, ntiles = 0, tps = 0, nsp = 0;
-  size_t off_ml = 0, off_po = 0, off_pml = 0, need = 0;
+  size_t off_ml = 0, off_po = 0, off_pml = 0, off_bad = 0, need = 0;
 };
 
 int make_prefix_plan(PrefixPlan& pl, int B, int Hq, int Hkv, int D, int max_seq, int shared_len) {
@@ -600,7 +605,8 @@ int make_prefix_plan(PrefixPlan& pl, int B, int Hq, int Hkv, int D, int max_seq,
   pl.off_ml = ws_o_bytes(B, Hkv, pl.ms, pl.G, D);
   pl.off_po = pl.off_ml + align256(static_cast<size_t>(B) * Hkv * pl.ms * pl.G * 2 * sizeof(float));
   pl.off_pml = pl.off_po + align256(static_cast<size_t>(Hkv) * pl.nsp * 256 * D * sizeof(float));
-  pl.need = pl.off_pml + align256(static_cast<size_t>(Hkv) * pl.nsp * 256 * 2 * sizeof(float));
+  pl.off_bad = pl.off_pml + align256(static_cast<size_t>(Hkv) * pl.nsp * 256 * 2 * sizeof(float));
+  pl.need = pl.off_bad + align256(static_cast<size_t>(B) * Hkv * pl.ms * sizeof(int32_t));
   return PHS_OK;
 }
 
@@ -682,12 +688,15 @@ int phs_attn_decode_shared_prefix(const void* q, int32_t num_q_heads, const phs_
   a.scale_log2 = scale_log2;
   a.skip_len = shared_len;
   a.force_partial = 1;
+  a.prefix_bad = reinterpret_cast<int32_t*>(ws + pl.off_bad);
   a.wait_prior_at_exit = 1;  // started beside the prefix pass (independent tokens)
   if ((st = launch_split_decode(D, tk3, tv3, tk3, tv3, a, batch, s, true))) return st;
   // 3. merge prefix and suffix partials
   PrefixMergeArgs m;
   std::memset(&m, 0, sizeof(m));
   m.seq_lens = seq_lens;
+  m.prefix_bad = a.prefix_bad;
+  m.bad_slots = Hkv * pl.ms;
   m.ws_o = a.ws_o;
   m.ws_ml = a.ws_ml;
   m.ws_po = pa.ws_o;
@@ -713,13 +722,15 @@ size_t phs_hybrid_stack_workspace_bytes(int32_t batch, int32_t num_q_heads,
 
 int phs_attn_decode_hybrid_stack(const phs_layer* layers, int32_t num_layers,
                                  int32_t num_q_heads, int32_t batch, const int32_t* block_table,
-                                 int32_t max_pages_per_seq, const int32_t* seq_lens,
-                                 int32_t max_seq_len, const int32_t* ring_ids,
-                                 const int32_t* ring_pos, float softmax_scale, int32_t do_append,
-                                 int32_t out_dtype, void* workspace, size_t workspace_bytes,
-                                 int32_t* dev_status, void* stream) {
+                                 int32_t max_pages_per_seq, const int32_t* page_refcount,
+                                 const int32_t* seq_lens, int32_t max_seq_len,
+                                 const int32_t* ring_ids, const int32_t* ring_pos,
+                                 float softmax_scale, int32_t do_append, int32_t out_dtype,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                 void* stream) {
   if (!layers || num_layers <= 0 || batch < 0 || !seq_lens) return PHS_EINVAL;
   if (out_dtype != PHS_OUT_BF16 && out_dtype != PHS_OUT_F32) return PHS_EINVAL;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return PHS_EINVAL;
   if (batch == 0) return PHS_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int st;
@@ -757,7 +768,7 @@ int phs_attn_decode_hybrid_stack(const phs_layer* layers, int32_t num_layers,
   if (nswa && !ring_pos) return PHS_EINVAL;
   DevInfo di;
   if ((st = dev_info(di))) return st;
-  if (nswa && swa_smem_bytes(D, num_q_heads / Hkv, batch) > di.smem_optin) return PHS_EUNSUPPORTED;
+  if (nswa && swa_smem_bytes(D, num_q_heads / Hkv) > di.smem_optin) return PHS_EUNSUPPORTED;
   if (nfull) {
     DecodePlan pl;
     if ((st = make_plan(pl, batch, num_q_heads, Hkv, D, max_seq_len, 0, false))) return st;
@@ -773,6 +784,7 @@ int phs_attn_decode_hybrid_stack(const phs_layer* layers, int32_t num_layers,
       p.table = full ? block_table : ring_ids;
       p.seq_lens = seq_lens;
       p.ring_pos = ring_pos;
+      p.refcount = full ? page_refcount : nullptr;
       p.status = dev_status;
       p.B = batch;
       p.Hkv = Hkv;
@@ -856,6 +868,7 @@ size_t phs_hybrid_stack_fused_workspace_bytes(int32_t batch, int32_t num_q_heads
 int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_layers,
                                        int32_t num_q_heads, int32_t batch,
                                        const int32_t* block_table, int32_t max_pages_per_seq,
+                                       const int32_t* page_refcount,
                                        const int32_t* seq_lens, int32_t max_seq_len,
                                        const int32_t* ring_ids, const int32_t* ring_pos,
                                        float softmax_scale, int32_t out_dtype, void* workspace,
@@ -900,7 +913,7 @@ int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_laye
   if (nswa && !ring_pos) return PHS_EINVAL;
   DevInfo di;
   if ((st = dev_info(di))) return st;
-  if (nswa && swa_smem_bytes(D, num_q_heads / Hkv, batch) > di.smem_optin) return PHS_EUNSUPPORTED;
+  if (nswa && swa_smem_bytes(D, num_q_heads / Hkv) > di.smem_optin) return PHS_EUNSUPPORTED;
   DecodePlan pl;
   if (nfull) {
     if ((st = make_plan(pl, batch, num_q_heads, Hkv, D, max_seq_len, 0, false))) return st;
@@ -922,6 +935,7 @@ int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_laye
     std::memset(m, 0, sizeof(*m));
     SplitArgs& a = p->a;
     a.block_table = block_table;
+    a.page_refcount = page_refcount;
     a.seq_lens = seq_lens;
     a.status = dev_status;
     a.num_pages = min_pages;
@@ -1093,22 +1107,56 @@ static __device__ __align__(256) unsigned char phs_noalloc_scratch[PHS_NOALLOC_S
 namespace phs {
 namespace {
 
-constexpr int kNoAllocMaxDevices = 64;
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of the scratch on the current device (looked up on the
-// first call per device), or null if the lookup fails.
+// Unique id of the calling thread's current CUDA context (0 if none or on
+// failure).  A context re-created after a device reset gets a new id, so a
+// cached device address is never reused across contexts.
+unsigned long long current_context_id() {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch in the current context: looked up with
+// cudaGetSymbolAddress on the first call in each context (after a device
+// reset the new context looks it up again), or null if the lookup fails.
 void* noalloc_scratch_on_current_device() {
   static std::mutex mu;
-  static void* addr[kNoAllocMaxDevices] = {};
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+  static std::map<unsigned long long, void*> addr;  // context id -> address
+  const unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, phs_noalloc_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
+  if (id != 0) {
+    auto it = addr.find(id);
+    if (it != addr.end()) return it->second;
   }
-  return addr[dev];
+  // first call in this context (or no context yet: the lookup makes the
+  // device's primary context current)
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, phs_noalloc_scratch) != cudaSuccess) return nullptr;
+  const unsigned long long now = current_context_id();
+  if (now != 0) addr[now] = p;
+  return p;
 }
 
 }  // namespace
@@ -1145,5 +1193,6 @@ extern "C" int phs_attn_decode_full_paged_noalloc(
   if (st) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launch_split_decode(c.pl.D, c.tk, c.tv, c.tk8, c.tv8, c.a, batch, s))) return st;
+  if (c.pl.max_splits == 1) return PHS_OK;  // every request finished in its only split
   return launch_merge(c.pl.D, c.m, batch, s);
 }

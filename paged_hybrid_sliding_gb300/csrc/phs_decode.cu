@@ -137,6 +137,27 @@ __device__ __forceinline__ int walk_chunks(WarpState<D, TWO>& st, const QFrags<D
   return -1;
 }
 
+// Shared-prefix call: CTA (b, h, s) checks its slice of request b's first
+// skip_len / 16 page ids against row 0's (the ids the prefix pass reads)
+// and records the result for the merge.  Kept out of line: it runs only in
+// that call and must not add to the decode loop's register pressure.
+__device__ __noinline__ void check_prefix_ids(const SplitArgs& a, int b, int h, int s) {
+  const int slots = a.Hkv * a.max_splits, slot = h * a.max_splits + s;
+  const int np = a.skip_len / kPage;
+  const int i0 = static_cast<int>(static_cast<long long>(np) * slot / slots);
+  const int i1 = static_cast<int>(static_cast<long long>(np) * (slot + 1) / slots);
+  const int32_t* row = a.block_table + static_cast<size_t>(b) * a.max_pages;
+  int bad = 0;
+  if (b > 0)
+    for (int i = i0 + static_cast<int>(threadIdx.x); i < i1; i += blockDim.x)
+      bad |= __ldg(row + i) != __ldg(a.block_table + i);
+  bad = __syncthreads_or(bad || a.seq_lens[b] < a.skip_len);
+  if (threadIdx.x == 0) {
+    a.prefix_bad[(static_cast<size_t>(b) * a.Hkv + h) * a.max_splits + s] = bad;
+    if (bad) set_status(a.status, PHS_ESHAPE);
+  }
+}
+
 // The work of one CTA: request b, KV head h, split s.  q/out/ws_o/ws_ml are
 // the layer's; `app` (k_new null: none) is an append fused into this
 // launch: the CTA holding token n-1 writes it into its page and patches its
@@ -159,6 +180,8 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
+
+  if (a.prefix_bad != nullptr) check_prefix_ids(a, b, h, s);
 
   int n = a.seq_lens[b];
   if (n > a.n_clamp) {  // longer than its block table or the stated bound
@@ -288,6 +311,11 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
     if (app.k_new == nullptr) return;
     const int r = n - 1 - (t0 + kPage * (warp + j * NW));
     if (r < 0 || r >= kPage) return;
+    if (a.page_refcount != nullptr && __ldg(a.page_refcount + ids[j]) != 1) {
+      // a shared page: leave it (and the staged copy of it) as it is
+      if (lane == 0) set_status(a.status, PHS_ESHARED);
+      return;
+    }
     const int op = lane >> 4, c = lane & 15;
     if (c < D / 8) {
       const size_t src = (static_cast<size_t>(b) * a.Hkv + h) * D + c * 8;

@@ -41,6 +41,14 @@ struct SplitArgs {
   float scale_log2;         // softmax_scale * log2(e)
   int skip_len;             // tokens [0, skip_len) are attended elsewhere (shared prefix)
   int force_partial;        // write partials even for single-split requests
+  // fused append (stack kernel): page reference counts, or null; a new
+  // token whose page count is not 1 is neither written nor attended from
+  // the input (the page is shared; copy on write is the caller's job)
+  const int32_t* page_refcount;
+  // shared-prefix call (skip_len > 0): per (request, KV head, split) CTA,
+  // 1 if its slice of the request's first skip_len / 16 page ids differs
+  // from row 0's, or the request is shorter than skip_len; else 0
+  int32_t* prefix_bad;
 };
 
 // New token of each request for an append fused into a decode kernel: the
@@ -95,6 +103,8 @@ struct PrefixArgs {
 
 struct PrefixMergeArgs {
   const int32_t* seq_lens;
+  const int32_t* prefix_bad;  // [B][Hkv][max_splits] from the own-token split
+  int bad_slots;              // Hkv * max_splits
   const float* ws_o;        // suffix partials (split kernel layout)
   const float* ws_ml;
   const float* ws_po;       // prefix partials
@@ -228,7 +238,7 @@ int launch_copy(void* dst, const void* src, size_t bytes, int num_sms, cudaStrea
 int launch_copy_pages(void* k, void* v, const int32_t* src, const int32_t* dst, int32_t n,
                       int64_t num_pages, int page_bytes, int32_t* status, cudaStream_t stream);
 
-int swa_smem_bytes(int D, int G, int batch);
+int swa_smem_bytes(int D, int G);
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device);
 // later calls are a lookup (no CUDA call, so launches stay cheap and safe to

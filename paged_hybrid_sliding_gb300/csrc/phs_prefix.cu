@@ -532,6 +532,21 @@ __global__ void __launch_bounds__(128) phs_merge_prefix_kernel(const PrefixMerge
   const int n = min(a.seq_lens[b], a.n_clamp);
   const int ns = n > a.shared_len ? min((n - a.shared_len + a.T - 1) / a.T, a.max_splits) : 0;
   const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
+  // a request whose table does not begin with the shared pages (or that is
+  // shorter than the shared prefix) was flagged by the own-token split: the
+  // prefix partials are not its own, so its output row is zeroed
+  int bad = 0;
+  for (int i = lane; i < a.bad_slots; i += 32)
+    bad |= a.prefix_bad[static_cast<size_t>(b) * a.bad_slots + i];
+  if (__any_sync(0xffffffffu, bad)) {
+    for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+      if (a.out_f32)
+        reinterpret_cast<float*>(a.out)[out_row0 + e] = 0.f;
+      else
+        reinterpret_cast<__nv_bfloat16*>(a.out)[out_row0 + e] = __float2bfloat16_rn(0.f);
+    }
+    return;
+  }
   for (int g = warp; g < G; g += 4) {
     const int r = b * G + g;
     // sources: prefix splits then suffix splits

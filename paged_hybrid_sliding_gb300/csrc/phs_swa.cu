@@ -41,17 +41,17 @@ constexpr int kSwaStages = PHS_SWA_STAGES;
 constexpr int kSwaWarps = PHS_SWA_WARPS;
 
 // Shared-memory layout for NW warps of S stages: [stages][bars][query
-// slots][info].
+// slots].  It does not depend on the batch: each warp reads its units'
+// ring id, newest slot and length from global memory, one unit ahead.
 struct SwaLayout {
-  int kv, qslot, stages_bytes, bar_off, q_off, info_off, total;
-  __host__ __device__ SwaLayout(int D, int G, int NW, int S, int B) {
+  int kv, qslot, stages_bytes, bar_off, q_off, total;
+  __host__ __device__ SwaLayout(int D, int G, int NW, int S) {
     kv = 64 * D;                                   // K + V tile of 16 tokens
     qslot = (G * D * 2 + 127) / 128 * 128;         // one group's queries
     stages_bytes = NW * S * kv;
     bar_off = stages_bytes;
     q_off = bar_off + NW * S * 8;
-    info_off = q_off + NW * S * qslot;
-    total = info_off + 12 * B + 1024;              // + base alignment slack
+    total = q_off + NW * S * qslot + 1024;         // + base alignment slack
   }
 };
 
@@ -71,18 +71,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   uint8_t* smem = swa_align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = p.B, Hkv = p.Hkv, G = p.G, W = p.W;
-  const SwaLayout L(D, G, NW, S, B);
-
-  // ---- per-request ring id, newest slot and length, cached in smem
-  int32_t* s_ring = reinterpret_cast<int32_t*>(smem + L.info_off);
-  int32_t* s_pos = s_ring + B;
-  int32_t* s_n = s_pos + B;
-  for (int i = threadIdx.x; i < B; i += blockDim.x) {
-    s_ring[i] = p.ring_ids ? p.ring_ids[i] : i;
-    s_pos[i] = p.ring_pos[i];
-    s_n[i] = p.seq_lens[i];
-  }
-  __syncthreads();
+  const SwaLayout L(D, G, NW, S);
 
   const int CPU = W / kPage;  // chunks per unit
   const int BH = B * Hkv;
@@ -102,6 +91,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const uint32_t qbase = smem_u32(smem + L.q_off) + warp * S * L.qslot;
   const uint64_t pol = policy_evict_first();
 
+  // unit k of this warp: its layer, request and KV head, and the request's
+  // ring id, newest slot and length (read from global memory; validated
+  // where used)
   auto unit_at = [&](int k) {
     SwaUnit u;
     const int id = gw + k * tw;
@@ -109,9 +101,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const int rem = id - u.l * BH;
     u.b = rem / Hkv;
     u.h = rem - u.b * Hkv;
-    u.ring = s_ring[u.b];
-    u.pos = s_pos[u.b];
-    u.n = s_n[u.b];
+    u.ring = p.ring_ids ? __ldg(p.ring_ids + u.b) : u.b;
+    u.pos = __ldg(p.ring_pos + u.b);
+    u.n = __ldg(p.seq_lens + u.b);
+    return u;
+  };
+  auto checked = [&](SwaUnit u) {
     u.ok = u.ring >= 0 && u.ring < p.num_rings[u.l] && u.pos >= 0 && u.pos < W && u.n >= 0;
     return u;
   };
@@ -119,7 +114,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   // issuer state (lane 0): unit index, chunk within it, stage
   int ik = 0, ic = 0, ist = 0;
   SwaUnit iu;
-  if (total > 0) iu = unit_at(0);
+  if (total > 0) iu = checked(unit_at(0));
   auto issue_next = [&]() {  // lane 0 only
     const uint32_t bar = bar0 + 8 * ist;
     const uint32_t dst = sbase + ist * L.kv;
@@ -145,7 +140,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     if (++ist == S) ist = 0;
     if (++ic == CPU) {
       ic = 0;
-      if (++ik < my_units) iu = unit_at(ik);
+      if (++ik < my_units) iu = checked(unit_at(ik));
     }
   };
 
@@ -160,6 +155,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
   int k = 0, c = 0, cst = 0;
   uint32_t phase = 0;
   SwaUnit u;
+  // the consumer's next unit, loaded while the current one streams
+  SwaUnit next;
+  if (total > 0) next = unit_at(0);
   int j = 0;
   for (; j < total; ++j) {
     const uint32_t bar = bar0 + 8 * cst;
@@ -171,7 +169,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const uint32_t sK = sbase + cst * L.kv;
     const uint32_t sV = sK + L.kv / 2;
     if (c == 0) {
-      u = unit_at(k);
+      u = checked(next);
+      if (k + 1 < my_units) next = unit_at(k + 1);
       st.reset();
       if (u.ok)
         load_q_bf16_smem<D, TWO>(qf, qbase + cst * L.qslot, G, lane);
@@ -287,7 +286,7 @@ template <int D, bool TWO, int MAXL, int NW, int S>
 static int launch_swa_t(const SwaParams<MAXL>& p, int num_sms, cudaStream_t stream,
                         bool dependent) {
   auto kern = phs_swa_decode_kernel<D, TWO, MAXL, NW, S>;
-  const int smem = SwaLayout(D, p.G, NW, S, p.B).total;
+  const int smem = SwaLayout(D, p.G, NW, S).total;
   if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
   const long long units = std::max(static_cast<long long>(p.num_layers),
                                    static_cast<long long>(p.num_merge_layers)) *
@@ -326,22 +325,20 @@ static int launch_swa_t(const SwaParams<MAXL>& p, int num_sms, cudaStream_t stre
 //   small    4 x kSwaStages: when the stream shape's shared memory does not fit.
 enum SwaMode { kSwaNone = 0, kSwaLatency, kSwaStream, kSwaSmall };
 
-SwaMode swa_mode(int D, int G, int batch, long long units, int num_sms, int smem_optin) {
-  if (units <= 4LL * num_sms &&
-      SwaLayout(D, G, 4, 4, batch).total <= smem_optin)
-    return kSwaLatency;
-  if (SwaLayout(D, G, kSwaWarps, kSwaStages, batch).total <= smem_optin) return kSwaStream;
-  if (SwaLayout(D, G, 4, kSwaStages, batch).total <= smem_optin) return kSwaSmall;
+SwaMode swa_mode(int D, int G, long long units, int num_sms, int smem_optin) {
+  if (units <= 4LL * num_sms && SwaLayout(D, G, 4, 4).total <= smem_optin) return kSwaLatency;
+  if (SwaLayout(D, G, kSwaWarps, kSwaStages).total <= smem_optin) return kSwaStream;
+  if (SwaLayout(D, G, 4, kSwaStages).total <= smem_optin) return kSwaSmall;
   return kSwaNone;
 }
 
-int swa_smem_bytes(int D, int G, int batch) { return SwaLayout(D, G, 4, kSwaStages, batch).total; }
+int swa_smem_bytes(int D, int G) { return SwaLayout(D, G, 4, kSwaStages).total; }
 
 template <int MAXL>
 int launch_swa_decode(int D, const SwaParams<MAXL>& p, int num_sms, int smem_optin,
                       cudaStream_t stream, bool dependent) {
   if (static_cast<long long>(p.num_layers) * p.B * p.Hkv > INT32_MAX / 2) return PHS_EUNSUPPORTED;
-  const SwaMode mode = swa_mode(D, p.G, p.B, static_cast<long long>(p.num_layers) * p.B * p.Hkv,
+  const SwaMode mode = swa_mode(D, p.G, static_cast<long long>(p.num_layers) * p.B * p.Hkv,
                                 num_sms, smem_optin);
   if (mode == kSwaNone) return PHS_EUNSUPPORTED;
   const bool two = p.G > 8;

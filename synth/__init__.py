@@ -179,20 +179,24 @@ def hybrid_stack(seed: int = 3, B: int = 256, lo: int = 4096, hi: int = 131072,
     return w
 
 
-def int8_block32(seed: int = 4, B: int = 32, n_pre: int = 65536, hot: int = 1024) -> Workload:
+def int8_block32(seed: int = 4, B: int = 32, n_pre: int = 65536, hot: int = 1024,
+                 steps: int = 1) -> Workload:
     """Batch 32, length 65536, 32 q / 8 KV heads, head_dim 128.  Tokens
     [0, qlen) are held as INT8 in 32-token pages, qlen the largest multiple
     of 32 leaving at least `hot` tokens (the new one included) in bf16.
-    K/V values: N(0,1) with 1% outliers N(0, 8^2)."""
+    K/V values: N(0,1) with 1% outliers N(0, 8^2).  The tables have room for
+    `steps` decode steps (lengths n_pre + 1 .. n_pre + steps, the INT8
+    length following the same rule)."""
     npre = np.full(B, n_pre, dtype=np.int32)
     w = Workload(f"int8_block32_b{B}_n{n_pre}", B=B, Hq=32, Hkv=8, D=128, n_pre=npre, seed=seed)
     n_after = npre + 1
     qlen = ((n_after - hot) // QBLOCK) * QBLOCK
     qlen = np.maximum(qlen, 0).astype(np.int32)
+    n_last = npre + max(int(steps), 1)
     # bf16 pages cover the whole logical range at setup (the quantiser reads
     # them); only pages at or past qlen stay referenced by decode.
-    w.block_table, w.num_pages = block_tables_from_permutation(pages_needed(n_after), seed + 2)
-    nq = (qlen // QBLOCK).astype(np.int64)
+    w.block_table, w.num_pages = block_tables_from_permutation(pages_needed(n_last), seed + 2)
+    nq = ((np.maximum(n_last - hot, 0) // QBLOCK)).astype(np.int64)
     qt, nqp = block_tables_from_permutation(np.maximum(nq, 1), seed + 3)
     w.extra.update(qlen=qlen, qtable=qt, num_qpages=nqp, outlier_p=0.01, outlier_sigma=8.0)
     return w

@@ -98,3 +98,48 @@ def test_host_errors():
     with pytest.raises(phs.PhsError) as e:   # tokens_per_split not a multiple of 32
         phs.attn_decode_full_paged(q, pool, bt, sl, 20, tokens_per_split=48)
     assert e.value.code == -7
+
+
+def test_stack_rejects_bad_scale_before_any_launch():
+    """A rejected hybrid-stack call launches nothing: no append has happened
+    when the scale is found to be invalid."""
+    B, Hq, Hkv, D, W = 2, 4, 2, 64, 16
+    pool = _pool()
+    ring = phs.RingPool(synth.normal_bf16((B, Hkv, W, D), 4, device="cuda"),
+                        synth.normal_bf16((B, Hkv, W, D), 5, device="cuda"))
+    kn = synth.normal_bf16((B, Hkv, D), 6, device="cuda")
+    layers = [phs.Layer(q=synth.normal_bf16((B, Hq, D), 7, device="cuda"),
+                        out=torch.empty((B, Hq, D), device="cuda"), paged=pool, k_new=kn,
+                        v_new=kn),
+              phs.Layer(q=synth.normal_bf16((B, Hq, D), 8, device="cuda"),
+                        out=torch.empty((B, Hq, D), device="cuda"), ring=ring, k_new=kn,
+                        v_new=kn)]
+    before = [t.clone() for t in (pool.k, pool.v, ring.k, ring.v)]
+    bt = dev(np.array([[0, 1], [2, 3]], np.int32))
+    sl = dev(np.array([20, 9], np.int32))
+    rp = dev(np.array([3, 8], np.int32))
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        for call in (phs.attn_decode_hybrid_stack, phs.attn_decode_hybrid_stack_fused):
+            with pytest.raises(phs.PhsError) as e:
+                call(layers, Hq, sl, 20, block_table=bt, ring_pos=rp, softmax_scale=bad)
+            assert e.value.code == -1
+    torch.cuda.synchronize()
+    for x, y in zip(before, (pool.k, pool.v, ring.k, ring.v)):
+        assert torch.equal(x, y)
+
+
+def test_too_many_kv_heads_for_one_append_cta_is_unsupported():
+    # 72 KV heads of 128 dims: 1,152 16-byte pieces per token row, more than
+    # one CTA of the append kernel covers
+    pool = phs.PagedPool(torch.zeros((2, 72, 16, 128), dtype=torch.bfloat16, device="cuda"),
+                         torch.zeros((2, 72, 16, 128), dtype=torch.bfloat16, device="cuda"))
+    kn = torch.zeros((1, 72, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(phs.PhsError) as e:
+        phs.kv_append_paged(pool, kn, kn, dev(np.array([[0]], np.int32)),
+                            dev(np.array([1], np.int32)))
+    assert e.value.code == -7
+    ring = phs.RingPool(torch.zeros((1, 72, 16, 128), dtype=torch.bfloat16, device="cuda"),
+                        torch.zeros((1, 72, 16, 128), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(phs.PhsError) as e:
+        phs.kv_append_ring(ring, kn, kn, dev(np.array([0], np.int32)))
+    assert e.value.code == -7

@@ -10,7 +10,7 @@ import torch
 import oracle
 import paged_hybrid_sliding_gb300 as phs
 import synth
-from gpu_util import assert_close, dev, out_np
+from gpu_util import assert_close, dev, out_np, sub_pool
 
 pytestmark = pytest.mark.gpu
 
@@ -108,3 +108,129 @@ def test_shared_prefix_full_size_sampled():
     assert int(st.item()) == 0
     rows = [0, B - 1]
     assert_close(out_np(out)[rows], _oracle_rows(pool, q, w.block_table, n, rows), "config 5")
+
+
+def test_shared_prefix_checks_every_row_against_row_0():
+    """The prefix pass reads row 0's page ids for everyone.  A request whose
+    table does not begin with them (one prefix id replaced by another valid
+    page of the pool), or that is shorter than the shared prefix, is
+    flagged on the device: PHS_ESHAPE in the status word, an all-zero
+    output row, and every other row as the oracle gives it."""
+    B, Hq, Hkv, shared_len = 8, 32, 8, 1024
+    rng = np.random.default_rng(31)
+    suffixes = [int(x) for x in rng.integers(1, 700, size=B)]
+    pool, q, bt, lens = _shared_case(B, Hq, Hkv, shared_len, suffixes, 31)
+    used = set(bt[bt >= 0].ravel().tolist())  # _shared_case leaves two pages unused
+    spare = next(i for i in range(pool.k.shape[0]) if i not in used)
+    bad_row, short_row = 3, 5
+    bt[bad_row, 17] = spare
+    lens[short_row] = shared_len - 10
+    for out_dtype in (torch.float32, torch.bfloat16):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.full((B, Hq, 128), float("nan"), dtype=out_dtype, device="cuda")
+        phs.attn_decode_shared_prefix(q, pool, dev(bt), dev(lens), int(lens.max()), shared_len,
+                                      out=out, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == -2  # PHS_ESHAPE
+        got = out_np(out)
+        assert np.all(got[bad_row] == 0) and np.all(got[short_row] == 0)
+        good = [b for b in range(B) if b not in (bad_row, short_row)]
+        assert_close(got[good], _oracle_rows(pool, q, bt, lens, good), "unflagged rows")
+
+
+def _prefix_steps(B, Hq, Hkv, shared_len, suffix, steps, seed, rows, D=128):
+    """The decode loop of a batch sharing a prefix: each step appends every
+    request's new token (page reference counts checked) and decodes through
+    the shared-prefix call; sampled rows are checked against the oracle at
+    every step, on a host copy of their pages that the oracle appends to."""
+    npref = shared_len // 16
+    own = (suffix + steps + 15) // 16
+    total = npref + B * own
+    perm = np.random.default_rng(seed).permutation(total).astype(np.int32)
+    bt = np.empty((B, npref + own), np.int32)
+    bt[:, :npref] = perm[:npref]
+    for b in range(B):
+        bt[b, npref:] = perm[npref + b * own:npref + (b + 1) * own]
+    rc = np.ones(total, np.int32)
+    rc[perm[:npref]] = B
+    kp = synth.normal_bf16((total, Hkv, 16, D), seed + 1, device="cuda")
+    vp = synth.normal_bf16((total, Hkv, 16, D), seed + 2, device="cuda")
+    pool = phs.PagedPool(kp, vp)
+    n_pre = np.full(B, shared_len + suffix, np.int32)
+    n_final = n_pre + steps
+    hk, bt_s = sub_pool(kp, bt, rows, n_final)
+    hv, _ = sub_pool(vp, bt, rows, n_final)
+    bt_d, rc_d = dev(bt), dev(rc)
+    max_seq = int(n_final.max())
+    ws = torch.empty(phs.shared_prefix_workspace_bytes(B, Hq, Hkv, D, max_seq, shared_len),
+                     dtype=torch.uint8, device="cuda")
+    for k in range(steps):
+        n_after = (n_pre + 1 + k).astype(np.int32)
+        q = synth.normal_bf16((B, Hq, D), seed + 10 + 3 * k, device="cuda")
+        kn = synth.normal_bf16((B, Hkv, D), seed + 11 + 3 * k, device="cuda")
+        vn = synth.normal_bf16((B, Hkv, D), seed + 12 + 3 * k, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sl = dev(n_after)
+        phs.kv_append_paged(pool, kn, vn, bt_d, sl, page_refcount=rc_d, status=st)
+        out = phs.attn_decode_shared_prefix(q, pool, bt_d, sl, max_seq, shared_len,
+                                            out_dtype=torch.float32, workspace=ws, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, k
+        assert oracle.append_paged(hk, hv, synth.bits(kn)[rows], synth.bits(vn)[rows], bt_s,
+                                   n_after[rows]) == 0
+        ref, s = oracle.decode_full_paged(synth.bits(q)[rows], hk, hv, bt_s, n_after[rows],
+                                          1 / math.sqrt(D))
+        assert s == 0
+        assert_close(out_np(out)[rows], ref, f"step {k}")
+
+
+def test_shared_prefix_decode_steps_with_append():
+    # 64 requests x 8 KV heads (256 query rows per head), suffixes crossing a
+    # page boundary during the walk (suffix 505 + 12 steps passes 512)
+    _prefix_steps(B=64, Hq=32, Hkv=8, shared_len=4096, suffix=505, steps=12, seed=900,
+                  rows=[0, 17, 63])
+
+
+@pytest.mark.slow
+def test_shared_prefix_full_size_steps_with_append():
+    """The shared-prefix workload's loop at full size: one 250,000-token
+    prefix shared by 64 requests with 512-token suffixes; append + prefix
+    decode over 4 steps, two sampled requests against the oracle each step
+    (the tensor-core pass covers the prefix's whole 64-token tiles, 249,984
+    tokens; the split kernel the remaining 16 and the suffix)."""
+    w = synth.shared_prefix()
+    assert w.extra["prefix_pages"] * 16 == 250_000
+    _prefix_steps_full(w, steps=4, rows=[0, w.B - 1])
+
+
+def _prefix_steps_full(w, steps, rows):
+    B, Hq, Hkv, D = w.B, w.Hq, w.Hkv, w.D
+    kp = synth.normal_bf16((w.num_pages, Hkv, 16, D), 951, device="cuda")
+    vp = synth.normal_bf16((w.num_pages, Hkv, 16, D), 952, device="cuda")
+    pool = phs.PagedPool(kp, vp)
+    n_final = w.n_pre + steps
+    hk, bt_s = sub_pool(kp, w.block_table, rows, n_final)
+    hv, _ = sub_pool(vp, w.block_table, rows, n_final)
+    bt, rcd = dev(w.block_table), dev(w.extra["refcount"])
+    shared = (w.extra["prefix_pages"] * 16 // 64) * 64
+    max_seq = int(w.n_pre.max()) + w.extra["steps"]
+    ws = torch.empty(phs.shared_prefix_workspace_bytes(B, Hq, Hkv, D, max_seq, shared),
+                     dtype=torch.uint8, device="cuda")
+    for k in range(steps):
+        n_after = (w.n_pre + 1 + k).astype(np.int32)
+        q = synth.normal_bf16((B, Hq, D), 960 + 3 * k, device="cuda")
+        kn = synth.normal_bf16((B, Hkv, D), 961 + 3 * k, device="cuda")
+        vn = synth.normal_bf16((B, Hkv, D), 962 + 3 * k, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sl = dev(n_after)
+        phs.kv_append_paged(pool, kn, vn, bt, sl, page_refcount=rcd, status=st)
+        out = phs.attn_decode_shared_prefix(q, pool, bt, sl, max_seq, shared,
+                                            out_dtype=torch.float32, workspace=ws, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, k
+        assert oracle.append_paged(hk, hv, synth.bits(kn)[rows], synth.bits(vn)[rows], bt_s,
+                                   n_after[rows]) == 0
+        ref, s = oracle.decode_full_paged(synth.bits(q)[rows], hk, hv, bt_s, n_after[rows],
+                                          w.softmax_scale)
+        assert s == 0
+        assert_close(out_np(out)[rows], ref, f"config 5 prefix path, step {k}")

@@ -203,3 +203,62 @@ def test_fused_stack_many_layers_equals_unfused(nfull, nswa):
             oracle.append_ring(k, v, kn, vn, None, rp)
             ref, _ = oracle.decode_swa_ring(q, k, v, None, rp, n_after, scale)
         assert_close(out_np(b[l].out), ref, f"layer {l}")
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_stack_refuses_append_into_shared_page(fused):
+    """Page reference counts in the stack calls ("Kimi K3 context caching"
+    page, section 1: a request writes its new tokens only into blocks of its
+    own).  Request 1's newest token falls in a page with count 2: that page
+    stays byte-identical in every Full layer, the status is PHS_ESHARED, the
+    other requests append as usual, and the outputs are those of the oracle
+    on the pools as they stand (request 1 attends to the page unchanged)."""
+    n, Hq, Hkv, D, lf = CASES[0]
+    n_after = np.array(n, dtype=np.int32)
+    bt, rp, host = _stack(n_after, Hq, Hkv, D, lf, seed=150)
+    num_pages = host[next(i for i, x in enumerate(lf) if x)][4].shape[0]
+    shared = int(bt[1, (n_after[1] - 1) // 16])
+    rc = np.ones(num_pages, np.int32)
+    rc[shared] = 2
+    layers = _device_layers(host, torch.float32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    call = phs.attn_decode_hybrid_stack_fused if fused else phs.attn_decode_hybrid_stack
+    call(layers, Hq, dev(n_after), int(n_after.max()), block_table=dev(bt), ring_pos=dev(rp),
+         page_refcount=dev(rc), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == -4  # PHS_ESHARED
+    scale = 1.0 / np.sqrt(D)
+    for l, (L, (full, q, kn, vn, k, v)) in enumerate(zip(layers, host)):
+        k, v = k.copy(), v.copy()
+        if full:
+            assert oracle.append_paged(k, v, kn, vn, bt, n_after, page_refcount=rc) == -4
+            ref, s = oracle.decode_full_paged(q, k, v, bt, n_after, scale)
+            pk, pv = _pools(L)
+            assert np.array_equal(synth.bits(pk)[shared], host[l][4][shared]), l
+            assert np.array_equal(synth.bits(pv)[shared], host[l][5][shared]), l
+        else:
+            oracle.append_ring(k, v, kn, vn, None, rp)
+            ref, s = oracle.decode_swa_ring(q, k, v, None, rp, n_after, scale)
+        assert s == 0
+        pk, pv = _pools(L)
+        assert np.array_equal(synth.bits(pk), k) and np.array_equal(synth.bits(pv), v), l
+        assert_close(out_np(L.out), ref, f"layer {l} ({'Full' if full else 'SWA'})")
+
+
+def test_stack_fused_equals_unfused_with_shared_page():
+    n, Hq, Hkv, D, lf = CASES[2]
+    n_after = np.array(n, dtype=np.int32)
+    bt, rp, host = _stack(n_after, Hq, Hkv, D, lf, seed=151)
+    num_pages = host[0][4].shape[0]
+    rc = np.ones(num_pages, np.int32)
+    rc[int(bt[2, (n_after[2] - 1) // 16])] = 3
+    a = _device_layers(host, torch.bfloat16)
+    b = _device_layers(host, torch.bfloat16)
+    common = dict(block_table=dev(bt), ring_pos=dev(rp), page_refcount=dev(rc))
+    phs.attn_decode_hybrid_stack(a, Hq, dev(n_after), int(n_after.max()), **common)
+    phs.attn_decode_hybrid_stack_fused(b, Hq, dev(n_after), int(n_after.max()), **common)
+    torch.cuda.synchronize()
+    for l, (La, Lb) in enumerate(zip(a, b)):
+        assert torch.equal(La.out, Lb.out), l
+        for x, y in zip(_pools(La), _pools(Lb)):
+            assert torch.equal(x, y), l
