@@ -204,6 +204,18 @@ class Arena:
 
 
 
+def repeat_for(fn, min_s):
+    """Run fn until at least min_s seconds have passed (once at least);
+    returns (mean seconds per call, calls)."""
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        t = time.perf_counter() - t0
+        if t >= min_s:
+            return t / n, n
+
+
 def rows_for_budget(n_after, order, per_token_s, budget_s):
     rows, acc = [], 0.0
     for b in order:
@@ -368,29 +380,31 @@ class PagedFullWorkload(Workload):
         phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl, self.max_seq,
                                    out=self.out, tokens_per_split=self.tps, workspace=self.ws)
 
-    def cpu_baseline(self, budget_s=8.0):
-        """The oracle as it stands on a sample of requests of this step."""
+    def cpu_baseline(self, budget_s=2.0, min_s=8.0):
+        """The oracle as it stands on a sample of requests of this step,
+        repeated for at least min_s seconds."""
         import oracle
         w = self.w
         t1, _ = self._oracle_time([0])
         rows = rows_for_budget(w.n_after, range(w.B), t1 / float(w.n_after[0]), budget_s)
-        t, toks = self._oracle_time(rows)
+        t, toks, reps = self._oracle_time(rows, min_s)
         kv_bytes = toks * w.Hkv * w.D * 2 * 2
         return {"value": kv_bytes / t / 1e9, "unit": "GB/s", "tokens_per_s": toks / t,
                 "cores": oracle.max_threads(), "kind": "oracle",
                 "sample": f"{len(rows)} of {w.B} requests of one decode step "
-                          f"({toks} tokens, all {w.Hq} query heads), fp64 oracle, {t:.2f} s"}
+                          f"({toks} tokens, all {w.Hq} query heads), fp64 oracle, "
+                          f"{t:.3f} s per call, mean of {reps} calls"}
 
-    def _oracle_time(self, rows):
+    def _oracle_time(self, rows, min_s=0.0):
         import oracle
         w = self.w
         hk, bt = host_pages(self.k, w.block_table, rows, w.n_after)
         hv, _ = host_pages(self.v, w.block_table, rows, w.n_after)
         qh = synth.bits(self.q)[rows]
         sl = w.n_after[rows]
-        t0 = time.perf_counter()
-        oracle.decode_full_paged(qh, hk, hv, bt, sl, w.softmax_scale)
-        return time.perf_counter() - t0, int(sl.sum())
+        t, reps = repeat_for(lambda: oracle.decode_full_paged(qh, hk, hv, bt, sl,
+                                                              w.softmax_scale), min_s)
+        return t, int(sl.sum()), reps
 
 
 class TinyHybridWorkload(Workload):
@@ -482,14 +496,12 @@ class TinyHybridWorkload(Workload):
         hkr, hvr = synth.bits(self.kr), synth.bits(self.vr)
         kn, vn = synth.bits(self.kn), synth.bits(self.vn)
         qf, qs = synth.bits(self.qf), synth.bits(self.qs)
-        reps = 200
-        t0 = time.perf_counter()
-        for _ in range(reps):
+        def one():
             oracle.append_paged(hk, hv, kn, vn, w.block_table, w.n_after)
             oracle.append_ring(hkr, hvr, kn, vn, None, w.ring_pos)
             oracle.decode_full_paged(qf, hk, hv, w.block_table, w.n_after, w.softmax_scale)
             oracle.decode_swa_ring(qs, hkr, hvr, None, w.ring_pos, w.n_after, w.softmax_scale)
-        t = (time.perf_counter() - t0) / reps
+        t, reps = repeat_for(one, 5.0)
         return {"value": self.bytes_per_step / t / 1e9, "unit": "GB/s",
                 "us_per_step": t * 1e6, "cores": oracle.max_threads(), "kind": "oracle",
                 "sample": f"the whole step (2 appends + 2 decodes), mean of {reps} repetitions"}
@@ -661,52 +673,58 @@ class HybridStackWorkload(Workload):
                 "frac": round(self.swa_bytes / t / 1e9 / peak, 4)}
         return out
 
-    def cpu_baseline(self, budget_s=12.0):
+    def cpu_baseline(self, pass_s=1.5, min_s=10.0):
         """The oracle on a sample of the step: requests of one Full layer and
-        the same requests in six SWA layers (the stack's 1 : 6 mix)."""
+        the same requests in six SWA layers (the stack's 1 : 6 mix), chosen
+        so that one pass takes about pass_s seconds, repeated for at least
+        min_s seconds."""
         import oracle
         w = self.w
         full = [L for L in self.layers if L.paged is not None]
         swa = [L for L in self.layers if L.ring is not None][:6]
         order = [int(b) for b in np.random.default_rng(11).permutation(w.B)]
 
-        def run(rows):
-            t, fb, sb = 0.0, 0, 0
+        def gather(rows):
+            x = {"sl": w.n_after[rows], "rp": w.ring_pos[rows], "swa": []}
             if full:
                 L = full[0]
-                hk, bt = host_pages(L.paged.k, w.block_table, rows, w.n_after)
-                hv, _ = host_pages(L.paged.v, w.block_table, rows, w.n_after)
-                qh = synth.bits(L.q)[rows]
-                t0 = time.perf_counter()
-                oracle.decode_full_paged(qh, hk, hv, bt, w.n_after[rows], w.softmax_scale)
-                t += time.perf_counter() - t0
-                fb = int(w.n_after[rows].sum())
+                x["hk"], x["bt"] = host_pages(L.paged.k, w.block_table, rows, w.n_after)
+                x["hv"], _ = host_pages(L.paged.v, w.block_table, rows, w.n_after)
+                x["qf"] = synth.bits(L.q)[rows]
             for L in swa:
-                kr, vr = synth.bits(L.ring.k[rows]), synth.bits(L.ring.v[rows])
-                qh = synth.bits(L.q)[rows]
-                t0 = time.perf_counter()
-                oracle.decode_swa_ring(qh, kr, vr, None, w.ring_pos[rows], w.n_after[rows],
-                                       w.softmax_scale)
-                t += time.perf_counter() - t0
-                sb += int(np.minimum(w.n_after[rows], w.W).sum())
-            return t, fb, sb
+                x["swa"].append((synth.bits(L.ring.k[rows]), synth.bits(L.ring.v[rows]),
+                                 synth.bits(L.q)[rows]))
+            return x
 
-        t1, fb1, sb1 = run(order[:1])
-        per_tok = t1 / max(1, fb1 + sb1)
-        est = [float(w.n_after[b]) + len(swa) * min(float(w.n_after[b]), w.W) for b in order]
+        def run(x):
+            if full:
+                oracle.decode_full_paged(x["qf"], x["hk"], x["hv"], x["bt"], x["sl"],
+                                         w.softmax_scale)
+            for kr, vr, qh in x["swa"]:
+                oracle.decode_swa_ring(qh, kr, vr, None, x["rp"], x["sl"], w.softmax_scale)
+
+        def tokens(rows):
+            fb = int(w.n_after[rows].sum()) if full else 0
+            return fb, int(np.minimum(w.n_after[rows], w.W).sum()) * len(swa)
+
+        t1, _ = repeat_for(lambda x=gather(order[:1]): run(x), 0.0)
+        per_tok = t1 / max(1, sum(tokens(order[:1])))
         rows, acc = [], 0.0
-        for b, e in zip(order, est):
-            if rows and acc + per_tok * e > budget_s:
+        for b in order:
+            e = per_tok * sum(tokens([b]))
+            if rows and acc + e > pass_s:
                 break
             rows.append(b)
-            acc += per_tok * e
-        t, fb, sb = run(rows)
+            acc += e
+        x = gather(rows)
+        t, reps = repeat_for(lambda: run(x), min_s)
+        fb, sb = tokens(rows)
         toks = fb + sb
         return {"value": toks * w.Hkv * w.D * 4 / t / 1e9, "unit": "GB/s",
                 "tokens_per_s": toks / t, "cores": oracle.max_threads(), "kind": "oracle",
                 "sample": f"{len(rows)} of {w.B} requests in {1 if full else 0} Full and "
                           f"{len(swa)} SWA layers ({fb} + {sb} attended tokens), fp64 oracle, "
-                          f"{t:.2f} s"}
+                          f"{t:.2f} s per pass, mean of {reps} passes"}
 
 
 class Int8Workload(Workload):
@@ -859,29 +877,37 @@ class Int8Workload(Workload):
                                    int8=self.i8, qtable=self.qt, qlens=self.ql_in,
                                    tokens_per_split=self.tps, out=self.out, workspace=self.ws)
 
-    def cpu_baseline(self):
+    def cpu_baseline(self, nrows=8, min_s=8.0):
+        """The oracle on the first nrows requests of step 0 (INT8 codes and
+        scales from the GPU quantiser, which the parity tests pin to the
+        oracle's), repeated for at least min_s seconds."""
         import oracle
         w = self.w
-        rows = [0]
+        rows = list(range(min(nrows, w.B)))
         n = self.n_walk[0]
         hk, bt = host_pages(self.k, w.block_table, rows, n)
         hv, _ = host_pages(self.v, w.block_table, rows, n)
-        nq = int(self.qlen0[0] // 32)
-        ids = self.qt[0, :nq].long()
+        nq = [int(self.qlen0[b] // 32) for b in rows]
+        ids = torch.cat([self.qt[b, :nq[i]].long() for i, b in enumerate(rows)])
+        qt = np.full((len(rows), max(nq)), -1, np.int32)
+        o = 0
+        for i, k in enumerate(nq):
+            qt[i, :k] = np.arange(o, o + k)
+            o += k
         i8 = dict(k_codes=self.i8.k.index_select(0, ids).cpu().numpy(),
                   v_codes=self.i8.v.index_select(0, ids).cpu().numpy(),
                   k_scale=self.i8.k_scale.index_select(0, ids).cpu().numpy(),
                   v_scale=self.i8.v_scale.index_select(0, ids).cpu().numpy(),
-                  qtable=np.arange(nq, dtype=np.int32)[None], qlens=self.qlen0[rows])
-        t0 = time.perf_counter()
-        oracle.decode_full_paged(synth.bits(self.q)[rows], hk, hv, bt, n[rows],
-                                 w.softmax_scale, int8=i8)
-        t = time.perf_counter() - t0
-        b = self.step_kernel_bytes(0) / w.B
-        return {"value": b / t / 1e9, "unit": "GB/s", "tokens_per_s": float(n[0]) / t,
+                  qtable=qt, qlens=self.qlen0[rows])
+        qh = synth.bits(self.q)[rows]
+        t, reps = repeat_for(lambda: oracle.decode_full_paged(qh, hk, hv, bt, n[rows],
+                                                              w.softmax_scale, int8=i8), min_s)
+        b = self.step_kernel_bytes(0) / w.B * len(rows)
+        toks = int(n[rows].sum())
+        return {"value": b / t / 1e9, "unit": "GB/s", "tokens_per_s": toks / t,
                 "cores": oracle.max_threads(), "kind": "oracle",
-                "sample": f"1 of {w.B} requests ({int(n[0])} tokens, INT8 + bf16 tail),"
-                          f" fp64 oracle, {t:.2f} s"}
+                "sample": f"{len(rows)} of {w.B} requests ({toks} tokens, INT8 + bf16 tail),"
+                          f" fp64 oracle, {t:.3f} s per call, mean of {reps} calls"}
 
 
 class SharedPrefixWorkload(Workload):
@@ -1000,21 +1026,24 @@ class SharedPrefixWorkload(Workload):
                                             out=self.out, tokens_per_split=self.tps,
                                             workspace=self.ws)
 
-    def cpu_baseline(self):
+    def cpu_baseline(self, nrows=4, min_s=8.0):
+        """The oracle on nrows requests of step 0 (the oracle reads every
+        request's prefix from its own gathered copy), repeated for at least
+        min_s seconds."""
         import oracle
         w = self.w
-        rows = [0]
+        rows = list(range(min(nrows, w.B)))
         n = w.n_pre + 1
         hk, bt = host_pages(self.k, w.block_table, rows, n)
         hv, _ = host_pages(self.v, w.block_table, rows, n)
-        t0 = time.perf_counter()
-        oracle.decode_full_paged(synth.bits(self.q)[rows], hk, hv, bt, n[rows], w.softmax_scale)
-        t = time.perf_counter() - t0
-        toks = int(n[0])
+        qh = synth.bits(self.q)[rows]
+        t, reps = repeat_for(lambda: oracle.decode_full_paged(qh, hk, hv, bt, n[rows],
+                                                              w.softmax_scale), min_s)
+        toks = int(n[rows].sum())
         return {"value": toks * w.Hkv * w.D * 4 / t / 1e9, "unit": "GB/s",
                 "tokens_per_s": toks / t, "cores": oracle.max_threads(), "kind": "oracle",
-                "sample": f"1 of {w.B} requests of one step ({toks} tokens), fp64 oracle, "
-                          f"{t:.2f} s"}
+                "sample": f"{len(rows)} of {w.B} requests of one step ({toks} tokens), fp64 "
+                          f"oracle, {t:.3f} s per call, mean of {reps} calls"}
 
 
 def make_workload(config, device, args):
