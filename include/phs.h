@@ -424,6 +424,8 @@ int phs_copy_d2d(void *dst, const void *src, size_t bytes, void *stream);
  * blocks. */
 typedef struct phs_page_allocator phs_page_allocator;
 phs_page_allocator *phs_page_allocator_create(int64_t num_pages); /* NULL on bad size */
+/* Releases the caller's handle; a radix tree created on the allocator keeps
+ * it alive (the object is freed when the last tree using it is destroyed). */
 void phs_page_allocator_destroy(phs_page_allocator *a);
 /* n fresh pages with count 1 into out_pages (host); PHS_ENOSPACE if fewer free. */
 int phs_page_alloc(phs_page_allocator *a, int32_t n, int32_t *out_pages);
@@ -448,11 +450,18 @@ int phs_copy_pages(const phs_paged_pool *pool, const int32_t *src_pages,
 
 /* Radix prefix tree over whole pages.
  * Source: "Kimi K3 context caching" page, sections 1 and 3 (global radix
- * tree, longest-prefix match, insert of newly computed blocks).  Only whole
- * pages are cached and shared.  The tree holds one reference on each page
- * it caches. */
+ * tree, longest-prefix match, insert of newly computed blocks) and "Xiaomi
+ * MiMo-V2.5 inference system" page, section 2 (prefix-tree rebuild: each
+ * node carries the Full segment index and the SWA mapping).  Only whole
+ * pages are cached and shared.  The tree holds one reference on each Full
+ * page it caches (in `alloc`) and on each SWA segment page it maps (in
+ * `swa_alloc`, may be NULL when no SWA KV is cached; must differ from
+ * `alloc`).  An SWA segment page is a 16-token snapshot of the SWA-layer KV
+ * of one cached page (see phs_swa_ring_save); its id means the same page
+ * in every SWA layer's segment pool. */
 typedef struct phs_radix_tree phs_radix_tree;
-phs_radix_tree *phs_radix_create(phs_page_allocator *alloc, int32_t page_size);
+phs_radix_tree *phs_radix_create(phs_page_allocator *alloc, phs_page_allocator *swa_alloc,
+                                 int32_t page_size);
 void phs_radix_destroy(phs_radix_tree *t); /* drops the tree's page references */
 /* Longest cached whole-page prefix of tokens[0..n): its page ids go to
  * out_pages (capacity max_pages, else PHS_ESHAPE), their number to
@@ -464,20 +473,32 @@ int phs_radix_match(phs_radix_tree *t, const int32_t *tokens, int64_t n, int32_t
 /* Same, cut back to the window-safe length of a hybrid stack.  Source:
  * "Xiaomi MiMo-V2.5 inference system" page, section 2 (prefix tree
  * rebuild): a match is valid only where at least the last W tokens still
- * have valid SWA slots.  Here: the longest page-aligned L <= match with
- * every token of [max(0, L - window), L) marked SWA-valid at insert. */
+ * have valid SWA slots.  Here: the longest page-aligned L <= match whose
+ * last min(L, window) tokens all lie in pages that map an SWA segment page
+ * (window a multiple of page_size, else PHS_EUNSUPPORTED).  Returns the
+ * L / page_size Full pages as phs_radix_match does, and in out_swa_pages
+ * (capacity max_swa_pages, else PHS_ESHAPE) the segment pages of that last
+ * window, in token order: min(L, window) / page_size of them, the first
+ * holding tokens [L - min(L, window), ... + page_size).  Each returned
+ * segment page gets one more reference in swa_alloc (the caller's: release
+ * it with phs_page_decref once phs_swa_ring_seed has copied it). */
 int phs_radix_match_window_safe(phs_radix_tree *t, const int32_t *tokens, int64_t n,
                                 int32_t window, int32_t *out_pages, int32_t max_pages,
-                                int32_t *out_num_pages);
+                                int32_t *out_num_pages, int32_t *out_swa_pages,
+                                int32_t max_swa_pages, int32_t *out_num_swa_pages);
 /* Cache the whole pages of tokens[0..n) with page ids pages[0..n/page_size).
  * Positions already cached keep the tree's pages (the caller's ids for them
- * are not referenced); new pages get a tree reference.  Token positions >=
- * swa_from are marked SWA-valid (their SWA KV is kept with the sequence,
- * e.g. n - W for a finished request; n for none). */
+ * are not referenced); new pages get a tree reference.  swa_pages (host,
+ * [n/page_size], may be NULL = none) gives, per page, the SWA segment page
+ * holding that page's SWA-layer KV, or -1; a cached page that has none
+ * takes the caller's (with a tree reference in swa_alloc), one that has one
+ * keeps it.  A finished request typically saves the pages of its last
+ * window (phs_swa_ring_save) and passes their segment ids here. */
 int phs_radix_insert(phs_radix_tree *t, const int32_t *tokens, int64_t n, const int32_t *pages,
-                     int64_t swa_from);
-/* Evict least-recently-used leaves whose pages only the tree references
- * until at least `pages` pages were freed or none is evictable. */
+                     const int32_t *swa_pages);
+/* Evict least-recently-used leaves whose pages (Full and SWA segment) only
+ * the tree references until at least `pages` Full pages were freed or none
+ * is evictable; their SWA segment pages are released too. */
 int phs_radix_evict(phs_radix_tree *t, int64_t pages, int64_t *out_freed);
 int64_t phs_radix_cached_pages(phs_radix_tree *t);
 /* Window-safe length as a plain function: the largest L <= match_len, L a
@@ -485,6 +506,42 @@ int64_t phs_radix_cached_pages(phs_radix_tree *t);
  * [max(0, L - window), L); 0 if none. */
 int64_t phs_window_safe_len(const uint8_t *swa_valid, int64_t match_len, int32_t window,
                             int32_t align);
+
+/* ------------------------------------------------------------------------
+ * SWA segment pages: snapshots of ring contents by whole pages, so that a
+ * cached prefix can seed a new request's ring.
+ * Source: "Xiaomi MiMo-V2.5 inference system" page, section 2 (dual pools:
+ * the SWA pool keeps only each request's last W tokens; a prefix-cache hit
+ * is usable only at a window-safe length, and the node's SWA mapping says
+ * where that window's SWA KV is).
+ * rings / segs: host arrays of num_layers descriptors, one per SWA layer
+ * (same window, Hkv and head_dim throughout); segs[l] is a segment pool in
+ * the Full-pool layout [num_seg_pages][Hkv][16][D] bf16.  A segment page id
+ * names the same page in every layer.  Token t of a request of length n
+ * sits at ring slot (ring_pos - (n - 1 - t)) mod W, as for decode.
+ *
+ * phs_swa_ring_save: for each entry i < count (device int32 arrays), copies
+ * tokens [16 * page_index[i], 16 * page_index[i] + 16) of the request whose
+ * ring is ring_ids[i], newest slot ring_pos[i], length seq_lens[i], into
+ * segment page seg_pages[i], in every layer.  The page must lie inside the
+ * ring's window [n - min(n, W), n), else PHS_ERANGE (entry skipped).
+ *
+ * phs_swa_ring_seed: for each request b < batch, writes the last
+ * min(n, W) tokens (n = seq_lens[b]) into ring ring_ids[b] (NULL =
+ * identity) so that its newest token sits at slot ring_pos[b]; token t is
+ * read from segment page seg_table[b][t / 16 - first] (device int32
+ * [batch][max_seg_pages]), first = (n - min(n, W)) / 16, at slot t % 16.
+ * Out-of-range ids record PHS_ERANGE and skip the token.  After seeding, a
+ * decode step appends token n at slot (ring_pos[b] + 1) mod W.
+ * ---------------------------------------------------------------------- */
+int phs_swa_ring_save(const phs_ring_pool *rings, const phs_paged_pool *segs, int32_t num_layers,
+                      const int32_t *ring_ids, const int32_t *ring_pos, const int32_t *seq_lens,
+                      const int32_t *page_index, const int32_t *seg_pages, int32_t count,
+                      int32_t *dev_status, void *stream);
+int phs_swa_ring_seed(const phs_ring_pool *rings, const phs_paged_pool *segs, int32_t num_layers,
+                      const int32_t *ring_ids, const int32_t *ring_pos, const int32_t *seq_lens,
+                      const int32_t *seg_table, int32_t max_seg_pages, int32_t batch,
+                      int32_t *dev_status, void *stream);
 
 const char *phs_status_str(int status);
 int32_t phs_version(void);

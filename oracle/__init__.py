@@ -33,19 +33,19 @@ _lib = None
 ORC_OK, ORC_EINVAL, ORC_ERANGE, ORC_ESHARED = 0, -1, -3, -4
 
 
-def build(force: bool = False, mutant: int = 0, out: str | None = None) -> str:
+def build(force: bool = False, src: str | None = None, out: str | None = None) -> str:
     """Compile the oracle with gcc (-O2 -fopenmp); returns the .so path.
-    mutant > 0 builds a planted-mistake variant (for the pin tests only)
-    at `out`."""
+    `src` / `out` build another copy of the source (the pin tests compile
+    planted-mistake copies of it this way)."""
     so = out or _SO
+    source = src or _SRC
     os.makedirs(os.path.dirname(so), exist_ok=True)
-    if (not force and mutant == 0 and os.path.exists(so)
+    if (not force and src is None and os.path.exists(so)
             and os.path.getmtime(so) >= os.path.getmtime(_SRC)):
         return so
     tmp = so + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
-           "-fno-fast-math", "-ffp-contract=off", f"-DORC_MUTANT={int(mutant)}", "-o", tmp,
-           _SRC, "-lm"]
+           "-fno-fast-math", "-ffp-contract=off", "-o", tmp, source, "-lm"]
     subprocess.check_call(cmd)
     os.replace(tmp, so)
     return so
@@ -76,6 +76,12 @@ def _load():
             lib.phs_oracle_decode_swa_ring.restype = I
             lib.phs_oracle_kv_tokens_stored.argtypes = [P, I, P, I, I]
             lib.phs_oracle_kv_tokens_stored.restype = L
+            lib.phs_oracle_swa_ring_save.argtypes = [P, P, L, I, I, I, P, P, L, I, P, P, P, P,
+                                                     P, I]
+            lib.phs_oracle_swa_ring_save.restype = I
+            lib.phs_oracle_swa_ring_seed.argtypes = [P, P, L, I, I, I, P, P, L, I, P, P, P, P,
+                                                     I, I]
+            lib.phs_oracle_swa_ring_seed.restype = I
             _lib = lib
     return _lib
 
@@ -176,6 +182,31 @@ def decode_swa_ring(q, k_ring, v_ring, ring_ids, ring_pos, seq_lens, scale, rows
         _ptr(rp), _ptr(sl), float(scale), _ptr(rws), 0 if rws is None else rws.shape[0],
         _ptr(out))
     return out, st
+
+
+def swa_ring_save(k_ring, v_ring, k_seg, v_seg, ring_ids, ring_pos, seq_lens, page_index,
+                  seg_pages):
+    """Copy whole pages of requests' SWA windows from the rings (uint16
+    [num_rings, Hkv, W, D]) into segment pages (uint16 [num_seg, Hkv, P, D],
+    in place).  Returns the oracle status."""
+    num_rings, Hkv, W, D = k_ring.shape
+    num_seg, _, P, _ = k_seg.shape
+    a = [_c(x, np.int32) for x in (ring_ids, ring_pos, seq_lens, page_index, seg_pages)]
+    return _load().phs_oracle_swa_ring_save(
+        _ptr(k_ring), _ptr(v_ring), num_rings, W, Hkv, D, _ptr(k_seg), _ptr(v_seg), num_seg, P,
+        *[_ptr(x) for x in a], a[0].shape[0])
+
+
+def swa_ring_seed(k_ring, v_ring, k_seg, v_seg, ring_ids, ring_pos, seq_lens, seg_table):
+    """Write each request's last min(n, W) tokens from its segment pages
+    (seg_table [B, max_seg]) into its ring (in place)."""
+    num_rings, Hkv, W, D = k_ring.shape
+    num_seg, _, P, _ = k_seg.shape
+    ri = _c(ring_ids, np.int32)
+    rp, sl, st = _c(ring_pos, np.int32), _c(seq_lens, np.int32), _c(seg_table, np.int32)
+    return _load().phs_oracle_swa_ring_seed(
+        _ptr(k_ring), _ptr(v_ring), num_rings, W, Hkv, D, _ptr(k_seg), _ptr(v_seg), num_seg, P,
+        _ptr(ri), _ptr(rp), _ptr(sl), _ptr(st), st.shape[1], sl.shape[0])
 
 
 def kv_tokens_stored(layer_is_full, seq_lens, W):

@@ -54,13 +54,6 @@
 #include <omp.h>
 #endif
 
-/* Planted-mistake builds for the pin tests (ORC_MUTANT = 1..10): each turns
- * on exactly one plausible bug, and the pin suite must catch every one.  The
- * normal build is ORC_MUTANT = 0 and contains none of them. */
-#ifndef ORC_MUTANT
-#define ORC_MUTANT 0
-#endif
-
 #define ORC_OK 0
 #define ORC_EINVAL -1
 #define ORC_ERANGE -3
@@ -107,7 +100,7 @@ int phs_oracle_append_paged(uint16_t *k_pool, uint16_t *v_pool, int64_t num_page
     for (int b = 0; b < B; ++b) {
         int64_t n = seq_lens[b];
         if (n < 1) continue; /* nothing appended for an empty request */
-        int64_t t = ORC_MUTANT == 6 ? n : n - 1;
+        int64_t t = n - 1; /* the new token's position */
         int64_t lp = t / P;
         if (lp >= max_pages) { status = ORC_ERANGE; continue; }
         int64_t page = block_table[(int64_t)b * max_pages + lp];
@@ -116,8 +109,7 @@ int phs_oracle_append_paged(uint16_t *k_pool, uint16_t *v_pool, int64_t num_page
         int64_t slot = t % P;
         for (int h = 0; h < Hkv; ++h) {
             for (int d = 0; d < D; ++d) {
-                int64_t dst = ORC_MUTANT == 8 ? ((page * P + slot) * Hkv + h) * D + d
-                                              : ((page * Hkv + h) * P + slot) * D + d;
+                int64_t dst = ((page * Hkv + h) * P + slot) * D + d;
                 int64_t src = ((int64_t)b * Hkv + h) * D + d;
                 k_pool[dst] = k_new[src];
                 v_pool[dst] = v_new[src];
@@ -166,11 +158,11 @@ int phs_oracle_append_ring(uint16_t *k_ring, uint16_t *v_ring, int64_t num_rings
  * [num_qpages][Hkv] fp32, through dst_qtable[b][j] for 32-token block j.
  * Blocks j in [first_qblock[b], first_qblock[b] + num_qblocks[b]).
  * ---------------------------------------------------------------------- */
-static float quant_scale(float absmax) { return absmax / (ORC_MUTANT == 10 ? 128.0f : 127.0f); }
+static float quant_scale(float absmax) { return absmax / 127.0f; }
 
 static int8_t quant_code(float x, float s) {
     if (s == 0.0f) return 0;
-    float r = ORC_MUTANT == 5 ? roundf(x / s) : rintf(x / s);
+    float r = rintf(x / s);
     if (r > 127.0f) r = 127.0f;
     if (r < -127.0f) r = -127.0f;
     return (int8_t)r;
@@ -248,7 +240,7 @@ static void attend_one(const double *q, int D, int64_t t0, int64_t t1, double sc
         get_row(ctx, t, 0, row);
         double acc = 0.0;
         for (int d = 0; d < D; ++d) acc += q[d] * row[d];
-        s[t - t0] = ORC_MUTANT == 3 ? acc : acc * scale;
+        s[t - t0] = acc * scale;
         if (s[t - t0] > m) m = s[t - t0];
     }
     double l = 0.0;
@@ -258,8 +250,7 @@ static void attend_one(const double *q, int D, int64_t t0, int64_t t1, double sc
         get_row(ctx, t, 1, row);
         for (int d = 0; d < D; ++d) out[d] += p * row[d];
     }
-    if (ORC_MUTANT != 9)
-        for (int d = 0; d < D; ++d) out[d] /= l;
+    for (int d = 0; d < D; ++d) out[d] /= l;
     free(s);
 }
 
@@ -292,7 +283,7 @@ static void full_row(const void *vctx, int64_t t, int is_v, double *row) {
             return;
         }
         const int8_t *codes = is_v ? c->v_codes : c->k_codes;
-        float s = ((is_v != (ORC_MUTANT == 7)) ? c->v_scale : c->k_scale)[qp * c->Hkv + c->h];
+        float s = (is_v ? c->v_scale : c->k_scale)[qp * c->Hkv + c->h];
         const int8_t *r = codes + ((qp * c->Hkv + c->h) * 32 + t % 32) * c->D;
         for (int d = 0; d < c->D; ++d) row[d] = (double)((float)r[d] * s);
         return;
@@ -305,8 +296,7 @@ static void full_row(const void *vctx, int64_t t, int is_v, double *row) {
         return;
     }
     const uint16_t *pool = is_v ? c->v_pool : c->k_pool;
-    const uint16_t *r = pool + (ORC_MUTANT == 8 ? ((page * c->P + t % c->P) * c->Hkv + c->h)
-                                                : ((page * c->Hkv + c->h) * c->P + t % c->P)) * c->D;
+    const uint16_t *r = pool + ((page * c->Hkv + c->h) * c->P + t % c->P) * c->D;
     for (int d = 0; d < c->D; ++d) row[d] = bf16_to_double(r[d]);
 }
 
@@ -332,7 +322,7 @@ int phs_oracle_decode_full_paged(const uint16_t *q, int B, int Hq, int Hkv, int 
     for (int64_t w = 0; w < (int64_t)nsel * Hq; ++w) {
         int b = rows ? rows[w / Hq] : (int)(w / Hq);
         int i = (int)(w % Hq);
-        int h = ORC_MUTANT == 1 ? i % Hkv : i / G;
+        int h = i / G;
         int local_bad = 0;
         full_ctx c = {k_pool, v_pool, num_pages, P, Hkv, D,
                       block_table + (int64_t)b * max_pages, max_pages,
@@ -357,8 +347,7 @@ typedef struct {
 
 static void ring_row(const void *vctx, int64_t t, int is_v, double *row) {
     const ring_ctx *c = (const ring_ctx *)vctx;
-    int64_t slot = ORC_MUTANT == 4 ? pos_mod(c->newest_slot + (c->n - 1 - t), c->W)
-                                   : pos_mod(c->newest_slot - (c->n - 1 - t), c->W);
+    int64_t slot = pos_mod(c->newest_slot - (c->n - 1 - t), c->W);
     const uint16_t *base = is_v ? c->v_ring : c->k_ring;
     const uint16_t *r = base + ((c->ring * c->Hkv + c->h) * c->W + slot) * c->D;
     for (int d = 0; d < c->D; ++d) row[d] = bf16_to_double(r[d]);
@@ -388,14 +377,95 @@ int phs_oracle_decode_swa_ring(const uint16_t *q, int B, int Hq, int Hkv, int D,
             bad = 1;
             continue;
         }
-        ring_ctx c = {k_ring, v_ring, r, W, Hkv, D, ORC_MUTANT == 1 ? i % Hkv : i / G,
-                      ring_pos[b], n};
+        ring_ctx c = {k_ring, v_ring, r, W, Hkv, D, i / G, ring_pos[b], n};
         double qd[256];
         for (int d = 0; d < D; ++d) qd[d] = bf16_to_double(q[((int64_t)b * Hq + i) * D + d]);
-        int64_t t0 = n > W ? n - W + (ORC_MUTANT == 2) : 0;
+        int64_t t0 = n > W ? n - W : 0;
         attend_one(qd, D, t0, n, scale, ring_row, &c, out + ((int64_t)b * Hq + i) * D);
     }
     return bad ? ORC_ERANGE : ORC_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * SWA segment pages (MiMo page, section 2: a prefix-cache hit of a hybrid
+ * stack is usable only at a window-safe length, and the tree's SWA mapping
+ * says where that window's SWA KV lives).  A segment page holds the
+ * SWA-layer KV of P consecutive tokens, layout [num_seg][Hkv][P][D] bf16.
+ * In a ring of W slots, token t of a request of length n sits at slot
+ * (ring_pos - (n - 1 - t)) mod W (as for decode).
+ *
+ * save: entry i copies tokens [P * page_index[i], P * page_index[i] + P) of
+ * the request whose ring is ring_ids[i] (newest slot ring_pos[i], length
+ * seq_lens[i]) into segment page seg_pages[i].  Every one of those tokens
+ * must be in the ring's window [n - min(n, W), n) (else ORC_ERANGE, entry
+ * skipped).
+ * ---------------------------------------------------------------------- */
+int phs_oracle_swa_ring_save(const uint16_t *k_ring, const uint16_t *v_ring, int64_t num_rings,
+                             int W, int Hkv, int D, uint16_t *k_seg, uint16_t *v_seg,
+                             int64_t num_seg, int P, const int32_t *ring_ids,
+                             const int32_t *ring_pos, const int32_t *seq_lens,
+                             const int32_t *page_index, const int32_t *seg_pages, int count) {
+    int status = ORC_OK;
+    for (int i = 0; i < count; ++i) {
+        int64_t r = ring_ids[i], pos = ring_pos[i], n = seq_lens[i], sp = seg_pages[i];
+        int64_t first = (int64_t)page_index[i] * P;
+        int64_t lo = n - (n < W ? n : W);
+        if (r < 0 || r >= num_rings || pos < 0 || pos >= W || sp < 0 || sp >= num_seg ||
+            page_index[i] < 0 || first < lo || first + P > n) {
+            status = ORC_ERANGE;
+            continue;
+        }
+        for (int64_t t = first; t < first + P; ++t) {
+            int64_t slot = pos_mod(pos - (n - 1 - t), W);
+            for (int h = 0; h < Hkv; ++h)
+                for (int d = 0; d < D; ++d) {
+                    int64_t src = ((r * Hkv + h) * W + slot) * D + d;
+                    int64_t dst = ((sp * Hkv + h) * P + t % P) * D + d;
+                    k_seg[dst] = k_ring[src];
+                    v_seg[dst] = v_ring[src];
+                }
+        }
+    }
+    return status;
+}
+
+/* seed: request b (length n = seq_lens[b], ring ring_ids[b] or b when
+ * ring_ids is NULL, newest slot ring_pos[b]) gets the last min(n, W) tokens
+ * written into its ring; token t is read from segment page
+ * seg_table[b][t / P - first] at slot t % P, first = (n - min(n, W)) / P.
+ * A token whose page id is missing or out of range is skipped (ORC_ERANGE). */
+int phs_oracle_swa_ring_seed(uint16_t *k_ring, uint16_t *v_ring, int64_t num_rings, int W,
+                             int Hkv, int D, const uint16_t *k_seg, const uint16_t *v_seg,
+                             int64_t num_seg, int P, const int32_t *ring_ids,
+                             const int32_t *ring_pos, const int32_t *seq_lens,
+                             const int32_t *seg_table, int max_seg, int B) {
+    int status = ORC_OK;
+    for (int b = 0; b < B; ++b) {
+        int64_t r = ring_ids ? ring_ids[b] : b, pos = ring_pos[b], n = seq_lens[b];
+        if (r < 0 || r >= num_rings || pos < 0 || pos >= W || n < 0) {
+            status = ORC_ERANGE;
+            continue;
+        }
+        int64_t lo = n - (n < W ? n : W);
+        int64_t first = lo / P;
+        for (int64_t t = lo; t < n; ++t) {
+            int64_t j = t / P - first;
+            int64_t sp = j < max_seg ? seg_table[(int64_t)b * max_seg + j] : -1;
+            if (sp < 0 || sp >= num_seg) {
+                status = ORC_ERANGE;
+                continue;
+            }
+            int64_t slot = pos_mod(pos - (n - 1 - t), W); /* seed: ring slot of token t */
+            for (int h = 0; h < Hkv; ++h)
+                for (int d = 0; d < D; ++d) {
+                    int64_t src = ((sp * Hkv + h) * P + t % P) * D + d;
+                    int64_t dst = ((r * Hkv + h) * W + slot) * D + d;
+                    k_ring[dst] = k_seg[src];
+                    v_ring[dst] = v_seg[src];
+                }
+        }
+    }
+    return status;
 }
 
 /* ------------------------------------------------------------------------

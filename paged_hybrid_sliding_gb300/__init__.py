@@ -28,7 +28,7 @@ __all__ = [
     "attn_decode_swa_ring", "attn_decode_hybrid_stack", "hybrid_stack_workspace_bytes",
     "attn_decode_hybrid_stack_fused", "hybrid_stack_fused_workspace_bytes",
     "hybrid_kv_tokens", "copy_d2d", "copy_pages", "PageAllocator", "RadixTree",
-    "window_safe_len", "lib", "PAGE", "QBLOCK",
+    "window_safe_len", "swa_ring_save", "swa_ring_seed", "lib", "PAGE", "QBLOCK",
 ]
 
 PAGE = 16
@@ -562,12 +562,16 @@ class PageAllocator:
 
 
 class RadixTree:
-    """Radix prefix tree over whole pages, holding references in `alloc`."""
+    """Radix prefix tree over whole pages, holding references in `alloc`
+    (Full pages) and `swa_alloc` (SWA segment pages, optional)."""
 
-    def __init__(self, alloc: PageAllocator, page_size: int = PAGE):
+    def __init__(self, alloc: PageAllocator, page_size: int = PAGE,
+                 swa_alloc: PageAllocator | None = None):
         self.alloc = alloc
+        self.swa_alloc = swa_alloc
         self.page_size = int(page_size)
-        self._h = lib().phs_radix_create(alloc._h, self.page_size)
+        self._h = lib().phs_radix_create(alloc._h, None if swa_alloc is None else swa_alloc._h,
+                                         self.page_size)
         if not self._h:
             raise ValueError("bad radix tree arguments")
 
@@ -582,34 +586,41 @@ class RadixTree:
         except Exception:
             pass
 
-    def _match(self, tokens, window=None):
+    def match(self, tokens):
+        """Matched page ids (each gets a reference for the caller)."""
         import numpy as np
         t = _i32(tokens)
         cap = t.shape[0] // self.page_size + 1
         out = np.empty(cap, dtype=np.int32)
         n = ctypes.c_int32()
-        if window is None:
-            st = lib().phs_radix_match(self._h, t.ctypes.data, t.shape[0], out.ctypes.data, cap,
-                                       ctypes.byref(n))
-        else:
-            st = lib().phs_radix_match_window_safe(self._h, t.ctypes.data, t.shape[0],
-                                                   int(window), out.ctypes.data, cap,
-                                                   ctypes.byref(n))
-        _check(st, "radix_match")
+        _check(lib().phs_radix_match(self._h, t.ctypes.data, t.shape[0], out.ctypes.data, cap,
+                                     ctypes.byref(n)), "radix_match")
         return out[:n.value].copy()
 
-    def match(self, tokens):
-        """Matched page ids (each gets a reference for the caller)."""
-        return self._match(tokens)
-
     def match_window_safe(self, tokens, window: int):
-        return self._match(tokens, window)
+        """(Full pages, SWA segment pages of the last window) of the longest
+        window-safe match; each id gets a reference for the caller."""
+        import numpy as np
+        t = _i32(tokens)
+        cap = t.shape[0] // self.page_size + 1
+        out = np.empty(cap, dtype=np.int32)
+        seg = np.empty(cap, dtype=np.int32)
+        n, ns = ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().phs_radix_match_window_safe(self._h, t.ctypes.data, t.shape[0], int(window),
+                                                 out.ctypes.data, cap, ctypes.byref(n),
+                                                 seg.ctypes.data, cap, ctypes.byref(ns)),
+               "radix_match_window_safe")
+        return out[:n.value].copy(), seg[:ns.value].copy()
 
-    def insert(self, tokens, pages, swa_from=None):
+    def insert(self, tokens, pages, swa_pages=None):
+        """Cache the whole pages of `tokens`; swa_pages: per page, the SWA
+        segment page holding its SWA-layer KV, or -1 (None: none)."""
         t, p = _i32(tokens), _i32(pages)
-        sf = t.shape[0] if swa_from is None else int(swa_from)
-        _check(lib().phs_radix_insert(self._h, t.ctypes.data, t.shape[0], p.ctypes.data, sf),
-               "radix_insert")
+        s = None if swa_pages is None else _i32(swa_pages)
+        if s is not None and s.shape[0] < t.shape[0] // self.page_size:
+            raise ValueError("swa_pages needs one entry per whole page")
+        _check(lib().phs_radix_insert(self._h, t.ctypes.data, t.shape[0], p.ctypes.data,
+                                      None if s is None else s.ctypes.data), "radix_insert")
 
     def evict(self, pages: int) -> int:
         freed = ctypes.c_int64()
@@ -618,6 +629,49 @@ class RadixTree:
 
     def cached_pages(self) -> int:
         return int(lib().phs_radix_cached_pages(self._h))
+
+
+def _pool_array(ctype, pools):
+    return (ctype * len(pools))(*[p.c() for p in pools])
+
+
+def swa_ring_save(rings, segs, ring_ids, ring_pos, seq_lens, page_index, seg_pages, status=None,
+                  stream=None):
+    """Snapshot whole pages of requests' SWA windows into segment pages, in
+    every SWA layer: entry i copies logical page page_index[i] of the
+    request with ring ring_ids[i] (newest slot ring_pos[i], length
+    seq_lens[i]) into segment page seg_pages[i].  rings: list of RingPool,
+    segs: list of PagedPool (one per SWA layer)."""
+    if len(rings) != len(segs) or not rings:
+        raise ValueError("one segment pool per ring pool")
+    for name, t in (("ring_ids", ring_ids), ("ring_pos", ring_pos), ("seq_lens", seq_lens),
+                    ("page_index", page_index), ("seg_pages", seg_pages)):
+        _need(t, torch.int32, name, 1)
+    _opt(status, torch.int32, "status")
+    _check(lib().phs_swa_ring_save(_pool_array(_lib.RingPoolC, rings),
+                                   _pool_array(_lib.PagedPoolC, segs), len(rings),
+                                   _ptr(ring_ids), _ptr(ring_pos), _ptr(seq_lens),
+                                   _ptr(page_index), _ptr(seg_pages), page_index.shape[0],
+                                   _ptr(status), _stream(stream)), "swa_ring_save")
+
+
+def swa_ring_seed(rings, segs, ring_pos, seq_lens, seg_table, ring_ids=None, status=None,
+                  stream=None):
+    """Fill each request's ring, in every SWA layer, with the last
+    min(n, W) tokens from the segment pages of its row of seg_table
+    ([B, max_seg] int32), newest token at slot ring_pos[b]."""
+    if len(rings) != len(segs) or not rings:
+        raise ValueError("one segment pool per ring pool")
+    _need(ring_pos, torch.int32, "ring_pos", 1)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(seg_table, torch.int32, "seg_table", 2)
+    _opt(ring_ids, torch.int32, "ring_ids", 1)
+    _opt(status, torch.int32, "status")
+    _check(lib().phs_swa_ring_seed(_pool_array(_lib.RingPoolC, rings),
+                                   _pool_array(_lib.PagedPoolC, segs), len(rings),
+                                   _ptr(ring_ids), _ptr(ring_pos), _ptr(seq_lens),
+                                   _ptr(seg_table), seg_table.shape[1], seq_lens.shape[0],
+                                   _ptr(status), _stream(stream)), "swa_ring_seed")
 
 
 def window_safe_len(swa_valid, match_len: int, window: int, align: int = 1) -> int:

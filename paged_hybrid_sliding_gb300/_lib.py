@@ -90,14 +90,19 @@ _SIGS = {
     "phs_page_free_count": (c_i64, [c_vp]),
     "phs_page_refcounts": (ctypes.c_int, [c_vp, c_vp]),
     "phs_page_cow": (ctypes.c_int, [c_vp, c_i32, P_i32]),
-    "phs_radix_create": (c_vp, [c_vp, c_i32]),
+    "phs_radix_create": (c_vp, [c_vp, c_vp, c_i32]),
     "phs_radix_destroy": (None, [c_vp]),
     "phs_radix_match": (ctypes.c_int, [c_vp, c_vp, c_i64, c_vp, c_i32, P_i32]),
-    "phs_radix_match_window_safe": (ctypes.c_int, [c_vp, c_vp, c_i64, c_i32, c_vp, c_i32, P_i32]),
-    "phs_radix_insert": (ctypes.c_int, [c_vp, c_vp, c_i64, c_vp, c_i64]),
+    "phs_radix_match_window_safe": (ctypes.c_int, [c_vp, c_vp, c_i64, c_i32, c_vp, c_i32, P_i32,
+                                                   c_vp, c_i32, P_i32]),
+    "phs_radix_insert": (ctypes.c_int, [c_vp, c_vp, c_i64, c_vp, c_vp]),
     "phs_radix_evict": (ctypes.c_int, [c_vp, c_i64, P_i64]),
     "phs_radix_cached_pages": (c_i64, [c_vp]),
     "phs_window_safe_len": (c_i64, [c_vp, c_i64, c_i32, c_i32]),
+    "phs_swa_ring_save": (ctypes.c_int, [_P(RingPoolC), _P(PagedPoolC), c_i32, c_vp, c_vp, c_vp,
+                                         c_vp, c_vp, c_i32, c_vp, c_vp]),
+    "phs_swa_ring_seed": (ctypes.c_int, [_P(RingPoolC), _P(PagedPoolC), c_i32, c_vp, c_vp, c_vp,
+                                         c_vp, c_i32, c_i32, c_vp, c_vp]),
 }
 
 # every symbol include/phs.h declares

@@ -1085,6 +1085,88 @@ int phs_copy_pages(const phs_paged_pool* pool, const int32_t* src_pages, const i
                            page_bytes, dev_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+namespace phs {
+namespace {
+
+// Shared checks and launch of the SWA segment save / seed calls.
+int swa_segment_call(const phs_ring_pool* rings, const phs_paged_pool* segs, int32_t num_layers,
+                     SegCopyParams<kSegMaxLayers>& p, int count, cudaStream_t s) {
+  if (!rings || !segs || num_layers <= 0) return PHS_EINVAL;
+  int st;
+  for (int l = 0; l < num_layers; ++l) {
+    if ((st = check_ring(&rings[l]))) return st;
+    if ((st = check_paged(&segs[l]))) return st;
+    if (rings[l].window != rings[0].window || rings[l].num_kv_heads != rings[0].num_kv_heads ||
+        rings[l].head_dim != rings[0].head_dim || segs[l].num_kv_heads != rings[0].num_kv_heads ||
+        segs[l].head_dim != rings[0].head_dim)
+      return PHS_ESHAPE;
+  }
+  if (count == 0) return PHS_OK;
+  p.Hkv = rings[0].num_kv_heads;
+  p.D = rings[0].head_dim;
+  p.W = rings[0].window;
+  for (int l0 = 0; l0 < num_layers; l0 += kSegMaxLayers) {
+    p.num_layers = std::min(kSegMaxLayers, num_layers - l0);
+    for (int k = 0; k < p.num_layers; ++k) {
+      const phs_ring_pool& R = rings[l0 + k];
+      const phs_paged_pool& S = segs[l0 + k];
+      p.layer[k] = SegCopyLayer{R.k, R.v, S.k, S.v, R.num_rings, S.num_pages};
+    }
+    if ((st = launch_swa_segment<kSegMaxLayers>(p, count, s))) return st;
+  }
+  return PHS_OK;
+}
+
+}  // namespace
+}  // namespace phs
+
+extern "C" {
+
+int phs_swa_ring_save(const phs_ring_pool* rings, const phs_paged_pool* segs, int32_t num_layers,
+                      const int32_t* ring_ids, const int32_t* ring_pos, const int32_t* seq_lens,
+                      const int32_t* page_index, const int32_t* seg_pages, int32_t count,
+                      int32_t* dev_status, void* stream) {
+  if (count < 0 || (count > 0 && (!ring_ids || !ring_pos || !seq_lens || !page_index ||
+                                   !seg_pages)))
+    return PHS_EINVAL;
+  SegCopyParams<kSegMaxLayers>* p = new SegCopyParams<kSegMaxLayers>();
+  std::memset(p, 0, sizeof(*p));
+  p->ring_ids = ring_ids;
+  p->ring_pos = ring_pos;
+  p->seq_lens = seq_lens;
+  p->page_index = page_index;
+  p->seg_pages = seg_pages;
+  p->status = dev_status;
+  p->save = 1;
+  const int st = swa_segment_call(rings, segs, num_layers, *p, count,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  delete p;
+  return st;
+}
+
+int phs_swa_ring_seed(const phs_ring_pool* rings, const phs_paged_pool* segs, int32_t num_layers,
+                      const int32_t* ring_ids, const int32_t* ring_pos, const int32_t* seq_lens,
+                      const int32_t* seg_table, int32_t max_seg_pages, int32_t batch,
+                      int32_t* dev_status, void* stream) {
+  if (batch < 0 || (batch > 0 && (!ring_pos || !seq_lens || !seg_table || max_seg_pages <= 0)))
+    return PHS_EINVAL;
+  SegCopyParams<kSegMaxLayers>* p = new SegCopyParams<kSegMaxLayers>();
+  std::memset(p, 0, sizeof(*p));
+  p->ring_ids = ring_ids;
+  p->ring_pos = ring_pos;
+  p->seq_lens = seq_lens;
+  p->seg_table = seg_table;
+  p->max_seg = max_seg_pages;
+  p->status = dev_status;
+  p->save = 0;
+  const int st = swa_segment_call(rings, segs, num_layers, *p, batch,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  delete p;
+  return st;
+}
+
 int phs_copy_d2d(void* dst, const void* src, size_t bytes, void* stream) {
   if (!dst || !src) return PHS_EINVAL;
   if (!aligned16(dst) || !aligned16(src) || (bytes & 15u)) return PHS_EALIGN;

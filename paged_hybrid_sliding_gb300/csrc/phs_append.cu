@@ -67,6 +67,81 @@ int launch_append(const AppendParams<MAXL>& p, cudaStream_t stream) {
 template int launch_append<1>(const AppendParams<1>&, cudaStream_t);
 template int launch_append<kAppendMaxLayers>(const AppendParams<kAppendMaxLayers>&, cudaStream_t);
 
+// ------------------------------------------------- SWA segment pages --
+// Save: CTA (i, layer) copies the 16 tokens of logical page page_index[i]
+// of a request from its ring into segment page seg_pages[i].  Seed: CTA
+// (b, layer) copies the last min(n, W) tokens of request b from the
+// segment pages listed in its row of seg_table into its ring.  Token t of
+// a request of length n sits at ring slot (ring_pos - (n - 1 - t)) mod W.
+// One thread per 16-byte piece of a token's row (all KV heads), K and V.
+template <int MAXL>
+__global__ void __launch_bounds__(256) phs_swa_segment_kernel(
+    const __grid_constant__ SegCopyParams<MAXL> p) {
+  const int i = blockIdx.x;
+  const SegCopyLayer& L = p.layer[blockIdx.y];
+  const int W = p.W, pieces = p.Hkv * p.D / 8;  // 16-byte pieces per token row
+  const int r = p.ring_ids ? p.ring_ids[i] : i;
+  const int pos = p.ring_pos[i];
+  const int n = p.seq_lens[i];
+  if (r < 0 || r >= L.num_rings || pos < 0 || pos >= W || n < 0) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) set_status(p.status, PHS_ERANGE);
+    return;
+  }
+  const int t_lo = n - min(n, W);  // the window [t_lo, n)
+  int t0, t1, fp = 0;
+  int seg = -1;
+  if (p.save) {
+    t0 = p.page_index[i] * kPage;
+    t1 = t0 + kPage;
+    seg = p.seg_pages[i];
+    if (p.page_index[i] < 0 || t0 < t_lo || t1 > n || seg < 0 || seg >= L.num_seg) {
+      if (threadIdx.x == 0 && blockIdx.y == 0) set_status(p.status, PHS_ERANGE);
+      return;
+    }
+  } else {
+    t0 = t_lo;
+    t1 = n;
+    fp = t_lo / kPage;
+  }
+  const int D8 = p.D / 8;
+  for (int e = threadIdx.x; e < (t1 - t0) * pieces; e += blockDim.x) {
+    const int t = t0 + e / pieces, rem = e % pieces;
+    const int h = rem / D8, c = rem % D8;
+    int sp = seg;
+    if (!p.save) {
+      const int j = t / kPage - fp;
+      sp = j < p.max_seg ? p.seg_table[static_cast<size_t>(i) * p.max_seg + j] : -1;
+      if (sp < 0 || sp >= L.num_seg) {
+        set_status(p.status, PHS_ERANGE);
+        continue;
+      }
+    }
+    int slot = (pos - (n - 1 - t)) % W;
+    if (slot < 0) slot += W;
+    const size_t ring_row = (static_cast<size_t>(r) * p.Hkv + h) * W + slot;
+    const size_t seg_row = (static_cast<size_t>(sp) * p.Hkv + h) * kPage + t % kPage;
+    const size_t ro = ring_row * D8 + c, so = seg_row * D8 + c;
+    if (p.save) {
+      reinterpret_cast<uint4*>(L.seg_k)[so] = reinterpret_cast<const uint4*>(L.ring_k)[ro];
+      reinterpret_cast<uint4*>(L.seg_v)[so] = reinterpret_cast<const uint4*>(L.ring_v)[ro];
+    } else {
+      reinterpret_cast<uint4*>(L.ring_k)[ro] = reinterpret_cast<const uint4*>(L.seg_k)[so];
+      reinterpret_cast<uint4*>(L.ring_v)[ro] = reinterpret_cast<const uint4*>(L.seg_v)[so];
+    }
+  }
+}
+
+template <int MAXL>
+int launch_swa_segment(const SegCopyParams<MAXL>& p, int count, cudaStream_t stream) {
+  if (count <= 0 || p.num_layers <= 0) return PHS_OK;
+  dim3 grid(count, p.num_layers);
+  phs_swa_segment_kernel<MAXL><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+}
+
+template int launch_swa_segment<kSegMaxLayers>(const SegCopyParams<kSegMaxLayers>&, int,
+                                               cudaStream_t);
+
 // ------------------------------------------------------------ page copy --
 // grid (n, 2): CTA (i, kv) copies page src[i] -> dst[i] of K (kv 0) or V.
 __global__ void __launch_bounds__(256) phs_copy_pages_kernel(uint4* k, uint4* v,

@@ -15,8 +15,14 @@
 //  - "Xiaomi MiMo-V2.5 inference system" page, section 2 (prefix cache tree
 //    rebuild): with SWA layers a match is valid only at a "window-safe
 //    length", where at least the last W tokens still have valid SWA slots;
-//    each node carries the Full segment index and the SWA mapping.
+//    each node carries the Full segment index and the SWA mapping.  Here
+//    the SWA mapping is, per cached page, the id of an SWA segment page (a
+//    16-token snapshot of that page's SWA-layer KV, saved from the finished
+//    request's ring by phs_swa_ring_save) or -1; a window-safe hit returns
+//    the segment pages of its last window, which phs_swa_ring_seed copies
+//    into the new request's ring.
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -30,9 +36,17 @@ struct phs_page_allocator {
   std::mutex mu;
   std::vector<int32_t> rc;         // reference count per page
   std::vector<int32_t> free_list;  // pages with count 0 (LIFO)
+  // the caller's handle plus one per radix tree using this allocator: the
+  // object is freed when the last of them lets go, so a tree may outlive
+  // the caller's destroy call
+  std::atomic<int> holders{1};
 };
 
 namespace {
+
+void release_allocator(phs_page_allocator* a) {
+  if (a && a->holders.fetch_sub(1) == 1) delete a;
+}
 
 int alloc_locked(phs_page_allocator* a, int32_t n, int32_t* out) {
   if (n < 0) return PHS_EINVAL;
@@ -78,7 +92,7 @@ phs_page_allocator* phs_page_allocator_create(int64_t num_pages) {
   return a;
 }
 
-void phs_page_allocator_destroy(phs_page_allocator* a) { delete a; }
+void phs_page_allocator_destroy(phs_page_allocator* a) { release_allocator(a); }
 
 int phs_page_alloc(phs_page_allocator* a, int32_t n, int32_t* out_pages) {
   if (!a || (n > 0 && !out_pages)) return PHS_EINVAL;
@@ -149,7 +163,7 @@ namespace {
 struct Node {
   std::vector<int32_t> tokens;  // a whole number of pages' tokens
   std::vector<int32_t> pages;   // tokens.size() / page_size page ids
-  std::vector<uint8_t> swa;     // per token: SWA KV cached for this position
+  std::vector<int32_t> swa;     // per page: SWA segment page id, or -1
   // by the tokens of the child's first page (sharing is by whole pages)
   std::map<std::vector<int32_t>, std::unique_ptr<Node>> children;
   Node* parent = nullptr;
@@ -161,6 +175,7 @@ struct Node {
 struct phs_radix_tree {
   std::mutex mu;
   phs_page_allocator* alloc = nullptr;
+  phs_page_allocator* swa_alloc = nullptr;  // SWA segment pages (may be null)
   int32_t P = 16;
   Node root;
   uint64_t clock = 0;
@@ -189,22 +204,22 @@ void split(phs_radix_tree* t, Node* c, int64_t k) {
   auto tail = std::make_unique<Node>();
   tail->tokens.assign(c->tokens.begin() + k * P, c->tokens.end());
   tail->pages.assign(c->pages.begin() + k, c->pages.end());
-  tail->swa.assign(c->swa.begin() + k * P, c->swa.end());
+  tail->swa.assign(c->swa.begin() + k, c->swa.end());
   tail->children = std::move(c->children);
   for (auto& kv : tail->children) kv.second->parent = tail.get();
   tail->parent = c;
   tail->last_access = c->last_access;
   c->tokens.resize(k * P);
   c->pages.resize(k);
-  c->swa.resize(k * P);
+  c->swa.resize(k);
   c->children.clear();
   std::vector<int32_t> key(tail->tokens.begin(), tail->tokens.begin() + P);
   c->children[std::move(key)] = std::move(tail);
 }
 
-// Walk the longest whole-page match; appends pages and SWA flags.
+// Walk the longest whole-page match; appends pages and their SWA segment ids.
 void walk_match(phs_radix_tree* t, const int32_t* tokens, int64_t n, std::vector<int32_t>& pages,
-                std::vector<uint8_t>& swa) {
+                std::vector<int32_t>& swa) {
   Node* cur = &t->root;
   int64_t idx = 0;
   const uint64_t now = ++t->clock;
@@ -215,7 +230,7 @@ void walk_match(phs_radix_tree* t, const int32_t* tokens, int64_t n, std::vector
     const int64_t k = pages_matching(t, c, tokens, idx, n);
     if (k == 0) break;
     pages.insert(pages.end(), c->pages.begin(), c->pages.begin() + k);
-    swa.insert(swa.end(), c->swa.begin(), c->swa.begin() + k * t->P);
+    swa.insert(swa.end(), c->swa.begin(), c->swa.begin() + k);
     for (Node* u = c; u; u = u->parent) u->last_access = now;
     idx += k * t->P;
     if (k < static_cast<int64_t>(c->pages.size())) break;
@@ -237,6 +252,15 @@ int finish_match(phs_radix_tree* t, std::vector<int32_t>& pages, int64_t keep_pa
   return PHS_OK;
 }
 
+// Drop the tree's references on the SWA segment pages of a node (ids >= 0).
+void release_swa_locked(phs_radix_tree* t, const std::vector<int32_t>& swa) {
+  if (!t->swa_alloc) return;
+  std::vector<int32_t> held;
+  for (int32_t s : swa)
+    if (s >= 0) held.push_back(s);
+  decref_locked(t->swa_alloc, held.data(), static_cast<int32_t>(held.size()));
+}
+
 void collect_leaves(Node* n, std::vector<Node*>& out) {
   for (auto& kv : n->children) {
     if (kv.second->children.empty())
@@ -250,11 +274,15 @@ void collect_leaves(Node* n, std::vector<Node*>& out) {
 
 extern "C" {
 
-phs_radix_tree* phs_radix_create(phs_page_allocator* alloc, int32_t page_size) {
-  if (!alloc || page_size <= 0) return nullptr;
+phs_radix_tree* phs_radix_create(phs_page_allocator* alloc, phs_page_allocator* swa_alloc,
+                                 int32_t page_size) {
+  if (!alloc || page_size <= 0 || swa_alloc == alloc) return nullptr;
   auto* t = new phs_radix_tree();
   t->alloc = alloc;
+  t->swa_alloc = swa_alloc;
   t->P = page_size;
+  alloc->holders.fetch_add(1);
+  if (swa_alloc) swa_alloc->holders.fetch_add(1);
   return t;
 }
 
@@ -265,13 +293,18 @@ void phs_radix_destroy(phs_radix_tree* t) {
   for (auto& kv : t->root.children) stack.push_back(kv.second.get());
   {
     std::lock_guard<std::mutex> lock(t->alloc->mu);
+    std::unique_lock<std::mutex> slock;
+    if (t->swa_alloc) slock = std::unique_lock<std::mutex>(t->swa_alloc->mu);
     while (!stack.empty()) {
       Node* n = stack.back();
       stack.pop_back();
       decref_locked(t->alloc, n->pages.data(), static_cast<int32_t>(n->pages.size()));
+      release_swa_locked(t, n->swa);
       for (auto& kv : n->children) stack.push_back(kv.second.get());
     }
   }
+  release_allocator(t->alloc);
+  release_allocator(t->swa_alloc);
   delete t;
 }
 
@@ -281,7 +314,7 @@ int phs_radix_match(phs_radix_tree* t, const int32_t* tokens, int64_t n, int32_t
     return PHS_EINVAL;
   std::lock_guard<std::mutex> lock(t->mu);
   std::vector<int32_t> pages;
-  std::vector<uint8_t> swa;
+  std::vector<int32_t> swa;
   walk_match(t, tokens, n, pages, swa);
   return finish_match(t, pages, static_cast<int64_t>(pages.size()), out_pages, max_pages,
                       out_num_pages);
@@ -289,27 +322,60 @@ int phs_radix_match(phs_radix_tree* t, const int32_t* tokens, int64_t n, int32_t
 
 int phs_radix_match_window_safe(phs_radix_tree* t, const int32_t* tokens, int64_t n,
                                 int32_t window, int32_t* out_pages, int32_t max_pages,
-                                int32_t* out_num_pages) {
+                                int32_t* out_num_pages, int32_t* out_swa_pages,
+                                int32_t max_swa_pages, int32_t* out_num_swa_pages) {
   if (!t || n < 0 || window <= 0 || (n > 0 && !tokens) || !out_num_pages ||
-      (max_pages > 0 && !out_pages))
+      (max_pages > 0 && !out_pages) || !out_num_swa_pages ||
+      (max_swa_pages > 0 && !out_swa_pages))
     return PHS_EINVAL;
+  if (window % t->P != 0) return PHS_EUNSUPPORTED;  // the window is whole pages
   std::lock_guard<std::mutex> lock(t->mu);
   std::vector<int32_t> pages;
-  std::vector<uint8_t> swa;
+  std::vector<int32_t> swa;
   walk_match(t, tokens, n, pages, swa);
-  const int64_t L = phs_window_safe_len(swa.data(), static_cast<int64_t>(swa.size()), window,
-                                        t->P);
+  // per-token validity: a token has SWA KV where its page has a segment page
+  std::vector<uint8_t> valid(pages.size() * static_cast<size_t>(t->P));
+  for (size_t i = 0; i < valid.size(); ++i) valid[i] = swa[i / t->P] >= 0 ? 1 : 0;
+  const int64_t L = phs_window_safe_len(valid.data(), static_cast<int64_t>(valid.size()),
+                                        window, t->P);
   if (L < 0) return static_cast<int>(L);
-  return finish_match(t, pages, L / t->P, out_pages, max_pages, out_num_pages);
+  const int64_t keep = L / t->P;
+  const int64_t first = (L - std::min<int64_t>(L, window)) / t->P;  // the last window's pages
+  const int64_t nswa = keep - first;
+  if (nswa > max_swa_pages) return PHS_ESHAPE;
+  if (nswa > 0 && !t->swa_alloc) return PHS_EINVAL;
+  std::vector<int32_t> seg(swa.begin() + first, swa.begin() + keep);
+  if (nswa > 0) {
+    std::lock_guard<std::mutex> slock(t->swa_alloc->mu);
+    const int st = incref_locked(t->swa_alloc, seg.data(), static_cast<int32_t>(nswa));
+    if (st) return st;
+  }
+  const int st = finish_match(t, pages, keep, out_pages, max_pages, out_num_pages);
+  if (st) {
+    if (nswa > 0) {
+      std::lock_guard<std::mutex> slock(t->swa_alloc->mu);
+      decref_locked(t->swa_alloc, seg.data(), static_cast<int32_t>(nswa));
+    }
+    return st;
+  }
+  std::copy(seg.begin(), seg.end(), out_swa_pages);
+  *out_num_swa_pages = static_cast<int32_t>(nswa);
+  return PHS_OK;
 }
 
 int phs_radix_insert(phs_radix_tree* t, const int32_t* tokens, int64_t n, const int32_t* pages,
-                     int64_t swa_from) {
+                     const int32_t* swa_pages) {
   if (!t || n < 0 || (n > 0 && (!tokens || !pages))) return PHS_EINVAL;
   std::lock_guard<std::mutex> lock(t->mu);
   const int64_t P = t->P;
   const int64_t np = n / P;  // only whole pages are shared
   const uint64_t now = ++t->clock;
+  auto swa_of = [&](int64_t page) { return swa_pages ? swa_pages[page] : -1; };
+  if (swa_pages) {
+    bool any = false;
+    for (int64_t i = 0; i < np; ++i) any = any || swa_pages[i] >= 0;
+    if (any && !t->swa_alloc) return PHS_EINVAL;
+  }
   Node* cur = &t->root;
   int64_t idx = 0;  // tokens consumed
   while (idx < np * P) {
@@ -319,8 +385,17 @@ int phs_radix_insert(phs_radix_tree* t, const int32_t* tokens, int64_t n, const 
       const int64_t k = pages_matching(t, c, tokens, idx, np * P);
       if (k > 0) {
         if (k < static_cast<int64_t>(c->pages.size())) split(t, c, k);
-        for (int64_t i = 0; i < k * P; ++i)
-          if (idx + i >= swa_from) c->swa[i] = 1;
+        // a cached page without SWA KV takes the caller's segment page (the
+        // tree takes a reference on it); one that has one keeps it
+        for (int64_t i = 0; i < k; ++i) {
+          const int32_t s = swa_of(idx / P + i);
+          if (c->swa[i] < 0 && s >= 0) {
+            std::lock_guard<std::mutex> slock(t->swa_alloc->mu);
+            const int st = incref_locked(t->swa_alloc, &s, 1);
+            if (st) return st;
+            c->swa[i] = s;
+          }
+        }
         c->last_access = now;
         idx += k * P;
         cur = c;
@@ -331,15 +406,26 @@ int phs_radix_insert(phs_radix_tree* t, const int32_t* tokens, int64_t n, const 
     auto leaf = std::make_unique<Node>();
     leaf->tokens.assign(tokens + idx, tokens + np * P);
     leaf->pages.assign(pages + idx / P, pages + np);
-    leaf->swa.resize(leaf->tokens.size());
-    for (size_t i = 0; i < leaf->swa.size(); ++i) leaf->swa[i] = (idx + i) >= swa_from ? 1 : 0;
+    leaf->swa.resize(leaf->pages.size());
+    for (size_t i = 0; i < leaf->swa.size(); ++i) leaf->swa[i] = swa_of(idx / P + i);
     leaf->parent = cur;
     leaf->last_access = now;
     {
       std::lock_guard<std::mutex> alock(t->alloc->mu);
-      const int st = incref_locked(t->alloc, leaf->pages.data(),
-                                   static_cast<int32_t>(leaf->pages.size()));
+      int st = incref_locked(t->alloc, leaf->pages.data(),
+                             static_cast<int32_t>(leaf->pages.size()));
       if (st) return st;
+      if (t->swa_alloc) {
+        std::vector<int32_t> held;
+        for (int32_t s : leaf->swa)
+          if (s >= 0) held.push_back(s);
+        std::lock_guard<std::mutex> slock(t->swa_alloc->mu);
+        st = incref_locked(t->swa_alloc, held.data(), static_cast<int32_t>(held.size()));
+        if (st) {
+          decref_locked(t->alloc, leaf->pages.data(), static_cast<int32_t>(leaf->pages.size()));
+          return st;
+        }
+      }
     }
     t->cached_pages += static_cast<int64_t>(leaf->pages.size());
     std::vector<int32_t> key(leaf->tokens.begin(), leaf->tokens.begin() + P);
@@ -361,9 +447,13 @@ int phs_radix_evict(phs_radix_tree* t, int64_t pages, int64_t* out_freed) {
     Node* victim = nullptr;
     {
       std::lock_guard<std::mutex> alock(t->alloc->mu);
+      std::unique_lock<std::mutex> slock;
+      if (t->swa_alloc) slock = std::unique_lock<std::mutex>(t->swa_alloc->mu);
       for (Node* l : leaves) {
         bool only_tree = true;
         for (int32_t p : l->pages) only_tree = only_tree && t->alloc->rc[p] == 1;
+        if (t->swa_alloc)
+          for (int32_t s : l->swa) only_tree = only_tree && (s < 0 || t->swa_alloc->rc[s] == 1);
         if (only_tree) {
           victim = l;
           break;
@@ -371,6 +461,7 @@ int phs_radix_evict(phs_radix_tree* t, int64_t pages, int64_t* out_freed) {
       }
       if (!victim) break;  // every cached leaf is in use by some request
       decref_locked(t->alloc, victim->pages.data(), static_cast<int32_t>(victim->pages.size()));
+      release_swa_locked(t, victim->swa);
     }
     freed += static_cast<int64_t>(victim->pages.size());
     t->cached_pages -= static_cast<int64_t>(victim->pages.size());

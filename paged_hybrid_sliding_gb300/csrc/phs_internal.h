@@ -213,6 +213,36 @@ struct AppendParams {
 template <int MAXL>
 int launch_append(const AppendParams<MAXL>& p, cudaStream_t stream);
 
+// ---------------------------------------------- SWA segment pages (save /
+// seed a ring from page snapshots of its window) --
+constexpr int kSegMaxLayers = 64;
+
+struct SegCopyLayer {
+  void* ring_k;
+  void* ring_v;
+  void* seg_k;   // segment pool, paged layout [num_seg][Hkv][16][D]
+  void* seg_v;
+  int64_t num_rings;
+  int64_t num_seg;
+};
+
+template <int MAXL>
+struct SegCopyParams {
+  SegCopyLayer layer[MAXL];
+  const int32_t* ring_ids;    // per entry (save) / request (seed); may be null (seed)
+  const int32_t* ring_pos;    // newest slot
+  const int32_t* seq_lens;    // tokens of the request
+  const int32_t* page_index;  // save: logical page to snapshot
+  const int32_t* seg_pages;   // save: destination segment page
+  const int32_t* seg_table;   // seed: [B][max_seg] segment pages of the window
+  int32_t* status;
+  int num_layers, Hkv, D, W, max_seg;
+  int save;                   // 1 save (ring -> segment), 0 seed (segment -> ring)
+};
+
+template <int MAXL>
+int launch_swa_segment(const SegCopyParams<MAXL>& p, int count, cudaStream_t stream);
+
 // ----------------------------------------------------------- quantiser --
 struct QuantArgs {
   const __nv_bfloat16* k_src;

@@ -194,21 +194,128 @@ def test_window_safe_len_brute_force(seed):
 
 
 def test_radix_window_safe_match():
-    # a finished request keeps the SWA KV of its last W tokens: a new request
-    # sharing its prefix may only resume where a whole window is covered
+    # a finished request keeps the SWA KV of its last W tokens (saved as
+    # segment pages): a new request sharing its prefix may only resume where
+    # a whole window is covered, and gets that window's segment pages
     a = phs.PageAllocator(64)
-    t = phs.RadixTree(a, P)
+    sa = phs.PageAllocator(16)
+    t = phs.RadixTree(a, P, swa_alloc=sa)
     W = 32
     s = list(range(160))               # 10 pages
-    t.insert(s, a.alloc(10), swa_from=160 - W)
+    seg = sa.alloc(2)
+    t.insert(s, a.alloc(10), swa_pages=[-1] * 8 + seg.tolist())
     full = t.match(s)
     assert len(full) == 10
-    safe = t.match_window_safe(s, W)
-    assert len(safe) == 10             # last 32 tokens valid: the whole match
-    safe = t.match_window_safe(s[:150], W)   # tail [118,144) is not SWA-valid
-    assert len(safe) == 0
-    # a second finished request marks more positions valid
-    t.insert(s[:128], np.arange(8, dtype=np.int32), swa_from=128 - W)
-    safe = t.match_window_safe(s[:150], W)
-    assert len(safe) * P == 144        # [96,160) valid now: [112,144) is covered
-    assert len(t.match_window_safe(s[:120], W)) == 0   # [80,112) is not
+    safe, sw = t.match_window_safe(s, W)
+    assert len(safe) == 10 and sw.tolist() == seg.tolist()
+    safe, sw = t.match_window_safe(s[:150], W)   # tail [112,144) has no SWA KV
+    assert len(safe) == 0 and len(sw) == 0
+    # a second finished request maps more pages
+    seg2 = sa.alloc(2)
+    t.insert(s[:128], np.arange(8, dtype=np.int32), swa_pages=[-1] * 6 + seg2.tolist())
+    safe, sw = t.match_window_safe(s[:150], W)
+    assert len(safe) * P == 144        # [96,160) mapped now: [112,144) is covered
+    assert sw.tolist() == [seg2[1], seg[0]]
+    safe, sw = t.match_window_safe(s[:120], W)
+    assert len(safe) == 0 and len(sw) == 0      # [80,112) is not
+    assert t.match_window_safe(s[:16], 64)[0].tolist() == []   # page 0 has no SWA KV
+    # every returned segment page carries a reference for the caller (on
+    # top of the saving requests' own and the tree's)
+    rc = sa.refcounts()
+    assert rc[seg[1]] == 3 and rc[seg2[1]] == 3 and rc[seg[0]] == 4 and rc[seg2[0]] == 2
+
+
+class HybridModel(RadixModel):
+    """Adds, per cached page, the SWA segment page (the first one given)."""
+
+    def __init__(self):
+        super().__init__()
+        self.swa_of = {}
+
+    def insert(self, tokens, pages, swa):
+        super().insert(tokens, pages)
+        for k in range(len(tokens) // P):
+            key = tuple(tokens[:(k + 1) * P])
+            if swa[k] >= 0 and self.swa_of.get(key, -1) < 0:
+                self.swa_of[key] = int(swa[k])
+
+    def match_window_safe(self, tokens, W):
+        pages = self.match(tokens)
+        swa = [self.swa_of.get(tuple(tokens[:(k + 1) * P]), -1) for k in range(len(pages))]
+        best = 0
+        for L in range(P, len(pages) * P + 1, P):
+            lo = L - min(L, W)
+            if all(swa[j] >= 0 for j in range(lo // P, L // P)):
+                best = L
+        lo = best - min(best, W)
+        return pages[:best // P], swa[lo // P:best // P]
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_radix_swa_mapping_matches_model(seed):
+    rng = np.random.default_rng(100 + seed)
+    W = 48
+    a = phs.PageAllocator(4096)
+    sa = phs.PageAllocator(2048)
+    t = phs.RadixTree(a, P, swa_alloc=sa)
+    model = HybridModel()
+    held, held_swa = [], []
+    for s in _random_sequences(rng, 60):
+        got, gsw = t.match_window_safe(s, W)
+        want, wsw = model.match_window_safe(s, W)
+        assert got.tolist() == want and gsw.tolist() == wsw
+        held.extend(got.tolist())
+        held_swa.extend(gsw.tolist())
+        npg = len(s) // P
+        fresh = a.alloc(npg - len(got))
+        held.extend(fresh.tolist())
+        pages = np.concatenate([got, fresh]).astype(np.int32)
+        # the finished request saved the segment pages of its last window
+        # (whole pages only; some requests saved none)
+        swa = np.full(npg, -1, np.int32)
+        if rng.random() < 0.8 and npg:
+            k = min(npg, W // P)
+            swa[npg - k:] = sa.alloc(k)
+            held_swa.extend(swa[npg - k:].tolist())
+        t.insert(s, pages, swa_pages=swa)
+        model.insert(s, pages, swa)
+    rc = np.zeros(2048, np.int64)
+    for p in held_swa:
+        rc[p] += 1
+    for p in set(model.swa_of.values()):
+        rc[p] += 1
+    assert np.array_equal(sa.refcounts(), rc)
+    # requests finished: evicting everything releases the SWA pages too
+    a.decref(held)
+    sa.decref(held_swa)
+    t.evict(10 ** 6)
+    assert a.free_count() == 4096 and sa.free_count() == 2048
+
+
+def test_radix_swa_mapping_argument_errors():
+    a = phs.PageAllocator(8)
+    t = phs.RadixTree(a, P)            # no SWA allocator
+    with pytest.raises(phs.PhsError):
+        t.insert(list(range(16)), a.alloc(1), swa_pages=[3])
+    with pytest.raises(ValueError):
+        phs.RadixTree(a, P, swa_alloc=a)
+    sa = phs.PageAllocator(4)
+    t2 = phs.RadixTree(a, P, swa_alloc=sa)
+    with pytest.raises(phs.PhsError) as e:   # the window must be whole pages
+        t2.match_window_safe(list(range(32)), 40)
+    assert e.value.code == -7
+
+
+def test_tree_keeps_its_allocators_alive():
+    # the caller may let go of the allocators before the tree: the tree's
+    # references keep them alive until it is destroyed
+    a, sa = phs.PageAllocator(8), phs.PageAllocator(4)
+    t = phs.RadixTree(a, P, swa_alloc=sa)
+    s = list(range(32))
+    t.insert(s, a.alloc(2), swa_pages=[-1, int(sa.alloc(1)[0])])
+    a.close()
+    sa.close()
+    assert len(t.match(s)) == 2
+    pages, seg = t.match_window_safe(s, 16)
+    assert len(pages) == 2 and len(seg) == 1
+    t.close()

@@ -366,3 +366,121 @@ def test_kv_tokens_stored_on_stack_workload():
     hyb = oracle.kv_tokens_stored(lf, w.n_after, 128)
     assert w.n_after.mean() >= 32768
     assert abs(hyb / full - 1 / 7) / (1 / 7) < 0.05
+
+
+# ------------------------------------------------- SWA segment pages --
+def _seg_case(rng, lens, W, Hkv=2, D=64, P=16):
+    """Dense sequences, and segment pages holding every page of each
+    (page ids from one permutation; pages of different requests disjoint)."""
+    k = [random_bf16(rng, (Hkv, n, D)) for n in lens]
+    v = [random_bf16(rng, (Hkv, n, D)) for n in lens]
+    ppr = [(n + P - 1) // P for n in lens]
+    nseg = sum(ppr) + 3
+    perm = rng.permutation(nseg)
+    bt = np.full((len(lens), max(ppr)), -1, np.int32)
+    o = 0
+    for b, c in enumerate(ppr):
+        bt[b, :c] = perm[o:o + c]
+        o += c
+    return k, v, bt, nseg
+
+
+def _window_table(bt, lens, W, P=16):
+    """Row b: the segment pages of request b's last window, in token order."""
+    rows = []
+    for b, n in enumerate(lens):
+        lo = n - min(n, W)
+        rows.append(bt[b, lo // P:(n + P - 1) // P])
+    width = max(len(r) for r in rows)
+    out = np.full((len(lens), width), -1, np.int32)
+    for b, r in enumerate(rows):
+        out[b, :len(r)] = r
+    return out
+
+
+@pytest.mark.parametrize("W", [16, 128])
+def test_ring_seeded_from_segment_pages_equals_dense_last_window(W):
+    # the ring a request resumes with holds exactly its last W tokens: SWA
+    # decode over it equals the library on the dense last-W window (lengths
+    # below W, page-aligned and not page-aligned)
+    rng = np.random.default_rng(300 + W)
+    lens = [5, W, W + 16, 3 * W + 9, 200]
+    B, D = len(lens), 64
+    k, v, bt, nseg = _seg_case(rng, lens, W)
+    ks, vs = dense_to_paged(k, bt, nseg), dense_to_paged(v, bt, nseg)
+    ids = rng.permutation(B + 2)[:B].astype(np.int32)
+    rp = rng.integers(0, W, size=B).astype(np.int32)
+    kr = random_bf16(rng, (B + 2, 2, W, D))
+    vr = random_bf16(rng, (B + 2, 2, W, D))
+    st = oracle.swa_ring_seed(kr, vr, ks, vs, ids, rp, lens, _window_table(bt, lens, W))
+    assert st == 0
+    q = random_bf16(rng, (B, 8, D))
+    out, st = oracle.decode_swa_ring(q, kr, vr, ids, rp, lens, 0.125)
+    assert st == 0
+    kw = [bf16_bits_to_f64(x[:, max(0, x.shape[1] - W):]) for x in k]
+    vw = [bf16_bits_to_f64(x[:, max(0, x.shape[1] - W):]) for x in v]
+    np.testing.assert_allclose(out, sdpa_reference(q, kw, vw, 0.125), rtol=1e-12, atol=1e-13)
+    # brute force: every window token sits where the ring formula puts it
+    for b, n in enumerate(lens):
+        for t in range(n - min(n, W), n):
+            assert np.array_equal(kr[ids[b], :, (rp[b] - (n - 1 - t)) % W], k[b][:, t])
+
+
+def test_ring_save_copies_whole_window_pages():
+    rng = np.random.default_rng(310)
+    W, D, n = 128, 64, 300          # window [172, 300): pages 11..17 are whole
+    k = [random_bf16(rng, (2, n, D))]
+    v = [random_bf16(rng, (2, n, D))]
+    rp = np.array([77], np.int32)
+    kr = dense_to_ring(k, rp, W, num_rings=2, ring_ids=[1])
+    vr = dense_to_ring(v, rp, W, num_rings=2, ring_ids=[1])
+    ks = np.zeros((9, 2, 16, D), np.uint16)
+    vs = np.zeros_like(ks)
+    pages = np.arange(11, 18, dtype=np.int32)
+    segs = np.arange(7, dtype=np.int32)[::-1].copy() + 2
+    one = np.ones(len(pages), np.int32)
+    st = oracle.swa_ring_save(kr, vr, ks, vs, one, np.full(len(pages), 77), one * n, pages, segs)
+    assert st == 0
+    for p, s in zip(pages, segs):
+        assert np.array_equal(ks[s], k[0][:, 16 * p:16 * p + 16])
+        assert np.array_equal(vs[s], v[0][:, 16 * p:16 * p + 16])
+    # page 10 starts before the window (tokens 160..171 were overwritten)
+    ks0 = ks.copy()
+    st = oracle.swa_ring_save(kr, vr, ks, vs, [1], [77], [n], [10], [0])
+    assert st == oracle.ORC_ERANGE and np.array_equal(ks, ks0)
+
+
+def test_ring_save_then_seed_round_trip():
+    # a finished request's whole window pages saved, then seeded into another
+    # ring at another newest slot: the SWA decode is unchanged
+    rng = np.random.default_rng(320)
+    W, D = 64, 64
+    lens = [192, 80]                 # page-aligned window starts: 128 and 16
+    k = [random_bf16(rng, (2, n, D)) for n in lens]
+    v = [random_bf16(rng, (2, n, D)) for n in lens]
+    rp = np.array([5, 60], np.int32)
+    kr = dense_to_ring(k, rp, W)
+    vr = dense_to_ring(v, rp, W)
+    q = random_bf16(rng, (2, 4, D))
+    ref, _ = oracle.decode_swa_ring(q, kr, vr, None, rp, lens, 0.2)
+    ks = np.zeros((10, 2, 16, D), np.uint16)
+    vs = np.zeros_like(ks)
+    e_ring, e_page, e_seg = [], [], []
+    table = np.full((2, W // 16), -1, np.int32)
+    s = 0
+    for b, n in enumerate(lens):
+        for j, p in enumerate(range((n - W) // 16, n // 16)):
+            e_ring.append(b)
+            e_page.append(p)
+            e_seg.append(s)
+            table[b, j] = s
+            s += 1
+    m = len(e_ring)
+    assert oracle.swa_ring_save(kr, vr, ks, vs, e_ring, rp[e_ring], np.array(lens)[e_ring],
+                                e_page, e_seg) == 0
+    rp2 = np.array([31, 2], np.int32)
+    kr2 = random_bf16(rng, (2, 2, W, D))
+    vr2 = random_bf16(rng, (2, 2, W, D))
+    assert oracle.swa_ring_seed(kr2, vr2, ks, vs, None, rp2, lens, table) == 0
+    out, _ = oracle.decode_swa_ring(q, kr2, vr2, None, rp2, lens, 0.2)
+    assert np.array_equal(out, ref) and m == 8
