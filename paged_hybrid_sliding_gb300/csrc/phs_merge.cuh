@@ -93,4 +93,88 @@ __device__ __forceinline__ void merge_request(const MergeArgs& a, const float* w
   }
 }
 
+// The same merge with one warp taking all G rows of (b, h), four rows at a
+// time with their loads interleaved, so each group of rows costs the
+// latency of one row (the persistent SWA kernel takes the Full layers'
+// merges this way, one warp per (layer, request, KV head)).
+template <int D>
+__device__ __forceinline__ void merge_request_rows4(const MergeArgs& a, const float* ws_o,
+                                                    const float* ws_ml, void* out, int b, int h) {
+  constexpr int V = D / 32;  // columns per lane (4 or 2)
+  constexpr int RB = 4;      // rows merged together
+  const int lane = threadIdx.x & 31;
+  const int G = a.G;
+  const int n = min(a.seq_lens[b], a.n_clamp);
+  const int qlen = a.qlens ? a.qlens[b] : 0;
+  const int ns = min(request_splits(n, qlen, a.T), a.max_splits);
+  if (ns <= 1) return;
+  const size_t part0 = (static_cast<size_t>(b) * a.Hkv + h) * a.max_splits;
+  const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
+  const float2* ml = reinterpret_cast<const float2*>(ws_ml) + part0 * G;
+  for (int r0 = 0; r0 < G; r0 += RB) {
+    float M[RB], Lsum[RB], acc[RB][V];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      M[r] = -INFINITY;
+      Lsum[r] = 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[r][i] = 0.f;
+    }
+    for (int s = lane; s < ns; s += 32)
+#pragma unroll
+      for (int r = 0; r < RB; ++r)
+        if (r0 + r < G) M[r] = fmaxf(M[r], ml[static_cast<size_t>(s) * G + r0 + r].x);
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M[r] = fmaxf(M[r], __shfl_xor_sync(0xffffffffu, M[r], o));
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      float wl[RB];
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        wl[r] = 0.f;
+        if (s0 + lane < ns && r0 + r < G) {
+          const float2 v = ml[static_cast<size_t>(s0 + lane) * G + r0 + r];
+          wl[r] = v.x == -INFINITY ? 0.f : exp2f(v.x - M[r]);
+          Lsum[r] += v.y * wl[r];
+        }
+      }
+      const int cnt = min(32, ns - s0);
+#pragma unroll 4
+      for (int k = 0; k < cnt; ++k) {
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          const float w = __shfl_sync(0xffffffffu, wl[r], k);
+          if (r0 + r < G) {
+            const float* src =
+                ws_o + ((part0 + s0 + k) * G + r0 + r) * D + lane * V;
+            if constexpr (V == 4) {
+              const float4 o = *reinterpret_cast<const float4*>(src);
+              acc[r][0] += w * o.x;
+              acc[r][1] += w * o.y;
+              acc[r][2] += w * o.z;
+              acc[r][3] += w * o.w;
+            } else {
+              const float2 o = *reinterpret_cast<const float2*>(src);
+              acc[r][0] += w * o.x;
+              acc[r][1] += w * o.y;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      if (r0 + r >= G) break;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Lsum[r] += __shfl_xor_sync(0xffffffffu, Lsum[r], o);
+      const float inv = Lsum[r] > 0.f ? 1.f / Lsum[r] : 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        store_out(out, out_row0 + static_cast<size_t>(r0 + r) * D + lane * V + i,
+                  acc[r][i] * inv, a.out_f32);
+    }
+  }
+}
+
 }  // namespace phs

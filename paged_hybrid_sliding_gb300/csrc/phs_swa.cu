@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       const int l = id / BH, rem = id - l * BH;
       const int b = rem / Hkv, h = rem - (rem / Hkv) * Hkv;
       const StackMergeLayer& M = p.merge_layer[l];
-      merge_request<D>(p.merge, M.ws_o, M.ws_ml, M.out, b, h, 0, 1);
+      merge_request_rows4<D>(p.merge, M.ws_o, M.ws_ml, M.out, b, h);
     }
   }
 }
