@@ -217,23 +217,20 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
   }
   const int my_n = warp < nch ? (nch - warp + NW - 1) / NW : 0;
 
-  // ---- chunk ids (physical page / INT8 page) and INT8 scales of this warp
+  // ---- chunk ids (physical page / INT8 page) of this warp; the INT8
+  // scales, which need the ids, are loaded after the first copies are issued
   int32_t* ids = reinterpret_cast<int32_t*>(smem + L::kIdsOff) + warp * kMaxChunksPerWarp * 3;
   float* kss = reinterpret_cast<float*>(ids + kMaxChunksPerWarp);
   float* vss = kss + kMaxChunksPerWarp;
   for (int j = lane; j < my_n; j += 32) {
     const int ci = warp + j * NW;
     int id;
-    float ks = 0.f, vs = 0.f;
     if (is_i8) {
       const int lq = t0 / kQBlock + ci;
       id = lq < a.max_qpages ? a.qtable[static_cast<size_t>(b) * a.max_qpages + lq] : -1;
       if (id < 0 || id >= a.num_qpages) {
         set_status(a.status, PHS_ERANGE);
         id = -1;
-      } else {
-        ks = __ldg(a.k_scale + static_cast<size_t>(id) * a.Hkv + h);
-        vs = __ldg(a.v_scale + static_cast<size_t>(id) * a.Hkv + h);
       }
     } else {
       const int lp = t0 / kPage + ci;  // < max_pages: n was clamped above
@@ -244,8 +241,6 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
       }
     }
     ids[j] = id;
-    kss[j] = ks;
-    vss[j] = vs;
   }
   const uint32_t bar0 = smem_u32(smem + L::kBarOff) + warp * S * 8;
   if (lane == 0) {
@@ -290,6 +285,13 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
     }
     for (int j = 0; j < S && j < my_n; ++j) issue(j);
   }
+  if (is_i8) {
+    for (int j = lane; j < my_n; j += 32) {
+      const int id = ids[j];
+      kss[j] = id >= 0 ? __ldg(a.k_scale + static_cast<size_t>(id) * a.Hkv + h) : 0.f;
+      vss[j] = id >= 0 ? __ldg(a.v_scale + static_cast<size_t>(id) * a.Hkv + h) : 0.f;
+    }
+  }
 
   // ---- queries of the group (overlaps the first loads)
   QFrags<D, TWO> qf;
@@ -298,6 +300,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
     load_q_f16_i8order(qf, qg, G, lane);
   else
     load_q_bf16(qf, qg, G, lane);
+  __syncwarp();  // every lane's scales are in shared memory
 
   WarpState<D, TWO> st;
   st.reset();
