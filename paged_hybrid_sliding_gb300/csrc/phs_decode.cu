@@ -161,8 +161,10 @@ __device__ __noinline__ void check_prefix_ids(const SplitArgs& a, int b, int h, 
 // The work of one CTA: request b, KV head h, split s.  q/out/ws_o/ws_ml are
 // the layer's; `app` (k_new null: none) is an append fused into this
 // launch: the CTA holding token n-1 writes it into its page and patches its
-// staged copy from the input before using it.
-template <int D, bool TWO>
+// staged copy from the input before using it.  MIXED: the launch may hold
+// INT8 splits (a.qlens set); without them the INT8 walk is compiled out,
+// which leaves the bf16 walk its registers (no spills).
+template <int D, bool TWO, bool MIXED>
 __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensorMap* tv,
                                            const CUtensorMap* tk8, const CUtensorMap* tv8,
                                            const SplitArgs& a, const __nv_bfloat16* q,
@@ -188,7 +190,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
     if (s == 0 && h == 0 && threadIdx.x == 0) set_status(a.status, PHS_ERANGE);
     n = a.n_clamp;
   }
-  const int qlen = a.qlens ? a.qlens[b] : 0;
+  const int qlen = MIXED && a.qlens ? a.qlens[b] : 0;
   const int T = a.T;
   const int ns = min(request_splits(n, qlen, T, a.skip_len), a.max_splits);
   if (ns < 0) {
@@ -204,7 +206,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
   if (s >= ns) return;
 
   const int nsq = (qlen + T - 1) / T;
-  const bool is_i8 = s < nsq;
+  const bool is_i8 = MIXED && s < nsq;
   int t0, t1, nch;
   if (is_i8) {
     t0 = s * T;
@@ -400,15 +402,15 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
 
 // request index fastest: CTAs that read the same shared-prefix pages for
 // different requests run close together in time and share them through L2
-template <int D, bool TWO>
+template <int D, bool TWO, bool MIXED>
 __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
     phs_split_decode_kernel(const __grid_constant__ CUtensorMap tk,
                             const __grid_constant__ CUtensorMap tv,
                             const __grid_constant__ CUtensorMap tk8,
                             const __grid_constant__ CUtensorMap tv8, const SplitArgs a) {
   const FusedAppend none{nullptr, nullptr, nullptr, nullptr};
-  split_body<D, TWO>(&tk, &tv, &tk8, &tv8, a, a.q, a.out, a.ws_o, a.ws_ml, none, blockIdx.x,
-                     blockIdx.y, blockIdx.z);
+  split_body<D, TWO, MIXED>(&tk, &tv, &tk8, &tv8, a, a.q, a.out, a.ws_o, a.ws_ml, none,
+                            blockIdx.x, blockIdx.y, blockIdx.z);
   // started early beside an independent grid: one CTA holds this grid open
   // until that grid has finished, so a launch that waits for this grid also
   // sees the other's results
@@ -419,14 +421,15 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
 // Every Full layer of a hybrid stack in one launch: blockIdx.z = layer *
 // max_splits + split; each layer brings its own pool maps, queries, output,
 // partials and new token.  Source: "Xiaomi MiMo-V2.5 inference system" page,
-// section 2 (layer-wise overlap of the step; whole-step replay).
+// section 2 (layer-wise overlap of the step; whole-step replay).  The Full
+// layers of a stack hold bf16 pages only.
 template <int D, bool TWO>
 __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
     phs_stack_full_kernel(const __grid_constant__ StackFullParams p) {
   const int l = blockIdx.z / p.a.max_splits, s = blockIdx.z - l * p.a.max_splits;
   const StackFullLayer& L = p.layer[l];
-  split_body<D, TWO>(&L.tk, &L.tv, &L.tk, &L.tv, p.a, L.q, L.out, L.ws_o, L.ws_ml, L.app,
-                     blockIdx.x, blockIdx.y, s);
+  split_body<D, TWO, false>(&L.tk, &L.tv, &L.tk, &L.tv, p.a, L.q, L.out, L.ws_o, L.ws_ml,
+                            L.app, blockIdx.x, blockIdx.y, s);
 }
 
 // Cross-split merge of one (request, KV head): warp w of the CTA merges
@@ -455,7 +458,8 @@ template <int D, bool TWO>
 static int launch_split_t(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tk8,
                           const CUtensorMap& tv8, const SplitArgs& a, int B, cudaStream_t stream,
                           bool dependent) {
-  auto kern = phs_split_decode_kernel<D, TWO>;
+  auto kern = a.qlens ? phs_split_decode_kernel<D, TWO, true>
+                      : phs_split_decode_kernel<D, TWO, false>;
   const int smem = SplitLayout<D>::kAlloc;
   if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
   dim3 grid(B, a.Hkv, a.max_splits);
@@ -502,7 +506,7 @@ static int launch_stack_full_t(const StackFullParams& p, int B, cudaStream_t str
 }
 
 int launch_stack_full(int D, const StackFullParams& p, int B, cudaStream_t stream) {
-  if (p.num_layers <= 0 || p.num_layers > kStackMaxFull) return PHS_EINVAL;
+  if (p.num_layers <= 0 || p.num_layers > kStackMaxFull || p.a.qlens) return PHS_EINVAL;
   if (static_cast<long long>(p.a.max_splits) * p.num_layers > 65535) return PHS_EUNSUPPORTED;
   const bool two = p.a.G > 8;
   if (D == 128)
