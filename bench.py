@@ -894,8 +894,8 @@ class Int8Workload(Workload):
         for i, k in enumerate(nq):
             qt[i, :k] = np.arange(o, o + k)
             o += k
-        i8 = dict(k_codes=self.i8.k.index_select(0, ids).cpu().numpy(),
-                  v_codes=self.i8.v.index_select(0, ids).cpu().numpy(),
+        gk, gv = self.i8.codes(ids)
+        i8 = dict(k_codes=gk.cpu().numpy(), v_codes=gv.cpu().numpy(),
                   k_scale=self.i8.k_scale.index_select(0, ids).cpu().numpy(),
                   v_scale=self.i8.v_scale.index_select(0, ids).cpu().numpy(),
                   qtable=qt, qlens=self.qlen0[rows])

@@ -99,10 +99,15 @@ typedef struct {
     int32_t head_dim;
 } phs_ring_pool;
 
-/* INT8 pool: 32-token pages of codes plus one fp32 scale per page and head. */
+/* INT8 pool: 32-token pages of codes plus one fp32 scale per page and head.
+ * A code x in [-127, 127] is stored as the byte x + 128.  K is token-major.
+ * V is transposed: one 32-byte row per head dim, and within each 16-token
+ * half of a row, byte p holds token 2(p/4) + (p%2) + 8((p/2)%2).  These are
+ * the orders in which the decode kernel's mma fragments read the codes.
+ * Each is 32 * D bytes per page and head. */
 typedef struct {
-    int8_t *k;            /* device, int8 [num_qpages][Hkv][32][D] */
-    int8_t *v;
+    uint8_t *k;           /* device, [num_qpages][Hkv][32 tokens][D] */
+    uint8_t *v;           /* device, [num_qpages][Hkv][D][32 tokens, order above] */
     float *k_scale;       /* device, fp32 [num_qpages][Hkv] */
     float *v_scale;
     int64_t num_qpages;
@@ -150,7 +155,8 @@ int phs_kv_append_ring(const phs_ring_pool *ring, const void *k_new, const void 
  * (tokens 32j .. 32j+31 through src_block_table), computes in IEEE fp32
  *     a = max |x|,  s = a / 127,  code = clamp(rint(x / s), -127, 127)
  * (rint rounds half to even; a == 0 gives s = 0 and all codes 0), and stores
- * the codes in INT8 page dst_qtable[b][j] and s in the matching scale slot.
+ * the codes in INT8 page dst_qtable[b][j] (in the stored form and layout of
+ * phs_int8_pool) and s in the matching scale slot.
  * max_qblocks bounds num_qblocks[b] (host int; sizes the grid).
  * ---------------------------------------------------------------------- */
 int phs_kv_quant_int8_block32(const phs_paged_pool *src, const int32_t *src_block_table,

@@ -130,33 +130,56 @@ class RingPool:
                         torch.empty(shape, dtype=torch.bfloat16, device=device))
 
 
+# Token held by byte p of a 16-token half of a stored V^T row (see Int8Pool).
+VT_TOKEN = tuple(2 * (p >> 2) + (p & 1) + 8 * ((p >> 1) & 1) for p in range(16))
+
+
 @dataclass
 class Int8Pool:
-    """INT8 pool: codes int8 [num_qpages, Hkv, 32, D], scales fp32 [num_qpages, Hkv]."""
+    """INT8 pool in its stored form (each code x as the byte x + 128):
+    k uint8 [num_qpages, Hkv, 32 tokens, D]; v uint8 [num_qpages, Hkv, D,
+    32] (transposed; byte p of each 16-token half holds token VT_TOKEN[p]);
+    scales fp32 [num_qpages, Hkv]."""
     k: torch.Tensor
     v: torch.Tensor
     k_scale: torch.Tensor
     v_scale: torch.Tensor
 
     def c(self):
-        _need(self.k, torch.int8, "int8.k", 4)
-        _need(self.v, torch.int8, "int8.v", 4)
+        _need(self.k, torch.uint8, "int8.k", 4)
+        _need(self.v, torch.uint8, "int8.v", 4)
         _need(self.k_scale, torch.float32, "int8.k_scale", 2)
         _need(self.v_scale, torch.float32, "int8.v_scale", 2)
         n, h, q, d = self.k.shape
-        if q != QBLOCK or self.v.shape != self.k.shape or tuple(self.k_scale.shape) != (n, h) \
-                or tuple(self.v_scale.shape) != (n, h):
+        if q != QBLOCK or tuple(self.v.shape) != (n, h, d, QBLOCK) \
+                or tuple(self.k_scale.shape) != (n, h) or tuple(self.v_scale.shape) != (n, h):
             raise ValueError("inconsistent INT8 pool shapes")
         return _lib.Int8PoolC(self.k.data_ptr(), self.v.data_ptr(), self.k_scale.data_ptr(),
                               self.v_scale.data_ptr(), n, h, d)
 
+    def codes(self, pages=None):
+        """The signed codes (int8) of all pages, or of the page ids in
+        `pages`, both token-major [pages, Hkv, 32, D]: a view of the stored
+        form for inspection, not used by the decode path."""
+        k, v = self.k, self.v
+        if pages is not None:
+            k, v = k.index_select(0, pages), v.index_select(0, pages)
+        order = torch.tensor([16 * hf + t for hf in range(2) for t in VT_TOKEN], device=v.device)
+        inv = torch.empty_like(order)
+        inv[order] = torch.arange(QBLOCK, device=v.device)
+        vt = v.transpose(-1, -2).index_select(-2, inv)  # [.., token, D]
+        return ((k.to(torch.int16) - 128).to(torch.int8),
+                (vt.to(torch.int16) - 128).to(torch.int8).contiguous())
+
     @staticmethod
     def empty(num_qpages, num_kv_heads, head_dim, device="cuda"):
-        shape = (num_qpages, num_kv_heads, QBLOCK, head_dim)
-        return Int8Pool(torch.empty(shape, dtype=torch.int8, device=device),
-                        torch.empty(shape, dtype=torch.int8, device=device),
-                        torch.empty((num_qpages, num_kv_heads), dtype=torch.float32, device=device),
-                        torch.empty((num_qpages, num_kv_heads), dtype=torch.float32, device=device))
+        return Int8Pool(
+            torch.empty((num_qpages, num_kv_heads, QBLOCK, head_dim), dtype=torch.uint8,
+                        device=device),
+            torch.empty((num_qpages, num_kv_heads, head_dim, QBLOCK), dtype=torch.uint8,
+                        device=device),
+            torch.empty((num_qpages, num_kv_heads), dtype=torch.float32, device=device),
+            torch.empty((num_qpages, num_kv_heads), dtype=torch.float32, device=device))
 
 
 # ------------------------------------------------------------------ append --

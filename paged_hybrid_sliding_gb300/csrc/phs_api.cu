@@ -138,6 +138,22 @@ int map_i8_rows(CUtensorMap* m, const void* base, int64_t rows, int D) {
   return r == CUDA_SUCCESS ? PHS_OK : PHS_ECUDA;
 }
 
+// int8 V^T codes (D x 32 bytes per block and head) viewed as rows of 128
+// bytes (4 head dims each); boxes of D/4 rows (a whole block) with the
+// 128-byte swizzle: the same copy shape as a K block.
+int map_i8_vt(CUtensorMap* m, const void* base, int64_t rows, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PHS_ECUDA;
+  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(D / 4)};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PHS_OK : PHS_ECUDA;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_dims(int Hq, int Hkv, int D) {
@@ -174,6 +190,7 @@ int check_int8(const phs_int8_pool* p) {
   if (!p || !p->k || !p->v || !p->k_scale || !p->v_scale) return PHS_EINVAL;
   if (p->num_qpages <= 0 || p->num_kv_heads <= 0) return PHS_EINVAL;
   if (p->head_dim != 64 && p->head_dim != 128) return PHS_EUNSUPPORTED;
+  // TMA row coordinates are int32: 32 K rows and D/4 V^T rows per block and head
   if (p->num_qpages * p->num_kv_heads * kQBlock > INT32_MAX) return PHS_EUNSUPPORTED;
   if (!aligned16(p->k) || !aligned16(p->v)) return PHS_EALIGN;
   return PHS_OK;
@@ -322,9 +339,9 @@ int prepare_decode(DecodeCall& c, const void* q, int Hq, const phs_paged_pool* p
   if ((st = map_bf16_kv(&c.tk, pool->k, rows, D))) return st;
   if ((st = map_bf16_kv(&c.tv, pool->v, rows, D))) return st;
   if (int8) {
-    const int64_t qrows = int8->num_qpages * Hkv * kQBlock;
-    if ((st = map_i8_rows(&c.tk8, int8->k, qrows, D))) return st;
-    if ((st = map_i8_rows(&c.tv8, int8->v, qrows, D))) return st;
+    const int64_t blocks = int8->num_qpages * Hkv;
+    if ((st = map_i8_rows(&c.tk8, int8->k, blocks * kQBlock, D))) return st;
+    if ((st = map_i8_vt(&c.tv8, int8->v, blocks * (D / 4), D))) return st;
   } else {
     c.tk8 = c.tk;  // unused by bf16-only launches
     c.tv8 = c.tv;

@@ -33,8 +33,8 @@ struct ChunkGeom {
 // address of fragment step i is (stage + lane offset) ^ (constant of i) + an
 // immediate: one logic op per fragment load instead of the full swizzle.
 struct FragOffsets {
-  uint32_t bk, bv;        // bf16 chunk: K (ldmatrix) and V (ldmatrix.trans)
-  uint32_t ik, iv0, iv1;  // INT8 chunk: K (ldmatrix), V rows 2q+{0,8} and 2q+{1,9}
+  uint32_t bk, bv;  // bf16 chunk: K (ldmatrix) and V (ldmatrix.trans)
+  uint32_t ik, iv;  // INT8 chunk: K rows (token order of kI8TokenPerm), V^T rows
 
   template <int D>
   __device__ __forceinline__ void init(int lane) {
@@ -43,19 +43,22 @@ struct FragOffsets {
     bk = (r + ((mi >> 1) << 3)) * 128 + ((((mi & 1) ^ r) & 7) << 4);
     // bf16 V (transposed): (tokens 8*(mi&1).., unit 2np + (mi>>1))
     bv = (r + ((mi & 1) << 3)) * 128 + ((((mi >> 1) ^ r) & 7) << 4);
-    const int gh = g >> 2, inner = (g & 3) * 4;
-    if constexpr (D == 128) {
-      // INT8 K rows of 128 bytes: row 8nt + r, unit 4hq + mi
-      ik = r * 128 + (((mi ^ r) & 7) << 4);
-      // INT8 V rows 2qd (+8) and 2qd+1 (+9), unit 2J + gh, byte 4*(g&3)
-      iv0 = (2 * qd) * 128 + (((gh ^ (2 * qd)) & 7) << 4) + inner;
-      iv1 = (2 * qd + 1) * 128 + (((gh ^ (2 * qd + 1)) & 7) << 4) + inner;
-    } else {
-      // 64-byte rows, 64-byte swizzle: unit ^= (row >> 1) & 3
-      ik = r * 64 + (((mi ^ (r >> 1)) & 3) << 4);
-      iv0 = (2 * qd) * 64 + (((gh ^ qd) & 3) << 4) + inner;
-      iv1 = (2 * qd + 1) * 64 + (((gh ^ qd) & 3) << 4) + inner;
-    }
+    (void)g;
+    (void)qd;
+    // INT8 K (A operand of S^T = K Q^T): matrix mi = (tokens 8(mi&1) + r,
+    // 16-byte unit mi>>1 of a k-step pair)
+    const int t = r + 8 * (mi & 1);
+    if constexpr (D == 128)
+      ik = t * 128 + ((((mi >> 1) ^ t) & 7) << 4);  // 128-byte rows and swizzle
+    else
+      ik = t * 64 + ((((mi >> 1) ^ (t >> 1)) & 3) << 4);  // 64-byte rows and swizzle
+    // INT8 V^T (A operand of O^T = V^T P^T): dim d is 32 bytes (16-byte
+    // units for tokens 0-15, 16-31) at unit 2(d&3) + half of 128-byte row
+    // d >> 2, with the 128-byte swizzle (unit ^= row & 7); matrix mi = (dims
+    // 8(mi&1) + r of a 16-dim tile, token half mi>>1).  Rows R, R+1 of one
+    // 8-dim phase take the 8 distinct units: no bank conflicts.
+    const int vrow = 2 * (mi & 1) + (r >> 2), vu = 2 * (r & 3) + (mi >> 1);
+    iv = vrow * 128 + (((vu ^ vrow) & 7) << 4);
   }
 };
 
@@ -65,9 +68,12 @@ struct FragOffsets {
 template <int D, bool TWO>
 struct WarpState {
   static constexpr int R = TWO ? 4 : 2;  // accumulators kept per mma tile
-  float o[D / 8][R];  // bf16-path layout: o[nt][0..1] = (row g, d 8nt+2q..+1)
-  float m[2];         // running max (log2 domain), rows g and g+8
-  float l[2];         // this lane's partial sum of exp2 (quad-reduced at the end)
+  // bf16 path: o[nt][0..1] = (row g, d 8nt+2q..+1) (+ row g+8: [2..3]).
+  // INT8 path (transposed): element (dt, nq, k) of flat index
+  // 4 (dt NQ + nq) + k holds (dim 16dt + g + 8(k>>1), query 8nq + 2q + (k&1))
+  float o[D / 8][R];
+  float m[4];  // running max (log2 domain): bf16 rows g, g+8; INT8 queries 8nq+2q+e at 2nq+e
+  float l[4];  // this lane's partial sum of exp2 (reduced across lanes at the end)
   float u;            // INT8 path: output is stored divided by this V scale
   float lu;           // log2(u)
 
@@ -76,8 +82,11 @@ struct WarpState {
     for (int i = 0; i < D / 8; ++i)
 #pragma unroll
       for (int r = 0; r < R; ++r) o[i][r] = 0.f;
-    m[0] = m[1] = -INFINITY;
-    l[0] = l[1] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      m[i] = -INFINITY;
+      l[i] = 0.f;
+    }
     u = 1.f;
     lu = 0.f;
   }
@@ -325,64 +334,156 @@ __device__ __forceinline__ void consume_bf16(WarpState<D, TWO>& st, const QFrags
 }
 
 // ----------------------------------------------------------------------
-// One 32-token INT8 chunk: K codes at sK, V codes at sV, each a 32 x D int8
-// tile (128-byte swizzle for D = 128, 64-byte swizzle for D = 64).  Scores
-// use f16 mma on the integer codes (exact in f16); the K scale is folded
-// into the score multiplier and the V scale into P (see softmax_i8), so the
-// only rounding beyond the bf16 path is P in f16.  The output accumulator
-// uses the INT8 column order: o[4J + e][0..1] hold columns 32J + 8q + e and
-// 32J + 8q + 4 + e of rows g (g+8).  Phases as for bf16 chunks.
+// One 32-token INT8 chunk: K codes at sK, a 32 x D tile (128-byte swizzle
+// for D = 128, 64-byte for D = 64), and V codes at sV, stored transposed as
+// a D x 32 tile (staged as D/4 rows of 128 bytes, 128-byte swizzle).  Codes are stored offset by 128 (byte
+// u = x + 128), so the low mantissa byte of the f16 1024.0 takes the byte
+// as it is: f16 1024 + u = x + 1152, exact.
+//
+// Both contractions run transposed, S^T = K Q^T and O^T = V^T P^T, so the
+// query group (at most 8 heads per n-tile) fills the n = 8 side of the
+// m16n8k16 tile instead of 16 rows of which at most 8 are live: half the
+// mma instructions of the untransposed form.  K and V^T fragments come
+// from ldmatrix on the code tiles (4 codes per lane and row, a permuted k
+// order matched by the other operand), and P^T from transposing the packed
+// scores in registers (movmatrix).  The K scale is folded into the score
+// multiplier and the V scale into P (see softmax_i8), so the only rounding
+// beyond the bf16 path is P in f16.  Phases as for bf16 chunks.
 // ----------------------------------------------------------------------
 template <int D, bool TWO>
 struct ScoresI8 {
-  float s[4][WarpState<D, TWO>::R];  // n-tiles of 8 tokens
+  static constexpr int NQ = TWO ? 2 : 1;  // query n-tiles of 8
+  float s[2][NQ][4];                      // [token tile][query tile][C fragment]
 };
+
+// 1024 (the f16 exponent) + 128 (the code offset); removed once per score
+// as 1152 * sum(q), not per element
+constexpr float kI8Bias = 1152.f;
+
+// four offset codes (bytes of w) -> f16x2 (byte0, byte1) and (byte2, byte3),
+// each x + 1152: the byte becomes the low mantissa byte of the f16 1024.0
+// (exponent byte 0x64)
+__device__ __forceinline__ void u8x4_to_f16x2x2_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(w), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(w), "r"(0x64646464u));
+}
+
+// the same, exact: x itself (bias subtracted per pair)
+__device__ __forceinline__ void u8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  uint32_t a, b;
+  u8x4_to_f16x2x2_biased(w, a, b);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// O^T accumulator element (dt, nq, k) inside the warp state (layout above)
+template <int D, bool TWO>
+__device__ __forceinline__ float& oT(WarpState<D, TWO>& st, int dt, int nq, int k) {
+  constexpr int R = WarpState<D, TWO>::R, NQ = TWO ? 2 : 1;
+  const int f = (dt * NQ + nq) * 4 + k;
+  return st.o[f / R][f % R];
+}
+
+// Sum of the f16 queries of this lane's score columns: query 8nq + 2q + e
+// at [nq][e] (the query fragments hold the sums of rows g, g+8).
+template <int D, bool TWO>
+__device__ __forceinline__ void query_sums_t(const QFrags<D, TWO>& qf, float (&qs)[2][2],
+                                             int lane) {
+  const int qd = lane & 3;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    qs[0][e] = __shfl_sync(0xffffffffu, qf.qsum[0], 4 * (2 * qd + e));
+    qs[1][e] = TWO ? __shfl_sync(0xffffffffu, qf.qsum[1], 4 * (2 * qd + e)) : 0.f;
+  }
+}
 
 template <int D, bool TWO>
 __device__ __forceinline__ void qk_i8(ScoresI8<D, TWO>& sc, const QFrags<D, TWO>& qf,
                                       const FragOffsets& fo, uint32_t sK) {
   constexpr int KS = D / 16;  // k-steps over the head dim
-  constexpr int R = WarpState<D, TWO>::R;
-  // S = Q (K + 1152): the codes enter the mma biased (exact in f16, one
-  // fewer instruction per pair); softmax_i8 removes 1152 * sum(q)
+  constexpr int NQ = TWO ? 2 : 1;
+  // S^T = (K + 1152) Q^T (the bias is removed in softmax_i8): per 16-token
+  // tile mt, k-steps in pairs from one ldmatrix.x4, even and odd k-steps in
+  // separate accumulation chains
   const uint32_t kbase = sK + fo.ik;
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt) {
-    float s2[R];
+  for (int mt = 0; mt < 2; ++mt) {
+    float s2[NQ][4];
 #pragma unroll
-    for (int e = 0; e < R; ++e) sc.s[nt][e] = s2[e] = 0.f;
+    for (int nq = 0; nq < NQ; ++nq)
 #pragma unroll
-    for (int hq = 0; hq < KS / 4; ++hq) {
-      // matrix mi = 16-byte column unit 4hq + mi of rows 8nt .. 8nt+7
-      const uint32_t addr = (kbase ^ (hq << 6)) + nt * 8 * D;
+      for (int k = 0; k < 4; ++k) sc.s[mt][nq][k] = s2[nq][k] = 0.f;
+#pragma unroll
+    for (int kp = 0; kp < KS / 2; ++kp) {
       uint32_t w[4];
-      ldsm_x4(addr, w[0], w[1], w[2], w[3]);
+      ldsm_x4((kbase ^ (kp << 5)) + mt * 16 * D, w[0], w[1], w[2], w[3]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int ks = 4 * hq + i;
-        uint32_t b0, b1;
-        i8x4_to_f16x2x2_biased(w[i], b0, b1);
-        if (i & 1)
-          mma_f16(s2, qf.a[ks][0], qf.a[ks][1], qf.a[ks][2], qf.a[ks][3], b0, b1);
-        else
-          mma_f16(sc.s[nt], qf.a[ks][0], qf.a[ks][1], qf.a[ks][2], qf.a[ks][3], b0, b1);
+      for (int i = 0; i < 2; ++i) {
+        const int ks = 2 * kp + i;
+        uint32_t a0, a1, a2, a3;
+        u8x4_to_f16x2x2_biased(w[2 * i], a0, a2);
+        u8x4_to_f16x2x2_biased(w[2 * i + 1], a1, a3);
+#pragma unroll
+        for (int nq = 0; nq < NQ; ++nq) {
+          const uint32_t b0 = qf.a[ks][nq ? 1 : 0], b1 = qf.a[ks][nq ? 3 : 2];
+          if (i)
+            mma_f16(s2[nq], a0, a1, a2, a3, b0, b1);
+          else
+            mma_f16(sc.s[mt][nq], a0, a1, a2, a3, b0, b1);
+        }
       }
     }
 #pragma unroll
-    for (int e = 0; e < R; ++e) sc.s[nt][e] += s2[e];
+    for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sc.s[mt][nq][k] += s2[nq][k];
   }
 }
 
-// Online softmax of an INT8 chunk.  The V scale enters through P: with the
-// output stored in units of st.u, a chunk scaled by v_scale contributes
-// P * (v_scale / st.u) * codes, so log2(v_scale / st.u) is added inside the
-// exponent; st.u moves (one rescale) only if that ratio leaves 2^+-8.
-// pa[row half][a0/a2 for k-step 0, a0/a2 for k-step 1] (f16).
+// Online-softmax update of one score column (a query) from this lane's 4
+// raw scores (the reduction runs over the 8 lanes of the same q).  As
+// softmax_row_update otherwise.
+__device__ __forceinline__ float softmax_col_update(float (&s)[4], float sl, float off, float lr,
+                                                    float inv_ratio, float& m, float& l) {
+  float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+  mx = mx * sl - off;
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+  const float m_new = fmaxf(m, mx);
+  const float alpha = ex2(m - m_new);
+  const float c = off + m_new - lr;
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    s[i] = ex2(fmaf(s[i], sl, -c));
+    sum += s[i];
+  }
+  l = l * alpha + sum * inv_ratio;
+  m = m_new;
+  return alpha;
+}
+
+// Online softmax of an INT8 chunk (every token valid).  The V scale enters
+// through P: with the output stored in units of st.u, a chunk scaled by
+// v_scale contributes P * (v_scale / st.u) * codes, so log2(v_scale / st.u)
+// is added inside the exponent; st.u moves (one rescale) only if that ratio
+// leaves 2^+-8.  pb[token tile kk][2 nq + {0, 1}]: the P^T operand (f16) of
+// tokens 16kk + 4q, 4q+1 and 4q+2, 4q+3 for query 8nq + g.
 template <int D, bool TWO>
-__device__ __forceinline__ void softmax_i8(WarpState<D, TWO>& st, const QFrags<D, TWO>& qf,
-                                           ScoresI8<D, TWO>& sc, uint32_t (&pa)[2][4],
+__device__ __forceinline__ void softmax_i8(WarpState<D, TWO>& st, const float (&qs)[2][2],
+                                           ScoresI8<D, TWO>& sc, uint32_t (&pb)[2][4],
                                            float k_scale, float v_scale, float scale_log2) {
-  constexpr int R = WarpState<D, TWO>::R;
+  constexpr int NQ = TWO ? 2 : 1;
   float lr = 0.f, inv_ratio = 1.f;
   if (v_scale > 0.f) {
     const float lv = lg2(v_scale);
@@ -392,7 +493,7 @@ __device__ __forceinline__ void softmax_i8(WarpState<D, TWO>& st, const QFrags<D
 #pragma unroll
       for (int nt = 0; nt < D / 8; ++nt)
 #pragma unroll
-        for (int e = 0; e < R; ++e) st.o[nt][e] *= f;
+        for (int e = 0; e < WarpState<D, TWO>::R; ++e) st.o[nt][e] *= f;
       st.u = v_scale;
       st.lu = lv;
       lr = 0.f;
@@ -400,67 +501,71 @@ __device__ __forceinline__ void softmax_i8(WarpState<D, TWO>& st, const QFrags<D
     inv_ratio = ex2(-lr);
   }
   const float sl = scale_log2 * k_scale;
+  float alpha[2][2];
 #pragma unroll
-  for (int rh = 0; rh < (TWO ? 2 : 1); ++rh) {
-    float x[8];
+  for (int nq = 0; nq < NQ; ++nq)
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      x[2 * nt] = sc.s[nt][2 * rh];
-      x[2 * nt + 1] = sc.s[nt][2 * rh + 1];
+    for (int e = 0; e < 2; ++e) {
+      // this lane's tokens of query 8nq + 2q + e: rows g, g+8 of both tiles
+      float x[4] = {sc.s[0][nq][e], sc.s[0][nq][2 + e], sc.s[1][nq][e], sc.s[1][nq][2 + e]};
+      // scores carry the code bias: subtract 1152 * sum(q) (times sl)
+      alpha[nq][e] = softmax_col_update(x, sl, kI8Bias * qs[nq][e] * sl, lr, inv_ratio,
+                                        st.m[2 * nq + e], st.l[2 * nq + e]);
+      sc.s[0][nq][e] = x[0];
+      sc.s[0][nq][2 + e] = x[1];
+      sc.s[1][nq][e] = x[2];
+      sc.s[1][nq][2 + e] = x[3];
     }
-    // scores carry the code bias: subtract 1152 * sum(q) (times sl)
-    const float alpha = softmax_row_update(x, sl, kI8Bias * qf.qsum[rh] * sl, lr, inv_ratio,
-                                           st.m[rh], st.l[rh]);
-    rescale_rows<D, R>(st.o, rh, alpha);
-    // k-step kk covers tokens 16kk .. 16kk+15 = score n-tiles 2kk, 2kk+1
-    pa[rh][0] = pack_f16(x[0], x[1]);
-    pa[rh][1] = pack_f16(x[2], x[3]);
-    pa[rh][2] = pack_f16(x[4], x[5]);
-    pa[rh][3] = pack_f16(x[6], x[7]);
+  // rescale the running output, skipped when no column of the warp moved
+  bool moved = false;
+#pragma unroll
+  for (int nq = 0; nq < NQ; ++nq) moved |= alpha[nq][0] != 1.f || alpha[nq][1] != 1.f;
+  if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+    for (int dt = 0; dt < D / 16; ++dt)
+#pragma unroll
+      for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) oT(st, dt, nq, k) *= alpha[nq][k & 1];
   }
-  if (!TWO) pa[1][0] = pa[1][1] = pa[1][2] = pa[1][3] = 0u;
+  // P^T operand: the 8 x 8 blocks (tile rows 0-7, 8-15) transposed
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+    for (int nq = 0; nq < NQ; ++nq) {
+      pb[kk][2 * nq] = movmatrix_t(pack_f16(sc.s[kk][nq][0], sc.s[kk][nq][1]));
+      pb[kk][2 * nq + 1] = movmatrix_t(pack_f16(sc.s[kk][nq][2], sc.s[kk][nq][3]));
+    }
+  if (!TWO) pb[0][2] = pb[0][3] = pb[1][2] = pb[1][3] = 0u;
 }
 
-// O += P V over 2 k-steps of 16 tokens (exact codes: a bias here would cost
-// output precision); V^T fragments built from 32-bit shared loads of 4
-// codes and byte interleaving.
+// O^T += V^T P^T over 2 k-steps of 16 tokens (exact codes: a bias here
+// would cost output precision).  One ldmatrix.x4 per 16-dim tile fetches
+// both k-steps' A fragments.
 template <int D, bool TWO>
-__device__ __forceinline__ void pv_i8(WarpState<D, TWO>& st, const uint32_t (&pa)[2][4],
+__device__ __forceinline__ void pv_i8(WarpState<D, TWO>& st, const uint32_t (&pb)[2][4],
                                       const FragOffsets& fo, uint32_t sV) {
-  const uint32_t vb0 = sV + fo.iv0, vb1 = sV + fo.iv1;
+  constexpr int NQ = TWO ? 2 : 1;
+  const uint32_t vbase = sV + fo.iv;
 #pragma unroll
-  for (int kk = 0; kk < 2; ++kk) {
+  for (int dt = 0; dt < D / 16; ++dt) {
+    uint32_t w[4];
+    // dims 16dt.. are rows 4dt.. of 128 bytes: (row & 7) gains 4 (dt & 1)
+    ldsm_x4((vbase ^ ((dt & 1) << 6)) + dt * 4 * 128, w[0], w[1], w[2], w[3]);
 #pragma unroll
-    for (int J = 0; J < D / 32; ++J) {
-      // rows 16kk + 2q + {0, 1, 8, 9}, 16-byte unit 2J + (g >> 2)
-      const uint32_t a0 = (vb0 ^ (J << 5)) + kk * 16 * D;
-      const uint32_t a1 = (vb1 ^ (J << 5)) + kk * 16 * D;
-      const uint32_t w0 = lds32(a0);
-      const uint32_t w1 = lds32(a1);
-      const uint32_t w2 = lds32(a0 + 8 * D);
-      const uint32_t w3 = lds32(a1 + 8 * D);
-      uint32_t lo01, hi01, lo23, hi23;
-      interleave_bytes(w0, w1, lo01, hi01);
-      interleave_bytes(w2, w3, lo23, hi23);
-      uint32_t b0[4], b1[4];
-      i8x4_to_f16x2x2(lo01, b0[0], b0[1]);
-      i8x4_to_f16x2x2(hi01, b0[2], b0[3]);
-      i8x4_to_f16x2x2(lo23, b1[0], b1[1]);
-      i8x4_to_f16x2x2(hi23, b1[2], b1[3]);
+    for (int kk = 0; kk < 2; ++kk) {
+      uint32_t a0, a1, a2, a3;
+      u8x4_to_f16x2x2(w[2 * kk], a0, a2);
+      u8x4_to_f16x2x2(w[2 * kk + 1], a1, a3);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        mma_f16(st.o[4 * J + e], pa[0][2 * kk], pa[1][2 * kk], pa[0][2 * kk + 1],
-                pa[1][2 * kk + 1], b0[e], b1[e]);
+      for (int nq = 0; nq < NQ; ++nq) {
+        float c[4] = {oT(st, dt, nq, 0), oT(st, dt, nq, 1), oT(st, dt, nq, 2), oT(st, dt, nq, 3)};
+        mma_f16(c, a0, a1, a2, a3, pb[kk][2 * nq], pb[kk][2 * nq + 1]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) oT(st, dt, nq, k) = c[k];
+      }
     }
   }
-}
-
-// Column (head-dim index) held by accumulator element (nt, e in {0,1}) of
-// lane quad position qd, for the two accumulator orders.
-template <bool I8ORDER>
-__device__ __forceinline__ int acc_col(int nt, int e, int qd) {
-  if (I8ORDER) return 32 * (nt >> 2) + 4 * (2 * qd + e) + (nt & 3);
-  return 8 * nt + 2 * qd + e;
 }
 
 }  // namespace phs

@@ -209,38 +209,6 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Four int8 codes x (bytes 0..3 of w) -> two f16x2 holding x + 1152 exactly:
-// (byte0, byte1) and (byte2, byte3).  The biased byte u = x + 128 (x XOR
-// 0x80) becomes the low mantissa byte of the f16 1024.0 (exponent byte
-// 0x64), i.e. the value 1024 + u.  The constant offset 1152 is removed once
-// per row by the caller (it contributes 1152 * sum(q) to a score and
-// 1152 * sum(p) to an output), not per element.
-__device__ __forceinline__ void i8x4_to_f16x2x2_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
-}
-
-constexpr float kI8Bias = 1152.f;  // 1024 (f16 exponent) + 128 (byte bias)
-
-// Exact variant: two f16x2 holding x itself (the bias subtracted per pair).
-__device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  uint32_t a, b;
-  i8x4_to_f16x2x2_biased(w, a, b);
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
-  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
-  lo = *reinterpret_cast<uint32_t*>(&ha);
-  hi = *reinterpret_cast<uint32_t*>(&hb);
-}
-
-// Byte interleave of two words: (a0, b0, a1, b1) and (a2, b2, a3, b3).
-__device__ __forceinline__ void interleave_bytes(uint32_t a, uint32_t b, uint32_t& lo,
-                                                 uint32_t& hi) {
-  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(lo) : "r"(a), "r"(b));
-  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(hi) : "r"(a), "r"(b));
-}
-
 // Hardware base-2 exponential and logarithm (PTX ex2/lg2.approx, flush to
 // zero).  Softmax arguments are <= 0 here, so results below 2^-126 flush to 0.
 __device__ __forceinline__ float ex2(float x) {

@@ -79,6 +79,8 @@ __device__ __forceinline__ int walk_chunks(WarpState<D, TWO>& st, const QFrags<D
   using Scores = typename std::conditional<I8, ScoresI8<D, TWO>, ScoresBf16<D, TWO>>::type;
   Scores sc;
   uint32_t pa[2][I8 ? 4 : 2];
+  float qs[2][2];  // INT8: query sums of this lane's score columns
+  if constexpr (I8) query_sums_t(qf, qs, lane);
   auto sK = [&](int j) { return sbase + (j % S) * kStage; };
   auto wait = [&](int j) {
     const bool done = mbar_wait(bar0 + 8 * (j % S), (j / S) & 1);
@@ -106,7 +108,7 @@ __device__ __forceinline__ int walk_chunks(WarpState<D, TWO>& st, const QFrags<D
   };
   auto softmax = [&](int j, uint32_t valid) {
     if constexpr (I8)
-      softmax_i8(st, qf, sc, pa, kss[j], vss[j], scale_log2);
+      softmax_i8(st, qs, sc, pa, kss[j], vss[j], scale_log2);
     else
       softmax_bf16(st, sc, pa, valid, scale_log2, lane);
   };
@@ -262,10 +264,10 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
       return;
     }
     mbar_arrive_expect_tx(bar, L::kStage);
-    if (is_i8) {
-      const int row = (id * a.Hkv + h) * kQBlock;
-      tma_load_2d(dst, tk8, 0, row, bar, pol);
-      tma_load_2d(dst + L::kStage / 2, tv8, 0, row, bar, pol);
+    if (is_i8) {  // K: 32 rows of D codes; V^T: D/4 rows of 128 bytes
+      const int kv = id * a.Hkv + h;
+      tma_load_2d(dst, tk8, 0, kv * kQBlock, bar, pol);
+      tma_load_2d(dst + L::kStage / 2, tv8, 0, kv * (D / 4), bar, pol);
     } else {
       const int row = (id * a.Hkv + h) * kPage;
       if constexpr (D == 128) {  // one 4 KB box per page: [half][16 rows]
@@ -348,28 +350,57 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
 
   // ---- warp result -> shared memory -> CTA merge
   const int g = lane >> 2, qd = lane & 3;
-  float lsum[2];
+  float lsum[4];
+  if (is_i8) {  // query columns: reduce over the 8 lanes of the same q
 #pragma unroll
-  for (int rh = 0; rh < 2; ++rh) lsum[rh] = warp_sum_quad(st.l[rh]);
-  const float oscale = is_i8 ? st.u : 1.f;
+    for (int i = 0; i < 4; ++i) {
+      float v = st.l[i];
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      lsum[i] = v;
+    }
+  } else {  // query rows: reduce over the quad
+#pragma unroll
+    for (int rh = 0; rh < 2; ++rh) lsum[rh] = warp_sum_quad(st.l[rh]);
+  }
   __syncthreads();  // every warp is done with its stages
   float* sO = reinterpret_cast<float*>(smem);
   float* sM = sO + NW * GR * D;
   float* sL = sM + NW * GR;
+  if (is_i8) {
+    // O^T element (dt, nq, k): dim 16dt + g + 8(k>>1), query 8nq + 2q + (k&1);
+    // the output is held in units of the V scale st.u
 #pragma unroll
-  for (int rh = 0; rh < (TWO ? 2 : 1); ++rh) {
-    const int row = g + 8 * rh;
-    if (row < G) {
+    for (int nq = 0; nq < (TWO ? 2 : 1); ++nq)
 #pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt)
+      for (int e = 0; e < 2; ++e) {
+        const int row = 8 * nq + 2 * qd + e;
+        if (row < G) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int col = is_i8 ? acc_col<true>(nt, e, qd) : acc_col<false>(nt, e, qd);
-          sO[(warp * GR + row) * D + col] = st.o[nt][2 * rh + e] * oscale;
+          for (int dt = 0; dt < D / 16; ++dt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+              sO[(warp * GR + row) * D + 16 * dt + 8 * hh + g] = oT(st, dt, nq, 2 * hh + e) * st.u;
+          if (g == 0) {
+            sM[warp * GR + row] = st.m[2 * nq + e];
+            sL[warp * GR + row] = lsum[2 * nq + e];
+          }
         }
-      if (qd == 0) {
-        sM[warp * GR + row] = st.m[rh];
-        sL[warp * GR + row] = lsum[rh];
+      }
+  } else {
+#pragma unroll
+    for (int rh = 0; rh < (TWO ? 2 : 1); ++rh) {
+      const int row = g + 8 * rh;
+      if (row < G) {
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) sO[(warp * GR + row) * D + 8 * nt + 2 * qd + e] = st.o[nt][2 * rh + e];
+        if (qd == 0) {
+          sM[warp * GR + row] = st.m[rh];
+          sL[warp * GR + row] = lsum[rh];
+        }
       }
     }
   }

@@ -14,6 +14,13 @@ namespace phs {
 constexpr int kPage = 16;    // tokens per Full-pool page
 constexpr int kQBlock = 32;  // tokens per INT8 page / scale group
 
+// Token held by byte p (0..15) of a 16-token half of an INT8 V^T row:
+// bytes 4q, 4q+1 hold tokens 2q, 2q+1 and bytes 4q+2, 4q+3 tokens 8+2q,
+// 9+2q.  The decode kernel transposes the two 8 x 8 blocks of a tile's
+// packed scores (movmatrix), which gives lane q the P^T operand of exactly
+// those tokens, in the order ldmatrix delivers bytes 4q..4q+3 of a V^T row.
+constexpr int kI8VtToken(int p) { return 2 * (p >> 2) + (p & 1) + 8 * ((p >> 1) & 1); }
+
 // ----------------------------------------------------- split-KV decode --
 struct SplitArgs {
   const __nv_bfloat16* q;   // [B][Hq][D]
@@ -248,8 +255,8 @@ struct QuantArgs {
   const __nv_bfloat16* k_src;
   const __nv_bfloat16* v_src;
   const int32_t* src_table;
-  int8_t* k_codes;
-  int8_t* v_codes;
+  uint8_t* k_codes;  // stored form of phs_int8_pool
+  uint8_t* v_codes;
   float* k_scale;
   float* v_scale;
   const int32_t* dst_qtable;

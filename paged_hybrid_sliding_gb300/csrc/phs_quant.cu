@@ -11,8 +11,14 @@
 // One CTA of four warps per (request, block, KV head): warps 0-1 quantise
 // K, warps 2-3 V, each warp one 16-token source page (a contiguous tile read
 // with 16-byte streaming loads and kept in registers).  The two halves of a
-// group combine their absmax through shared memory; codes go out with
-// 8-byte stores in the same piece order.
+// group combine their absmax through shared memory.
+//
+// Stored form (the layout the decode kernels' fragments want): each code
+// is kept as the byte x + 128.  K codes are token-major, 32 rows of D bytes
+// per block and head, written with 8-byte stores in piece order.  V codes
+// are transposed, D rows of 32 bytes (one per head dim); within each
+// 16-token half of a row, byte p holds token kI8VtToken(p).  The V warps
+// stage their codes in shared memory and write the rows as 16-byte pieces.
 #include "phs_common.cuh"
 #include "phs_internal.h"
 
@@ -22,6 +28,9 @@ namespace phs {
 // nearest integer (ties to even, the default rounding) and keeps it in the
 // low mantissa bits, so the code byte is the low byte of the sum's bits.
 constexpr float kRoundMagic = 12582912.0f;
+// The same plus 128: fl(rint(y) + 128 + 1.5 * 2^23) (128 is even, so the
+// ties still go to even) leaves the stored byte x + 128 in the low bits.
+constexpr float kRoundMagicOffset = 12582912.0f + 128.0f;
 
 // Packed fp32 pairs (two lanes of work per instruction on the FMA pipe,
 // each rounded to nearest as the scalar instruction would) and the
@@ -71,6 +80,7 @@ __global__ void __launch_bounds__(128, 8) phs_quant_kernel(const QuantArgs a) {
   const int which = warp >> 1;  // 0 = K, 1 = V
   const int half = warp & 1;    // tokens 16*half .. 16*half+15 = source page 2j+half
   __shared__ float s_amax[4];
+  __shared__ __align__(16) uint8_t s_v[kQBlock * D];  // V codes, token-major
   if (jr >= a.num_qblocks[b]) return;
   const int j = a.first_qblock[b] + jr;
   if (j < 0 || j >= a.dst_max_qpages) {
@@ -91,7 +101,7 @@ __global__ void __launch_bounds__(128, 8) phs_quant_kernel(const QuantArgs a) {
     return;
   }
   const __nv_bfloat16* src = which ? a.v_src : a.k_src;
-  int8_t* codes = which ? a.v_codes : a.k_codes;
+  uint8_t* codes = which ? a.v_codes : a.k_codes;
   float* scales = which ? a.v_scale : a.k_scale;
   // one contiguous 16 x D tile: lane takes 16-byte pieces lane, lane + 32, ...
   const uint4* tile =
@@ -128,9 +138,11 @@ __global__ void __launch_bounds__(128, 8) phs_quant_kernel(const QuantArgs a) {
   // code 0.  The rounding steps run on packed pairs (two elements per
   // instruction, each rounded as the scalar operation would be).
   const bool always_divide = !(rs < INFINITY);
-  const uint64_t rs2 = f2_pack(rs, rs), magic2 = f2_pack(kRoundMagic, kRoundMagic);
-  uint2* out = reinterpret_cast<uint2*>(codes + ((static_cast<size_t>(qp) * a.Hkv + h) * kQBlock +
-                                                 kPage * half) * D);
+  const uint64_t rs2 = f2_pack(rs, rs), magic2 = f2_pack(kRoundMagicOffset, kRoundMagicOffset);
+  const size_t block = static_cast<size_t>(qp) * a.Hkv + h;  // (block, head) of 32 x D codes
+  // K: straight to the pool; V: into the shared token-major tile
+  uint2* out = which ? reinterpret_cast<uint2*>(s_v + kPage * half * D)
+                     : reinterpret_cast<uint2*>(codes + (block * kQBlock + kPage * half) * D);
 #pragma unroll
   for (int it = 0; it < kIters; ++it) {
     const uint32_t* v = reinterpret_cast<const uint32_t*>(&x[it]);
@@ -153,7 +165,7 @@ __global__ void __launch_bounds__(128, 8) phs_quant_kernel(const QuantArgs a) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float xv = __uint_as_float(e & 1 ? v[e >> 1] & 0xFFFF0000u : v[e >> 1] << 16);
-        t[e] = __float_as_uint(__fadd_rn(rintf(__fdiv_rn(xv, s)), kRoundMagic));
+        t[e] = __float_as_uint(__fadd_rn(rintf(__fdiv_rn(xv, s)), kRoundMagicOffset));
       }
     }
     uint32_t w[2];
@@ -165,7 +177,25 @@ __global__ void __launch_bounds__(128, 8) phs_quant_kernel(const QuantArgs a) {
     }
     out[it * 32 + lane] = make_uint2(w[0], w[1]);
   }
-  if (threadIdx.x == 64 * which && half == 0) scales[static_cast<size_t>(qp) * a.Hkv + h] = s;
+  if (threadIdx.x == 64 * which && half == 0) scales[block] = s;
+  __syncthreads();  // the V tile is complete
+  if (which) {
+    // V^T piece (d, th): dim d, tokens 16th + kI8VtToken(0..15), 16 bytes
+    uint4* vt = reinterpret_cast<uint4*>(codes + block * kQBlock * D);
+    for (int i = threadIdx.x - 64; i < 2 * D; i += 64) {
+      const int th = i / D, d = i % D;  // a warp reads 32 consecutive bytes of a token row
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          v |= static_cast<uint32_t>(s_v[(16 * th + kI8VtToken(4 * k + b)) * D + d]) << (8 * b);
+        w[k] = v;
+      }
+      vt[2 * d + th] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
 }
 
 int launch_quant(const QuantArgs& a, int max_qblocks, int B, cudaStream_t stream) {

@@ -64,3 +64,35 @@ def test_hybrid_kv_tokens_matches_oracle():
     assert f == oracle.kv_tokens_stored(lf * 0 + lf, wl.n_after, 128) - s
     allf = oracle.kv_tokens_stored(np.ones(70, np.int32), wl.n_after, 128)
     assert abs((f + s) / allf - 1 / 7) / (1 / 7) < 0.05
+
+
+def test_int8_pool_codes_reads_the_stored_form():
+    """Int8Pool.codes() undoes the stored form include/phs.h states for
+    phs_int8_pool: byte x + 128; K token-major; V one 32-byte row per head
+    dim, byte p of 16-token half hf holding token 16 hf + 2(p/4) + (p%2) +
+    8((p/2)%2).  The stored pool is written here element by element from
+    that statement."""
+    import torch
+    g = torch.Generator().manual_seed(7)
+    n, h, D = 2, 3, 8
+    kc = torch.randint(-127, 128, (n, h, 32, D), generator=g)
+    vc = torch.randint(-127, 128, (n, h, 32, D), generator=g)
+    k = torch.empty((n, h, 32, D), dtype=torch.uint8)
+    v = torch.empty((n, h, D, 32), dtype=torch.uint8)
+    for i in range(n):
+        for j in range(h):
+            for t in range(32):
+                for d in range(D):
+                    k[i, j, t, d] = int(kc[i, j, t, d]) + 128
+            for d in range(D):
+                for hf in range(2):
+                    for p in range(16):
+                        t = 16 * hf + 2 * (p // 4) + p % 2 + 8 * ((p // 2) % 2)
+                        v[i, j, d, 16 * hf + p] = int(vc[i, j, t, d]) + 128
+    pool = phs.Int8Pool(k, v, torch.zeros(n, h), torch.zeros(n, h))
+    gk, gv = pool.codes()
+    assert gk.dtype == torch.int8 and torch.equal(gk.long(), kc)
+    assert gv.dtype == torch.int8 and torch.equal(gv.long(), vc)
+    gk1, gv1 = pool.codes(torch.tensor([1]))
+    assert torch.equal(gk1.long(), kc[1:]) and torch.equal(gv1.long(), vc[1:])
+    assert sorted(phs.VT_TOKEN) == list(range(16))

@@ -101,7 +101,7 @@ def test_quant_int8_bitexact(D, Hkv):
     src = phs.PagedPool(bf16_dev(kp), bf16_dev(vp))
     dst = phs.Int8Pool.empty(nq, Hkv, D)
     for t in (dst.k, dst.v):
-        t.zero_()
+        t.fill_(128)  # the stored form of code 0
     dst.k_scale.zero_()
     dst.v_scale.zero_()
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -109,8 +109,9 @@ def test_quant_int8_bitexact(D, Hkv):
                               status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    assert np.array_equal(dst.k.cpu().numpy(), kc)
-    assert np.array_equal(dst.v.cpu().numpy(), vc)
+    gk, gv = dst.codes()
+    assert np.array_equal(gk.cpu().numpy(), kc)
+    assert np.array_equal(gv.cpu().numpy(), vc)
     assert np.array_equal(dst.k_scale.cpu().numpy().view(np.uint32), ks.view(np.uint32))
     assert np.array_equal(dst.v_scale.cpu().numpy().view(np.uint32), vs.view(np.uint32))
     assert (ks == 0).any()  # the zero group really was zero
@@ -150,6 +151,7 @@ def test_quant_int8_half_integer_quotients_bitexact(scale_pow):
     phs.kv_quant_int8_block32(src, dev(bt), dst, dev(qt), dev(np.zeros(1, np.int32)),
                               dev(np.array([2], np.int32)), 2)
     torch.cuda.synchronize()
-    assert np.array_equal(dst.k.cpu().numpy(), kc)
-    assert np.array_equal(dst.v.cpu().numpy(), vc)
+    gk, gv = dst.codes()
+    assert np.array_equal(gk.cpu().numpy(), kc)
+    assert np.array_equal(gv.cpu().numpy(), vc)
     assert np.array_equal(dst.k_scale.cpu().numpy(), ks)

@@ -174,8 +174,9 @@ def test_config4_full_size_sampled():
                                      nqb[rows]) == 0
     gpu_ids = torch.from_numpy(np.concatenate([qt[b, :nqb[b]] for b in rows]).astype(np.int64))
     gpu_ids = gpu_ids.cuda()
-    assert np.array_equal(i8.k.index_select(0, gpu_ids).cpu().numpy(), kc)
-    assert np.array_equal(i8.v.index_select(0, gpu_ids).cpu().numpy(), vc)
+    gk, gv = i8.codes(gpu_ids)
+    assert np.array_equal(gk.cpu().numpy(), kc)
+    assert np.array_equal(gv.cpu().numpy(), vc)
     assert np.array_equal(i8.k_scale.index_select(0, gpu_ids).cpu().numpy(), ks)
     assert np.array_equal(i8.v_scale.index_select(0, gpu_ids).cpu().numpy(), vs)
     qh, knh, vnh = synth.bits(q)[rows], synth.bits(kn)[rows], synth.bits(vn)[rows]

@@ -218,15 +218,17 @@ def test_int8_decode(D, Hq, Hkv, tps):
     c = int8_case(lens, qlens, Hq, Hkv, D, seed=300 + D + Hq)
     src = phs.PagedPool(bf16_dev(c["kp"]), bf16_dev(c["vp"]))
     i8 = phs.Int8Pool.empty(c["nq"], Hkv, D)
-    for t in (i8.k, i8.v, i8.k_scale, i8.v_scale):
+    for t in (i8.k, i8.v):
+        t.fill_(128)  # the stored form of code 0
+    for t in (i8.k_scale, i8.v_scale):
         t.zero_()
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     phs.kv_quant_int8_block32(src, dev(c["bt"]), i8, dev(c["qt"]),
                               dev(np.zeros(len(lens), np.int32)), dev(c["nqb"]),
                               int(c["nqb"].max()), status=st)
     torch.cuda.synchronize()
-    assert np.array_equal(i8.k.cpu().numpy(), c["kc"]) and np.array_equal(i8.v.cpu().numpy(),
-                                                                           c["vc"])
+    gk, gv = i8.codes()
+    assert np.array_equal(gk.cpu().numpy(), c["kc"]) and np.array_equal(gv.cpu().numpy(), c["vc"])
     assert np.array_equal(i8.k_scale.cpu().numpy(), c["ks"])
     # the bf16 copy of the INT8 region is not read by decode: scribble on it
     for b, ql in enumerate(c["qlens"]):

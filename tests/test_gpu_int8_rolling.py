@@ -50,13 +50,14 @@ def test_int8_hot_to_warm_handoff_over_steps():
 
     def same_int8():
         torch.cuda.synchronize()
-        return (np.array_equal(i8.k.cpu().numpy(), hkc) and np.array_equal(i8.v.cpu().numpy(), hvc)
+        gk, gv = i8.codes()
+        return (np.array_equal(gk.cpu().numpy(), hkc) and np.array_equal(gv.cpu().numpy(), hvc)
                 and np.array_equal(i8.k_scale.cpu().numpy(), hks)
                 and np.array_equal(i8.v_scale.cpu().numpy(), hvs))
 
     # set-up: the warm zone [0, qlen) quantised once
-    i8.k.zero_()
-    i8.v.zero_()
+    i8.k.fill_(128)  # the stored form of code 0
+    i8.v.fill_(128)
     i8.k_scale.zero_()
     i8.v_scale.zero_()
     quantise(np.zeros(B, np.int32), (qlen // QB).astype(np.int32))

@@ -97,7 +97,8 @@ def test_noalloc_int8_region():
         torch.cuda.synchronize()
         assert int(st.item()) == 0
         assert_close(out_np(out), out_np(ref), "INT8 no-allocation vs workspace entry point")
-    codes = dict(k_codes=i8.k.cpu().numpy(), v_codes=i8.v.cpu().numpy(),
+    gk, gv = i8.codes()
+    codes = dict(k_codes=gk.cpu().numpy(), v_codes=gv.cpu().numpy(),
                  k_scale=i8.k_scale.cpu().numpy(), v_scale=i8.v_scale.cpu().numpy(),
                  qtable=qt, qlens=qlen)
     hk, hv = synth.bits(pool.k), synth.bits(pool.v)
