@@ -101,13 +101,14 @@ typedef struct {
 
 /* INT8 pool: 32-token pages of codes plus one fp32 scale per page and head.
  * A code x in [-127, 127] is stored as the byte x + 128.  K is token-major.
- * V is transposed: one 32-byte row per head dim, and within each 16-token
- * half of a row, byte p holds token 2(p/4) + (p%2) + 8((p/2)%2).  These are
- * the orders in which the decode kernel's mma fragments read the codes.
- * Each is 32 * D bytes per page and head. */
+ * V is transposed per 16-token half of the page: D rows of 16 bytes (one per
+ * head dim) for tokens 0-15, then D rows for tokens 16-31; byte p of a row
+ * holds token 2(p/4) + (p%2) + 8((p/2)%2) of its half.  These are the orders
+ * in which the decode kernel's mma fragments read the codes.  Each is
+ * 32 * D bytes per page and head. */
 typedef struct {
     uint8_t *k;           /* device, [num_qpages][Hkv][32 tokens][D] */
-    uint8_t *v;           /* device, [num_qpages][Hkv][D][32 tokens, order above] */
+    uint8_t *v;           /* device, [num_qpages][Hkv][2 halves][D][16 tokens, order above] */
     float *k_scale;       /* device, fp32 [num_qpages][Hkv] */
     float *v_scale;
     int64_t num_qpages;

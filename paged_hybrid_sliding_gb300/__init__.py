@@ -137,9 +137,9 @@ VT_TOKEN = tuple(2 * (p >> 2) + (p & 1) + 8 * ((p >> 1) & 1) for p in range(16))
 @dataclass
 class Int8Pool:
     """INT8 pool in its stored form (each code x as the byte x + 128):
-    k uint8 [num_qpages, Hkv, 32 tokens, D]; v uint8 [num_qpages, Hkv, D,
-    32] (transposed; byte p of each 16-token half holds token VT_TOKEN[p]);
-    scales fp32 [num_qpages, Hkv]."""
+    k uint8 [num_qpages, Hkv, 32 tokens, D]; v uint8 [num_qpages, Hkv, 2,
+    D, 16] (transposed per 16-token half; byte p of a row holds token
+    VT_TOKEN[p] of its half); scales fp32 [num_qpages, Hkv]."""
     k: torch.Tensor
     v: torch.Tensor
     k_scale: torch.Tensor
@@ -147,11 +147,11 @@ class Int8Pool:
 
     def c(self):
         _need(self.k, torch.uint8, "int8.k", 4)
-        _need(self.v, torch.uint8, "int8.v", 4)
+        _need(self.v, torch.uint8, "int8.v", 5)
         _need(self.k_scale, torch.float32, "int8.k_scale", 2)
         _need(self.v_scale, torch.float32, "int8.v_scale", 2)
         n, h, q, d = self.k.shape
-        if q != QBLOCK or tuple(self.v.shape) != (n, h, d, QBLOCK) \
+        if q != QBLOCK or tuple(self.v.shape) != (n, h, 2, d, QBLOCK // 2) \
                 or tuple(self.k_scale.shape) != (n, h) or tuple(self.v_scale.shape) != (n, h):
             raise ValueError("inconsistent INT8 pool shapes")
         return _lib.Int8PoolC(self.k.data_ptr(), self.v.data_ptr(), self.k_scale.data_ptr(),
@@ -164,10 +164,12 @@ class Int8Pool:
         k, v = self.k, self.v
         if pages is not None:
             k, v = k.index_select(0, pages), v.index_select(0, pages)
+        # stored row 16 hf + p (half hf, byte p) holds token 16 hf + VT_TOKEN[p]
         order = torch.tensor([16 * hf + t for hf in range(2) for t in VT_TOKEN], device=v.device)
         inv = torch.empty_like(order)
         inv[order] = torch.arange(QBLOCK, device=v.device)
-        vt = v.transpose(-1, -2).index_select(-2, inv)  # [.., token, D]
+        rows = v.transpose(-1, -2).reshape(*v.shape[:2], QBLOCK, v.shape[3])  # [.., 16 hf + p, D]
+        vt = rows.index_select(-2, inv)  # [.., token, D]
         return ((k.to(torch.int16) - 128).to(torch.int8),
                 (vt.to(torch.int16) - 128).to(torch.int8).contiguous())
 
@@ -176,7 +178,7 @@ class Int8Pool:
         return Int8Pool(
             torch.empty((num_qpages, num_kv_heads, QBLOCK, head_dim), dtype=torch.uint8,
                         device=device),
-            torch.empty((num_qpages, num_kv_heads, head_dim, QBLOCK), dtype=torch.uint8,
+            torch.empty((num_qpages, num_kv_heads, 2, head_dim, QBLOCK // 2), dtype=torch.uint8,
                         device=device),
             torch.empty((num_qpages, num_kv_heads), dtype=torch.float32, device=device),
             torch.empty((num_qpages, num_kv_heads), dtype=torch.float32, device=device))

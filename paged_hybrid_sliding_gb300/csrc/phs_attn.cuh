@@ -52,13 +52,13 @@ struct FragOffsets {
       ik = t * 128 + ((((mi >> 1) ^ t) & 7) << 4);  // 128-byte rows and swizzle
     else
       ik = t * 64 + ((((mi >> 1) ^ (t >> 1)) & 3) << 4);  // 64-byte rows and swizzle
-    // INT8 V^T (A operand of O^T = V^T P^T): dim d is 32 bytes (16-byte
-    // units for tokens 0-15, 16-31) at unit 2(d&3) + half of 128-byte row
-    // d >> 2, with the 128-byte swizzle (unit ^= row & 7); matrix mi = (dims
-    // 8(mi&1) + r of a 16-dim tile, token half mi>>1).  Rows R, R+1 of one
-    // 8-dim phase take the 8 distinct units: no bank conflicts.
-    const int vrow = 2 * (mi & 1) + (r >> 2), vu = 2 * (r & 3) + (mi >> 1);
-    iv = vrow * 128 + (((vu ^ vrow) & 7) << 4);
+    // INT8 V^T (A operand of O^T = V^T P^T): token half th is D rows of 16
+    // bytes, i.e. 128-byte row th D/8 + d/8 holds dims d..d+7 of that half,
+    // staged with the 128-byte swizzle (unit ^= row & 7).  Matrix mi = (dims
+    // 8(mi&1) + r of a 16-dim tile, token half mi>>1): its 8 rows are the 8
+    // units of one 128-byte row, so no bank conflicts.
+    const int vrow = (mi >> 1) * (D / 8) + (mi & 1);
+    iv = vrow * 128 + (((r ^ vrow) & 7) << 4);
   }
 };
 
@@ -335,8 +335,9 @@ __device__ __forceinline__ void consume_bf16(WarpState<D, TWO>& st, const QFrags
 
 // ----------------------------------------------------------------------
 // One 32-token INT8 chunk: K codes at sK, a 32 x D tile (128-byte swizzle
-// for D = 128, 64-byte for D = 64), and V codes at sV, stored transposed as
-// a D x 32 tile (staged as D/4 rows of 128 bytes, 128-byte swizzle).  Codes are stored offset by 128 (byte
+// for D = 128, 64-byte for D = 64), and V codes at sV, stored transposed:
+// two 16-token halves of D rows of 16 bytes (staged as D/4 rows of 128
+// bytes, 128-byte swizzle).  Codes are stored offset by 128 (byte
 // u = x + 128), so the low mantissa byte of the f16 1024.0 takes the byte
 // as it is: f16 1024 + u = x + 1152, exact.
 //
@@ -550,8 +551,9 @@ __device__ __forceinline__ void pv_i8(WarpState<D, TWO>& st, const uint32_t (&pb
 #pragma unroll
   for (int dt = 0; dt < D / 16; ++dt) {
     uint32_t w[4];
-    // dims 16dt.. are rows 4dt.. of 128 bytes: (row & 7) gains 4 (dt & 1)
-    ldsm_x4((vbase ^ ((dt & 1) << 6)) + dt * 4 * 128, w[0], w[1], w[2], w[3]);
+    // dims 16dt.. of a half are its 128-byte rows 2dt, 2dt+1: (row & 7)
+    // gains 2dt mod 8
+    ldsm_x4((vbase ^ (((2 * dt) & 7) << 4)) + dt * 2 * 128, w[0], w[1], w[2], w[3]);
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       uint32_t a0, a1, a2, a3;

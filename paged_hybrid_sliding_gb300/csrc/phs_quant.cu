@@ -16,9 +16,10 @@
 // Stored form (the layout the decode kernels' fragments want): each code
 // is kept as the byte x + 128.  K codes are token-major, 32 rows of D bytes
 // per block and head, written with 8-byte stores in piece order.  V codes
-// are transposed, D rows of 32 bytes (one per head dim); within each
-// 16-token half of a row, byte p holds token kI8VtToken(p).  The V warps
-// stage their codes in shared memory and write the rows as 16-byte pieces.
+// are transposed per 16-token half: D rows of 16 bytes (one per head dim)
+// for tokens 0-15, then D rows for tokens 16-31; byte p of a row holds
+// token kI8VtToken(p) of its half.  Each V warp stages its 16 tokens' codes
+// in shared memory and writes its half (2 KB, contiguous).
 #include "phs_common.cuh"
 #include "phs_internal.h"
 
@@ -178,22 +179,33 @@ __global__ void __launch_bounds__(128, 8) phs_quant_kernel(const QuantArgs a) {
     out[it * 32 + lane] = make_uint2(w[0], w[1]);
   }
   if (threadIdx.x == 64 * which && half == 0) scales[block] = s;
-  __syncthreads();  // the V tile is complete
   if (which) {
-    // V^T piece (d, th): dim d, tokens 16th + kI8VtToken(0..15), 16 bytes
+    // V^T: each V warp transposes its own 16-token half (the rows it just
+    // staged), lane w taking dims 4w..4w+3.  Output word q of a dim's
+    // 16-byte row holds tokens 2q, 2q+1, 2q+8, 2q+9 of the half
+    // (kI8VtToken): the 4 x 4 byte transpose of those 4 token rows' words w
+    // (two levels of byte permutes).
+    __syncwarp();
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(s_v);
     uint4* vt = reinterpret_cast<uint4*>(codes + block * kQBlock * D);
-    for (int i = threadIdx.x - 64; i < 2 * D; i += 64) {
-      const int th = i / D, d = i % D;  // a warp reads 32 consecutive bytes of a token row
-      uint32_t w[4];
+    constexpr int W = D / 4;  // words per token row
+    for (int w = lane; w < W; w += 32) {
+      uint32_t o[4][4];  // [dim k][word q]
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t v = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-          v |= static_cast<uint32_t>(s_v[(16 * th + kI8VtToken(4 * k + b)) * D + d]) << (8 * b);
-        w[k] = v;
+      for (int q = 0; q < 4; ++q) {
+        const int t0 = 16 * half + kI8VtToken(4 * q);  // tokens t0, t0+1, t0+8, t0+9
+        const uint32_t r0 = sw[t0 * W + w], r1 = sw[(t0 + 1) * W + w];
+        const uint32_t r2 = sw[(t0 + 8) * W + w], r3 = sw[(t0 + 9) * W + w];
+        const uint32_t a = __byte_perm(r0, r1, 0x5140), b = __byte_perm(r0, r1, 0x7362);
+        const uint32_t c = __byte_perm(r2, r3, 0x5140), d = __byte_perm(r2, r3, 0x7362);
+        o[0][q] = __byte_perm(a, c, 0x5410);
+        o[1][q] = __byte_perm(a, c, 0x7632);
+        o[2][q] = __byte_perm(b, d, 0x5410);
+        o[3][q] = __byte_perm(b, d, 0x7632);
       }
-      vt[2 * d + th] = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        vt[half * D + 4 * w + k] = make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
     }
   }
 }

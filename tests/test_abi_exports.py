@@ -68,8 +68,8 @@ def test_hybrid_kv_tokens_matches_oracle():
 
 def test_int8_pool_codes_reads_the_stored_form():
     """Int8Pool.codes() undoes the stored form include/phs.h states for
-    phs_int8_pool: byte x + 128; K token-major; V one 32-byte row per head
-    dim, byte p of 16-token half hf holding token 16 hf + 2(p/4) + (p%2) +
+    phs_int8_pool: byte x + 128; K token-major; V per 16-token half hf, one
+    16-byte row per head dim, byte p holding token 16 hf + 2(p/4) + (p%2) +
     8((p/2)%2).  The stored pool is written here element by element from
     that statement."""
     import torch
@@ -78,7 +78,7 @@ def test_int8_pool_codes_reads_the_stored_form():
     kc = torch.randint(-127, 128, (n, h, 32, D), generator=g)
     vc = torch.randint(-127, 128, (n, h, 32, D), generator=g)
     k = torch.empty((n, h, 32, D), dtype=torch.uint8)
-    v = torch.empty((n, h, D, 32), dtype=torch.uint8)
+    v = torch.empty((n, h, 2, D, 16), dtype=torch.uint8)
     for i in range(n):
         for j in range(h):
             for t in range(32):
@@ -88,7 +88,7 @@ def test_int8_pool_codes_reads_the_stored_form():
                 for hf in range(2):
                     for p in range(16):
                         t = 16 * hf + 2 * (p // 4) + p % 2 + 8 * ((p // 2) % 2)
-                        v[i, j, d, 16 * hf + p] = int(vc[i, j, t, d]) + 128
+                        v[i, j, hf, d, p] = int(vc[i, j, t, d]) + 128
     pool = phs.Int8Pool(k, v, torch.zeros(n, h), torch.zeros(n, h))
     gk, gv = pool.codes()
     assert gk.dtype == torch.int8 and torch.equal(gk.long(), kc)
