@@ -210,7 +210,8 @@ def int8_case(lens, qlens, Hq, Hkv, D, seed):
     return c
 
 
-@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 8, 2), (128, 32, 2), (128, 8, 8)])
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 8, 2), (128, 32, 2), (128, 8, 8),
+                                     (128, 24, 4), (64, 20, 2)])
 @pytest.mark.parametrize("tps", [0, 64, 256])
 def test_int8_decode(D, Hq, Hkv, tps):
     lens = [33, 1100, 2100, 1056, 5000, 40]
