@@ -18,9 +18,8 @@
 // per block and head, written with 8-byte stores in piece order.  V codes
 // are transposed per 16-token half: D rows of 16 bytes (one per head dim)
 // for tokens 0-15, then D rows for tokens 16-31; byte p of a row holds
-// token kI8VtToken(p) of its half.  The V warps read their page by columns
-// (each lane the same 4 dims of every token), so a lane's codes pack
-// straight into V^T rows; each V warp writes its half (contiguous).
+// token kI8VtToken(p) of its half.  Each V warp stages its 16 tokens' codes
+// in shared memory and writes its half (2 KB, contiguous).
 #include "phs_common.cuh"
 #include "phs_internal.h"
 
@@ -75,19 +74,14 @@ __device__ __forceinline__ float fmin3(float a, float b, float c) {
 
 template <int D>
 __global__ void __launch_bounds__(128, 8) phs_quant_kernel(const QuantArgs a) {
-  constexpr int kPieces = D / 8;                // 16-byte pieces per token row
-  constexpr int kIters = kPage * kPieces / 32;  // 8-element units per lane
-  // V warps read the tile by columns: lane (tg, w) takes 8 bytes (dims
-  // 4w..4w+3) of tokens tg*kTpl .. tg*kTpl + kTpl - 1 of the page
-  constexpr int kW8 = D / 4;            // 8-byte words per token row (32 or 16)
-  constexpr int kTg = 32 / kW8;         // token groups across the warp (1 or 2)
-  constexpr int kTpl = kPage / kTg;     // tokens per lane (16 or 8)
-  static_assert(kTpl == 2 * kIters, "a V unit is two tokens x 4 dims");
+  constexpr int kPieces = D / 8;              // 16-byte pieces per token row
+  constexpr int kIters = kPage * kPieces / 32;  // pieces of one page tile per lane
   const int jr = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int which = warp >> 1;  // 0 = K, 1 = V
   const int half = warp & 1;    // tokens 16*half .. 16*half+15 = source page 2j+half
   __shared__ float s_amax[4];
+  __shared__ __align__(16) uint8_t s_v[kQBlock * D];  // V codes, token-major
   if (jr >= a.num_qblocks[b]) return;
   const int j = a.first_qblock[b] + jr;
   if (j < 0 || j >= a.dst_max_qpages) {
@@ -110,33 +104,19 @@ __global__ void __launch_bounds__(128, 8) phs_quant_kernel(const QuantArgs a) {
   const __nv_bfloat16* src = which ? a.v_src : a.k_src;
   uint8_t* codes = which ? a.v_codes : a.k_codes;
   float* scales = which ? a.v_scale : a.k_scale;
-  const __nv_bfloat16* tile_base = src + (static_cast<size_t>(page) * a.Hkv + h) * kPage * D;
-  const int w = lane % kW8, tg = lane / kW8;  // V lanes
-  // one contiguous 16 x D tile in 8-element units x[u] (elements e: word
-  // e >> 1, half e & 1).  K: unit u is 16-byte piece u * 32 + lane (8 dims
-  // of one token).  V: unit u is tokens tg*kTpl + 2u, +1 (e >> 2) x dims
-  // 4w + (e & 3).  Every load is a warp-wide contiguous read.
+  // one contiguous 16 x D tile: lane takes 16-byte pieces lane, lane + 32, ...
+  const uint4* tile =
+      reinterpret_cast<const uint4*>(src + (static_cast<size_t>(page) * a.Hkv + h) * kPage * D);
   uint4 x[kIters];
-  if (which) {
-    const uint2* t2 = reinterpret_cast<const uint2*>(tile_base) + w;
 #pragma unroll
-    for (int u = 0; u < kIters; ++u) {
-      const uint2 lo = __ldcs(t2 + (tg * kTpl + 2 * u) * kW8);
-      const uint2 hi = __ldcs(t2 + (tg * kTpl + 2 * u + 1) * kW8);
-      x[u] = make_uint4(lo.x, lo.y, hi.x, hi.y);
-    }
-  } else {
-    const uint4* t4 = reinterpret_cast<const uint4*>(tile_base);
-#pragma unroll
-    for (int u = 0; u < kIters; ++u) x[u] = __ldcs(t4 + u * 32 + lane);
-  }
+  for (int it = 0; it < kIters; ++it) x[it] = __ldcs(tile + it * 32 + lane);
   // absmax in packed bf16 (exact: the max of |x| is one of the inputs).
   // max.xorsign.abs keeps max(|a|, |b|) as the magnitude (its sign is
   // dropped below): one instruction per pair
   uint32_t m2 = 0u;
 #pragma unroll
-  for (int u = 0; u < kIters; ++u) {
-    const uint32_t* v = reinterpret_cast<const uint32_t*>(&x[u]);
+  for (int it = 0; it < kIters; ++it) {
+    const uint32_t* v = reinterpret_cast<const uint32_t*>(&x[it]);
 #pragma unroll
     for (int k = 0; k < 4; ++k) asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v[k]));
   }
@@ -152,7 +132,7 @@ __global__ void __launch_bounds__(128, 8) phs_quant_kernel(const QuantArgs a) {
   // code = rint(x / s) with x / s the IEEE quotient.  y = x * fl(1/s) is
   // within |x/s| * (2^-23 + 2^-48) + ulp/2 <= 1.9e-5 of that quotient (|x/s|
   // <= 127.5), so rint(y) equals rint(x / s) unless y lies within 1.9e-5 of
-  // a half-integer: a unit of 8 codes holding such an element takes the
+  // a half-integer: a group of 8 codes holding such an element takes the
   // IEEE division for all 8 (rare).  A scale so small that 1/s overflows
   // (subnormal groups) always divides.  |rint(x / s)| <= 127 by
   // construction, so no clamp is needed.  s == 0 gives rs == 0 and every
@@ -161,14 +141,13 @@ __global__ void __launch_bounds__(128, 8) phs_quant_kernel(const QuantArgs a) {
   const bool always_divide = !(rs < INFINITY);
   const uint64_t rs2 = f2_pack(rs, rs), magic2 = f2_pack(kRoundMagicOffset, kRoundMagicOffset);
   const size_t block = static_cast<size_t>(qp) * a.Hkv + h;  // (block, head) of 32 x D codes
-  uint2* kout = reinterpret_cast<uint2*>(codes + (block * kQBlock + kPage * half) * D);
-  // V: 16-bit token pairs (tokens 2u, 2u+1 of the lane's group) of dims
-  // 2kk (low half) and 2kk + 1 (high half) in pr[u][kk]
-  uint32_t pr[kIters][2];
+  // K: straight to the pool; V: into the shared token-major tile
+  uint2* out = which ? reinterpret_cast<uint2*>(s_v + kPage * half * D)
+                     : reinterpret_cast<uint2*>(codes + (block * kQBlock + kPage * half) * D);
 #pragma unroll
-  for (int u = 0; u < kIters; ++u) {
-    const uint32_t* v = reinterpret_cast<const uint32_t*>(&x[u]);
-    uint32_t t[8];  // fl(rint(code) + 128 + 1.5 * 2^23): the stored byte in the low bits
+  for (int it = 0; it < kIters; ++it) {
+    const uint32_t* v = reinterpret_cast<const uint32_t*>(&x[it]);
+    uint32_t t[8];  // fl(rint(code) + 1.5 * 2^23): the code in the low byte
     float dmax = 0.f, dmin = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -190,61 +169,43 @@ __global__ void __launch_bounds__(128, 8) phs_quant_kernel(const QuantArgs a) {
         t[e] = __float_as_uint(__fadd_rn(rintf(__fdiv_rn(xv, s)), kRoundMagicOffset));
       }
     }
-    if (which) {
+    uint32_t w[2];
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const uint32_t lo = __byte_perm(t[2 * kk], t[4 + 2 * kk], 0x0040);
-        const uint32_t hi = __byte_perm(t[2 * kk + 1], t[5 + 2 * kk], 0x0040);
-        pr[u][kk] = __byte_perm(lo, hi, 0x5410);
-      }
-    } else {
-      uint32_t wd[2];
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const uint32_t lo = __byte_perm(t[4 * k], t[4 * k + 1], 0x0040);
-        const uint32_t hi = __byte_perm(t[4 * k + 2], t[4 * k + 3], 0x0040);
-        wd[k] = __byte_perm(lo, hi, 0x5410);
-      }
-      kout[u * 32 + lane] = make_uint2(wd[0], wd[1]);
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t lo = __byte_perm(t[4 * k], t[4 * k + 1], 0x0040);
+      const uint32_t hi = __byte_perm(t[4 * k + 2], t[4 * k + 3], 0x0040);
+      w[k] = __byte_perm(lo, hi, 0x5410);
     }
+    out[it * 32 + lane] = make_uint2(w[0], w[1]);
   }
   if (threadIdx.x == 64 * which && half == 0) scales[block] = s;
   if (which) {
-    // V^T row of dim d (this warp's half): word q holds token pairs q (low
-    // 16 bits: tokens 2q, 2q+1) and q + 4 (tokens 2q+8, 2q+9) -- the order
-    // kI8VtToken gives.  D = 128: both pairs are this lane's (units q, q+4).
-    // D = 64: tokens 0-7 are lane group 0's and 8-15 group 1's; the groups
-    // swap the pairs of the dims the other one writes (group 0 writes dims
-    // 4w, 4w+1, group 1 dims 4w+2, 4w+3).
-    uint4* vt = reinterpret_cast<uint4*>(codes + block * kQBlock * D) + half * D;
-    if constexpr (kTg == 1) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t wq[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          wq[q] = __byte_perm(pr[q][k >> 1], pr[q + 4][k >> 1], k & 1 ? 0x7632 : 0x5410);
-        vt[4 * w + k] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-      }
-    } else {
-      uint32_t mine[2][4];  // [kk][q]: words of dims 4w + 2tg + kk
+    // V^T: each V warp transposes its own 16-token half (the rows it just
+    // staged), lane w taking dims 4w..4w+3.  Output word q of a dim's
+    // 16-byte row holds tokens 2q, 2q+1, 2q+8, 2q+9 of the half
+    // (kI8VtToken): the 4 x 4 byte transpose of those 4 token rows' words w
+    // (two levels of byte permutes).
+    __syncwarp();
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(s_v);
+    uint4* vt = reinterpret_cast<uint4*>(codes + block * kQBlock * D);
+    constexpr int W = D / 4;  // words per token row
+    for (int w = lane; w < W; w += 32) {
+      uint32_t o[4][4];  // [dim k][word q]
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        // send the two pairs of the dims the partner writes
-        const uint32_t p0 = pr[q][0], p1 = pr[q][1];
-        const uint32_t got = __shfl_xor_sync(0xffffffffu, tg ? p0 : p1, 16);
-        const uint32_t own = tg ? p1 : p0;
-        if (tg == 0) {  // own pairs low (tokens 2q, 2q+1), partner's high
-          mine[0][q] = __byte_perm(own, got, 0x5410);
-          mine[1][q] = __byte_perm(own, got, 0x7632);
-        } else {  // partner's pairs low, own high (tokens 2q+8, 2q+9)
-          mine[0][q] = __byte_perm(got, own, 0x5410);
-          mine[1][q] = __byte_perm(got, own, 0x7632);
-        }
+        const int t0 = 16 * half + kI8VtToken(4 * q);  // tokens t0, t0+1, t0+8, t0+9
+        const uint32_t r0 = sw[t0 * W + w], r1 = sw[(t0 + 1) * W + w];
+        const uint32_t r2 = sw[(t0 + 8) * W + w], r3 = sw[(t0 + 9) * W + w];
+        const uint32_t a = __byte_perm(r0, r1, 0x5140), b = __byte_perm(r0, r1, 0x7362);
+        const uint32_t c = __byte_perm(r2, r3, 0x5140), d = __byte_perm(r2, r3, 0x7362);
+        o[0][q] = __byte_perm(a, c, 0x5410);
+        o[1][q] = __byte_perm(a, c, 0x7632);
+        o[2][q] = __byte_perm(b, d, 0x5410);
+        o[3][q] = __byte_perm(b, d, 0x7632);
       }
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
-        vt[4 * w + 2 * tg + kk] = make_uint4(mine[kk][0], mine[kk][1], mine[kk][2], mine[kk][3]);
+      for (int k = 0; k < 4; ++k)
+        vt[half * D + 4 * w + k] = make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
     }
   }
 }
