@@ -1085,6 +1085,27 @@ def time_copy(device, nbytes=4 << 30, reps=10):
     return 2 * nbytes / best / 1e9
 
 
+def time_read(device, nbytes=4 << 30, reps=10):
+    """Read-side yardstick: the streaming read-checksum kernel over a buffer
+    larger than L2 (GB/s of bytes read)."""
+    import paged_hybrid_sliding_gb300 as phs
+    a = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    a.fill_(1)
+    sink = torch.zeros(1, dtype=torch.int32, device=device)
+    for _ in range(3):
+        phs.read_checksum(a, sink)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = float("inf")
+    for _ in range(reps):
+        s.record()
+        phs.read_checksum(a, sink)
+        e.record()
+        e.synchronize()
+        best = min(best, s.elapsed_time(e) / 1e3)
+    del a
+    return nbytes / best / 1e9
+
+
 def slowest_rank_time(t, world, device=None):
     """Timed-region length of the slowest rank (the job's time).  Replicas
     exchange nothing else: this MAX is the only collective."""
@@ -1100,7 +1121,7 @@ def job_throughput(bytes_per_step, steps, world, t):
     return bytes_per_step * steps * world / t / 1e9
 
 
-def measure(wl, steps, warmup, world, device, use_graph, copy_gbs, with_cpu):
+def measure(wl, steps, warmup, world, device, use_graph, copy_gbs, with_cpu, read_gbs=None):
     """Warm-up, then exactly `steps` steps timed with CUDA events between
     barriers (max over ranks); the dominant kernel timed by events around
     its launch on its stream on every `stride`-th step; then the same number
@@ -1191,6 +1212,8 @@ def measure(wl, steps, warmup, world, device, use_graph, copy_gbs, with_cpu):
         "pct_of_peak": round(100 * value / world / peak, 2),
         "copy_gbs": round(copy_gbs, 1),
         "pct_of_copy": round(100 * value / world / copy_gbs, 2),
+        **({"read_gbs": round(read_gbs, 1),
+            "pct_of_read": round(100 * value / world / read_gbs, 2)} if read_gbs else {}),
         "e2e": {"value": round(e2e_bytes * world / t_e2e / 1e9, 1),
                 "unit": "GB/s", "h2d_bytes_per_step": wl.h2d_bytes,
                 "d2h_bytes_per_step": wl.d2h_bytes, "steps": steps,
@@ -1256,6 +1279,7 @@ def run_gpu(args, rank, world, local_rank):
     import paged_hybrid_sliding_gb300 as phs
     phs.lib()
     copy_gbs = time_copy(device)
+    read_gbs = time_read(device)
     configs = [args.config] if args.config else list(SUITE)
     lines = {}
     for c in configs:
@@ -1266,7 +1290,7 @@ def run_gpu(args, rank, world, local_rank):
         steps = args.steps if (args.config or c == SUITE[0]) else max(args.steps,
                                                                       SUITE_MIN_STEPS[c])
         lines[c] = measure(wl, steps, args.warmup, world, device, use_graph, copy_gbs,
-                           with_cpu=rank == 0 and not args.no_cpu_baseline)
+                           with_cpu=rank == 0 and not args.no_cpu_baseline, read_gbs=read_gbs)
         del wl
         gc.collect()
         torch.cuda.empty_cache()

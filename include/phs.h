@@ -418,6 +418,13 @@ int phs_hybrid_kv_tokens(const int32_t *layer_is_full_host, int32_t num_layers,
  * multiple of 16. */
 int phs_copy_d2d(void *dst, const void *src, size_t bytes, void *stream);
 
+/* Streaming read of a device buffer, the in-run read-side HBM yardstick
+ * (the decode kernels read almost only, and a read stream runs faster than
+ * a copy's combined read + write rate).  XORs every 32-bit word of
+ * src[0, bytes) into *dev_sink (device, uint32, 4-byte aligned; not
+ * cleared first).  src 16-byte aligned, bytes a multiple of 16. */
+int phs_read_checksum(const void *src, size_t bytes, uint32_t *dev_sink, void *stream);
+
 /* ========================================================================
  * Host-side cache bookkeeping that produces the block tables and page
  * reference counts the kernels consume.  Host memory in, host memory out;

@@ -27,7 +27,7 @@ __all__ = [
     "attn_decode_shared_prefix", "shared_prefix_workspace_bytes",
     "attn_decode_swa_ring", "attn_decode_hybrid_stack", "hybrid_stack_workspace_bytes",
     "attn_decode_hybrid_stack_fused", "hybrid_stack_fused_workspace_bytes",
-    "hybrid_kv_tokens", "copy_d2d", "copy_pages", "PageAllocator", "RadixTree",
+    "hybrid_kv_tokens", "copy_d2d", "read_checksum", "copy_pages", "PageAllocator", "RadixTree",
     "window_safe_len", "swa_ring_save", "swa_ring_seed", "lib", "PAGE", "QBLOCK",
 ]
 
@@ -519,6 +519,16 @@ def copy_d2d(dst, src, stream=None):
         raise ValueError("copy_d2d size mismatch")
     _check(lib().phs_copy_d2d(_ptr(dst), _ptr(src), src.numel() * src.element_size(),
                               _stream(stream)), "copy_d2d")
+
+
+def read_checksum(src, sink, stream=None):
+    """HBM read kernel: XOR every 32-bit word of `src` (contiguous, a
+    multiple of 16 bytes) into sink[0] (CUDA int32 tensor, not cleared)."""
+    _need(sink, torch.int32, "sink")
+    if not src.is_contiguous():
+        raise ValueError("src must be contiguous")
+    _check(lib().phs_read_checksum(_ptr(src), src.numel() * src.element_size(), _ptr(sink),
+                                   _stream(stream)), "read_checksum")
 
 
 # ------------------------------------------------------- cache bookkeeping --

@@ -81,6 +81,7 @@ _SIGS = {
     "phs_hybrid_stack_fused_workspace_bytes": (c_size, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32]),
     "phs_hybrid_kv_tokens": (ctypes.c_int, [c_vp, c_i32, c_vp, c_i32, c_i32, P_i64, P_i64]),
     "phs_copy_d2d": (ctypes.c_int, [c_vp, c_vp, c_size, c_vp]),
+    "phs_read_checksum": (ctypes.c_int, [c_vp, c_size, c_vp, c_vp]),
     "phs_copy_pages": (ctypes.c_int, [_P(PagedPoolC), c_vp, c_vp, c_i32, c_vp, c_vp]),
     "phs_page_allocator_create": (c_vp, [c_i64]),
     "phs_page_allocator_destroy": (None, [c_vp]),

@@ -1203,6 +1203,16 @@ int phs_copy_d2d(void* dst, const void* src, size_t bytes, void* stream) {
   return launch_copy(dst, src, bytes, di.sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int phs_read_checksum(const void* src, size_t bytes, uint32_t* dev_sink, void* stream) {
+  if (!src || !dev_sink) return PHS_EINVAL;
+  if (!aligned16(src) || (bytes & 15u)) return PHS_EALIGN;
+  if ((reinterpret_cast<uintptr_t>(dev_sink) & 3u) != 0) return PHS_EALIGN;
+  DevInfo di;
+  int st = dev_info(di);
+  if (st) return st;
+  return launch_read(src, bytes, di.sms, dev_sink, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

@@ -272,6 +272,7 @@ int launch_quant(const QuantArgs& a, int max_qblocks, int B, cudaStream_t stream
 
 // ---------------------------------------------------------------- copy --
 int launch_copy(void* dst, const void* src, size_t bytes, int num_sms, cudaStream_t stream);
+int launch_read(const void* src, size_t bytes, int num_sms, uint32_t* sink, cudaStream_t stream);
 int launch_copy_pages(void* k, void* v, const int32_t* src, const int32_t* dst, int32_t n,
                       int64_t num_pages, int page_bytes, int32_t* status, cudaStream_t stream);
 

@@ -125,6 +125,20 @@ def test_copy_kernel():
     assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("nbytes", [16, 4096 + 16, 1 << 24, (1 << 26) + 48])
+def test_read_checksum_kernel(nbytes):
+    """The read yardstick really reads every word: its XOR fold equals the
+    host's, on sizes with ragged tails past whole 4-load rounds."""
+    g = torch.Generator().manual_seed(nbytes)
+    x = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, generator=g)
+    want = np.bitwise_xor.reduce(x.numpy().view(np.uint32))
+    sink = torch.tensor([0x1234], dtype=torch.int32, device="cuda")
+    phs.read_checksum(x.cuda(), sink)
+    torch.cuda.synchronize()
+    got = np.array([sink.item()], dtype=np.int32).view(np.uint32)[0]
+    assert got == (want ^ np.uint32(0x1234))
+
+
 @pytest.mark.parametrize("scale_pow", [0, -1, 1, -20])
 def test_quant_int8_half_integer_quotients_bitexact(scale_pow):
     """Groups whose absmax is 127 * 2^p, so s = 2^p exactly and x / s lands
