@@ -955,7 +955,7 @@ class SharedPrefixWorkload(Workload):
         self.tokens_per_step = self.step_tokens(0)
         self.bytes_per_step = self.step_bytes(0)
         self.kernel_bytes = self.step_kernel_bytes(0)
-        self.launches_per_step = 4 if prefix_kernel else 3
+        self.launches_per_step = 3  # prefix: tensor pass, own-token split (+ append), merge
         # tensor work of the prefix pass: QK and PV over B*G rows x D per token
         self.prefix_flops = 4 * B * Hq * D * self.shared_len
         self.extra = {"batch": B, "logical_bytes_step0": self.bytes_per_step,
@@ -994,15 +994,18 @@ class SharedPrefixWorkload(Workload):
     def step(self, ev=None):
         phs = self.phs
         sl = self.sls[self.advance()]
-        phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, sl, page_refcount=self.rc)
-        if ev is not None:
-            ev[0].record()
-        if self.prefix_kernel:
+        if self.prefix_kernel:  # one call: the append is fused into the own-token split
+            if ev is not None:
+                ev[0].record()
             phs.attn_decode_shared_prefix(self.q, self.pool, self.bt, sl, self.max_seq,
-                                          self.shared_len, out=self.out, workspace=self.ws)
+                                          self.shared_len, out=self.out, workspace=self.ws,
+                                          k_new=self.kn, v_new=self.vn, page_refcount=self.rc)
             if ev is not None:
                 ev[1].record()
             return
+        phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, sl, page_refcount=self.rc)
+        if ev is not None:
+            ev[0].record()
         phs.attn_decode_full_paged_split(self.q, self.pool, self.bt, sl, self.max_seq, self.ws,
                                          self.out, tokens_per_split=self.tps)
         if ev is not None:
@@ -1015,13 +1018,14 @@ class SharedPrefixWorkload(Workload):
                 [(self.out, self.h_out)])
 
     def e2e_compute(self, k):
-        self.phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl_in,
-                                 page_refcount=self.rc)
         if self.prefix_kernel:
             self.phs.attn_decode_shared_prefix(self.q, self.pool, self.bt, self.sl_in,
                                                self.max_seq, self.shared_len, out=self.out,
-                                               workspace=self.ws)
+                                               workspace=self.ws, k_new=self.kn, v_new=self.vn,
+                                               page_refcount=self.rc)
         else:
+            self.phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl_in,
+                                     page_refcount=self.rc)
             self.phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl_in, self.max_seq,
                                             out=self.out, tokens_per_split=self.tps,
                                             workspace=self.ws)

@@ -295,6 +295,15 @@ int phs_attn_decode_full_paged_noalloc(const void *q, int32_t num_q_heads,
  * differ from row 0's, or whose seq_lens[b] < shared_len, records
  * PHS_ESHAPE in *dev_status and gets an all-zero output row; the other
  * requests are unaffected.
+ * Fused append (k_new and v_new both given, device bf16 [batch][Hkv][D],
+ * 16-byte aligned; both NULL: none): the step's new token of each request,
+ * token seq_lens[b] - 1, is written into its page by the CTA that attends
+ * it, which attends it from k_new/v_new.  The result equals
+ * phs_kv_append_paged (with the same page_refcount) followed by this call.
+ * A page whose count is not 1 is not written (PHS_ESHARED), and its tokens
+ * are attended as the page holds them.  A new token inside the shared
+ * prefix (seq_lens[b] == shared_len) is never written and records
+ * PHS_ESHARED.
  * ---------------------------------------------------------------------- */
 size_t phs_shared_prefix_workspace_bytes(int32_t batch, int32_t num_q_heads,
                                          int32_t num_kv_heads, int32_t head_dim,
@@ -305,7 +314,9 @@ int phs_attn_decode_shared_prefix(const void *q, int32_t num_q_heads, const phs_
                                   const int32_t *seq_lens, int32_t max_seq_len, int32_t batch,
                                   int32_t shared_len, float softmax_scale, void *out,
                                   int32_t out_dtype, void *workspace, size_t workspace_bytes,
-                                  int32_t *dev_status, void *stream);
+                                  const void *k_new, const void *v_new,
+                                  const int32_t *page_refcount, int32_t *dev_status,
+                                  void *stream);
 
 /* ------------------------------------------------------------------------
  * Sliding-window decode over the SWA ring.

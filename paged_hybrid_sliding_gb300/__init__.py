@@ -328,21 +328,33 @@ def shared_prefix_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, ma
 
 def attn_decode_shared_prefix(q, pool: PagedPool, block_table, seq_lens, max_seq_len: int,
                               shared_len: int, softmax_scale=None, out=None,
-                              out_dtype=torch.bfloat16, workspace=None, status=None, stream=None):
+                              out_dtype=torch.bfloat16, workspace=None, k_new=None, v_new=None,
+                              page_refcount=None, status=None, stream=None):
     """Decode for a batch whose block tables all start with the same
     shared_len / 16 prefix pages: the prefix is attended once per KV head
     for all requests on the tensor cores, each request's own tokens by the
-    split-KV kernel, then merged.  Same result as attn_decode_full_paged."""
+    split-KV kernel, then merged.  Same result as attn_decode_full_paged.
+    k_new / v_new ([B, Hkv, D] bf16): append token seq_lens[b] - 1 in the
+    same call (as kv_append_paged with page_refcount, then this call)."""
     pc, _, out = _decode_args(q, pool, block_table, seq_lens, None, None, None, out, out_dtype,
                               status)
     B, Hq, D = q.shape
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+            _need(t, torch.bfloat16, name, 3)
+            if tuple(t.shape) != (B, pool.k.shape[1], D):
+                raise ValueError(f"{name} must be [batch, Hkv, D]")
+    _opt(page_refcount, torch.int32, "page_refcount", 1)
     scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
     need = shared_prefix_workspace_bytes(B, Hq, pool.k.shape[1], D, max_seq_len, shared_len)
     ws = _workspace(workspace, need, q.device)
     _check(lib().phs_attn_decode_shared_prefix(
         _ptr(q), Hq, ctypes.byref(pc), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
         int(max_seq_len), B, int(shared_len), scale, _ptr(out), _out_code(out.dtype), _ptr(ws),
-        ws.numel(), _ptr(status), _stream(stream)), "attn_decode_shared_prefix")
+        ws.numel(), _ptr(k_new), _ptr(v_new), _ptr(page_refcount), _ptr(status), _stream(stream)),
+        "attn_decode_shared_prefix")
     return out
 
 

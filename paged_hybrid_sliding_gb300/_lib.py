@@ -66,7 +66,7 @@ _SIGS = {
     "phs_shared_prefix_workspace_bytes": (c_size, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32]),
     "phs_attn_decode_shared_prefix": (ctypes.c_int, [c_vp, c_i32, _P(PagedPoolC), c_vp, c_i32, c_vp,
                                                      c_i32, c_i32, c_i32, c_f32, c_vp, c_i32, c_vp,
-                                                     c_size, c_vp, c_vp]),
+                                                     c_size, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "phs_attn_merge_splits": (ctypes.c_int, [c_i32, c_i32, c_i32, c_i32, c_vp, c_i32, c_vp, c_i32,
                                              c_i32, c_vp, c_i32, c_vp, c_size, c_vp]),
     "phs_attn_decode_swa_ring": (ctypes.c_int, [c_vp, c_i32, _P(RingPoolC), c_vp, c_vp, c_vp,

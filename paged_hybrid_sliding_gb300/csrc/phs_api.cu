@@ -653,10 +653,14 @@ int phs_attn_decode_shared_prefix(const void* q, int32_t num_q_heads, const phs_
                                   const int32_t* seq_lens, int32_t max_seq_len, int32_t batch,
                                   int32_t shared_len, float softmax_scale, void* out,
                                   int32_t out_dtype, void* workspace, size_t workspace_bytes,
-                                  int32_t* dev_status, void* stream) {
+                                  const void* k_new, const void* v_new,
+                                  const int32_t* page_refcount, int32_t* dev_status,
+                                  void* stream) {
   int st = check_paged(pool);
   if (st) return st;
   if (!q || !block_table || !seq_lens || !out) return PHS_EINVAL;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PHS_EINVAL;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PHS_EALIGN;
   if (max_pages_per_seq <= 0 || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
     return PHS_EINVAL;
   if (out_dtype != PHS_OUT_BF16 && out_dtype != PHS_OUT_F32) return PHS_EINVAL;
@@ -717,6 +721,13 @@ int phs_attn_decode_shared_prefix(const void* q, int32_t num_q_heads, const phs_
   a.force_partial = 1;
   a.prefix_bad = reinterpret_cast<int32_t*>(ws + pl.off_bad);
   a.wait_prior_at_exit = 1;  // started beside the prefix pass (independent tokens)
+  if (k_new) {  // the new tokens are own tokens: the own-token split appends them
+    a.app = FusedAppend{reinterpret_cast<const __nv_bfloat16*>(k_new),
+                        reinterpret_cast<const __nv_bfloat16*>(v_new),
+                        reinterpret_cast<__nv_bfloat16*>(pool->k),
+                        reinterpret_cast<__nv_bfloat16*>(pool->v)};
+    a.page_refcount = page_refcount;
+  }
   if ((st = launch_split_decode(D, tk3, tv3, tk3, tv3, a, batch, s, true))) return st;
   // 3. merge prefix and suffix partials
   PrefixMergeArgs m;

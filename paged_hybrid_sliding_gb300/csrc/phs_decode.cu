@@ -201,6 +201,10 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
   }
   const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
   if (ns == 0) {  // empty request: zero output (unless another kernel owns it)
+    // a fused append whose new token falls inside the shared prefix (n ==
+    // skip_len): its page is one of the shared ones, so it is not written
+    if (app.k_new != nullptr && n >= 1 && n - 1 < a.skip_len && s == 0 && threadIdx.x == 0)
+      set_status(a.status, PHS_ESHARED);
     if (s == 0 && !a.force_partial)
       for (int e = threadIdx.x; e < G * D; e += blockDim.x) store_out(out, out_row0 + e, 0.f, a.out_f32);
     return;
@@ -433,15 +437,17 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
 
 // request index fastest: CTAs that read the same shared-prefix pages for
 // different requests run close together in time and share them through L2
-template <int D, bool TWO, bool MIXED>
+// APP: the launch carries a fused append (a.app); without it the patch code
+// is compiled out, which keeps the plain split free of spills.
+template <int D, bool TWO, bool MIXED, bool APP>
 __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
     phs_split_decode_kernel(const __grid_constant__ CUtensorMap tk,
                             const __grid_constant__ CUtensorMap tv,
                             const __grid_constant__ CUtensorMap tk8,
                             const __grid_constant__ CUtensorMap tv8, const SplitArgs a) {
   const FusedAppend none{nullptr, nullptr, nullptr, nullptr};
-  split_body<D, TWO, MIXED>(&tk, &tv, &tk8, &tv8, a, a.q, a.out, a.ws_o, a.ws_ml, none,
-                            blockIdx.x, blockIdx.y, blockIdx.z);
+  split_body<D, TWO, MIXED>(&tk, &tv, &tk8, &tv8, a, a.q, a.out, a.ws_o, a.ws_ml,
+                            APP ? a.app : none, blockIdx.x, blockIdx.y, blockIdx.z);
   // started early beside an independent grid: one CTA holds this grid open
   // until that grid has finished, so a launch that waits for this grid also
   // sees the other's results
@@ -489,8 +495,10 @@ template <int D, bool TWO>
 static int launch_split_t(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tk8,
                           const CUtensorMap& tv8, const SplitArgs& a, int B, cudaStream_t stream,
                           bool dependent) {
-  auto kern = a.qlens ? phs_split_decode_kernel<D, TWO, true>
-                      : phs_split_decode_kernel<D, TWO, false>;
+  if (a.qlens && a.app.k_new) return PHS_EUNSUPPORTED;  // no fused append over INT8 pages
+  auto kern = a.qlens        ? phs_split_decode_kernel<D, TWO, true, false>
+              : a.app.k_new ? phs_split_decode_kernel<D, TWO, false, true>
+                            : phs_split_decode_kernel<D, TWO, false, false>;
   const int smem = SplitLayout<D>::kAlloc;
   if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
   dim3 grid(B, a.Hkv, a.max_splits);

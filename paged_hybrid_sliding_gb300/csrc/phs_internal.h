@@ -22,6 +22,16 @@ constexpr int kQBlock = 32;  // tokens per INT8 page / scale group
 constexpr int kI8VtToken(int p) { return 2 * (p >> 2) + (p & 1) + 8 * ((p >> 1) & 1); }
 
 // ----------------------------------------------------- split-KV decode --
+// New token of each request for an append fused into a decode kernel: the
+// kernel writes it to its page (or ring slot) and attends to it from these
+// inputs instead of reading it back.  k_new null: no append.
+struct FusedAppend {
+  const __nv_bfloat16* k_new;  // [B][Hkv][D]
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* k_pool;       // paged [num_pages][Hkv][16][D] / ring [rings][Hkv][W][D]
+  __nv_bfloat16* v_pool;
+};
+
 struct SplitArgs {
   const __nv_bfloat16* q;   // [B][Hq][D]
   const int32_t* block_table;
@@ -48,7 +58,7 @@ struct SplitArgs {
   float scale_log2;         // softmax_scale * log2(e)
   int skip_len;             // tokens [0, skip_len) are attended elsewhere (shared prefix)
   int force_partial;        // write partials even for single-split requests
-  // fused append (stack kernel): page reference counts, or null; a new
+  // fused append: page reference counts, or null; a new
   // token whose page count is not 1 is neither written nor attended from
   // the input (the page is shared; copy on write is the caller's job)
   const int32_t* page_refcount;
@@ -56,17 +66,12 @@ struct SplitArgs {
   // 1 if its slice of the request's first skip_len / 16 page ids differs
   // from row 0's, or the request is shorter than skip_len; else 0
   int32_t* prefix_bad;
+  // append fused into a split launch (the shared-prefix call's own-token
+  // split; k_new null: none).  The stack kernel takes each layer's from its
+  // own parameter block instead.
+  FusedAppend app;
 };
 
-// New token of each request for an append fused into a decode kernel: the
-// kernel writes it to its page (or ring slot) and attends to it from these
-// inputs instead of reading it back.  k_new null: no append.
-struct FusedAppend {
-  const __nv_bfloat16* k_new;  // [B][Hkv][D]
-  const __nv_bfloat16* v_new;
-  __nv_bfloat16* k_pool;       // paged [num_pages][Hkv][16][D] / ring [rings][Hkv][W][D]
-  __nv_bfloat16* v_pool;
-};
 
 // ------------------------------------- hybrid stack: Full layers at once --
 constexpr int kStackMaxFull = 16;  // Full layers per launch

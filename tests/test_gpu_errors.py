@@ -98,6 +98,10 @@ def test_host_errors():
     with pytest.raises(phs.PhsError) as e:   # tokens_per_split not a multiple of 32
         phs.attn_decode_full_paged(q, pool, bt, sl, 20, tokens_per_split=48)
     assert e.value.code == -7
+    with pytest.raises(phs.PhsError) as e:   # group of 34 query heads per KV head (max 16)
+        phs.attn_decode_full_paged(synth.normal_bf16((1, 68, 64), 3, device="cuda"), pool, bt,
+                                   sl, 20)
+    assert e.value.code == -7
 
 
 def test_stack_rejects_bad_scale_before_any_launch():

@@ -138,11 +138,12 @@ def test_shared_prefix_checks_every_row_against_row_0():
         assert_close(got[good], _oracle_rows(pool, q, bt, lens, good), "unflagged rows")
 
 
-def _prefix_steps(B, Hq, Hkv, shared_len, suffix, steps, seed, rows, D=128):
+def _prefix_steps(B, Hq, Hkv, shared_len, suffix, steps, seed, rows, D=128, fused=False):
     """The decode loop of a batch sharing a prefix: each step appends every
     request's new token (page reference counts checked) and decodes through
-    the shared-prefix call; sampled rows are checked against the oracle at
-    every step, on a host copy of their pages that the oracle appends to."""
+    the shared-prefix call (fused: one call that also appends); sampled rows
+    are checked against the oracle at every step, on a host copy of their
+    pages that the oracle appends to."""
     npref = shared_len // 16
     own = (suffix + steps + 15) // 16
     total = npref + B * own
@@ -171,9 +172,14 @@ def _prefix_steps(B, Hq, Hkv, shared_len, suffix, steps, seed, rows, D=128):
         vn = synth.normal_bf16((B, Hkv, D), seed + 12 + 3 * k, device="cuda")
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
         sl = dev(n_after)
-        phs.kv_append_paged(pool, kn, vn, bt_d, sl, page_refcount=rc_d, status=st)
+        if fused:
+            kw = dict(k_new=kn, v_new=vn, page_refcount=rc_d)
+        else:
+            kw = {}
+            phs.kv_append_paged(pool, kn, vn, bt_d, sl, page_refcount=rc_d, status=st)
         out = phs.attn_decode_shared_prefix(q, pool, bt_d, sl, max_seq, shared_len,
-                                            out_dtype=torch.float32, workspace=ws, status=st)
+                                            out_dtype=torch.float32, workspace=ws, status=st,
+                                            **kw)
         torch.cuda.synchronize()
         assert int(st.item()) == 0, k
         assert oracle.append_paged(hk, hv, synth.bits(kn)[rows], synth.bits(vn)[rows], bt_s,
@@ -184,20 +190,22 @@ def _prefix_steps(B, Hq, Hkv, shared_len, suffix, steps, seed, rows, D=128):
         assert_close(out_np(out)[rows], ref, f"step {k}")
 
 
-def test_shared_prefix_decode_steps_with_append():
+@pytest.mark.parametrize("fused", [False, True])
+def test_shared_prefix_decode_steps_with_append(fused):
     # 64 requests x 8 KV heads (256 query rows per head), suffixes crossing a
     # page boundary during the walk (suffix 505 + 12 steps passes 512)
     _prefix_steps(B=64, Hq=32, Hkv=8, shared_len=4096, suffix=505, steps=12, seed=900,
-                  rows=[0, 17, 63])
+                  rows=[0, 17, 63], fused=fused)
 
 
 @pytest.mark.slow
 def test_shared_prefix_full_size_steps_with_append():
     """The shared-prefix workload's loop at full size: one 250,000-token
-    prefix shared by 64 requests with 512-token suffixes; append + prefix
-    decode over 4 steps, two sampled requests against the oracle each step
-    (the tensor-core pass covers the prefix's whole 64-token tiles, 249,984
-    tokens; the split kernel the remaining 16 and the suffix)."""
+    prefix shared by 64 requests with 512-token suffixes; the bench's one
+    call per step (the append fused into the prefix decode) over 4 steps,
+    two sampled requests against the oracle each step (the tensor-core pass
+    covers the prefix's whole 64-token tiles, 249,984 tokens; the split
+    kernel the remaining 16 and the suffix)."""
     w = synth.shared_prefix()
     assert w.extra["prefix_pages"] * 16 == 250_000
     _prefix_steps_full(w, steps=4, rows=[0, w.B - 1])
@@ -223,9 +231,9 @@ def _prefix_steps_full(w, steps, rows):
         vn = synth.normal_bf16((B, Hkv, D), 962 + 3 * k, device="cuda")
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
         sl = dev(n_after)
-        phs.kv_append_paged(pool, kn, vn, bt, sl, page_refcount=rcd, status=st)
         out = phs.attn_decode_shared_prefix(q, pool, bt, sl, max_seq, shared,
-                                            out_dtype=torch.float32, workspace=ws, status=st)
+                                            out_dtype=torch.float32, workspace=ws, status=st,
+                                            k_new=kn, v_new=vn, page_refcount=rcd)
         torch.cuda.synchronize()
         assert int(st.item()) == 0, k
         assert oracle.append_paged(hk, hv, synth.bits(kn)[rows], synth.bits(vn)[rows], bt_s,
@@ -234,3 +242,70 @@ def _prefix_steps_full(w, steps, rows):
                                           w.softmax_scale)
         assert s == 0
         assert_close(out_np(out)[rows], ref, f"config 5 prefix path, step {k}")
+
+
+def _fused_vs_unfused(B, Hq, Hkv, shared_len, suffixes, seed, rc_override=None, lens_override=None):
+    """One step both ways on identical pools: kv_append_paged then the
+    shared-prefix call, and the call with the append fused in.  Returns
+    (outputs, statuses, pools) of the two, and the case."""
+    pool, q, bt, lens = _shared_case(B, Hq, Hkv, shared_len, suffixes, seed)
+    if lens_override:
+        for b, n in lens_override.items():
+            lens[b] = n
+    rc = np.ones(pool.k.shape[0], np.int32)
+    rc[bt[0, :shared_len // 16]] = B
+    for page, count in (rc_override or {}).items():
+        rc[page] = count
+    kn = synth.normal_bf16((B, Hkv, 128), seed + 20, device="cuda")
+    vn = synth.normal_bf16((B, Hkv, 128), seed + 21, device="cuda")
+    pools = [phs.PagedPool(pool.k.clone(), pool.v.clone()) for _ in range(2)]
+    bt_d, sl, rc_d = dev(bt), dev(lens), dev(rc)
+    outs, sts = [], []
+    for fused, p in zip((False, True), pools):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if not fused:
+            phs.kv_append_paged(p, kn, vn, bt_d, sl, page_refcount=rc_d, status=st)
+        kw = dict(k_new=kn, v_new=vn, page_refcount=rc_d) if fused else {}
+        out = phs.attn_decode_shared_prefix(q, p, bt_d, sl, int(lens.max()), shared_len,
+                                            out_dtype=torch.float32, status=st, **kw)
+        torch.cuda.synchronize()
+        outs.append(out_np(out))
+        sts.append(int(st.item()))
+    return outs, sts, pools, (pool, q, bt, lens, kn, vn)
+
+
+def test_shared_prefix_fused_append_equals_append_then_decode():
+    """The append fused into the shared-prefix call (the own-token split
+    writes each new token and attends it from the input) gives the
+    unfused result bit for bit: outputs and pools.  The suffixes put the
+    new token at the first and the last slot of a page and in between."""
+    B, Hq, Hkv, shared_len = 16, 32, 8, 1024
+    suffixes = [1, 16, 17, 32, 100, 511, 512, 513, 7, 640, 3, 255, 256, 257, 48, 49]
+    outs, sts, pools, (pool, q, bt, lens, _, _) = _fused_vs_unfused(B, Hq, Hkv, shared_len,
+                                                                    suffixes, 41)
+    assert sts == [0, 0]
+    assert np.array_equal(outs[0], outs[1])
+    assert torch.equal(pools[0].k, pools[1].k) and torch.equal(pools[0].v, pools[1].v)
+    rows = [0, 6, 9, 15]
+    assert_close(outs[1][rows], _oracle_rows(pools[1], q, bt, lens, rows), "fused vs oracle")
+
+
+def test_shared_prefix_fused_append_refuses_shared_pages():
+    """A request whose newest page has a reference count of 2, and one whose
+    new token would fall inside the shared prefix (seq_lens == shared_len):
+    neither page is written, PHS_ESHARED is recorded, and both ways give the
+    same outputs and pools (the refused tokens attended as the pages hold
+    them)."""
+    B, Hq, Hkv, shared_len = 8, 32, 8, 512
+    suffixes = [40, 70, 33, 90, 16, 120, 64, 5]
+    pool, _, bt, lens = _shared_case(B, Hq, Hkv, shared_len, suffixes, 43)
+    shared_row, at_prefix = 2, 5
+    page = int(bt[shared_row, (lens[shared_row] - 1) // 16])
+    before = pool.k[page].clone()
+    outs, sts, pools, _ = _fused_vs_unfused(B, Hq, Hkv, shared_len, suffixes, 43,
+                                            rc_override={page: 2},
+                                            lens_override={at_prefix: shared_len})
+    assert sts == [-4, -4]  # PHS_ESHARED both ways
+    assert np.array_equal(outs[0], outs[1])
+    assert torch.equal(pools[0].k, pools[1].k) and torch.equal(pools[0].v, pools[1].v)
+    assert torch.equal(pools[1].k[page], before)
