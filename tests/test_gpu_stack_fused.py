@@ -61,6 +61,8 @@ CASES = [
     ([1, 16, 17, 130, 1025, 2048, 3001, 4096], 32, 8, 128, [0, 1, 0, 0, 1, 0, 1]),
     ([5, 128, 129, 700, 1040], 4, 2, 64, [1, 0, 1, 0]),
     ([33, 2049, 4000], 32, 2, 128, [1, 0]),  # G = 16: two row tiles per warp
+    ([64, 300, 2500], 8, 8, 64, [1, 0, 1]),  # G = 1: one live row per tile
+    ([17, 900, 3000, 48], 24, 4, 128, [0, 1, 1]),  # G = 6: rows 6 and 7 of the tile masked
 ]
 
 
