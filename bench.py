@@ -319,7 +319,8 @@ class Workload:
 
 
 class PagedFullWorkload(Workload):
-    """Paged Full-attention decode, batch 64 (one step = append + decode)."""
+    """Paged Full-attention decode, batch 64 (one step = append + decode,
+    the append fused into the split launch)."""
 
     def __init__(self, device, seed=2, batch=64, tokens_per_split=0):
         import paged_hybrid_sliding_gb300 as phs
@@ -349,7 +350,7 @@ class PagedFullWorkload(Workload):
         tables = int(synth.pages_needed(w.n_after).sum()) * 4 + B * 4
         self.bytes_per_step = kv + qo + app + tables
         self.kernel_bytes = kv + B * Hq * D * 2 + tables
-        self.launches_per_step = 3
+        self.launches_per_step = 2  # split (with the append) + merge
         self.extra = {"batch": B, "tokens_per_split": self.tps}
         # the step's inputs in one staged buffer: one host->device copy per step
         self.inp = Arena(device, [self.q, self.kn, self.vn, self.bt, self.sl])
@@ -361,11 +362,12 @@ class PagedFullWorkload(Workload):
     def step(self, ev=None):
         phs = self.phs
         self.advance()
-        phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl)
         if ev is not None:
             ev[0].record()
+        # the append fused into the split launch
         phs.attn_decode_full_paged_split(self.q, self.pool, self.bt, self.sl, self.max_seq,
-                                         self.ws, self.out, tokens_per_split=self.tps)
+                                         self.ws, self.out, tokens_per_split=self.tps,
+                                         k_new=self.kn, v_new=self.vn)
         if ev is not None:
             ev[1].record()
         phs.attn_merge_splits(self.out, self.w.Hkv, self.sl, self.max_seq, self.ws,
@@ -375,10 +377,9 @@ class PagedFullWorkload(Workload):
         return [(self.inp.host, self.inp.dev)], [(self.out, self.h_out)]
 
     def e2e_compute(self, k):
-        phs = self.phs
-        phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl)
-        phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl, self.max_seq,
-                                   out=self.out, tokens_per_split=self.tps, workspace=self.ws)
+        self.phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl, self.max_seq,
+                                        out=self.out, tokens_per_split=self.tps,
+                                        workspace=self.ws, k_new=self.kn, v_new=self.vn)
 
     def cpu_baseline(self, budget_s=2.0, min_s=8.0):
         """The oracle as it stands on a sample of requests of this step,
@@ -731,8 +732,9 @@ class Int8Workload(Workload):
     """Batch 32, 65,536 cached tokens: tokens [0, qlen) as INT8 (one fp32
     absmax/127 scale per 32 tokens per KV head, quantised on the GPU at set
     up), the rest bf16; K/V N(0,1) with 1% N(0, 8^2) outliers.  One step =
-    append into the bf16 tail + (when a tail reaches 1056 tokens) the
-    quantisation of its oldest bf16 block + split-KV decode + merge.  The
+    (when a tail reaches 1056 tokens) the quantisation of its oldest bf16
+    block + split-KV decode with the append into the bf16 tail fused in +
+    merge.  The
     steps walk 64 decode positions (lengths 65,537 .. 65,600, each request's
     INT8 length growing by 32 at steps 31 and 63), then start over."""
 
@@ -805,7 +807,7 @@ class Int8Workload(Workload):
         self.tokens_per_step = int(self.n_walk[0].sum())
         self.kernel_bytes = self.step_kernel_bytes(0)
         self.bytes_per_step = self.step_bytes(0)
-        self.launches_per_step = 3  # + one quantiser launch at steps 31 and 63
+        self.launches_per_step = 2  # split (with the append) + merge; + one quantiser launch at steps 31 and 63
         i8_tok = int(self.qlen0.sum())
         bf_tok = int((w.n_after - self.qlen0).sum())
         self.extra = {"batch": B, "int8_tokens_step0": i8_tok, "bf16_tokens_step0": bf_tok,
@@ -852,13 +854,14 @@ class Int8Workload(Workload):
         k = self.advance()
         phs = self.phs
         sl, ql = self.sls[k], self.qls[k]
-        phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, sl)
-        self._age(k)
+        self._age(k)  # reads the oldest bf16 block, far behind the new token
         if ev is not None:
             ev[0].record()
+        # the append fused into the split launch (the new token is in the bf16 tail)
         phs.attn_decode_full_paged_split(self.q, self.pool, self.bt, sl, self.max_seq,
                                          self.ws, self.out, int8=self.i8, qtable=self.qt,
-                                         qlens=ql, tokens_per_split=self.tps)
+                                         qlens=ql, tokens_per_split=self.tps, k_new=self.kn,
+                                         v_new=self.vn)
         if ev is not None:
             ev[1].record()
         phs.attn_merge_splits(self.out, self.w.Hkv, sl, self.max_seq, self.ws, qlens=ql,
@@ -870,12 +873,11 @@ class Int8Workload(Workload):
                  (self.h_qls[c], self.ql_in)], [(self.out, self.h_out)])
 
     def e2e_compute(self, k):
-        phs = self.phs
-        phs.kv_append_paged(self.pool, self.kn, self.vn, self.bt, self.sl_in)
         self._age(k % self.cycle)
-        phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl_in, self.max_seq,
-                                   int8=self.i8, qtable=self.qt, qlens=self.ql_in,
-                                   tokens_per_split=self.tps, out=self.out, workspace=self.ws)
+        self.phs.attn_decode_full_paged(self.q, self.pool, self.bt, self.sl_in, self.max_seq,
+                                        int8=self.i8, qtable=self.qt, qlens=self.ql_in,
+                                        tokens_per_split=self.tps, out=self.out,
+                                        workspace=self.ws, k_new=self.kn, v_new=self.vn)
 
     def cpu_baseline(self, nrows=8, min_s=8.0):
         """The oracle on the first nrows requests of step 0 (INT8 codes and

@@ -203,6 +203,15 @@ int32_t phs_decode_tokens_per_split(int32_t batch, int32_t num_kv_heads, int32_t
  * workspace: device, at least phs_decode_workspace_bytes(...) bytes, 256-byte
  * aligned; contents need no initialisation and are overwritten.
  * Requests with seq_lens[b] == 0 get an all-zero output row.
+ * Fused append (k_new and v_new both given, device bf16 [batch][Hkv][D],
+ * 16-byte aligned; both NULL: none): each request's new token, token
+ * seq_lens[b] - 1, is written into its bf16 page by the CTA that attends
+ * it, which attends it from k_new/v_new.  The result equals
+ * phs_kv_append_paged (with the same page_refcount) followed by this call.
+ * A page whose count is not 1 is not written (PHS_ESHARED), and its tokens
+ * are attended as the page holds them.  A new token inside the request's
+ * INT8 region (seq_lens[b] - 1 < qlens[b]) is not written and records
+ * PHS_ERANGE.
  * ---------------------------------------------------------------------- */
 int phs_attn_decode_full_paged(const void *q, int32_t num_q_heads, const phs_paged_pool *pool,
                                const int32_t *block_table, int32_t max_pages_per_seq,
@@ -211,7 +220,9 @@ int phs_attn_decode_full_paged(const void *q, int32_t num_q_heads, const phs_pag
                                int32_t max_qpages_per_seq, const int32_t *qlens,
                                int32_t batch, float softmax_scale, int32_t tokens_per_split,
                                void *out, int32_t out_dtype, void *workspace,
-                               size_t workspace_bytes, int32_t *dev_status, void *stream);
+                               size_t workspace_bytes, const void *k_new, const void *v_new,
+                               const int32_t *page_refcount, int32_t *dev_status,
+                               void *stream);
 
 /* The two phases of phs_attn_decode_full_paged, exposed separately so that
  * each kernel can be timed on its own.  The split phase writes every
@@ -226,7 +237,9 @@ int phs_attn_decode_full_paged_split(const void *q, int32_t num_q_heads,
                                      const int32_t *qlens, int32_t batch, float softmax_scale,
                                      int32_t tokens_per_split, void *out, int32_t out_dtype,
                                      void *workspace, size_t workspace_bytes,
-                                     int32_t *dev_status, void *stream);
+                                     const void *k_new, const void *v_new,
+                                     const int32_t *page_refcount, int32_t *dev_status,
+                                     void *stream);
 
 /* Cross-split merge: for each (request, query head) with more than one
  * split, M = max_s m_s, L = sum_s l_s 2^(m_s - M),

@@ -264,6 +264,19 @@ def _decode_args(q, pool, block_table, seq_lens, int8, qtable, qlens, out, out_d
     return pc, ic, out
 
 
+def _append_args(k_new, v_new, page_refcount, B, Hkv, D):
+    """Checks of a fused append's new tokens ([B, Hkv, D] bf16, both or
+    neither) and page reference counts."""
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+            _need(t, torch.bfloat16, name, 3)
+            if tuple(t.shape) != (B, Hkv, D):
+                raise ValueError(f"{name} must be [batch, Hkv, D]")
+    _opt(page_refcount, torch.int32, "page_refcount", 1)
+
+
 def _workspace(workspace, nbytes, device):
     if workspace is None:
         # a zero size means the library rejects the shape: let the call
@@ -276,12 +289,16 @@ def _workspace(workspace, nbytes, device):
 def attn_decode_full_paged(q, pool: PagedPool, block_table, seq_lens, max_seq_len: int,
                            softmax_scale=None, int8: Int8Pool | None = None, qtable=None,
                            qlens=None, tokens_per_split=0, out=None, out_dtype=torch.bfloat16,
-                           workspace=None, status=None, stream=None):
+                           workspace=None, k_new=None, v_new=None, page_refcount=None,
+                           status=None, stream=None):
     """Split-KV decode over the paged pool (optionally INT8 below qlens[b]);
-    returns out [B, Hq, D]."""
+    returns out [B, Hq, D].  k_new / v_new ([B, Hkv, D] bf16): append token
+    seq_lens[b] - 1 in the same call (as kv_append_paged with page_refcount,
+    then this call)."""
     pc, ic, out = _decode_args(q, pool, block_table, seq_lens, int8, qtable, qlens, out,
                                out_dtype, status)
     B, Hq, D = q.shape
+    _append_args(k_new, v_new, page_refcount, B, pool.k.shape[1], D)
     scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
     need = decode_workspace_bytes(B, Hq, pool.k.shape[1], D, max_seq_len, tokens_per_split,
                                   int8 is not None)
@@ -290,8 +307,8 @@ def attn_decode_full_paged(q, pool: PagedPool, block_table, seq_lens, max_seq_le
         _ptr(q), Hq, ctypes.byref(pc), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
         int(max_seq_len), None if ic is None else ctypes.byref(ic), _ptr(qtable),
         0 if qtable is None else qtable.shape[1], _ptr(qlens), B, scale, int(tokens_per_split),
-        _ptr(out), _out_code(out.dtype), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
-        "attn_decode_full_paged")
+        _ptr(out), _out_code(out.dtype), _ptr(ws), ws.numel(), _ptr(k_new), _ptr(v_new),
+        _ptr(page_refcount), _ptr(status), _stream(stream)), "attn_decode_full_paged")
     return out
 
 
@@ -339,14 +356,7 @@ def attn_decode_shared_prefix(q, pool: PagedPool, block_table, seq_lens, max_seq
     pc, _, out = _decode_args(q, pool, block_table, seq_lens, None, None, None, out, out_dtype,
                               status)
     B, Hq, D = q.shape
-    if (k_new is None) != (v_new is None):
-        raise ValueError("k_new and v_new go together")
-    if k_new is not None:
-        for t, name in ((k_new, "k_new"), (v_new, "v_new")):
-            _need(t, torch.bfloat16, name, 3)
-            if tuple(t.shape) != (B, pool.k.shape[1], D):
-                raise ValueError(f"{name} must be [batch, Hkv, D]")
-    _opt(page_refcount, torch.int32, "page_refcount", 1)
+    _append_args(k_new, v_new, page_refcount, B, pool.k.shape[1], D)
     scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
     need = shared_prefix_workspace_bytes(B, Hq, pool.k.shape[1], D, max_seq_len, shared_len)
     ws = _workspace(workspace, need, q.device)
@@ -360,19 +370,23 @@ def attn_decode_shared_prefix(q, pool: PagedPool, block_table, seq_lens, max_seq
 
 def attn_decode_full_paged_split(q, pool: PagedPool, block_table, seq_lens, max_seq_len: int,
                                  workspace, out, softmax_scale=None, int8=None, qtable=None,
-                                 qlens=None, tokens_per_split=0, status=None, stream=None):
-    """Split phase only (see attn_merge_splits)."""
+                                 qlens=None, tokens_per_split=0, k_new=None, v_new=None,
+                                 page_refcount=None, status=None, stream=None):
+    """Split phase only (see attn_merge_splits); k_new / v_new as for
+    attn_decode_full_paged."""
     pc, ic, out = _decode_args(q, pool, block_table, seq_lens, int8, qtable, qlens, out,
                                out.dtype, status)
     B, Hq, D = q.shape
+    _append_args(k_new, v_new, page_refcount, B, pool.k.shape[1], D)
     scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
     _need(workspace, torch.uint8, "workspace", 1)
     _check(lib().phs_attn_decode_full_paged_split(
         _ptr(q), Hq, ctypes.byref(pc), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
         int(max_seq_len), None if ic is None else ctypes.byref(ic), _ptr(qtable),
         0 if qtable is None else qtable.shape[1], _ptr(qlens), B, scale, int(tokens_per_split),
-        _ptr(out), _out_code(out.dtype), _ptr(workspace), workspace.numel(), _ptr(status),
-        _stream(stream)), "attn_decode_full_paged_split")
+        _ptr(out), _out_code(out.dtype), _ptr(workspace), workspace.numel(), _ptr(k_new),
+        _ptr(v_new), _ptr(page_refcount), _ptr(status), _stream(stream)),
+        "attn_decode_full_paged_split")
     return out
 
 

@@ -54,11 +54,12 @@ _SIGS = {
     "phs_attn_decode_full_paged": (ctypes.c_int, [c_vp, c_i32, _P(PagedPoolC), c_vp, c_i32, c_vp,
                                                   c_i32, _P(Int8PoolC), c_vp, c_i32, c_vp, c_i32,
                                                   c_f32, c_i32, c_vp, c_i32, c_vp, c_size, c_vp,
-                                                  c_vp]),
+                                                  c_vp, c_vp, c_vp, c_vp]),
     "phs_attn_decode_full_paged_split": (ctypes.c_int, [c_vp, c_i32, _P(PagedPoolC), c_vp, c_i32,
                                                         c_vp, c_i32, _P(Int8PoolC), c_vp, c_i32,
                                                         c_vp, c_i32, c_f32, c_i32, c_vp, c_i32,
-                                                        c_vp, c_size, c_vp, c_vp]),
+                                                        c_vp, c_size, c_vp, c_vp, c_vp, c_vp,
+                                                        c_vp]),
     "phs_attn_decode_full_paged_noalloc": (ctypes.c_int, [c_vp, c_i32, _P(PagedPoolC), c_vp,
                                                           c_i32, c_vp, c_i32, _P(Int8PoolC), c_vp,
                                                           c_i32, c_vp, c_i32, c_f32, c_i32, c_vp,

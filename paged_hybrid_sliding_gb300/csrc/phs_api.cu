@@ -278,10 +278,13 @@ int prepare_decode(DecodeCall& c, const void* q, int Hq, const phs_paged_pool* p
                    const int32_t* block_table, int max_pages, const int32_t* seq_lens,
                    int max_seq, const phs_int8_pool* int8, const int32_t* qtable, int max_qpages,
                    const int32_t* qlens, int B, float softmax_scale, int tps, void* out,
-                   int out_dtype, void* workspace, size_t ws_size, int32_t* dev_status) {
+                   int out_dtype, void* workspace, size_t ws_size, const void* k_new,
+                   const void* v_new, const int32_t* page_refcount, int32_t* dev_status) {
   int st = check_paged(pool);
   if (st) return st;
   if (!q || !block_table || !seq_lens || !out) return PHS_EINVAL;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PHS_EINVAL;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PHS_EALIGN;
   if (max_pages <= 0 || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return PHS_EINVAL;
   if (out_dtype != PHS_OUT_BF16 && out_dtype != PHS_OUT_F32) return PHS_EINVAL;
   const int D = pool->head_dim, Hkv = pool->num_kv_heads;
@@ -320,6 +323,13 @@ int prepare_decode(DecodeCall& c, const void* q, int Hq, const phs_paged_pool* p
   c.a.max_splits = c.pl.max_splits;
   c.a.out_f32 = out_dtype == PHS_OUT_F32;
   c.a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  if (k_new) {  // the step's append, fused into the split launch
+    c.a.app = FusedAppend{reinterpret_cast<const __nv_bfloat16*>(k_new),
+                          reinterpret_cast<const __nv_bfloat16*>(v_new),
+                          reinterpret_cast<__nv_bfloat16*>(pool->k),
+                          reinterpret_cast<__nv_bfloat16*>(pool->v)};
+    c.a.page_refcount = page_refcount;
+  }
 
   std::memset(&c.m, 0, sizeof(c.m));
   c.m.seq_lens = seq_lens;
@@ -488,13 +498,14 @@ int phs_attn_decode_full_paged_split(const void* q, int32_t num_q_heads,
                                      const int32_t* qtable, int32_t max_qpages_per_seq,
                                      const int32_t* qlens, int32_t batch, float softmax_scale,
                                      int32_t tokens_per_split, void* out, int32_t out_dtype,
-                                     void* workspace, size_t workspace_bytes,
+                                     void* workspace, size_t workspace_bytes, const void* k_new,
+                                     const void* v_new, const int32_t* page_refcount,
                                      int32_t* dev_status, void* stream) {
   DecodeCall c;
   int st = prepare_decode(c, q, num_q_heads, pool, block_table, max_pages_per_seq, seq_lens,
                           max_seq_len, int8, qtable, max_qpages_per_seq, qlens, batch,
                           softmax_scale, tokens_per_split, out, out_dtype, workspace,
-                          workspace_bytes, dev_status);
+                          workspace_bytes, k_new, v_new, page_refcount, dev_status);
   if (st) return st;
   return launch_split_decode(c.pl.D, c.tk, c.tv, c.tk8, c.tv8, c.a, batch,
                              reinterpret_cast<cudaStream_t>(stream));
@@ -539,12 +550,13 @@ int phs_attn_decode_full_paged(const void* q, int32_t num_q_heads, const phs_pag
                                int32_t max_qpages_per_seq, const int32_t* qlens, int32_t batch,
                                float softmax_scale, int32_t tokens_per_split, void* out,
                                int32_t out_dtype, void* workspace, size_t workspace_bytes,
-                               int32_t* dev_status, void* stream) {
+                               const void* k_new, const void* v_new,
+                               const int32_t* page_refcount, int32_t* dev_status, void* stream) {
   DecodeCall c;
   int st = prepare_decode(c, q, num_q_heads, pool, block_table, max_pages_per_seq, seq_lens,
                           max_seq_len, int8, qtable, max_qpages_per_seq, qlens, batch,
                           softmax_scale, tokens_per_split, out, out_dtype, workspace,
-                          workspace_bytes, dev_status);
+                          workspace_bytes, k_new, v_new, page_refcount, dev_status);
   if (st) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launch_split_decode(c.pl.D, c.tk, c.tv, c.tk8, c.tv8, c.a, batch, s))) return st;
@@ -888,7 +900,8 @@ int phs_attn_decode_hybrid_stack(const phs_layer* layers, int32_t num_layers,
     st = phs_attn_decode_full_paged(L.q, num_q_heads, &L.paged, block_table, max_pages_per_seq,
                                     seq_lens, max_seq_len, nullptr, nullptr, 0, nullptr, batch,
                                     softmax_scale, 0, L.out, out_dtype, workspace,
-                                    workspace_bytes, dev_status, stream);
+                                    workspace_bytes, nullptr, nullptr, nullptr, dev_status,
+                                    stream);
     if (st) return st;
   }
   return PHS_OK;
@@ -1319,7 +1332,8 @@ extern "C" int phs_attn_decode_full_paged_noalloc(
   DecodeCall c;
   st = prepare_decode(c, q, num_q_heads, pool, block_table, max_pages_per_seq, seq_lens,
                       max_seq_len, int8, qtable, max_qpages_per_seq, qlens, batch, softmax_scale,
-                      tps, out, out_dtype, scratch, PHS_NOALLOC_SCRATCH_BYTES, dev_status);
+                      tps, out, out_dtype, scratch, PHS_NOALLOC_SCRATCH_BYTES, nullptr, nullptr,
+                      nullptr, dev_status);
   if (st) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launch_split_decode(c.pl.D, c.tk, c.tv, c.tk8, c.tv8, c.a, batch, s))) return st;

@@ -125,7 +125,7 @@ __device__ __forceinline__ int walk_chunks(WarpState<D, TWO>& st, const QFrags<D
     if (!wait(j)) return j;
     const uint32_t valid = prepare(j);
     if (ids[j] >= 0) {
-      patch(j, sK(j));  // a fused append's new token, taken from the input
+      patch(j, sK(j));  // the stack kernel's fused append: the new row from the input
       qk(j);
       softmax(j, valid);
       pv(j);
@@ -162,11 +162,17 @@ __device__ __noinline__ void check_prefix_ids(const SplitArgs& a, int b, int h, 
 
 // The work of one CTA: request b, KV head h, split s.  q/out/ws_o/ws_ml are
 // the layer's; `app` (k_new null: none) is an append fused into this
-// launch: the CTA holding token n-1 writes it into its page and patches its
-// staged copy from the input before using it.  MIXED: the launch may hold
-// INT8 splits (a.qlens set); without them the INT8 walk is compiled out,
-// which leaves the bf16 walk its registers (no spills).
-template <int D, bool TWO, bool MIXED>
+// launch, done one of two ways:
+//   WRITE_FIRST (single-layer launches): the CTA holding token n-1 writes it
+//     into its page before it issues its copies, which then read it back --
+//     nothing in the chunk loop, so no register cost there;
+//   otherwise (the stack kernel, whose layers may share one pool): it writes
+//     the page and patches its staged copy from the input in the loop, so
+//     each layer attends its own token even when another layer of the same
+//     launch writes the same slot.
+// MIXED: the launch may hold INT8 splits (a.qlens set); without them the
+// INT8 walk is compiled out, which leaves the bf16 walk its registers.
+template <int D, bool TWO, bool MIXED, bool WRITE_FIRST>
 __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensorMap* tv,
                                            const CUtensorMap* tk8, const CUtensorMap* tv8,
                                            const SplitArgs& a, const __nv_bfloat16* q,
@@ -188,6 +194,8 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
   if (a.prefix_bad != nullptr) check_prefix_ids(a, b, h, s);
 
   int n = a.seq_lens[b];
+  // a fused append has a slot for the new token only inside the table
+  const bool appends = app.k_new != nullptr && n >= 1 && n <= a.n_clamp;
   if (n > a.n_clamp) {  // longer than its block table or the stated bound
     if (s == 0 && h == 0 && threadIdx.x == 0) set_status(a.status, PHS_ERANGE);
     n = a.n_clamp;
@@ -199,6 +207,11 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
     if (s == 0 && h == 0 && threadIdx.x == 0) set_status(a.status, PHS_ERANGE);
     return;
   }
+  // a fused append writes bf16 pages only: a new token inside the request's
+  // INT8 region is not written and is an error
+  if (MIXED && app.k_new != nullptr && n >= 1 && n - 1 < qlen && s == 0 && h == 0 &&
+      threadIdx.x == 0)
+    set_status(a.status, PHS_ERANGE);
   const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
   if (ns == 0) {  // empty request: zero output (unless another kernel owns it)
     // a fused append whose new token falls inside the shared prefix (n ==
@@ -283,6 +296,34 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
       }
     }
   };
+  // fused append, before any copy is issued: the warp whose chunk holds
+  // token n - 1 (the request's last token, so in this split only if it is the
+  // last bf16 split) writes the new row into its page -- unless the page is
+  // shared -- and the chunk's copy reads it back like any other row.  The
+  // proxy fences order those generic stores before the copies.
+  if (WRITE_FIRST && appends && !is_i8 && n - 1 >= t0 && n - 1 < t1) {
+    const int ci = (n - 1 - t0) / kPage;  // chunk within the split
+    if (ci % NW == warp) {
+      const int id = ids[ci / NW], r = (n - 1) % kPage;
+      if (id >= 0) {
+        if (a.page_refcount != nullptr && __ldg(a.page_refcount + id) != 1) {
+          if (lane == 0) set_status(a.status, PHS_ESHARED);  // a shared page: left as it is
+        } else {
+          const int op = lane >> 4, c = lane & 15;  // lanes 0-15 K, 16-31 V
+          if (c < D / 8) {
+            const size_t src = (static_cast<size_t>(b) * a.Hkv + h) * D + c * 8;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>((op ? app.v_new : app.k_new) + src));
+            __nv_bfloat16* pool = op ? app.v_pool : app.k_pool;
+            *reinterpret_cast<uint4*>(
+                pool + ((static_cast<size_t>(id) * a.Hkv + h) * kPage + r) * D + c * 8) = v;
+            fence_proxy_async_global();
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) fence_proxy_async_global();
+    }
+  }
   if (lane == 0) {
     if (is_i8) {
       prefetch_tmap(tk8);
@@ -315,13 +356,16 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
   FragOffsets fo;
   fo.init<D>(lane);
   auto no_patch = [](int, uint32_t) {};
-  // fused append: row (n-1) % 16 of the chunk holding token n-1; lanes 0-15
-  // carry K, 16-31 V, 16 bytes each (the staged tile is [half][16 rows][128 B]
-  // with the 128-byte swizzle)
+  // in-loop append (stack kernel): row (n-1) % 16 of the chunk holding token
+  // n-1; lanes 0-15 carry K, 16-31 V, 16 bytes each (the staged tile is
+  // [half][16 rows][128 B] with the 128-byte swizzle)
   auto patch = [&](int j, uint32_t stage) {
     if (app.k_new == nullptr) return;
     const int r = n - 1 - (t0 + kPage * (warp + j * NW));
     if (r < 0 || r >= kPage) return;
+    // (a length past the table was clamped: no slot for its new token; read
+    // again here so that nothing extra stays live across the loop)
+    if (__ldg(a.seq_lens + b) > a.n_clamp) return;
     if (a.page_refcount != nullptr && __ldg(a.page_refcount + ids[j]) != 1) {
       // a shared page: leave it (and the staged copy of it) as it is
       if (lane == 0) set_status(a.status, PHS_ESHARED);
@@ -340,11 +384,16 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
     }
     __syncwarp();
   };
-  const int failed =
-      is_i8 ? walk_chunks<true, D, TWO, S>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem, t0,
-                                           t1, warp, a.scale_log2, lane, issue, no_patch)
-            : walk_chunks<false, D, TWO, S>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem,
-                                            t0, t1, warp, a.scale_log2, lane, issue, patch);
+  int failed;
+  if (is_i8)
+    failed = walk_chunks<true, D, TWO, S>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem, t0,
+                                          t1, warp, a.scale_log2, lane, issue, no_patch);
+  else if constexpr (WRITE_FIRST)
+    failed = walk_chunks<false, D, TWO, S>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem,
+                                           t0, t1, warp, a.scale_log2, lane, issue, no_patch);
+  else
+    failed = walk_chunks<false, D, TWO, S>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem,
+                                           t0, t1, warp, a.scale_log2, lane, issue, patch);
   if (failed >= 0 && lane == 0) {
     // gave up: record it and drain (bounded) the loads still in flight
     set_status(a.status, PHS_ETIMEOUT);
@@ -437,17 +486,14 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
 
 // request index fastest: CTAs that read the same shared-prefix pages for
 // different requests run close together in time and share them through L2
-// APP: the launch carries a fused append (a.app); without it the patch code
-// is compiled out, which keeps the plain split free of spills.
-template <int D, bool TWO, bool MIXED, bool APP>
+template <int D, bool TWO, bool MIXED>
 __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
     phs_split_decode_kernel(const __grid_constant__ CUtensorMap tk,
                             const __grid_constant__ CUtensorMap tv,
                             const __grid_constant__ CUtensorMap tk8,
                             const __grid_constant__ CUtensorMap tv8, const SplitArgs a) {
-  const FusedAppend none{nullptr, nullptr, nullptr, nullptr};
-  split_body<D, TWO, MIXED>(&tk, &tv, &tk8, &tv8, a, a.q, a.out, a.ws_o, a.ws_ml,
-                            APP ? a.app : none, blockIdx.x, blockIdx.y, blockIdx.z);
+  split_body<D, TWO, MIXED, true>(&tk, &tv, &tk8, &tv8, a, a.q, a.out, a.ws_o, a.ws_ml, a.app,
+                                  blockIdx.x, blockIdx.y, blockIdx.z);
   // started early beside an independent grid: one CTA holds this grid open
   // until that grid has finished, so a launch that waits for this grid also
   // sees the other's results
@@ -465,8 +511,8 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
     phs_stack_full_kernel(const __grid_constant__ StackFullParams p) {
   const int l = blockIdx.z / p.a.max_splits, s = blockIdx.z - l * p.a.max_splits;
   const StackFullLayer& L = p.layer[l];
-  split_body<D, TWO, false>(&L.tk, &L.tv, &L.tk, &L.tv, p.a, L.q, L.out, L.ws_o, L.ws_ml,
-                            L.app, blockIdx.x, blockIdx.y, s);
+  split_body<D, TWO, false, false>(&L.tk, &L.tv, &L.tk, &L.tv, p.a, L.q, L.out, L.ws_o, L.ws_ml,
+                                   L.app, blockIdx.x, blockIdx.y, s);
 }
 
 // Cross-split merge of one (request, KV head): warp w of the CTA merges
@@ -495,10 +541,8 @@ template <int D, bool TWO>
 static int launch_split_t(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tk8,
                           const CUtensorMap& tv8, const SplitArgs& a, int B, cudaStream_t stream,
                           bool dependent) {
-  if (a.qlens && a.app.k_new) return PHS_EUNSUPPORTED;  // no fused append over INT8 pages
-  auto kern = a.qlens        ? phs_split_decode_kernel<D, TWO, true, false>
-              : a.app.k_new ? phs_split_decode_kernel<D, TWO, false, true>
-                            : phs_split_decode_kernel<D, TWO, false, false>;
+  auto kern = a.qlens ? phs_split_decode_kernel<D, TWO, true>
+                      : phs_split_decode_kernel<D, TWO, false>;
   const int smem = SplitLayout<D>::kAlloc;
   if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
   dim3 grid(B, a.Hkv, a.max_splits);

@@ -98,7 +98,7 @@ def test_split_kernel_wait_runs_out_and_returns(wait_lib):
     btd, sld = dev(bt), dev(lens)
     rc = wait_lib.phs_attn_decode_full_paged(
         _vp(q), Hq, ctypes.byref(pc), _vp(btd), bt.shape[1], _vp(sld), ms, None, None, 0, None,
-        B, 1 / np.sqrt(D), 0, _vp(out), 1, _vp(ws), ws.numel(), _vp(st),
+        B, 1 / np.sqrt(D), 0, _vp(out), 1, _vp(ws), ws.numel(), None, None, None, _vp(st),
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == 0
     torch.cuda.synchronize()               # the launch returned: the stream drains
