@@ -27,10 +27,9 @@ namespace phs {
 
 // Magic-number rounding: for |y| < 2^22, fl(y + 1.5 * 2^23) rounds y to the
 // nearest integer (ties to even, the default rounding) and keeps it in the
-// low mantissa bits, so the code byte is the low byte of the sum's bits.
-constexpr float kRoundMagic = 12582912.0f;
-// The same plus 128: fl(rint(y) + 128 + 1.5 * 2^23) (128 is even, so the
-// ties still go to even) leaves the stored byte x + 128 in the low bits.
+// low mantissa bits.  With 128 added to the constant (128 is even, so the
+// ties still go to even) the low byte of the sum's bits is the stored byte
+// x + 128.
 constexpr float kRoundMagicOffset = 12582912.0f + 128.0f;
 
 // Packed fp32 pairs (two lanes of work per instruction on the FMA pipe,
