@@ -58,6 +58,7 @@ def _oracle_rows(pool, q, bt, lens, rows, D=128):
     (16, 32, 2, 512, 6, 700),      # G = 16, 256 rows
     (6, 32, 8, 256, 7, 5000),      # own tokens over several splits: merged with the prefix
     (64, 8, 8, 1024, 8, 700),      # G = 1: one row per request and KV head, 64 rows
+    (40, 32, 8, 2368, 9, 700),     # 37 halves: a partial last S tile; rows 160
 ])
 def test_shared_prefix_matches_oracle_and_paged_path(B, Hq, Hkv, shared_len, seed, max_suffix):
     rng = np.random.default_rng(seed)
