@@ -520,9 +520,15 @@ __global__ void __launch_bounds__(kPfxThreads, 1)
 
 // Merge of the shared-prefix partials with each request's suffix partials.
 // One CTA per (request, KV head); warp w merges query rows w, w+4, ...
+// Every load a row needs -- the sources' (m, l), this lane's four columns of
+// each source's O, and the request's prefix flags -- is issued before any
+// of them is used, so the merge costs one memory round trip per chunk of
+// sources (the partials were just written and sit in L2); chunks combine
+// with a running maximum.
+constexpr int kMergeChunk = 24;  // sources per round trip (24 float4 per lane)
+
 __global__ void __launch_bounds__(128) phs_merge_prefix_kernel(const PrefixMergeArgs a) {
   constexpr int D = 128;
-  constexpr int V = D / 32;
   const int b = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // launched as a dependent of the own-token split, which does not complete
@@ -531,6 +537,7 @@ __global__ void __launch_bounds__(128) phs_merge_prefix_kernel(const PrefixMerge
   const int G = a.G;
   const int n = min(a.seq_lens[b], a.n_clamp);
   const int ns = n > a.shared_len ? min((n - a.shared_len + a.T - 1) / a.T, a.max_splits) : 0;
+  const int total = a.num_psplits + ns;  // sources: prefix splits, then suffix splits
   const size_t out_row0 = (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * G) * D;
   // a request whose table does not begin with the shared pages (or that is
   // shorter than the shared prefix) was flagged by the own-token split: the
@@ -538,69 +545,69 @@ __global__ void __launch_bounds__(128) phs_merge_prefix_kernel(const PrefixMerge
   int bad = 0;
   for (int i = lane; i < a.bad_slots; i += 32)
     bad |= a.prefix_bad[static_cast<size_t>(b) * a.bad_slots + i];
-  if (__any_sync(0xffffffffu, bad)) {
-    for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-      if (a.out_f32)
-        reinterpret_cast<float*>(a.out)[out_row0 + e] = 0.f;
-      else
-        reinterpret_cast<__nv_bfloat16*>(a.out)[out_row0 + e] = __float2bfloat16_rn(0.f);
-    }
-    return;
-  }
   for (int g = warp; g < G; g += 4) {
     const int r = b * G + g;
-    // sources: prefix splits then suffix splits
-    const int total = a.num_psplits + ns;
-    auto ml_of = [&](int s) -> float2 {
-      if (s < a.num_psplits)
-        return reinterpret_cast<const float2*>(
-            a.ws_pml)[(static_cast<size_t>(h) * a.num_psplits + s) * kPfxRows + r];
-      const size_t part = (static_cast<size_t>(b) * a.Hkv + h) * a.max_splits + (s - a.num_psplits);
-      return reinterpret_cast<const float2*>(a.ws_ml)[part * G + g];
-    };
-    // split s's output row: prefix splits kPfxRows rows apart, then the
-    // suffix splits G rows apart (a select, so the loads can be hoisted)
+    const float2* pml = reinterpret_cast<const float2*>(a.ws_pml) +
+                        static_cast<size_t>(h) * a.num_psplits * kPfxRows + r;
+    const float2* sml = reinterpret_cast<const float2*>(a.ws_ml) +
+                        (static_cast<size_t>(b) * a.Hkv + h) * a.max_splits * G + g;
+    // source s's output row: prefix splits kPfxRows rows apart, then the
+    // suffix splits G rows apart
     const float* po = a.ws_po + ((static_cast<size_t>(h) * a.num_psplits) * kPfxRows + r) * D;
-    const float* so = a.ws_o + (((static_cast<size_t>(b) * a.Hkv + h) * a.max_splits) * G + g) * D -
-                      static_cast<ptrdiff_t>(a.num_psplits) * G * D;
-    auto o_of = [&](int s) -> const float* {
-      return s < a.num_psplits ? po + static_cast<size_t>(s) * kPfxRows * D
-                               : so + static_cast<ptrdiff_t>(s) * G * D;
+    const float* so = a.ws_o + (((static_cast<size_t>(b) * a.Hkv + h) * a.max_splits) * G + g) * D;
+    auto o_of = [&](int s) -> const float4* {
+      return reinterpret_cast<const float4*>(
+                 s < a.num_psplits ? po + static_cast<size_t>(s) * kPfxRows * D
+                                   : so + static_cast<size_t>(s - a.num_psplits) * G * D) +
+             lane;
     };
-    float M = -INFINITY;
-    for (int s = lane; s < total; s += 32) M = fmaxf(M, ml_of(s).x);
+    float M = -INFINITY, lsum = 0.f;  // lsum: this lane's share of the weighted row sums
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < total; s0 += kMergeChunk) {
+      const int cnt = min(kMergeChunk, total - s0);
+      const int sl = s0 + lane;
+      const float2 ml = lane < cnt ? (sl < a.num_psplits ? pml[static_cast<size_t>(sl) * kPfxRows]
+                                                         : sml[static_cast<size_t>(sl - a.num_psplits) * G])
+                                   : make_float2(-INFINITY, 0.f);
+      float4 o[kMergeChunk];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Lsum = 0.f;
-    float acc[V] = {0.f, 0.f, 0.f, 0.f};
-    for (int s0 = 0; s0 < total; s0 += 32) {
-      float wl = 0.f;
-      if (s0 + lane < total) {
-        const float2 v = ml_of(s0 + lane);
-        wl = v.x == -INFINITY ? 0.f : exp2f(v.x - M);
-        Lsum += v.y * wl;
+      for (int k = 0; k < kMergeChunk; ++k)
+        o[k] = k < cnt ? *o_of(s0 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+      float mc = ml.x;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, off));
+      const float mn = fmaxf(M, mc);
+      if (mn == -INFINITY) continue;  // no tokens in any source so far
+      const float keep = M == -INFINITY ? 0.f : exp2f(M - mn);
+      const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mn);
+      lsum = lsum * keep + ml.y * w;
+      acc.x *= keep;
+      acc.y *= keep;
+      acc.z *= keep;
+      acc.w *= keep;
+#pragma unroll
+      for (int k = 0; k < kMergeChunk; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w, k);
+        acc.x += wk * o[k].x;
+        acc.y += wk * o[k].y;
+        acc.z += wk * o[k].z;
+        acc.w += wk * o[k].w;
       }
-      const int cnt = min(32, total - s0);
-#pragma unroll 16
-      for (int k = 0; k < cnt; ++k) {  // up to 16 split loads in flight per lane
-        const float w = __shfl_sync(0xffffffffu, wl, k);
-        const float4 o = *reinterpret_cast<const float4*>(o_of(s0 + k) + lane * V);
-        acc[0] += w * o.x;
-        acc[1] += w * o.y;
-        acc[2] += w * o.z;
-        acc[3] += w * o.w;
-      }
+      M = mn;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      const size_t idx = out_row0 + static_cast<size_t>(g) * D + lane * V + i;
-      if (a.out_f32)
-        reinterpret_cast<float*>(a.out)[idx] = acc[i] * inv;
-      else
-        reinterpret_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(acc[i] * inv);
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const bool zero = __any_sync(0xffffffffu, bad) != 0;
+    const float res[4] = {zero ? 0.f : acc.x * inv, zero ? 0.f : acc.y * inv,
+                          zero ? 0.f : acc.z * inv, zero ? 0.f : acc.w * inv};
+    const size_t idx = out_row0 + static_cast<size_t>(g) * D + lane * 4;
+    if (a.out_f32) {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + idx) =
+          make_float4(res[0], res[1], res[2], res[3]);
+    } else {
+      __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(a.out) + idx;
+      *reinterpret_cast<uint2*>(ob) = make_uint2(pack_bf16(res[0], res[1]), pack_bf16(res[2], res[3]));
     }
   }
 }
