@@ -76,6 +76,12 @@ def test_shared_prefix_matches_oracle_and_paged_path(B, Hq, Hkv, shared_len, see
     rows = sorted(set([0, B - 1, B // 2]))
     assert_close(got[rows], _oracle_rows(pool, q, bt, lens, rows), f"B={B} shared={shared_len}")
     assert_close(got, out_np(ref_gpu), "vs per-request decode")
+    # bf16 output is the fp32 result rounded once: bit for bit
+    out16 = phs.attn_decode_shared_prefix(q, pool, dev(bt), dev(lens), int(lens.max()), shared_len,
+                                          out_dtype=torch.bfloat16, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(out16, out.to(torch.bfloat16))
 
 
 def test_shared_prefix_rejects_bad_shapes():
