@@ -1286,9 +1286,9 @@ def run_gpu(args, rank, world, local_rank):
     phs.lib()
     copy_gbs = time_copy(device)
     read_gbs = time_read(device)
-    configs = [args.config] if args.config else list(SUITE)
+    run_list = [args.config] if args.config else list(SUITE)
     lines = {}
-    for c in configs:
+    for c in run_list:
         wl = make_workload(c, device, args)
         use_graph = args.graph if args.graph is not None else c == 1
         if use_graph and not wl.graphable:
@@ -1300,9 +1300,9 @@ def run_gpu(args, rank, world, local_rank):
         del wl
         gc.collect()
         torch.cuda.empty_cache()
-    head = lines[configs[0]]
-    if len(configs) > 1:
-        head["configs"] = {str(c): lines[c] for c in configs[1:]}
+    head = lines[run_list[0]]
+    if len(run_list) > 1:
+        head["configs"] = {str(c): lines[c] for c in run_list[1:]}
         head["suite"] = ("the headline is the 70-layer hybrid stack (the largest workload); "
                          "the other workloads were measured in the same run, each line with "
                          "its own steps, roofline, e2e and CPU-oracle baseline")
