@@ -177,9 +177,11 @@ size_t phs_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t nu
                                   int32_t head_dim, int32_t max_seq_len,
                                   int32_t tokens_per_split, int32_t has_int8);
 
-/* The split length (tokens) the decode call uses for these arguments: the
- * longest of 4096, 2048, ..., 128 that gives a max_seq_len request at least
- * 8 splits and whose grid (batch x num_kv_heads x the splits of a
+/* The split length (tokens) the decode call uses for these arguments: 256
+ * when max_seq_len is 129..256 and batch x num_kv_heads is at most the
+ * GPU's SM count (one split per request, no merge); otherwise the longest
+ * of 4096, 2048, ..., 128 that gives a max_seq_len request at least 8
+ * splits and whose grid (batch x num_kv_heads x the splits of a
  * max_seq_len request) has at least 16 CTAs per SM, else 128;
  * tokens_per_split > 0 is returned as given. */
 int32_t phs_decode_tokens_per_split(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len,

@@ -270,13 +270,17 @@ def test_split_and_merge_entry_points_match_composed_call():
 
 # ------------------------------------------------------------ split plan --
 def test_split_length_planner():
-    # the longest of 4096, 2048, ..., 128 tokens that gives the longest
-    # request at least 8 splits and whose grid (batch x KV heads x splits of
-    # the longest request) still has 16 CTAs per SM, else 128; an explicit
-    # length is kept; the workspace follows the chosen length
+    # 256 when the longest request has 129..256 tokens and batch x KV heads
+    # fits the SMs (one split each); else the longest of 4096, 2048, ..., 128
+    # tokens that gives the longest request at least 8 splits and whose grid
+    # (batch x KV heads x splits of the longest request) still has 16 CTAs
+    # per SM, else 128; an explicit length is kept; the workspace follows
+    # the chosen length
     sms = torch.cuda.get_device_properties(0).multi_processor_count
 
     def rule(B, Hkv, n):
+        if 128 < n <= 256 and B * Hkv <= sms:
+            return 256  # one split per request: no merge after the decode
         t = 4096
         while t > 128 and 8 * t > n:
             t //= 2
@@ -285,7 +289,8 @@ def test_split_length_planner():
         return t
 
     for B, Hkv, n in [(64, 8, 32769), (32, 8, 65537), (256, 8, 131073), (2, 1, 600_000),
-                      (1, 1, 100), (8, 8, 8000)]:
+                      (1, 1, 100), (8, 8, 8000), (2, 2, 201), (2, 2, 128), (2, 2, 257),
+                      (64, 8, 200)]:
         t = phs.decode_tokens_per_split(B, Hkv, n)
         assert t == rule(B, Hkv, n), (B, Hkv, n)
         ws = phs.decode_workspace_bytes(B, 4 * Hkv, Hkv, 128, n)
