@@ -146,13 +146,13 @@ def test_swa_ring_decode(W, D, Hq, Hkv):
     assert_close(out_np(out), ref, f"W={W} D={D}")
 
 
-@pytest.mark.parametrize("B", [4, 700, 7200])
+@pytest.mark.parametrize("B", [4, 300, 700, 7200])
 def test_swa_ring_decode_launch_shapes(B):
-    # the SWA launch picks its shape from the work and shared memory: 4 warps
-    # x 4 stages when every (request, KV head) unit has a warp of its own (4
-    # units), 8 warps x 2 stages for many units (700), and 4 warps x 2 stages
-    # when the per-request table of a very large batch leaves too little
-    # shared memory for 8 warps (7200)
+    # the SWA launch picks its shape from the work: one CTA per (request, KV
+    # head) unit with its chunks spread over 4 warps when every unit has an
+    # SM of its own (4 units), 4 warps x 4 stages when every unit has a warp
+    # of its own in one wave (300), and 8 persistent warps x 2 stages for
+    # many units (700, 7200)
     W, D, Hq, Hkv = 16, 128, 4, 1
     lens = np.random.default_rng(B).integers(1, 3 * W, B).astype(np.int32)
     c = ring_case(lens, W, Hq, Hkv, D, seed=B)

@@ -5,8 +5,9 @@ without a fault, the test builds a variant of the library from a patched
 copy of the sources (never the product build): the wait limit is cut to
 2 ms and the TMA producer of one warp skips both the copy and the arrival of
 one stage, so that nothing is in flight for it and its consumer's wait
-cannot complete.  Covered: the split-KV kernel and the SWA ring kernel (the
-tensor-core shared-prefix kernel is left out).  Other requests must come
+cannot complete.  Covered: the split-KV kernel and both SWA ring kernels,
+the persistent one and the one-CTA-per-unit latency shape (the tensor-core
+shared-prefix kernel is left out).  Other requests must come
 out exactly as the product library computes them."""
 import ctypes
 import os
@@ -33,10 +34,14 @@ PATCHES = {
                        "  auto issue = [&](int j) {  // lane 0 only\n"
                        "    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && "
                        "warp == 0 && j == 1) return;\n")],
-    # SWA kernel: block 0, warp 0 never issues the second chunk of its first unit
+    # SWA kernels: block 0, warp 0 never issues the second chunk of its
+    # first unit (persistent kernel) or its second chunk (one CTA per unit)
     "phs_swa.cu": [("    if (!iu.ok) {\n",
                     "    if (blockIdx.x == 0 && warp == 0 && ik == 0 && ic == 1) {\n"
-                    "    } else if (!iu.ok) {\n")],
+                    "    } else if (!iu.ok) {\n"),
+                   ("  auto issue = [&](int jj) {  // lane 0: chunk warp + NW jj into stage jj % S\n",
+                    "  auto issue = [&](int jj) {  // lane 0: chunk warp + NW jj into stage jj % S\n"
+                    "    if (blockIdx.x == 0 && warp == 0 && jj == 1) return;\n")],
 }
 
 
@@ -109,13 +114,16 @@ def test_split_kernel_wait_runs_out_and_returns(wait_lib):
     assert torch.equal(again, ref)
 
 
-def test_swa_kernel_wait_runs_out_and_returns(wait_lib):
-    B, Hq, Hkv, D, W = 4, 16, 2, 128, 128
+@pytest.mark.parametrize("B", [4, 80])  # 8 units: one CTA each; 160 units: persistent warps
+def test_swa_kernel_wait_runs_out_and_returns(wait_lib, B):
+    Hq, Hkv, D, W = 16, 2, 128, 128
     ring = phs.RingPool(synth.normal_bf16((B, Hkv, W, D), 9, device="cuda"),
                         synth.normal_bf16((B, Hkv, W, D), 10, device="cuda"))
     q = synth.normal_bf16((B, Hq, D), 11, device="cuda")
-    rp = dev(np.array([3, 127, 64, 0], np.int32))
-    sl = dev(np.array([500, 90, 128, 7000], np.int32))
+    rng = np.random.default_rng(B)
+    pos = np.concatenate([[3, 127, 64, 0], rng.integers(0, W, B - 4)]).astype(np.int32)
+    lens = np.concatenate([[500, 90, 128, 7000], rng.integers(1, 3 * W, B - 4)]).astype(np.int32)
+    rp, sl = dev(pos), dev(lens)
     ref = phs.attn_decode_swa_ring(q, ring, rp, sl, out_dtype=torch.float32)
     out = torch.zeros_like(ref)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
