@@ -328,6 +328,9 @@ int prepare_decode(DecodeCall& c, const void* q, int Hq, const phs_paged_pool* p
   c.a.max_splits = c.pl.max_splits;
   c.a.out_f32 = out_dtype == PHS_OUT_F32;
   c.a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  DevInfo di;
+  if ((st = dev_info(di))) return st;
+  c.a.num_sms = di.sms;
   if (k_new) {  // the step's append, fused into the split launch
     c.a.app = FusedAppend{reinterpret_cast<const __nv_bfloat16*>(k_new),
                           reinterpret_cast<const __nv_bfloat16*>(v_new),
@@ -548,6 +551,33 @@ int phs_attn_merge_splits(int32_t batch, int32_t num_q_heads, int32_t num_kv_hea
   return launch_merge(head_dim, m, batch, reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+// The decode call; allow_wide = false keeps 4 warps per CTA whatever the
+// grid (the unfused stack decides for the whole step, as the fused one does).
+int decode_full_paged(const void* q, int32_t num_q_heads, const phs_paged_pool* pool,
+                      const int32_t* block_table, int32_t max_pages_per_seq,
+                      const int32_t* seq_lens, int32_t max_seq_len, const phs_int8_pool* int8,
+                      const int32_t* qtable, int32_t max_qpages_per_seq, const int32_t* qlens,
+                      int32_t batch, float softmax_scale, int32_t tokens_per_split, void* out,
+                      int32_t out_dtype, void* workspace, size_t workspace_bytes,
+                      const void* k_new, const void* v_new, const int32_t* page_refcount,
+                      int32_t* dev_status, void* stream, bool allow_wide) {
+  DecodeCall c;
+  int st = prepare_decode(c, q, num_q_heads, pool, block_table, max_pages_per_seq, seq_lens,
+                          max_seq_len, int8, qtable, max_qpages_per_seq, qlens, batch,
+                          softmax_scale, tokens_per_split, out, out_dtype, workspace,
+                          workspace_bytes, k_new, v_new, page_refcount, dev_status);
+  if (st) return st;
+  if (!allow_wide) c.a.num_sms = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_split_decode(c.pl.D, c.tk, c.tv, c.tk8, c.tv8, c.a, batch, s))) return st;
+  if (c.pl.max_splits == 1) return PHS_OK;  // every request finished in its only split
+  return launch_merge(c.pl.D, c.m, batch, s);
+}
+
+}  // namespace
+
 int phs_attn_decode_full_paged(const void* q, int32_t num_q_heads, const phs_paged_pool* pool,
                                const int32_t* block_table, int32_t max_pages_per_seq,
                                const int32_t* seq_lens, int32_t max_seq_len,
@@ -557,16 +587,10 @@ int phs_attn_decode_full_paged(const void* q, int32_t num_q_heads, const phs_pag
                                int32_t out_dtype, void* workspace, size_t workspace_bytes,
                                const void* k_new, const void* v_new,
                                const int32_t* page_refcount, int32_t* dev_status, void* stream) {
-  DecodeCall c;
-  int st = prepare_decode(c, q, num_q_heads, pool, block_table, max_pages_per_seq, seq_lens,
-                          max_seq_len, int8, qtable, max_qpages_per_seq, qlens, batch,
-                          softmax_scale, tokens_per_split, out, out_dtype, workspace,
-                          workspace_bytes, k_new, v_new, page_refcount, dev_status);
-  if (st) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = launch_split_decode(c.pl.D, c.tk, c.tv, c.tk8, c.tv8, c.a, batch, s))) return st;
-  if (c.pl.max_splits == 1) return PHS_OK;  // every request finished in its only split
-  return launch_merge(c.pl.D, c.m, batch, s);
+  return decode_full_paged(q, num_q_heads, pool, block_table, max_pages_per_seq, seq_lens,
+                           max_seq_len, int8, qtable, max_qpages_per_seq, qlens, batch,
+                           softmax_scale, tokens_per_split, out, out_dtype, workspace,
+                           workspace_bytes, k_new, v_new, page_refcount, dev_status, stream, true);
 }
 
 int phs_attn_decode_swa_ring(const void* q, int32_t num_q_heads, const phs_ring_pool* ring,
@@ -828,10 +852,14 @@ int phs_attn_decode_hybrid_stack(const phs_layer* layers, int32_t num_layers,
   DevInfo di;
   if ((st = dev_info(di))) return st;
   if (nswa && swa_smem_bytes(D, num_q_heads / Hkv) > di.smem_optin) return PHS_EUNSUPPORTED;
+  // 8 warps per split CTA only if all Full layers' grids together fit one
+  // wave (the fused call's launch shape, so both give the same results)
+  bool wide = false;
   if (nfull) {
     DecodePlan pl;
     if ((st = make_plan(pl, batch, num_q_heads, Hkv, D, max_seq_len, 0, false))) return st;
     if (!workspace || workspace_bytes < pl.need) return PHS_EWORKSPACE;
+    wide = 1LL * batch * Hkv * pl.max_splits * nfull <= di.sms;
   }
 
   // ---- appends: all Full layers in one launch, all SWA layers in one
@@ -906,11 +934,10 @@ int phs_attn_decode_hybrid_stack(const phs_layer* layers, int32_t num_layers,
   for (int i = 0; i < num_layers; ++i) {
     const phs_layer& L = layers[i];
     if (!L.is_full) continue;
-    st = phs_attn_decode_full_paged(L.q, num_q_heads, &L.paged, block_table, max_pages_per_seq,
-                                    seq_lens, max_seq_len, nullptr, nullptr, 0, nullptr, batch,
-                                    softmax_scale, 0, L.out, out_dtype, workspace,
-                                    workspace_bytes, nullptr, nullptr, nullptr, dev_status,
-                                    stream);
+    st = decode_full_paged(L.q, num_q_heads, &L.paged, block_table, max_pages_per_seq, seq_lens,
+                           max_seq_len, nullptr, nullptr, 0, nullptr, batch, softmax_scale, 0,
+                           L.out, out_dtype, workspace, workspace_bytes, nullptr, nullptr, nullptr,
+                           dev_status, stream, wide);
     if (st) return st;
   }
   return PHS_OK;
@@ -1008,6 +1035,8 @@ int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_laye
     a.max_splits = pl.max_splits;
     a.out_f32 = out_dtype == PHS_OUT_F32;
     a.scale_log2 = scale_log2;
+    // 8 warps per CTA only if all Full layers' grids together fit one wave
+    a.num_sms = 1LL * batch * Hkv * pl.max_splits * nfull <= di.sms ? di.sms : 0;
     MergeArgs& ma = m->a;
     ma.seq_lens = seq_lens;
     ma.Hq = num_q_heads;

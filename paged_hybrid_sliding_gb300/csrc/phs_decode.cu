@@ -48,15 +48,16 @@ constexpr int kMaxChunksPerWarp = 64;  // tokens_per_split <= 4096
 #define PHS_SPLIT_MIN_CTAS 3
 #endif
 
-template <int D>
+// NW: warps per CTA (4; 8 for the single-wave bf16 launches)
+template <int D, int NW = kSplitWarps>
 struct SplitLayout {
   static constexpr int kStage = ChunkGeom<D>::kStageBytes;
   static constexpr int kStages = (D == 128) ? PHS_SPLIT_STAGES_128 : 4;
-  static constexpr int kStagesBytes = kSplitWarps * kStages * kStage;
+  static constexpr int kStagesBytes = NW * kStages * kStage;
   static constexpr int kIdsOff = kStagesBytes;
-  static constexpr int kIdsBytes = kSplitWarps * kMaxChunksPerWarp * 12;
+  static constexpr int kIdsBytes = NW * kMaxChunksPerWarp * 12;
   static constexpr int kBarOff = kIdsOff + kIdsBytes;
-  static constexpr int kBytes = kBarOff + kSplitWarps * kStages * 8;
+  static constexpr int kBytes = kBarOff + NW * kStages * 8;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
@@ -67,7 +68,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // One warp's walk over its chunks of a split.  Stage j is handed back to
 // TMA (chunk j + S) right after chunk j is folded into the warp state.
 // Returns the index of a chunk whose bounded wait gave up, or -1.
-template <bool I8, int D, bool TWO, int S, typename Issue, typename Patch>
+template <bool I8, int D, bool TWO, int S, int NW, typename Issue, typename Patch>
 __device__ __forceinline__ int walk_chunks(WarpState<D, TWO>& st, const QFrags<D, TWO>& qf,
                                            const FragOffsets& fo, int my_n, const int32_t* ids,
                                            const float* kss, const float* vss, uint32_t bar0,
@@ -75,7 +76,6 @@ __device__ __forceinline__ int walk_chunks(WarpState<D, TWO>& st, const QFrags<D
                                            int warp, float scale_log2, int lane, Issue&& issue,
                                            Patch&& patch) {
   constexpr int kStage = ChunkGeom<D>::kStageBytes;
-  constexpr int NW = kSplitWarps;
   using Scores = typename std::conditional<I8, ScoresI8<D, TWO>, ScoresBf16<D, TWO>>::type;
   Scores sc;
   uint32_t pa[2][I8 ? 4 : 2];
@@ -172,15 +172,14 @@ __device__ __noinline__ void check_prefix_ids(const SplitArgs& a, int b, int h, 
 //     launch writes the same slot.
 // MIXED: the launch may hold INT8 splits (a.qlens set); without them the
 // INT8 walk is compiled out, which leaves the bf16 walk its registers.
-template <int D, bool TWO, bool MIXED, bool WRITE_FIRST>
+template <int D, bool TWO, bool MIXED, bool WRITE_FIRST, int NW = kSplitWarps>
 __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensorMap* tv,
                                            const CUtensorMap* tk8, const CUtensorMap* tv8,
                                            const SplitArgs& a, const __nv_bfloat16* q,
                                            void* out, float* ws_o, float* ws_ml,
                                            const FusedAppend& app, int b, int h, int s) {
-  using L = SplitLayout<D>;
+  using L = SplitLayout<D, NW>;
   constexpr int S = L::kStages;
-  constexpr int NW = kSplitWarps;
   constexpr int GR = TWO ? 16 : 8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -386,13 +385,13 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
   };
   int failed;
   if (is_i8)
-    failed = walk_chunks<true, D, TWO, S>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem, t0,
+    failed = walk_chunks<true, D, TWO, S, NW>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem, t0,
                                           t1, warp, a.scale_log2, lane, issue, no_patch);
   else if constexpr (WRITE_FIRST)
-    failed = walk_chunks<false, D, TWO, S>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem,
+    failed = walk_chunks<false, D, TWO, S, NW>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem,
                                            t0, t1, warp, a.scale_log2, lane, issue, no_patch);
   else
-    failed = walk_chunks<false, D, TWO, S>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem,
+    failed = walk_chunks<false, D, TWO, S, NW>(st, qf, fo, my_n, ids, kss, vss, bar0, sbase, smem,
                                            t0, t1, warp, a.scale_log2, lane, issue, patch);
   if (failed >= 0 && lane == 0) {
     // gave up: record it and drain (bounded) the loads still in flight
@@ -486,13 +485,13 @@ __device__ __forceinline__ void split_body(const CUtensorMap* tk, const CUtensor
 
 // request index fastest: CTAs that read the same shared-prefix pages for
 // different requests run close together in time and share them through L2
-template <int D, bool TWO, bool MIXED>
-__global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
+template <int D, bool TWO, bool MIXED, int NW = kSplitWarps>
+__global__ void __launch_bounds__(NW * 32, NW == kSplitWarps ? PHS_SPLIT_MIN_CTAS : 1)
     phs_split_decode_kernel(const __grid_constant__ CUtensorMap tk,
                             const __grid_constant__ CUtensorMap tv,
                             const __grid_constant__ CUtensorMap tk8,
                             const __grid_constant__ CUtensorMap tv8, const SplitArgs a) {
-  split_body<D, TWO, MIXED, true>(&tk, &tv, &tk8, &tv8, a, a.q, a.out, a.ws_o, a.ws_ml, a.app,
+  split_body<D, TWO, MIXED, true, NW>(&tk, &tv, &tk8, &tv8, a, a.q, a.out, a.ws_o, a.ws_ml, a.app,
                                   blockIdx.x, blockIdx.y, blockIdx.z);
   // started early beside an independent grid: one CTA holds this grid open
   // until that grid has finished, so a launch that waits for this grid also
@@ -506,12 +505,12 @@ __global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
 // partials and new token.  Source: "Xiaomi MiMo-V2.5 inference system" page,
 // section 2 (layer-wise overlap of the step; whole-step replay).  The Full
 // layers of a stack hold bf16 pages only.
-template <int D, bool TWO>
-__global__ void __launch_bounds__(kSplitWarps * 32, PHS_SPLIT_MIN_CTAS)
+template <int D, bool TWO, int NW = kSplitWarps>
+__global__ void __launch_bounds__(NW * 32, NW == kSplitWarps ? PHS_SPLIT_MIN_CTAS : 1)
     phs_stack_full_kernel(const __grid_constant__ StackFullParams p) {
   const int l = blockIdx.z / p.a.max_splits, s = blockIdx.z - l * p.a.max_splits;
   const StackFullLayer& L = p.layer[l];
-  split_body<D, TWO, false, false>(&L.tk, &L.tv, &L.tk, &L.tv, p.a, L.q, L.out, L.ws_o, L.ws_ml,
+  split_body<D, TWO, false, false, NW>(&L.tk, &L.tv, &L.tk, &L.tv, p.a, L.q, L.out, L.ws_o, L.ws_ml,
                                    L.app, blockIdx.x, blockIdx.y, s);
 }
 
@@ -537,22 +536,31 @@ __global__ void __launch_bounds__(128) phs_stack_merge_kernel(const __grid_const
 }
 
 // ------------------------------------------------------------ launchers --
+// A bf16 launch whose grid has at most one CTA per SM (a latency-bound small
+// step) runs 8 warps per CTA, halving each warp's chain of chunks.
+static bool single_wave(const SplitArgs& a, long long ctas) {
+  return a.qlens == nullptr && a.num_sms > 0 && ctas <= a.num_sms;
+}
+
 template <int D, bool TWO>
 static int launch_split_t(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tk8,
                           const CUtensorMap& tv8, const SplitArgs& a, int B, cudaStream_t stream,
                           bool dependent) {
-  auto kern = a.qlens ? phs_split_decode_kernel<D, TWO, true>
-                      : phs_split_decode_kernel<D, TWO, false>;
-  const int smem = SplitLayout<D>::kAlloc;
+  const bool wide = single_wave(a, 1LL * B * a.Hkv * a.max_splits);
+  auto kern = wide ? phs_split_decode_kernel<D, TWO, false, 2 * kSplitWarps>
+              : a.qlens ? phs_split_decode_kernel<D, TWO, true>
+                        : phs_split_decode_kernel<D, TWO, false>;
+  const int nw = wide ? 2 * kSplitWarps : kSplitWarps;
+  const int smem = wide ? SplitLayout<D, 2 * kSplitWarps>::kAlloc : SplitLayout<D>::kAlloc;
   if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
   dim3 grid(B, a.Hkv, a.max_splits);
   if (!dependent) {
-    kern<<<grid, kSplitWarps * 32, smem, stream>>>(tk, tv, tk8, tv8, a);
+    kern<<<grid, nw * 32, smem, stream>>>(tk, tv, tk8, tv8, a);
     return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kSplitWarps * 32);
+  cfg.blockDim = dim3(nw * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -580,11 +588,13 @@ int launch_split_decode(int D, const CUtensorMap& tk, const CUtensorMap& tv,
 
 template <int D, bool TWO>
 static int launch_stack_full_t(const StackFullParams& p, int B, cudaStream_t stream) {
-  auto kern = phs_stack_full_kernel<D, TWO>;
-  const int smem = SplitLayout<D>::kAlloc;
+  const bool wide = single_wave(p.a, 1LL * B * p.a.Hkv * p.a.max_splits * p.num_layers);
+  auto kern = wide ? phs_stack_full_kernel<D, TWO, 2 * kSplitWarps> : phs_stack_full_kernel<D, TWO>;
+  const int nw = wide ? 2 * kSplitWarps : kSplitWarps;
+  const int smem = wide ? SplitLayout<D, 2 * kSplitWarps>::kAlloc : SplitLayout<D>::kAlloc;
   if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
   dim3 grid(B, p.a.Hkv, p.a.max_splits * p.num_layers);
-  kern<<<grid, kSplitWarps * 32, smem, stream>>>(p);
+  kern<<<grid, nw * 32, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
 }
 

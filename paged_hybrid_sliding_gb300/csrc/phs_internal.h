@@ -70,6 +70,10 @@ struct SplitArgs {
   // split; k_new null: none).  The stack kernel takes each layer's from its
   // own parameter block instead.
   FusedAppend app;
+  // SMs of the device (0: unknown).  A bf16 launch whose grid has at most
+  // one CTA per SM runs 8 warps per CTA instead of 4, so that each warp's
+  // chain of chunks is half as long (latency-bound small steps).
+  int num_sms;
 };
 
 
