@@ -459,11 +459,12 @@ class TinyHybridWorkload(Workload):
         self.bytes_per_step = (full_tok + swa_tok) * tok_bytes + 2 * 2 * B * Hq * D * 2 + \
             2 * 2 * B * Hkv * D * 2
         self.kernel_bytes = self.bytes_per_step
-        self.kernel = ("the whole step (" + ("Full split + SWA launch, append fused"
+        self.kernel = ("the whole step (" + ("one launch: Full splits + SWA units, append fused"
                                              if fused else "2 appends, SWA, split") + ")")
-        # fused: Full split (append fused, one split: no merge) + SWA decode;
-        # else 2 appends, SWA decode, split
-        self.launches_per_step = 2 if fused else 4
+        # fused: one launch for the whole step (every request in one split,
+        # so no merge, and the Full and SWA work in one wave); else 2 appends,
+        # SWA decode, split
+        self.launches_per_step = 1 if fused else 4
         self.extra = {"batch": B, "layers": "1 Full + 1 SWA(W=128)",
                       "append_fused_into_attention": fused}
         self.h2d_bytes = self.inp.nbytes

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <memory>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -1013,6 +1014,18 @@ int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_laye
   std::memset(&fold_merges, 0, sizeof(fold_merges));
   int fold_layers = 0;
 
+  // A small step (every request in one split, so nothing to merge, and the
+  // Full CTAs and SWA units together in one wave) goes in one launch that
+  // runs both kinds of layer (phs_stack_small_kernel); the parameter blocks
+  // below are built as for the two launches and handed to it.
+  std::unique_ptr<StackSmallParams> small;
+  if (nfull && nswa && nfull < kStackMaxFull && nswa < kSwaMaxLayers && pl.max_splits == 1 &&
+      1LL * batch * Hkv * (nfull + nswa) <= di.sms &&
+      stack_small_smem_bytes(D, num_q_heads / Hkv, di.smem_optin) > 0) {
+    small.reset(new StackSmallParams());
+    std::memset(small.get(), 0, sizeof(StackSmallParams));
+  }
+
   // ---- launch 1 (per 16 Full layers): split-KV decode of every Full layer,
   // each CTA holding a request's newest token also appends it
   if (nfull) {
@@ -1077,7 +1090,10 @@ int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_laye
     }
     if (st == PHS_OK && k) {
       p->num_layers = k;
-      st = launch_stack_full(D, *p, batch, s);
+      if (small)
+        small->full = *p;  // launched with the SWA layers below
+      else
+        st = launch_stack_full(D, *p, batch, s);
       // the last batch of Full layers is merged by the SWA launch when there
       // is one (two launches per step); otherwise by a merge launch
       if (st == PHS_OK && pl.max_splits > 1) {
@@ -1137,8 +1153,16 @@ int phs_attn_decode_hybrid_stack_fused(const phs_layer* layers, int32_t num_laye
         p->num_merge_layers = 0;
       }
     }
-    if (st == PHS_OK && p->num_layers)
-      st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, di.smem_optin, s, nfull > 0);
+    if (st == PHS_OK && p->num_layers) {
+      if (small) {
+        small->swa = *p;
+        small->B = batch;
+        small->full_ctas = batch * Hkv * nfull;
+        st = launch_stack_small(D, *small, batch * Hkv * p->num_layers, s);
+      } else {
+        st = launch_swa_decode<kSwaMaxLayers>(D, *p, di.sms, di.smem_optin, s, nfull > 0);
+      }
+    }
     delete p;
     if (st) return st;
   }

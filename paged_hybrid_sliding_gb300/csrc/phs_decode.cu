@@ -28,6 +28,7 @@
 #include "phs_attn.cuh"
 #include "phs_internal.h"
 #include "phs_merge.cuh"
+#include "phs_swa_chunk.cuh"
 
 namespace phs {
 
@@ -514,6 +515,37 @@ __global__ void __launch_bounds__(NW * 32, NW == kSplitWarps ? PHS_SPLIT_MIN_CTA
                                    L.app, blockIdx.x, blockIdx.y, s);
 }
 
+// A whole small hybrid step in one launch (every request in one split, so
+// nothing to merge, and all CTAs in one wave): CTAs [0, full_ctas) run the
+// Full layers' splits, the rest one SWA unit each.  Both bodies are the
+// ones the two separate launches run, so the results are the same; the step
+// pays one launch instead of two (2-layer hybrid step at batch 2, replayed as
+// a CUDA graph: 8.2 -> 6.2 us; two launches cost the same whether dependent or
+// parallel).  Source: "Xiaomi MiMo-V2.5 inference system" page, section 2
+// (the step's layers in few launches; whole-step replay).
+template <int D, bool TWO>
+__global__ void __launch_bounds__(2 * kSplitWarps * 32, 1)
+    phs_stack_small_kernel(const __grid_constant__ StackSmallParams p) {
+  const int i = blockIdx.x;
+  if (i < p.full_ctas) {
+    const int B = p.B, Hkv = p.full.a.Hkv;
+    const int b = i % B, h = (i / B) % Hkv, l = i / (B * Hkv);
+    const StackFullLayer& L = p.full.layer[l];
+    split_body<D, TWO, false, false, 2 * kSplitWarps>(&L.tk, &L.tv, &L.tk, &L.tv, p.full.a, L.q,
+                                                      L.out, L.ws_o, L.ws_ml, L.app, b, h, 0);
+  } else {
+    swa_chunked_unit<D, TWO, kSwaMaxLayers>(p.swa, i - p.full_ctas);
+  }
+}
+
+int stack_small_smem_bytes(int D, int G, int smem_optin) {
+  const int split = D == 128 ? SplitLayout<128, 2 * kSplitWarps>::kAlloc
+                             : SplitLayout<64, 2 * kSplitWarps>::kAlloc;
+  const int swa = SwaChunkLayout(D, G).total;
+  const int need = split > swa ? split : swa;
+  return need <= smem_optin ? need : 0;
+}
+
 // Cross-split merge of one (request, KV head): warp w of the CTA merges
 // query rows w, w+4, ...
 template <int D>
@@ -596,6 +628,28 @@ static int launch_stack_full_t(const StackFullParams& p, int B, cudaStream_t str
   dim3 grid(B, p.a.Hkv, p.a.max_splits * p.num_layers);
   kern<<<grid, nw * 32, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+}
+
+template <int D, bool TWO>
+static int launch_stack_small_t(const StackSmallParams& p, int swa_units, int smem,
+                                cudaStream_t stream) {
+  auto kern = phs_stack_small_kernel<D, TWO>;
+  if (ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem) != PHS_OK) return PHS_ECUDA;
+  kern<<<static_cast<unsigned>(p.full_ctas + swa_units), 2 * kSplitWarps * 32, smem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PHS_OK : PHS_ECUDA;
+}
+
+int launch_stack_small(int D, const StackSmallParams& p, int swa_units, cudaStream_t stream) {
+  if (p.full.a.max_splits != 1 || p.full.num_layers <= 0 || p.swa.num_layers <= 0) return PHS_EINVAL;
+  const int smem = stack_small_smem_bytes(D, p.full.a.G, 1 << 30);
+  const bool two = p.full.a.G > 8;
+  if (D == 128)
+    return two ? launch_stack_small_t<128, true>(p, swa_units, smem, stream)
+               : launch_stack_small_t<128, false>(p, swa_units, smem, stream);
+  if (D == 64)
+    return two ? launch_stack_small_t<64, true>(p, swa_units, smem, stream)
+               : launch_stack_small_t<64, false>(p, swa_units, smem, stream);
+  return PHS_EUNSUPPORTED;
 }
 
 int launch_stack_full(int D, const StackFullParams& p, int B, cudaStream_t stream) {

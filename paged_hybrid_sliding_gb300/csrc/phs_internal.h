@@ -201,6 +201,21 @@ template <int MAXL>
 int launch_swa_decode(int D, const SwaParams<MAXL>& p, int num_sms, int smem_optin,
                       cudaStream_t stream, bool dependent = false);
 
+// ---------------------------------------------- one-launch small step --
+// A whole small hybrid step in one launch: CTAs [0, full_ctas) run the Full
+// layers' splits (one split per request, 8 warps), the rest one SWA unit
+// each (the chunked shape).
+struct StackSmallParams {
+  StackFullParams full;
+  SwaParams<kSwaMaxLayers> swa;
+  int B;
+  int full_ctas;  // B x Hkv x Full layers
+};
+
+// Dynamic shared memory of the one-launch step (0: does not fit).
+int stack_small_smem_bytes(int D, int G, int smem_optin);
+int launch_stack_small(int D, const StackSmallParams& p, int swa_units, cudaStream_t stream);
+
 // -------------------------------------------------------------- append --
 constexpr int kAppendMaxLayers = 64;
 

@@ -38,10 +38,10 @@ PATCHES = {
     # first unit (persistent kernel) or its second chunk (one CTA per unit)
     "phs_swa.cu": [("    if (!iu.ok) {\n",
                     "    if (blockIdx.x == 0 && warp == 0 && ik == 0 && ic == 1) {\n"
-                    "    } else if (!iu.ok) {\n"),
-                   ("  auto issue = [&](int jj) {  // lane 0: chunk warp + NW jj into stage jj % S\n",
-                    "  auto issue = [&](int jj) {  // lane 0: chunk warp + NW jj into stage jj % S\n"
-                    "    if (blockIdx.x == 0 && warp == 0 && jj == 1) return;\n")],
+                    "    } else if (!iu.ok) {\n")],
+    "phs_swa_chunk.cuh": [("  auto issue = [&](int jj) {  // lane 0: chunk warp + NW jj into stage jj % S\n",
+                           "  auto issue = [&](int jj) {  // lane 0: chunk warp + NW jj into stage jj % S\n"
+                           "    if (blockIdx.x == 0 && warp == 0 && jj == 1) return;\n")],
 }
 
 
