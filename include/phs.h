@@ -405,8 +405,11 @@ size_t phs_hybrid_stack_workspace_bytes(int32_t batch, int32_t num_q_heads,
  * at once and one persistent launch for up to 64 SWA layers, whose warps
  * also run the Full layers' cross-split merges after their SWA work (a
  * stack without SWA layers gets a merge launch instead).  Config 3, 10
- * Full + 60 SWA: two launches per step instead of twenty-three.  The Full layers' partials live side by side, so the
- * workspace is phs_hybrid_stack_fused_workspace_bytes (256-byte aligned).
+ * Full + 60 SWA: two launches per step instead of twenty-three.  A small
+ * step (every request in one split, fewer than 16 Full and 64 SWA layers,
+ * and all its CTAs in one wave) goes in a single launch.  The Full layers'
+ * partials live side by side, so the workspace is
+ * phs_hybrid_stack_fused_workspace_bytes (256-byte aligned).
  * Outputs and pool contents equal those of the unfused call.
  * Errors as phs_attn_decode_hybrid_stack (PHS_EINVAL also for a missing
  * k_new/v_new); block-table ids must be valid for every Full pool.  With
