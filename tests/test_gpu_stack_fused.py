@@ -172,6 +172,42 @@ def test_fused_stack_errors():
     assert phs.hybrid_stack_fused_workspace_bytes(8, 32, 8, 128, 4096, 10) == 10 * one
 
 
+@pytest.mark.parametrize("D,Hq,Hkv,out_dtype", [(128, 8, 2, torch.float32),
+                                                (64, 32, 2, torch.bfloat16),
+                                                (128, 32, 8, torch.float32)])
+def test_small_step_one_launch_equals_unfused(D, Hq, Hkv, out_dtype):
+    """Short requests (one split each) and a few layers of each kind: the
+    fused call runs the whole step in one launch (Full splits and SWA units
+    side by side).  Outputs and pools equal the unfused call's bit for bit;
+    the last layer of each kind matches the oracle."""
+    n_after = np.array([1, 16, 17, 100, 200, 256], dtype=np.int32)
+    lf = [1, 0, 0, 1, 0]  # 2 Full + 3 SWA layers
+    bt, rp, host = _stack(n_after, Hq, Hkv, D, lf, seed=140 + D + Hq, out_dtype=out_dtype)
+    a = _device_layers(host, out_dtype)
+    b = _device_layers(host, out_dtype)
+    common = dict(block_table=dev(bt), ring_pos=dev(rp))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    phs.attn_decode_hybrid_stack(a, Hq, dev(n_after), int(n_after.max()), do_append=True, **common)
+    phs.attn_decode_hybrid_stack_fused(b, Hq, dev(n_after), int(n_after.max()), status=st, **common)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for l, (La, Lb) in enumerate(zip(a, b)):
+        assert torch.equal(La.out, Lb.out), l
+        for x, y in zip(_pools(La), _pools(Lb)):
+            assert torch.equal(x, y), l
+    scale = 1.0 / np.sqrt(D)
+    for l in (3, 4):  # the last Full and the last SWA layer
+        full, q, kn, vn, k, v = host[l]
+        k, v = k.copy(), v.copy()
+        if full:
+            oracle.append_paged(k, v, kn, vn, bt, n_after)
+            ref, _ = oracle.decode_full_paged(q, k, v, bt, n_after, scale)
+        else:
+            oracle.append_ring(k, v, kn, vn, None, rp)
+            ref, _ = oracle.decode_swa_ring(q, k, v, None, rp, n_after, scale)
+        assert_close(out_np(b[l].out), ref, f"layer {l}")
+
+
 @pytest.mark.parametrize("nfull,nswa", [(1, 66), (18, 2)])
 def test_fused_stack_many_layers_equals_unfused(nfull, nswa):
     # more SWA layers than one launch carries (64: a second SWA launch, a
