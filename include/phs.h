@@ -404,8 +404,9 @@ size_t phs_hybrid_stack_workspace_bytes(int32_t batch, int32_t num_q_heads,
  * reading it back.  Launches: one split-KV launch for up to 16 Full layers
  * at once and one persistent launch for up to 64 SWA layers, whose warps
  * also run the Full layers' cross-split merges after their SWA work (a
- * stack without SWA layers gets a merge launch instead).  Config 3, 10
- * Full + 60 SWA: two launches per step instead of twenty-three.  A small
+ * stack without SWA layers gets a merge launch instead).  A 70-layer
+ * stack of 10 Full + 60 SWA layers: two launches per step instead of
+ * twenty-three.  A small
  * step (every request in one split, fewer than 16 Full and 64 SWA layers,
  * and all its CTAs in one wave) goes in a single launch.  The Full layers'
  * partials live side by side, so the workspace is
