@@ -13,7 +13,9 @@
 // request's newest slot also appends the new token (ring write + patch of
 // the staged row from the input), and the warps take the Full layers'
 // cross-split merges after their SWA units, once the split launch before
-// them has finished (programmatic dependent launch).
+// them has finished (programmatic dependent launch).  Small steps (at most
+// one unit per SM) take the chunked shape instead: one CTA per unit, its
+// chunks spread over the CTA's warps (phs_swa_chunk.cuh).
 //
 // Sources: "Xiaomi MiMo-V2.5 inference system" page, section 1 (SWA layers
 // keep and attend to the most recent 128 tokens) and section 2 (ring
