@@ -57,6 +57,16 @@ def test_full_decode_ragged(D, Hq, Hkv, out_dtype):
     assert_close(got, ref_full(c), f"D={D} G={Hq // Hkv} {out_dtype}")
 
 
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 32, 2), (128, 24, 4), (64, 4, 2)])
+def test_full_decode_single_wave_eight_warps(D, Hq, Hkv):
+    # a grid of at most one CTA per SM runs 8 warps per CTA: short requests
+    # (one 256-token split each), and longer ones in one explicit long split
+    c = paged_case([1, 16, 17, 100, 200, 256], Hq, Hkv, D, seed=300 + D + Hq)
+    assert_close(run_full(c), ref_full(c), f"short D={D} G={Hq // Hkv}")
+    c = paged_case([300, 1000, 2049], Hq, Hkv, D, seed=310 + D + Hq)
+    assert_close(run_full(c, tps=4096), ref_full(c), f"long D={D} G={Hq // Hkv}")
+
+
 @pytest.mark.parametrize("tps", [32, 64, 256, 1024, 4096])
 def test_full_decode_any_split(tps):
     c = paged_case([3, 64, 700, 3000, 4096], 32, 8, 128, seed=7)

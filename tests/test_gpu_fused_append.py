@@ -102,6 +102,22 @@ def test_fused_append_equals_append_then_decode(D, Hq, Hkv, tps, phases):
         assert_close(outs[1], ref, "fused append vs oracle")
 
 
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 32, 2)])
+def test_fused_append_single_wave(D, Hq, Hkv):
+    # short requests: one split each, a grid of at most one CTA per SM (8
+    # warps per CTA); the new token at the first, a middle and the last slot
+    # of its page
+    c = _case([1, 16, 17, 100, 200, 256], Hq, Hkv, D, seed=90 + D)
+    outs, sts, pools = _two_ways(c)
+    assert sts == [0, 0]
+    _same(outs, pools)
+    kp, vp = synth.bits(pools[1].k), synth.bits(pools[1].v)
+    ref, s = oracle.decode_full_paged(synth.bits(c["q"]), kp, vp, c["bt"], c["lens"],
+                                      1 / math.sqrt(D))
+    assert s == 0
+    assert_close(outs[1], ref, "single-wave fused append vs oracle")
+
+
 @pytest.mark.parametrize("tps", [0, 512])
 def test_fused_append_with_int8_region(tps):
     # INT8 below qlens, the new token in the bf16 tail
