@@ -269,6 +269,23 @@ class Workload:
         host copies happen inside the loop.  A latency-bound step (where the
         staging would cost more than it hides) copies in and out directly."""
         if not self.e2e_pipelined:
+            if getattr(self, "e2e_graph", False):
+                # the step as the timed loop replays it: one CUDA graph
+                # holding the host-to-device copy, the API call and the
+                # device-to-host copy (pinned host buffers, every step)
+                if getattr(self, "_e2e_g", None) is None:
+                    ins, outs = self.e2e_io(0)
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        for h, d in ins:
+                            d.copy_(h, non_blocking=True)
+                        self.e2e_compute(0)
+                        for src, h in outs:
+                            h.copy_(src, non_blocking=True)
+                    self._e2e_g = g
+                for _ in range(steps):
+                    self._e2e_g.replay()
+                return
             for k in range(steps):
                 ins, outs = self.e2e_io(k)
                 for h, d in ins:
@@ -1184,7 +1201,8 @@ def measure(wl, steps, warmup, world, device, use_graph, copy_gbs, with_cpu, rea
 
     # end to end through the public API with host buffers, the same number
     # of steps as the timed loop (copies overlapped with compute, as a
-    # serving loop would)
+    # serving loop would; a graph-replayed step replays its copies with it)
+    wl.e2e_graph = graph is not None and wl.graphable and not wl.e2e_pipelined
     wl.e2e_run(3)
     torch.cuda.synchronize()
     if world > 1:
@@ -1229,7 +1247,9 @@ def measure(wl, steps, warmup, world, device, use_graph, copy_gbs, with_cpu, rea
                            "copy streams, double-buffered device staging)"
                            if wl.e2e_pipelined else
                            "every step's inputs up and outputs down through pinned host "
-                           "buffers, in line with the step")},
+                           "buffers, in line with the step" + (
+                               " (the copies and the API call replayed as one CUDA graph)"
+                               if getattr(wl, "e2e_graph", False) else ""))},
         "gpu_launches": wl.launches_per_step * steps + sum(
             1 for i in step_ids if i in getattr(wl, "ages", {})),
         "clocks": clk.summary(),
