@@ -69,7 +69,8 @@ __device__ __forceinline__ void swa_chunked_unit(const SwaParams<MAXL>& p, int u
   u.pos = __ldg(p.ring_pos + u.b);
   u.n = __ldg(p.seq_lens + u.b);
   u.ok = u.ring >= 0 && u.ring < p.num_rings[u.l] && u.pos >= 0 && u.pos < W && u.n >= 0;
-  const uint32_t bar0 = sb + L.bar_off + warp * S * 8;  // this warp's stage barriers
+  // this warp's stage barriers and stages (used by warps < NW only)
+  const uint32_t bar0 = sb + L.bar_off + warp * S * 8;
   const uint32_t qbar = sb + L.bar_off + NW * S * 8;
   const uint32_t sbase = sb + warp * S * L.kv;
   const uint32_t qs = sb + L.q_off;
